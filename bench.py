@@ -1,0 +1,456 @@
+#!/usr/bin/env python
+"""Throughput of the routed FP8 block-scaled MoE layer on GB300 (one JSON line on stdout).
+
+A step is one pass of the whole layer -- moe_route then moe_fp8_forward (prepare, gate/up
++ SiLU*up requantisation, down, combine) -- over one batch of synthetic tokens. The default
+workload is decode: hidden 2048, intermediate 768, 128 experts, top-8 renormalised, one
+token per step, stepping through 10,000 seeded tokens. Other workloads (--workload):
+verify, verify_skewed (M=12), wide (M=1..64, h6144/i768/e128/top4), prefill, prefill_zipf
+(M=4096).
+
+value   tokens/s with inputs resident in HBM, timed with CUDA events around CUDA-graph
+        replays of the steps; 8 weight replicas (decode/verify/wide) or 2 (prefill) are
+        rotated step by step so that no step reuses L2-resident weights.
+e2e     the same metric through the public API with host buffers: per step the hidden
+        rows are copied from pinned host memory, route + forward run eagerly, and the
+        output is copied back to pinned host memory, all inside the timed region.
+roofline the dominant kernel (gate/up) timed alone with CUDA events on its stream, its
+        algorithmic bytes (or FLOPs) per launch divided by the mean launch time.
+cpu_baseline the oracle (plain C++ on the host cores) on a bounded sample of the same
+        workload (rank 0, N=1 only).
+
+--impl reference times that oracle as the reference arm.
+Multi-GPU (torchrun): every rank runs its own replica of the workload on its own tokens
+(the layer is data-parallel over tokens; no collective on the data path); value sums the
+ranks' tokens over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s; achieved HBM GB/s (decode) / FP8 TFLOP/s (prefill)"
+
+WORKLOADS = {
+    "decode": dict(cfg="decode", M=1, desc="decode M=1: h2048 i768 e128 top-8 renormalised, "
+                                          "1 token per step over 10k seeded tokens"),
+    "verify": dict(cfg="verify", M=12, desc="speculative verify M=12: h2048 i768 e128 top-8"),
+    "verify_skewed": dict(cfg="verify_skewed", M=12,
+                          desc="speculative verify M=12, +3.0 logit bias on experts 0-3"),
+    "wide": dict(cfg="wide", M=64, desc="wide expert: h6144 i768 e128 top-4"),
+    "prefill": dict(cfg="prefill", M=4096, desc="prefill M=4096: h2048 i768 e128 top-8, "
+                                                "router logits ~N(0,1)"),
+    "prefill_zipf": dict(cfg="prefill_zipf", M=4096,
+                         desc="prefill M=4096: h2048 i768 e128 top-8, Zipf(1.1) expert load"),
+}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=None)
+    p.add_argument("--warmup", type=int, default=None)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
+    p.add_argument("--m", type=int, default=None, help="tokens per step (wide sweep)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------- helpers
+def per_expert_bytes(H, I):
+    w13 = 2 * I * H + (2 * I // 128) * (H // 128) * 4
+    w2 = H * I + (H // 128) * (I // 128) * 4
+    return w13, w2
+
+
+def algorithmic(H, I, E, K, M, distinct):
+    """Bytes and FLOPs one step must move / do at minimum."""
+    w13, w2 = per_expert_bytes(H, I)
+    R = M * K
+    byts = distinct * (w13 + w2) + H * E * 2 + M * H * 2 * 2 + M * K * 8
+    flops = 2 * M * H * E + 6 * H * I * R
+    gateup_bytes = distinct * w13 + M * H + M * (H // 128) * 4 + R * I + R * (I // 128) * 4
+    gateup_flops = 4 * H * I * R
+    return byts, flops, gateup_bytes, gateup_flops
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fp8_block_scaled_router_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        if n.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, n), "rb") as f:
+                h.update(n.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current sources."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f)
+        rec = d.get(workload, {}).get(kernel)
+        if rec and rec.get("source_hash") == kernel_source_hash():
+            return rec["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id):
+        self.bus_id = bus_id
+        self.rows = []
+        self.proc = None
+        self.err = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.bus_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception as e:  # no nvidia-smi
+            self.err = str(e)
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.rows and time.time() - t0 < 5:
+            time.sleep(0.02)
+        self.rows.clear()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 7:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": self.err}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = list(self.rows)
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ----------------------------------------------------------------------------- oracle arm
+def oracle_tokens_per_s(x, M, budget_s=15.0, max_tokens=None):
+    """Time the oracle (route + FFN) on a bounded sample of tokens on all host cores."""
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    K = x.shape.top_k
+    total = x.hidden.shape[0]
+
+    def run(n):
+        hid = x.hidden[:n]
+        t0 = time.perf_counter()
+        if x.ids is not None:
+            ids, w = x.ids[:n], x.weights[:n]
+        else:
+            ids, w = oracle.route(hid, x.router_w, x.bias, K)
+        oracle.moe_forward(hid, ids, w, x.w13, x.s13, x.w2, x.s2, nthreads=cores)
+        return time.perf_counter() - t0
+
+    n = min(cores, total)
+    dt = run(n)
+    per_tok = dt / n
+    n2 = int(min(total, max(n, budget_s / max(per_tok, 1e-9))))
+    if max_tokens:
+        n2 = min(n2, max_tokens)
+    if n2 > n:
+        n, dt = n2, run(n2)
+    return n / dt, cores, n, dt
+
+
+def reference_arm(args, wl, world, rank):
+    if rank != 0:
+        return
+    from fp8_block_scaled_router_gb300 import inputs
+    import oracle
+    oracle.build()
+    M = args.m or wl["M"]
+    x = inputs.make(wl["cfg"], tokens=10000 if wl["cfg"] == "decode" else None,
+                    M=M if wl["cfg"] == "wide" else None)
+    steps = args.steps or 3
+    warm = args.warmup if args.warmup is not None else 1
+    tps, cores, n, dt = oracle_tokens_per_s(x, M, budget_s=20.0)
+    line = {"impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": 0,
+            "steps": steps, "warmup": warm, "ms_per_step": 1e3 * M / tps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64-exact block sums, f32 chains",
+            "data": "synthetic",
+            "config": {"workload": wl["desc"], "M": M, "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{n} tokens of the workload (route + expert FFN), "
+                                       f"{dt:.1f} s, std::thread over tokens"},
+            "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- our arm
+def ours_arm(args, wl, world, rank, local):
+    import torch
+    from fp8_block_scaled_router_gb300 import _lib as L
+    from fp8_block_scaled_router_gb300 import build as B
+    from fp8_block_scaled_router_gb300 import inputs
+
+    B.build()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    cfg = wl["cfg"]
+    decode = cfg == "decode"
+    M = args.m or wl["M"]
+    prefill = M >= 1024
+    ntok = 10000 if decode else M
+    x = inputs.make(cfg, tokens=ntok if decode else None, M=M if cfg == "wide" else None)
+    H, I, E, K = x.shape.hidden, x.shape.inter, x.shape.num_experts, x.shape.top_k
+    # each rank steps through its own token stream (a different slice of the seeded rows)
+    if decode and world > 1:
+        x.hidden = np.roll(x.hidden, -rank * (ntok // world), axis=0)
+
+    def dev(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
+
+    n_rep = 2 if prefill else 8
+    w13_0, s13_0, w2_0, s2_0 = dev(x.w13), dev(x.s13), dev(x.w2), dev(x.s2)
+    reps = [(w13_0, s13_0, w2_0, s2_0)] + [(w13_0.clone(), s13_0.clone(), w2_0.clone(), s2_0.clone())
+                                           for _ in range(n_rep - 1)]
+    router = dev(x.router_w)
+    bias = None if x.bias is None else dev(x.bias)
+    shape = L.make_shape(H, I, E, K, M)
+    ws = torch.empty(L.moe_fp8_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
+    L.moe_fp8_workspace_init(ws, shape)
+    hidden_all = dev(x.hidden)                      # [ntok][H]
+    nbatches = hidden_all.shape[0] // M
+    given_ids = None if x.ids is None else (dev(x.ids), dev(x.weights))
+    ids = torch.empty((nbatches, M, K), dtype=torch.int32, device="cuda")
+    wts = torch.empty((nbatches, M, K), dtype=torch.float32, device="cuda")
+    out = torch.empty((nbatches, M, H), dtype=torch.int16, device="cuda")
+
+    def step(i, stream=None):
+        b = i % nbatches
+        hid = hidden_all[b * M:(b + 1) * M]
+        w13, s13, w2, s2 = reps[i % n_rep]
+        L.moe_route(hid, router, bias, M, shape, True, ids[b], wts[b], stream=stream)
+        if given_ids is not None:   # Zipf workload: the expert load is given, not routed
+            ii, ww = given_ids
+        else:
+            ii, ww = ids[b], wts[b]
+        L.moe_fp8_forward(hid, ii, ww, M, w13, s13, w2, s2, out[b], ws, shape, stream=stream)
+
+    kernels_per_step = 5  # route, prepare, gate/up, down, combine
+
+    # distinct experts per step (accounting only)
+    for i in range(min(nbatches, 64)):
+        step(i)
+    torch.cuda.synchronize()
+    src = given_ids[0] if given_ids is not None else ids
+    sample = src.reshape(-1, M * K)[: min(nbatches, 64)].cpu().numpy() if given_ids is None else \
+        src.reshape(1, -1).cpu().numpy()
+    distinct = float(np.mean([len(np.unique(r)) for r in sample]))
+    alg_bytes, alg_flops, gu_bytes, gu_flops = algorithmic(H, I, E, K, M, distinct)
+
+    # ---- CUDA graphs of G steps each
+    steps = args.steps or (50000 if decode else (2000 if M <= 64 else 20))
+    warm = max(3, args.warmup if args.warmup is not None else (200 if decode else 5))
+    G = 500 if decode else (50 if M <= 64 else 1)
+    n_graphs = max(1, min(20, nbatches // G)) if decode else 1
+    graphs = []
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for gi in range(n_graphs):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for j in range(G):
+                    step(gi * G + j)
+            graphs.append(g)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    reps_needed = max(1, -(-steps // G))
+    steps = reps_needed * G
+    for i in range(max(1, -(-warm // G))):
+        graphs[i % n_graphs].replay()
+    torch.cuda.synchronize()
+
+    props = torch.cuda.get_device_properties(local)
+    uuid = str(getattr(props, "uuid", ""))
+    sel = ("GPU-" + uuid if uuid and not uuid.startswith("GPU-") else uuid) or str(local)
+    sampler = ClockSampler(sel) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall = time.perf_counter()
+    ev0.record()
+    for i in range(reps_needed):
+        graphs[i % n_graphs].replay()
+    ev1.record()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    clocks = sampler.stop() if sampler else None
+    if dist:
+        t = torch.tensor([elapsed], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+        dist.barrier()
+    value = world * steps * M / elapsed
+    ms_per_step = 1e3 * elapsed / steps
+
+    # ---- dominant kernel alone: gate/up, events on its own stream
+    ks = torch.cuda.Stream()
+    n_k = 300 if M <= 64 else 10
+    times = []
+    with torch.cuda.stream(ks):
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(n_k)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(n_k)]
+        for i in range(n_k):
+            b = i % nbatches
+            hid = hidden_all[b * M:(b + 1) * M]
+            w13, s13, w2, s2 = reps[i % n_rep]
+            ii = given_ids[0] if given_ids is not None else ids[b]
+            L.moe_fp8_prepare(hid, ii, M, ws, shape, stream=ks)
+            e0[i].record(ks)
+            L.moe_fp8_gate_up(w13, s13, M, ws, shape, stream=ks)
+            e1[i].record(ks)
+            L.moe_fp8_down(w2, s2, M, ws, shape, stream=ks)
+    ks.synchronize()
+    times = [a.elapsed_time(b) / 1e3 for a, b in zip(e0, e1)][n_k // 10:]
+    t_gu = float(np.mean(times))
+    hbm, bf16, bf16_sus, peak_src = load_peaks()
+    if prefill:
+        fp8_peak = 2.0 * bf16  # FP8 dense rate = 2x the measured bf16 rate (nominal ratio)
+        roof = {"bound": "tensor", "kernel": "gate_up", "achieved": gu_flops / t_gu / 1e12,
+                "peak": fp8_peak, "unit": "TFLOP/s", "frac": gu_flops / t_gu / 1e12 / fp8_peak,
+                "peak_source": f"{peak_src} bf16 x 2 (fp8/bf16 nominal ratio)"}
+    else:
+        roof = {"bound": "hbm", "kernel": "gate_up", "achieved": gu_bytes / t_gu / 1e9, "peak": hbm,
+                "unit": "GB/s", "frac": gu_bytes / t_gu / 1e9 / hbm, "peak_source": f"{peak_src} hbm_gbs"}
+    roof["traffic"] = recorded_traffic("gate_up", args.workload)
+    roof["alg_per_launch"] = gu_flops if prefill else gu_bytes
+    roof["mean_launch_us"] = t_gu * 1e6
+
+    # ---- end to end through the public API with host buffers
+    e2e_steps = min(steps, 3000 if decode else (500 if M <= 64 else 10))
+    host_in = torch.empty((nbatches, M, H), dtype=torch.int16).pin_memory()
+    host_in.copy_(hidden_all.view(nbatches, M, H).cpu())
+    host_out = torch.empty((nbatches, M, H), dtype=torch.int16).pin_memory()
+    stage = torch.empty((2, M, H), dtype=torch.int16, device="cuda")
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    cs = torch.cuda.current_stream()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record()
+    for i in range(e2e_steps):
+        b = i % nbatches
+        hid = stage[i % 2]
+        hid.copy_(host_in[b], non_blocking=True)
+        w13, s13, w2, s2 = reps[i % n_rep]
+        L.moe_route(hid, router, bias, M, shape, True, ids[b], wts[b])
+        ii, ww = (given_ids if given_ids is not None else (ids[b], wts[b]))
+        L.moe_fp8_forward(hid, ii, ww, M, w13, s13, w2, s2, out[b], ws, shape)
+        host_out[b].copy_(out[b], non_blocking=True)
+    a1.record()
+    torch.cuda.synchronize()
+    e2e_t = a0.elapsed_time(a1) / 1e3
+    if dist:
+        t = torch.tensor([e2e_t], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_t = float(t.item())
+    e2e = {"value": world * e2e_steps * M / e2e_t, "unit": "tokens/s",
+           "h2d_bytes_per_step": M * H * 2, "d2h_bytes_per_step": M * H * 2, "steps": e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tps, cores, n, dt = oracle_tokens_per_s(x, M, budget_s=15.0)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{n} tokens of the same workload (route + expert FFN), {dt:.1f} s, "
+                         f"std::thread over tokens"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+                "steps": steps, "warmup": warm, "ms_per_step": ms_per_step, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 (f32 accumulate)",
+                "data": "synthetic",
+                "config": {"workload": wl["desc"], "M": M, "hidden": H, "inter": I, "experts": E,
+                           "top_k": K, "distinct_experts_per_step": distinct,
+                           "l2": f"inputs larger than L2: {n_rep} weight replicas "
+                                 f"({n_rep * (x.w13.nbytes + x.w2.nbytes) / 1e9:.2f} GB) rotated per step",
+                           "timing": f"CUDA graphs of {G} steps, events, wall {t_wall:.3f} s"},
+                "achieved_gbs": alg_bytes * steps / elapsed / 1e9 / 1 * world,
+                "achieved_tflops": alg_flops * steps / elapsed / 1e12 * world,
+                "alg_bytes_per_step": alg_bytes, "alg_flops_per_step": alg_flops,
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": kernels_per_step * steps, "clocks": clocks}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_info()
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        reference_arm(args, wl, world, rank)
+    else:
+        ours_arm(args, wl, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

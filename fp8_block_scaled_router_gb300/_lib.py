@@ -1,0 +1,176 @@
+"""ctypes binding of libmoe_fp8.so (the C ABI of include/moe_fp8.h).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA kernels.
+Tensors are torch CUDA tensors (or raw integer device pointers); the stream defaults to
+torch's current stream. A non-zero status raises :class:`MoEError` unless ``check=False``.
+The library must have been built (``fp8_block_scaled_router_gb300.build``); a missing
+library raises at load time -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB
+
+_lock = threading.Lock()
+_lib = None
+
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
+          4: "MOE_ERR_LAUNCH"}
+STATUS_BAD_EXPERT_ID = 0x1
+STATUS_WAIT_TIMEOUT = 0x2
+
+EXPORTS = ("moe_fp8_version", "moe_fp8_workspace_bytes", "moe_fp8_workspace_init", "moe_route",
+           "moe_fp8_forward", "moe_fp8_prepare", "moe_fp8_gate_up", "moe_fp8_down",
+           "moe_fp8_combine", "moe_fp8_workspace_view", "moe_fp8_read_status")
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} returned {STATUS.get(code, code)}")
+        self.code = code
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("inter", ctypes.c_int32),
+                ("num_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
+                ("max_tokens", ctypes.c_int32)]
+
+
+class WsView(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("qa", "sa", "row_src", "perm_row", "act", "act_scale", "y", "expert_offsets")]
+
+
+def load(path: str = LIB):
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(f"libmoe_fp8.so not built ({path}); run "
+                                   "python -m fp8_block_scaled_router_gb300.build")
+            lib = ctypes.CDLL(path)
+            vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+            sp = ctypes.POINTER(Shape)
+            lib.moe_fp8_version.restype = ctypes.c_char_p
+            lib.moe_fp8_workspace_bytes.argtypes = [sp]
+            lib.moe_fp8_workspace_bytes.restype = sz
+            lib.moe_fp8_workspace_init.argtypes = [vp, sz, sp, vp]
+            lib.moe_route.argtypes = [vp, vp, vp, i32, sp, i32, vp, vp, vp]
+            lib.moe_fp8_forward.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, sz, sp, vp]
+            lib.moe_fp8_prepare.argtypes = [vp, vp, i32, vp, sz, sp, vp]
+            lib.moe_fp8_gate_up.argtypes = [vp, vp, i32, vp, sz, sp, vp]
+            lib.moe_fp8_down.argtypes = [vp, vp, i32, vp, sz, sp, vp]
+            lib.moe_fp8_combine.argtypes = [vp, i32, vp, vp, sz, sp, vp]
+            lib.moe_fp8_workspace_view.argtypes = [vp, sz, sp, ctypes.POINTER(WsView)]
+            lib.moe_fp8_read_status.argtypes = [vp, vp, vp]
+            for f in EXPORTS[2:]:
+                if f != "moe_fp8_workspace_bytes":
+                    getattr(lib, f).restype = i32
+            _lib = lib
+    return _lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _nbytes(x):
+    return x if isinstance(x, int) else x.numel() * x.element_size()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn, code, check):
+    if check and code != 0:
+        raise MoEError(fn, code)
+    return code
+
+
+def make_shape(hidden, inter, num_experts, top_k, max_tokens) -> Shape:
+    return Shape(hidden, inter, num_experts, top_k, max_tokens)
+
+
+def moe_fp8_version() -> str:
+    return load().moe_fp8_version().decode()
+
+
+def moe_fp8_workspace_bytes(shape: Shape) -> int:
+    return int(load().moe_fp8_workspace_bytes(ctypes.byref(shape)))
+
+
+def moe_fp8_workspace_init(workspace, shape: Shape, stream=None, ws_bytes=None, check=True):
+    nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return _check("moe_fp8_workspace_init",
+                  load().moe_fp8_workspace_init(_ptr(workspace), nb, ctypes.byref(shape), _stream(stream)),
+                  check)
+
+
+def moe_route(hidden, router_w, bias, M, shape: Shape, renormalize, topk_ids, topk_w, stream=None,
+              check=True):
+    return _check("moe_route", load().moe_route(_ptr(hidden), _ptr(router_w), _ptr(bias), int(M),
+                                                ctypes.byref(shape), int(bool(renormalize)),
+                                                _ptr(topk_ids), _ptr(topk_w), _stream(stream)), check)
+
+
+def moe_fp8_forward(hidden, topk_ids, topk_w, M, w13, w13_scale, w2, w2_scale, out, workspace,
+                    shape: Shape, stream=None, ws_bytes=None, check=True):
+    nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return _check("moe_fp8_forward", load().moe_fp8_forward(
+        _ptr(hidden), _ptr(topk_ids), _ptr(topk_w), int(M), _ptr(w13), _ptr(w13_scale), _ptr(w2),
+        _ptr(w2_scale), _ptr(out), _ptr(workspace), nb, ctypes.byref(shape), _stream(stream)), check)
+
+
+def moe_fp8_prepare(hidden, topk_ids, M, workspace, shape: Shape, stream=None, ws_bytes=None, check=True):
+    nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return _check("moe_fp8_prepare", load().moe_fp8_prepare(
+        _ptr(hidden), _ptr(topk_ids), int(M), _ptr(workspace), nb, ctypes.byref(shape),
+        _stream(stream)), check)
+
+
+def moe_fp8_gate_up(w13, w13_scale, M, workspace, shape: Shape, stream=None, ws_bytes=None, check=True):
+    nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return _check("moe_fp8_gate_up", load().moe_fp8_gate_up(
+        _ptr(w13), _ptr(w13_scale), int(M), _ptr(workspace), nb, ctypes.byref(shape),
+        _stream(stream)), check)
+
+
+def moe_fp8_down(w2, w2_scale, M, workspace, shape: Shape, stream=None, ws_bytes=None, check=True):
+    nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return _check("moe_fp8_down", load().moe_fp8_down(
+        _ptr(w2), _ptr(w2_scale), int(M), _ptr(workspace), nb, ctypes.byref(shape), _stream(stream)),
+        check)
+
+
+def moe_fp8_combine(topk_w, M, out, workspace, shape: Shape, stream=None, ws_bytes=None, check=True):
+    nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return _check("moe_fp8_combine", load().moe_fp8_combine(
+        _ptr(topk_w), int(M), _ptr(out), _ptr(workspace), nb, ctypes.byref(shape), _stream(stream)),
+        check)
+
+
+def moe_fp8_workspace_view(workspace, shape: Shape, ws_bytes=None) -> WsView:
+    nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    v = WsView()
+    _check("moe_fp8_workspace_view",
+           load().moe_fp8_workspace_view(_ptr(workspace), nb, ctypes.byref(shape), ctypes.byref(v)), True)
+    return v
+
+
+def moe_fp8_read_status(workspace, host_dst, stream=None, check=True):
+    """host_dst: a pinned torch uint32/int32 CPU tensor of >= 1 element (or a host pointer)."""
+    return _check("moe_fp8_read_status", load().moe_fp8_read_status(
+        _ptr(workspace), _ptr(host_dst), _stream(stream)), check)

@@ -1,0 +1,195 @@
+// api.cu -- the C ABI (include/moe_fp8.h): host-side validation, workspace layout and the
+// launch sequence. No call allocates, frees, synchronises or reads device memory.
+//
+// Sources: "NetraRuntime/netra-kernel" README (stable C ABI that launches on a
+// caller-provided stream; exact profile guards, unsupported contracts are refused) and
+// older kernel-lab README "Design" (dispatch without allocation, synchronisation,
+// filesystem access, environment parsing or symbol lookup); docs/compiler/architecture.md
+// (caller-local kernel arguments so concurrent calls cannot mix pointers).
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace moe {
+cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const float* bias, int M,
+                         int H, int E, int K, int renorm, int32_t* ids, float* wts, cudaStream_t st);
+cudaError_t launch_prep(const uint16_t* hidden, const int32_t* ids, int M, int H, int E, int K,
+                        const WsPtrs& ws, cudaStream_t st);
+cudaError_t launch_gateup_gemv(const uint8_t* w13, const float* s13, int H, int I, int K,
+                               int64_t max_tiles, const WsPtrs& ws, cudaStream_t st);
+cudaError_t launch_down_gemv(const uint8_t* w2, const float* s2w, int H, int I, int64_t max_tiles,
+                             const WsPtrs& ws, cudaStream_t st);
+cudaError_t launch_combine(const float* topk_w, int M, int H, int K, uint16_t* out, const WsPtrs& ws,
+                           cudaStream_t st);
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The compiled contract set.
+bool shape_supported(const moe_fp8_shape_t* s) {
+  if (!s) return false;
+  const int H = s->hidden, I = s->inter, E = s->num_experts, K = s->top_k;
+  if (H < 128 || H > 8192 || H % 128) return false;
+  if (I < 128 || I > 4096 || I % 128) return false;
+  if (!(E == 8 || E == 16 || E == 32 || E == 64 || E == 128 || E == 256)) return false;
+  if (K < 1 || K > 16 || K > E) return false;
+  if (s->max_tokens < 1 || s->max_tokens > (1 << 20) / K) return false;
+  return true;
+}
+
+moe_status_t check_common(const moe_fp8_shape_t* s, int32_t M) {
+  if (!s) return MOE_ERR_INVALID_ARG;
+  if (!shape_supported(s)) return MOE_ERR_UNSUPPORTED;
+  if (M < 0 || M > s->max_tokens) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status_t check_ws(void* ws, size_t bytes, const moe_fp8_shape_t* s, Layout* L) {
+  if (!ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  *L = make_layout(*s);
+  if (bytes < L->total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+moe_status_t launched(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH; }
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_fp8_version(void) { return "moe_fp8 0.1.0 (sm_103a)"; }
+
+size_t moe_fp8_workspace_bytes(const moe_fp8_shape_t* shape) {
+  if (!shape_supported(shape)) return 0;
+  return make_layout(*shape).total;
+}
+
+moe_status_t moe_fp8_workspace_init(void* workspace, size_t workspace_bytes,
+                                    const moe_fp8_shape_t* shape, cudaStream_t stream) {
+  if (!shape) return MOE_ERR_INVALID_ARG;
+  if (!shape_supported(shape)) return MOE_ERR_UNSUPPORTED;
+  Layout L;
+  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  return launched(cudaMemsetAsync(static_cast<char*>(workspace) + L.header, 0, sizeof(Header), stream));
+}
+
+moe_status_t moe_route(const void* hidden, const void* router_w, const float* bias, int32_t M,
+                       const moe_fp8_shape_t* shape, int32_t renormalize, int32_t* topk_ids,
+                       float* topk_w, cudaStream_t stream) {
+  if (moe_status_t st = check_common(shape, M)) return st;
+  if (!hidden || !router_w || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(hidden) || !aligned16(router_w) || !aligned16(topk_ids) || !aligned16(topk_w) ||
+      (bias && !aligned16(bias)))
+    return MOE_ERR_INVALID_ARG;
+  if (M == 0) return MOE_OK;
+  return launched(launch_route(static_cast<const uint16_t*>(hidden),
+                               static_cast<const uint16_t*>(router_w), bias, M, shape->hidden,
+                               shape->num_experts, shape->top_k, renormalize ? 1 : 0, topk_ids,
+                               topk_w, stream));
+}
+
+moe_status_t moe_fp8_prepare(const void* hidden, const int32_t* topk_ids, int32_t M,
+                             void* workspace, size_t workspace_bytes,
+                             const moe_fp8_shape_t* shape, cudaStream_t stream) {
+  if (moe_status_t st = check_common(shape, M)) return st;
+  if (!hidden || !topk_ids || !aligned16(hidden) || !aligned16(topk_ids)) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  if (M == 0) return MOE_OK;
+  const WsPtrs ws = ws_ptrs(workspace, L);
+  return launched(launch_prep(static_cast<const uint16_t*>(hidden), topk_ids, M, shape->hidden,
+                              shape->num_experts, shape->top_k, ws, stream));
+}
+
+moe_status_t moe_fp8_gate_up(const uint8_t* w13, const float* w13_scale, int32_t M,
+                             void* workspace, size_t workspace_bytes,
+                             const moe_fp8_shape_t* shape, cudaStream_t stream) {
+  if (moe_status_t st = check_common(shape, M)) return st;
+  if (!w13 || !w13_scale || !aligned16(w13) || !aligned16(w13_scale)) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  if (M == 0) return MOE_OK;
+  const WsPtrs ws = ws_ptrs(workspace, L);
+  const int64_t R = (int64_t)M * shape->top_k;
+  return launched(launch_gateup_gemv(w13, w13_scale, shape->hidden, shape->inter, shape->top_k,
+                                     max_tiles_for(R, shape->num_experts, kTileRows), ws, stream));
+}
+
+moe_status_t moe_fp8_down(const uint8_t* w2, const float* w2_scale, int32_t M, void* workspace,
+                          size_t workspace_bytes, const moe_fp8_shape_t* shape,
+                          cudaStream_t stream) {
+  if (moe_status_t st = check_common(shape, M)) return st;
+  if (!w2 || !w2_scale || !aligned16(w2) || !aligned16(w2_scale)) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  if (M == 0) return MOE_OK;
+  const WsPtrs ws = ws_ptrs(workspace, L);
+  const int64_t R = (int64_t)M * shape->top_k;
+  return launched(launch_down_gemv(w2, w2_scale, shape->hidden, shape->inter,
+                                   max_tiles_for(R, shape->num_experts, kTileRows), ws, stream));
+}
+
+moe_status_t moe_fp8_combine(const float* topk_w, int32_t M, void* out, void* workspace,
+                             size_t workspace_bytes, const moe_fp8_shape_t* shape,
+                             cudaStream_t stream) {
+  if (moe_status_t st = check_common(shape, M)) return st;
+  if (!topk_w || !out || !aligned16(topk_w) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  if (M == 0) return MOE_OK;
+  const WsPtrs ws = ws_ptrs(workspace, L);
+  return launched(launch_combine(topk_w, M, shape->hidden, shape->top_k, static_cast<uint16_t*>(out),
+                                 ws, stream));
+}
+
+moe_status_t moe_fp8_forward(const void* hidden, const int32_t* topk_ids, const float* topk_w,
+                             int32_t M, const uint8_t* w13, const float* w13_scale,
+                             const uint8_t* w2, const float* w2_scale, void* out,
+                             void* workspace, size_t workspace_bytes,
+                             const moe_fp8_shape_t* shape, cudaStream_t stream) {
+  if (moe_status_t st = check_common(shape, M)) return st;
+  if (!hidden || !topk_ids || !topk_w || !w13 || !w13_scale || !w2 || !w2_scale || !out)
+    return MOE_ERR_INVALID_ARG;
+  for (const void* p : {hidden, (const void*)topk_ids, (const void*)topk_w, (const void*)w13,
+                        (const void*)w13_scale, (const void*)w2, (const void*)w2_scale, (const void*)out})
+    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  if (M == 0) return MOE_OK;
+  if (moe_status_t st = moe_fp8_prepare(hidden, topk_ids, M, workspace, workspace_bytes, shape, stream))
+    return st;
+  if (moe_status_t st = moe_fp8_gate_up(w13, w13_scale, M, workspace, workspace_bytes, shape, stream))
+    return st;
+  if (moe_status_t st = moe_fp8_down(w2, w2_scale, M, workspace, workspace_bytes, shape, stream))
+    return st;
+  return moe_fp8_combine(topk_w, M, out, workspace, workspace_bytes, shape, stream);
+}
+
+moe_status_t moe_fp8_workspace_view(void* workspace, size_t workspace_bytes,
+                                    const moe_fp8_shape_t* shape, moe_fp8_ws_view_t* view) {
+  if (!shape || !view) return MOE_ERR_INVALID_ARG;
+  if (!shape_supported(shape)) return MOE_ERR_UNSUPPORTED;
+  Layout L;
+  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  const WsPtrs ws = ws_ptrs(workspace, L);
+  view->qa = ws.qa;
+  view->sa = ws.sa;
+  view->row_src = ws.row_src;
+  view->perm_row = ws.perm_row;
+  view->act = ws.act;
+  view->act_scale = ws.act_scale;
+  view->y = ws.y;
+  view->expert_offsets = ws.offsets;
+  return MOE_OK;
+}
+
+moe_status_t moe_fp8_read_status(const void* workspace, uint32_t* host_dst, cudaStream_t stream) {
+  if (!workspace || !host_dst || !aligned16(workspace)) return MOE_ERR_INVALID_ARG;
+  return launched(cudaMemcpyAsync(host_dst, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,51 @@
+// combine.cu -- top-k weighted combine (the route reducer).
+//
+// Sources: "NetraRuntime/netra-kernel" README, prefill-pair build section (the route
+// reducer is its own operation with its own reduction order); "Inferact/amd-kernels"
+// README (expert partials are summed in a fixed order, never with atomic adds).
+//
+// out[t][h] = bf16_rn( sum over slots j ascending of w[t][j] * y[perm_row[t][j]][h] ),
+// FP32 multiply then add, from 0; skipped pairs (perm_row < 0) contribute nothing.
+// One thread owns 8 consecutive columns: two 128-bit loads of y per slot, one 128-bit
+// store of 8 BF16 values.
+#include "common.cuh"
+
+namespace moe {
+
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ topk_w, int M,
+                                                      int H, int K, uint16_t* __restrict__ out,
+                                                      WsPtrs ws) {
+  const int t = blockIdx.x;
+  const int h = (blockIdx.y * 256 + threadIdx.x) * 8;
+  if (t >= M || h >= H) return;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  for (int j = 0; j < K; ++j) {
+    const int p = ws.perm_row[t * K + j];
+    if (p < 0) continue;
+    const float w = topk_w[t * K + j];
+    const float4 y0 = *reinterpret_cast<const float4*>(ws.y + (size_t)p * H + h);
+    const float4 y1 = *reinterpret_cast<const float4*>(ws.y + (size_t)p * H + h + 4);
+    const float y[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(w, y[i]));
+  }
+  uint32_t packed[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat16 a = __float2bfloat16_rn(acc[2 * i]);
+    const __nv_bfloat16 b = __float2bfloat16_rn(acc[2 * i + 1]);
+    packed[i] = (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
+  }
+  *reinterpret_cast<uint4*>(out + (size_t)t * H + h) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+}
+
+cudaError_t launch_combine(const float* topk_w, int M, int H, int K, uint16_t* out, const WsPtrs& ws,
+                           cudaStream_t st) {
+  dim3 grid(M, (H + 2047) / 2048);
+  combine_kernel<<<grid, 256, 0, st>>>(topk_w, M, H, K, out, ws);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

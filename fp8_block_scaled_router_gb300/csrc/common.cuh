@@ -1,0 +1,132 @@
+// common.cuh -- device helpers and the workspace layout shared by the library's kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe_fp8.h"
+
+namespace moe {
+
+constexpr int kBlock = 128;  // block-scale grid: 128x128 for weights, 1x128 for activations
+
+// --------------------------------------------------------------------------------------
+// Workspace layout (caller-owned, sized for max_tokens). Every region starts on a 256-byte
+// boundary. R = max_tokens * K routed rows.
+// --------------------------------------------------------------------------------------
+struct Header {             // first 256 bytes
+  uint32_t status;          // MOE_STATUS_* bits, cleared by moe_fp8_workspace_init
+  uint32_t n_tiles;         // tiles written by the last prepare
+  uint32_t pad[62];
+};
+
+struct Tile {               // a run of up to `tile_rows` expert-sorted rows of one expert
+  int32_t expert;
+  int32_t row0;
+  int32_t nrows;
+  int32_t pad;
+};
+
+struct Layout {
+  size_t header, qa, sa, offsets, row_src, perm_row, tiles, act, act_scale, y, total;
+  int64_t R, max_tiles;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Rows per tile of the grouped GEMMs.
+constexpr int kTileRows = 16;
+
+inline int64_t max_tiles_for(int64_t R, int E, int tile_rows) {
+  // sum over experts of ceil(n_e / tile_rows) <= R / tile_rows + (non-empty experts)
+  return R / tile_rows + (R < E ? R : E) + 1;
+}
+
+inline Layout make_layout(const moe_fp8_shape_t& s) {
+  Layout L{};
+  const int64_t H = s.hidden, I = s.inter, E = s.num_experts, K = s.top_k, Mx = s.max_tokens;
+  L.R = Mx * K;
+  L.max_tiles = max_tiles_for(L.R, (int)E, kTileRows);
+  size_t o = 0;
+  L.header = o;    o = align256(o + sizeof(Header));
+  L.qa = o;        o = align256(o + (size_t)(Mx * H));
+  L.sa = o;        o = align256(o + (size_t)(Mx * (H / kBlock)) * 4);
+  L.offsets = o;   o = align256(o + (size_t)(E + 1) * 4);
+  L.row_src = o;   o = align256(o + (size_t)L.R * 4);
+  L.perm_row = o;  o = align256(o + (size_t)L.R * 4);
+  L.tiles = o;     o = align256(o + (size_t)L.max_tiles * sizeof(Tile));
+  L.act = o;       o = align256(o + (size_t)(L.R * I));
+  L.act_scale = o; o = align256(o + (size_t)(L.R * (I / kBlock)) * 4);
+  L.y = o;         o = align256(o + (size_t)(L.R * H) * 4);
+  L.total = o;
+  return L;
+}
+
+// Device pointers into one workspace.
+struct WsPtrs {
+  Header* hdr;
+  uint8_t* qa;
+  float* sa;
+  int32_t* offsets;
+  int32_t* row_src;
+  int32_t* perm_row;
+  Tile* tiles;
+  uint8_t* act;
+  float* act_scale;
+  float* y;
+};
+
+inline WsPtrs ws_ptrs(void* ws, const Layout& L) {
+  char* b = static_cast<char*>(ws);
+  return WsPtrs{reinterpret_cast<Header*>(b + L.header), reinterpret_cast<uint8_t*>(b + L.qa),
+                reinterpret_cast<float*>(b + L.sa), reinterpret_cast<int32_t*>(b + L.offsets),
+                reinterpret_cast<int32_t*>(b + L.row_src), reinterpret_cast<int32_t*>(b + L.perm_row),
+                reinterpret_cast<Tile*>(b + L.tiles), reinterpret_cast<uint8_t*>(b + L.act),
+                reinterpret_cast<float*>(b + L.act_scale), reinterpret_cast<float*>(b + L.y)};
+}
+
+// --------------------------------------------------------------------------------------
+// Numeric helpers (device).
+// --------------------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Per-128 quantiser scale: amax / 448 with IEEE division; 1.0 for an all-zero group.
+__device__ __forceinline__ float quant_scale(float amax) {
+  return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
+}
+
+// Round-to-nearest-even, saturating E4M3 encode of two values (low byte = a).
+__device__ __forceinline__ uint16_t e4m3x2_encode(float a, float b) {
+  return static_cast<uint16_t>(
+      __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
+
+// Decode two E4M3 codes (low byte first) to float2 (exact: E4M3 is a subset of FP16).
+__device__ __forceinline__ float2 e4m3x2_decode(uint16_t two) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
+  return __half22float2(*reinterpret_cast<__half2*>(&h));
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+}
+
+__device__ __forceinline__ void set_status(Header* hdr, uint32_t bits) {
+  atomicOr(&hdr->status, bits);  // a flag word, never a value accumulation
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Upper bound on any device wait (a wait that runs out sets MOE_STATUS_WAIT_TIMEOUT).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+}  // namespace moe

@@ -1,0 +1,167 @@
+/* moe_fp8.h -- C ABI of the GB300 (sm_103a) routed FP8 block-scaled MoE FFN library.
+ *
+ * One layer of a routed mixture-of-experts FFN whose expert weights are FP8 E4M3 with one
+ * FP32 scale per 128x128 block:
+ *   route      softmax + top-k over BF16 router logits           (moe_route)
+ *   prepare    hidden -> FP8 per token per 128 columns; counting-sort permutation of the
+ *              (token, slot) pairs into expert-contiguous tiles     (moe_fp8_prepare)
+ *   gate/up    block-scaled grouped GEMM + fused SiLU(gate)*up with requantisation to FP8
+ *              at one scale per routed row per 128 columns          (moe_fp8_gate_up)
+ *   down       block-scaled grouped GEMM                            (moe_fp8_down)
+ *   combine    top-k weighted sum in slot order, no atomics         (moe_fp8_combine)
+ * moe_fp8_forward runs prepare -> gate/up -> down -> combine.
+ *
+ * Sources (web pages; each entry point names the passage that defines it):
+ *   [NK]   "NetraRuntime/netra-kernel" README
+ *   [NKL]  "NetraRuntime/netra-kernel" older kernel-lab README
+ *   [ARCH] netra-kernel docs/compiler/architecture.md
+ *   [AMDK] "Inferact/amd-kernels" README
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, 16-byte aligned, with
+ *     the row-major layouts stated below. The library never allocates, frees, copies to
+ *     the host or synchronises ([NKL] "Design": the dispatch path avoids allocation,
+ *     synchronisation, filesystem access, environment parsing and symbol lookup).
+ *   - Work is enqueued on `stream` (0 = legacy default stream) and returns at once.
+ *     Nothing in the library keeps per-call state between calls: two calls on different
+ *     streams with different workspaces may run concurrently ([ARCH], caller-local
+ *     kernel arguments). Calls sharing one workspace must be ordered on one stream.
+ *   - Host-side validation runs before any launch and returns MOE_ERR_INVALID_ARG (null or
+ *     misaligned pointer, M out of range), MOE_ERR_UNSUPPORTED (shape outside the compiled
+ *     set: [NK] exact contracts, no approximate dispatch; there is no fallback path) or
+ *     MOE_ERR_WORKSPACE (workspace too small). A launch error is MOE_ERR_LAUNCH.
+ *   - Errors the device finds (an expert id outside [0, E), a bounded wait that ran out)
+ *     never trap: they set bits of a status word in the workspace, read back with
+ *     moe_fp8_read_status.
+ *   - Numerics (the contract; [NK] lists accumulation, rounding and reduction order as
+ *     part of an operation's identity): see each call.
+ */
+#ifndef MOE_FP8_H_
+#define MOE_FP8_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,
+  MOE_ERR_UNSUPPORTED = 2,
+  MOE_ERR_WORKSPACE = 3,
+  MOE_ERR_LAUNCH = 4
+} moe_status_t;
+
+/* Device status bits (moe_fp8_read_status). */
+#define MOE_STATUS_BAD_EXPERT_ID 0x1u /* an id < 0 or >= E was skipped (contributes 0) */
+#define MOE_STATUS_WAIT_TIMEOUT 0x2u  /* a bounded device wait gave up; outputs invalid */
+
+/* Layer shape. hidden (H) and inter (I) are multiples of 128 (the block-scale grid),
+ * H <= 8192, I <= 4096; num_experts (E) in {8,16,32,64,128,256}; 1 <= top_k (K) <= min(E,16).
+ * max_tokens bounds M for every call that uses one workspace. */
+typedef struct {
+  int32_t hidden;
+  int32_t inter;
+  int32_t num_experts;
+  int32_t top_k;
+  int32_t max_tokens;
+} moe_fp8_shape_t;
+
+/* Library version string (static storage). */
+const char* moe_fp8_version(void);
+
+/* Bytes of caller-owned device workspace that moe_fp8_forward and the stage calls need
+ * for this shape (pure host arithmetic; 0 if the shape is unsupported). [ARCH]: the
+ * standalone graph owns its deterministic static intermediates. */
+size_t moe_fp8_workspace_bytes(const moe_fp8_shape_t* shape);
+
+/* Clear the workspace's status word. Call once after allocating a workspace (enqueued on
+ * `stream`); every other region is fully rewritten by each forward call. */
+moe_status_t moe_fp8_workspace_init(void* workspace, size_t workspace_bytes,
+                                    const moe_fp8_shape_t* shape, cudaStream_t stream);
+
+/* Router: [NK] capability table (BF16 routing) and prefill-pair section ("semantic
+ * routing" stage of the routed MoE producer).
+ *   hidden    BF16 [M][H] row-major
+ *   router_w  BF16 [H][E] (E contiguous)
+ *   bias      FP32 [E] added to every logit, or NULL
+ *   topk_ids  int32 [M][K] out; slot j holds the expert with the j-th largest logit
+ *             (ties to the lower expert index)
+ *   topk_w    FP32 [M][K] out; renormalize != 0: softmax over the K selected logits,
+ *             else the softmax over all E logits read at the selected experts
+ * logit[t][e] = sum over 128-wide chunks c ascending of an FP32 fma chain over the
+ * chunk's k ascending (from 0), then + bias[e]. Top-k ids are a pure function of these
+ * logits. M = 0 is a no-op. Needs no workspace. */
+moe_status_t moe_route(const void* hidden, const void* router_w, const float* bias, int32_t M,
+                       const moe_fp8_shape_t* shape, int32_t renormalize, int32_t* topk_ids,
+                       float* topk_w, cudaStream_t stream);
+
+/* The routed expert FFN ([ARCH] accepted M=1 MoE objects: gate/up, SiLU+quant and
+ * down/reduce; [NK] prefill-pair section: producer stages plus a separate route reducer
+ * with its own fixed reduction order; [AMDK] reduction rule: fixed order, no atomics).
+ *   hidden     BF16 [M][H]
+ *   topk_ids   int32 [M][K]     (ids outside [0,E) are skipped and flagged)
+ *   topk_w     FP32 [M][K]
+ *   w13        E4M3 [E][2I][H]  rows 0..I-1 gate, I..2I-1 up; K (=H) contiguous
+ *   w13_scale  FP32 [E][2I/128][H/128]
+ *   w2         E4M3 [E][H][I]   K (=I) contiguous
+ *   w2_scale   FP32 [E][H/128][I/128]
+ *   out        BF16 [M][H]; rows >= M are never written
+ * Numerics: hidden and the activation are quantised per row per 128 columns with
+ * scale = amax/448 (1.0 for an all-zero group) and round-to-nearest-even saturating E4M3
+ * codes; each GEMM output is sum over 128-blocks kb ascending of P_kb * (sa_kb * sw_kb)
+ * in FP32 (P_kb = the block's FP8 dot product on the tensor core or in FP32);
+ * act = silu(g) * u in FP32; out = bf16(sum over slots j ascending of w_j * y_j).
+ * 0 <= M <= max_tokens; M = 0 is a no-op. */
+moe_status_t moe_fp8_forward(const void* hidden, const int32_t* topk_ids, const float* topk_w,
+                             int32_t M, const uint8_t* w13, const float* w13_scale,
+                             const uint8_t* w2, const float* w2_scale, void* out,
+                             void* workspace, size_t workspace_bytes,
+                             const moe_fp8_shape_t* shape, cudaStream_t stream);
+
+/* The four stages of moe_fp8_forward as separate calls, for callers that interleave them
+ * with other work or time them one by one. They communicate through the workspace and
+ * must be enqueued in this order on one stream with the same M and shape. */
+moe_status_t moe_fp8_prepare(const void* hidden, const int32_t* topk_ids, int32_t M,
+                             void* workspace, size_t workspace_bytes,
+                             const moe_fp8_shape_t* shape, cudaStream_t stream);
+moe_status_t moe_fp8_gate_up(const uint8_t* w13, const float* w13_scale, int32_t M,
+                             void* workspace, size_t workspace_bytes,
+                             const moe_fp8_shape_t* shape, cudaStream_t stream);
+moe_status_t moe_fp8_down(const uint8_t* w2, const float* w2_scale, int32_t M, void* workspace,
+                          size_t workspace_bytes, const moe_fp8_shape_t* shape,
+                          cudaStream_t stream);
+moe_status_t moe_fp8_combine(const float* topk_w, int32_t M, void* out, void* workspace,
+                             size_t workspace_bytes, const moe_fp8_shape_t* shape,
+                             cudaStream_t stream);
+
+/* Debug view of the workspace (device pointers into it, valid after moe_fp8_prepare /
+ * moe_fp8_gate_up / moe_fp8_down of the same M): hidden codes qa u8 [M][H], hidden scales
+ * sa f32 [M][H/128], expert-sorted routed rows: row_src i32 [R] (flat pair index t*K+j of
+ * sorted row r), perm_row i32 [M*K] (sorted row of pair t*K+j, -1 if skipped), act codes
+ * u8 [R][I], act scales f32 [R][I/128], y f32 [R][H]; R = M*K. Any out pointer may be
+ * NULL. */
+typedef struct {
+  uint8_t* qa;
+  float* sa;
+  int32_t* row_src;
+  int32_t* perm_row;
+  uint8_t* act;
+  float* act_scale;
+  float* y;
+  int32_t* expert_offsets; /* i32 [E+1] start of each expert's rows */
+} moe_fp8_ws_view_t;
+moe_status_t moe_fp8_workspace_view(void* workspace, size_t workspace_bytes,
+                                    const moe_fp8_shape_t* shape, moe_fp8_ws_view_t* view);
+
+/* Copy the workspace's status word to host memory `host_dst` (asynchronous on `stream`;
+ * the caller synchronises before reading it). */
+moe_status_t moe_fp8_read_status(const void* workspace, uint32_t* host_dst, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_FP8_H_ */

@@ -1,0 +1,138 @@
+"""Host-side checks of the C ABI (no GPU needed, nothing is launched).
+
+The library must load and export every function include/moe_fp8.h declares, and every
+validation error path must return its status before any CUDA call (the netra-kernel
+README's exact contract guards: an unsupported contract is refused, never approximated).
+Each call below fails validation, so no kernel is ever launched with these fake pointers.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from fp8_block_scaled_router_gb300 import _lib as L
+from fp8_block_scaled_router_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_fp8.h")
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced (validation fails first)
+MIS = 0x10008   # misaligned
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return L.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(L.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], capture_output=True, text=True,
+                         check=True).stdout
+    syms = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for f in declared_functions():
+        assert f in syms, f
+        assert hasattr(lib, f)
+
+
+def test_version(lib):
+    assert "sm_103a" in L.moe_fp8_version()
+
+
+def shape(**kw):
+    d = dict(hidden=2048, inter=768, num_experts=128, top_k=8, max_tokens=16)
+    d.update(kw)
+    return L.make_shape(**d)
+
+
+@pytest.mark.parametrize("kw", [dict(hidden=200), dict(hidden=0), dict(hidden=16384), dict(inter=100),
+                                dict(inter=8192), dict(num_experts=100), dict(num_experts=512),
+                                dict(top_k=0), dict(top_k=17), dict(num_experts=8, top_k=9),
+                                dict(max_tokens=0)])
+def test_unsupported_shapes(lib, kw):
+    s = shape(**kw)
+    assert L.moe_fp8_workspace_bytes(s) == 0
+    code = L.moe_route(FAKE, FAKE, None, 1, s, 1, FAKE, FAKE, stream=0, check=False)
+    assert code == 2  # MOE_ERR_UNSUPPORTED
+    code = L.moe_fp8_forward(FAKE, FAKE, FAKE, 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, s, stream=0,
+                             ws_bytes=1 << 40, check=False)
+    assert code == 2
+
+
+def test_workspace_size_monotone_and_aligned(lib):
+    a = L.moe_fp8_workspace_bytes(shape(max_tokens=1))
+    b = L.moe_fp8_workspace_bytes(shape(max_tokens=64))
+    c = L.moe_fp8_workspace_bytes(shape(max_tokens=4096))
+    assert 0 < a < b < c and a % 256 == 0 and c % 256 == 0
+    # the y buffer alone (R x H FP32) is part of it
+    assert c >= 4096 * 8 * 2048 * 4
+
+
+def test_forward_argument_errors(lib):
+    s = shape()
+    need = L.moe_fp8_workspace_bytes(s)
+    args = [FAKE] * 8
+    # M out of range
+    for M in (-1, 17):
+        assert L.moe_fp8_forward(*args[:3], M, *args[3:8], FAKE, s, stream=0, ws_bytes=need,
+                                 check=False) == 1
+    # each null / misaligned pointer
+    for i in range(8):
+        for bad in (0, MIS):
+            a = list(args)
+            a[i] = bad
+            assert L.moe_fp8_forward(*a[:3], 4, *a[3:8], FAKE, s, stream=0, ws_bytes=need,
+                                     check=False) == 1, (i, bad)
+    # workspace null, misaligned, too small
+    assert L.moe_fp8_forward(*args[:3], 4, *args[3:8], 0, s, stream=0, ws_bytes=need, check=False) == 1
+    assert L.moe_fp8_forward(*args[:3], 4, *args[3:8], MIS, s, stream=0, ws_bytes=need, check=False) == 1
+    assert L.moe_fp8_forward(*args[:3], 4, *args[3:8], FAKE, s, stream=0, ws_bytes=need - 1,
+                             check=False) == 3
+
+
+def test_stage_and_route_argument_errors(lib):
+    s = shape()
+    need = L.moe_fp8_workspace_bytes(s)
+    assert L.moe_fp8_prepare(0, FAKE, 1, FAKE, s, stream=0, ws_bytes=need, check=False) == 1
+    assert L.moe_fp8_prepare(FAKE, FAKE, 1, FAKE, s, stream=0, ws_bytes=16, check=False) == 3
+    assert L.moe_fp8_gate_up(FAKE, MIS, 1, FAKE, s, stream=0, ws_bytes=need, check=False) == 1
+    assert L.moe_fp8_down(FAKE, FAKE, 99, FAKE, s, stream=0, ws_bytes=need, check=False) == 1
+    assert L.moe_fp8_combine(FAKE, 1, 0, FAKE, s, stream=0, ws_bytes=need, check=False) == 1
+    assert L.moe_route(FAKE, FAKE, MIS, 1, s, 1, FAKE, FAKE, stream=0, check=False) == 1
+    assert L.moe_route(FAKE, 0, None, 1, s, 1, FAKE, FAKE, stream=0, check=False) == 1
+    assert L.moe_route(FAKE, FAKE, None, -3, s, 1, FAKE, FAKE, stream=0, check=False) == 1
+    assert L.moe_fp8_workspace_init(FAKE, s, stream=0, ws_bytes=need - 256, check=False) == 3
+    assert L.moe_fp8_read_status(0, FAKE, stream=0, check=False) == 1
+    v = L.WsView()
+    assert lib.moe_fp8_workspace_view(FAKE, 0, ctypes.byref(s), ctypes.byref(v)) == 3
+
+
+def test_zero_tokens_is_a_no_op(lib):
+    """M = 0 returns MOE_OK after validation without touching the GPU (fake pointers)."""
+    s = shape()
+    need = L.moe_fp8_workspace_bytes(s)
+    assert L.moe_route(FAKE, FAKE, None, 0, s, 1, FAKE, FAKE, stream=0, check=False) == 0
+    assert L.moe_fp8_forward(FAKE, FAKE, FAKE, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, s, stream=0,
+                             ws_bytes=need, check=False) == 0
+
+
+def test_workspace_view_offsets(lib):
+    s = shape(max_tokens=4)
+    need = L.moe_fp8_workspace_bytes(s)
+    v = L.moe_fp8_workspace_view(FAKE, s, ws_bytes=need)
+    offs = [v.qa, v.sa, v.expert_offsets, v.row_src, v.perm_row, v.act, v.act_scale, v.y]
+    assert all(o % 256 == 0 for o in offs)
+    assert offs == sorted(offs) and offs[0] > FAKE and v.y < FAKE + need
+    assert v.y + 4 * 8 * 2048 * 4 <= FAKE + need

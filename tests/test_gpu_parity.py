@@ -1,0 +1,222 @@
+"""GPU parity: the CUDA library (called through its C ABI) against the CPU oracle on the same
+seeded inputs, at every workload shape; tolerances are stated in tests/gpu_harness.py.
+
+Workloads follow the netra-kernel pages' regimes for the Qwen3.6 FP8 MoE (decode M=1,
+speculative verify M=12, prefill) and the amd-kernels wide-expert shape token
+(h6144_i768_e128_top4, token count a runtime argument, CUDA-graph padding rows).
+"""
+import numpy as np
+import pytest
+import torch
+
+from fp8_block_scaled_router_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from gpu_harness import (GpuMoE, check_act, check_out, check_permutation, oracle_forward,
+                             oracle_route, to_dev, u16)
+
+_CACHE = {}
+
+
+def workload(name, **kw):
+    key = (name, tuple(sorted(kw.items())))
+    if key not in _CACHE:
+        _CACHE[key] = inputs.make(name, **kw)
+    return _CACHE[key]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build_lib():
+    from fp8_block_scaled_router_gb300 import build
+    import oracle
+    build.build()
+    oracle.build()
+    yield
+    _CACHE.clear()
+
+
+def gpu_for(x, max_tokens):
+    return GpuMoE(x, max_tokens)
+
+
+# ------------------------------------------------------------------ routing
+ROUTE_CASES = [("tiny", 4), ("decode", 64), ("decode", 1), ("verify", 12), ("verify_skewed", 12),
+               ("wide", 64), ("prefill", 4096)]
+
+
+@pytest.mark.parametrize("name,M", ROUTE_CASES, ids=[f"{n}-M{m}" for n, m in ROUTE_CASES])
+def test_route_parity(name, M):
+    x = workload(name) if name != "decode" else workload(name, tokens=64)
+    g = gpu_for(x, M)
+    hid = to_dev(x.hidden[:M])
+    ids, w = g.route(hid, M)
+    torch.cuda.synchronize()
+    ids_o, w_o = oracle_route(x, rows=slice(0, M))
+    assert np.array_equal(ids.cpu().numpy(), ids_o)
+    wg = w.cpu().numpy()
+    assert np.all(np.abs(wg - w_o) <= 2e-6 * w_o)
+
+
+def test_route_not_renormalised():
+    x = workload("decode", tokens=64)
+    g = gpu_for(x, 64)
+    ids, w = g.route(to_dev(x.hidden[:64]), 64, renorm=False)
+    torch.cuda.synchronize()
+    ids_o, w_o = oracle_route(x, rows=slice(0, 64), renorm=False)
+    assert np.array_equal(ids.cpu().numpy(), ids_o)
+    assert np.all(np.abs(w.cpu().numpy() - w_o) <= 2e-6 * w_o)
+
+
+def test_route_rows_beyond_m_untouched():
+    x = workload("verify")
+    g = gpu_for(x, 12)
+    ids = torch.full((16, 8), -777, dtype=torch.int32, device="cuda")
+    w = torch.full((16, 8), -7.0, dtype=torch.float32, device="cuda")
+    from fp8_block_scaled_router_gb300 import _lib as L
+    L.moe_route(to_dev(x.hidden[:12]), g.router, g.bias, 12, g.shape, True, ids, w)
+    torch.cuda.synchronize()
+    assert torch.all(ids[12:] == -777) and torch.all(w[12:] == -7.0)
+
+
+# ------------------------------------------------------------------ forward
+def run_forward_case(x, M, max_tokens=None, zero_rows=None):
+    g = gpu_for(x, max_tokens or M)
+    hidden = x.hidden[:M].copy()
+    if zero_rows is not None:
+        hidden[zero_rows] = 0
+    if x.ids is not None:
+        ids_o, w_o = x.ids[:M], x.weights[:M]
+    else:
+        import oracle
+        ids_o, w_o = oracle.route(hidden, x.router_w, x.bias, x.shape.top_k)
+    out = g.forward(to_dev(hidden), to_dev(ids_o), to_dev(w_o), M)
+    torch.cuda.synchronize()
+    ws = g.ws_arrays(M)
+    out_o, dbg = oracle_forward(x, hidden, ids_o, w_o, debug=True)
+    return g, ids_o, ws, u16(out), out_o, dbg
+
+
+def check_all(x, M, ids_o, ws, out, out_o, dbg, what):
+    assert np.array_equal(ws["qa"], dbg["qa"]), f"{what}: hidden codes"
+    assert np.array_equal(ws["sa"], dbg["sa"]), f"{what}: hidden scales"
+    check_permutation(ws, ids_o, x.shape.num_experts)
+    check_act(ws, dbg, x.shape.top_k, what)
+    check_out(out, out_o, what)
+
+
+FWD_CASES = [("tiny", 4), ("verify", 12), ("verify_skewed", 12)]
+
+
+@pytest.mark.parametrize("name,M", FWD_CASES, ids=[f"{n}-M{m}" for n, m in FWD_CASES])
+def test_forward_parity(name, M):
+    x = workload(name)
+    _, ids_o, ws, out, out_o, dbg = run_forward_case(x, M)
+    check_all(x, M, ids_o, ws, out, out_o, dbg, name)
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 32, 64])
+def test_wide_sweep_with_padding_rows(M):
+    x = workload("wide")
+    pad = inputs.wide_padding_rows(M)
+    _, ids_o, ws, out, out_o, dbg = run_forward_case(x, M, max_tokens=64, zero_rows=pad)
+    check_all(x, M, ids_o, ws, out, out_o, dbg, f"wide M={M}")
+    if len(pad):
+        assert np.all(out[pad] == 0)
+
+
+def test_decode_tokens_one_per_launch():
+    """Decode: one token per launch over 48 seeded tokens, each compared with the oracle."""
+    x = workload("decode", tokens=48)
+    g = gpu_for(x, 1)
+    import oracle
+    ids_o, w_o = oracle.route(x.hidden, x.router_w, None, 8)
+    outs = []
+    for t in range(48):
+        outs.append(u16(g.forward(to_dev(x.hidden[t:t + 1]), to_dev(ids_o[t:t + 1]),
+                                  to_dev(w_o[t:t + 1]), 1)))
+    out_o = oracle_forward(x, x.hidden, ids_o, w_o)
+    for t in range(48):
+        check_out(outs[t], out_o[t:t + 1], f"decode token {t}")
+
+
+def test_many_tiles_with_ragged_tails():
+    """300 tokens over 16 experts (top-8): ~150 rows per expert, several 16-row tiles and a
+    ragged last tile per expert; full oracle comparison."""
+    x = workload("decode", E=16, tokens=300)
+    _, ids_o, ws, out, out_o, dbg = run_forward_case(x, 300)
+    counts = np.bincount(ids_o.ravel(), minlength=16)
+    assert np.any(counts % 16 != 0) and counts.min() > 16
+    check_all(x, 300, ids_o, ws, out, out_o, dbg, "ragged")
+
+
+@pytest.mark.parametrize("name", ["prefill", "prefill_zipf"])
+def test_prefill_full_size_sampled(name):
+    """Full M=4096 launch; the oracle evaluates 40 sampled tokens one by one (each token's
+    output depends only on its own row, ids and weights)."""
+    x = workload(name)
+    M = 4096
+    g = gpu_for(x, M)
+    if x.ids is not None:
+        ids_o, w_o = x.ids, x.weights
+    else:
+        import oracle
+        ids_o, w_o = oracle.route(x.hidden, x.router_w, None, 8)
+    out = u16(g.forward(to_dev(x.hidden), to_dev(ids_o), to_dev(w_o), M))
+    ws = g.ws_arrays(M)
+    check_permutation(ws, ids_o, x.shape.num_experts)
+    rng = np.random.default_rng(99)
+    rows = np.sort(rng.choice(M, 40, replace=False))
+    out_o, dbg = oracle_forward(x, x.hidden[rows], ids_o[rows], w_o[rows], debug=True)
+    assert np.array_equal(ws["qa"][rows], dbg["qa"]) and np.array_equal(ws["sa"][rows], dbg["sa"])
+    check_out(out[rows], out_o, name)
+    # activation codes of the sampled tokens' routed rows
+    K = 8
+    sub = dict(row_src=np.array([t * K + j for t in range(len(rows)) for j in range(K)]))
+    pr = ws["perm_row"]
+    src_rows = np.array([pr[r * K + j] for r in rows for j in range(K)])
+    sub["act"] = ws["act"][src_rows]
+    sub["act_scale"] = ws["act_scale"][src_rows]
+    check_act(sub, dbg, K, name)
+
+
+def test_output_rows_beyond_m_untouched():
+    x = workload("verify")
+    g = gpu_for(x, 16)
+    import oracle
+    ids_o, w_o = oracle.route(x.hidden[:12], x.router_w, None, 8)
+    out = torch.full((16, 2048), 0x7ABC, dtype=torch.int16, device="cuda")
+    g.forward(to_dev(x.hidden[:12]), to_dev(ids_o), to_dev(w_o), 12, out=out)
+    torch.cuda.synchronize()
+    assert torch.all(out[12:] == 0x7ABC)
+
+
+def test_invalid_ids_flagged_and_skipped():
+    x = workload("tiny")
+    g = gpu_for(x, 4)
+    import oracle
+    ids_o, w_o = oracle.route(x.hidden, x.router_w, None, 2)
+    bad = ids_o.copy()
+    bad[0, 1] = -1
+    bad[2, 0] = 99
+    assert g.status() == 0
+    out = u16(g.forward(to_dev(x.hidden), to_dev(bad), to_dev(w_o), 4))
+    assert g.status() & 0x1
+    out_o = oracle_forward(x, x.hidden, bad, w_o)
+    check_out(out, out_o, "invalid ids")
+    g2 = gpu_for(x, 4)
+    g2.forward(to_dev(x.hidden), to_dev(ids_o), to_dev(w_o), 4)
+    assert g2.status() == 0
+
+
+def test_end_to_end_gpu_route_feeds_forward():
+    x = workload("verify_skewed")
+    g = gpu_for(x, 12)
+    hid = to_dev(x.hidden[:12])
+    ids, w = g.route(hid, 12)
+    out = u16(g.forward(hid, ids, w, 12))
+    import oracle
+    ids_o, w_o = oracle.route(x.hidden[:12], x.router_w, x.bias, 8)
+    assert np.array_equal(ids.cpu().numpy(), ids_o)
+    check_out(out, oracle_forward(x, x.hidden[:12], ids_o, w_o), "e2e")
