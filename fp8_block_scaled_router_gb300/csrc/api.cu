@@ -19,6 +19,10 @@ cudaError_t launch_gateup_gemv(const uint8_t* w13, const float* s13, int H, int 
                                int64_t max_tiles, const WsPtrs& ws, cudaStream_t st);
 cudaError_t launch_down_gemv(const uint8_t* w2, const float* s2w, int H, int I, int64_t max_tiles,
                              const WsPtrs& ws, cudaStream_t st);
+cudaError_t launch_pair_gateup(const uint8_t* w13, const float* s13, const int32_t* ids, int M, int H,
+                               int I, int E, int K, const WsPtrs& ws, cudaStream_t st);
+cudaError_t launch_pair_down(const uint8_t* w2, const float* s2w, const int32_t* ids, int M, int H, int I,
+                             int E, int K, const WsPtrs& ws, cudaStream_t st);
 cudaError_t launch_combine(const float* topk_w, int M, int H, int K, uint16_t* out, const WsPtrs& ws,
                            cudaStream_t st);
 }  // namespace moe
@@ -115,6 +119,9 @@ moe_status_t moe_fp8_gate_up(const uint8_t* w13, const float* w13_scale, int32_t
   if (M == 0) return MOE_OK;
   const WsPtrs ws = ws_ptrs(workspace, L);
   const int64_t R = (int64_t)M * shape->top_k;
+  if (use_pair_mode(R))
+    return launched(launch_pair_gateup(w13, w13_scale, ws.pair_expert, M, shape->hidden, shape->inter,
+                                       shape->num_experts, shape->top_k, ws, stream));
   return launched(launch_gateup_gemv(w13, w13_scale, shape->hidden, shape->inter, shape->top_k,
                                      max_tiles_for(R, shape->num_experts, kTileRows), ws, stream));
 }
@@ -129,6 +136,9 @@ moe_status_t moe_fp8_down(const uint8_t* w2, const float* w2_scale, int32_t M, v
   if (M == 0) return MOE_OK;
   const WsPtrs ws = ws_ptrs(workspace, L);
   const int64_t R = (int64_t)M * shape->top_k;
+  if (use_pair_mode(R))
+    return launched(launch_pair_down(w2, w2_scale, ws.pair_expert, M, shape->hidden, shape->inter,
+                                     shape->num_experts, shape->top_k, ws, stream));
   return launched(launch_down_gemv(w2, w2_scale, shape->hidden, shape->inter,
                                    max_tiles_for(R, shape->num_experts, kTileRows), ws, stream));
 }

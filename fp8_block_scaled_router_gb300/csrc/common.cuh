@@ -31,7 +31,7 @@ struct Tile {               // a run of up to `tile_rows` expert-sorted rows of 
 };
 
 struct Layout {
-  size_t header, qa, sa, offsets, row_src, perm_row, tiles, act, act_scale, y, total;
+  size_t header, qa, sa, offsets, row_src, perm_row, pair_expert, tiles, act, act_scale, y, total;
   int64_t R, max_tiles;
 };
 
@@ -39,6 +39,12 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Rows per tile of the grouped GEMMs.
 constexpr int kTileRows = 16;
+
+// Up to this many routed rows (M*K) every (token, slot) pair is its own GEMM unit ("pair
+// mode": no sort, weights of an expert chosen by several pairs are re-read from L2);
+// above it the rows are sorted into expert tiles.
+constexpr int kPairMaxRows = 256;
+inline bool use_pair_mode(int64_t R) { return R <= kPairMaxRows; }
 
 inline int64_t max_tiles_for(int64_t R, int E, int tile_rows) {
   // sum over experts of ceil(n_e / tile_rows) <= R / tile_rows + (non-empty experts)
@@ -57,6 +63,7 @@ inline Layout make_layout(const moe_fp8_shape_t& s) {
   L.offsets = o;   o = align256(o + (size_t)(E + 1) * 4);
   L.row_src = o;   o = align256(o + (size_t)L.R * 4);
   L.perm_row = o;  o = align256(o + (size_t)L.R * 4);
+  L.pair_expert = o; o = align256(o + (size_t)L.R * 4);
   L.tiles = o;     o = align256(o + (size_t)L.max_tiles * sizeof(Tile));
   L.act = o;       o = align256(o + (size_t)(L.R * I));
   L.act_scale = o; o = align256(o + (size_t)(L.R * (I / kBlock)) * 4);
@@ -73,6 +80,7 @@ struct WsPtrs {
   int32_t* offsets;
   int32_t* row_src;
   int32_t* perm_row;
+  int32_t* pair_expert;  // [R] expert of each routed pair, -1 if skipped (pair mode)
   Tile* tiles;
   uint8_t* act;
   float* act_scale;
@@ -84,7 +92,7 @@ inline WsPtrs ws_ptrs(void* ws, const Layout& L) {
   return WsPtrs{reinterpret_cast<Header*>(b + L.header), reinterpret_cast<uint8_t*>(b + L.qa),
                 reinterpret_cast<float*>(b + L.sa), reinterpret_cast<int32_t*>(b + L.offsets),
                 reinterpret_cast<int32_t*>(b + L.row_src), reinterpret_cast<int32_t*>(b + L.perm_row),
-                reinterpret_cast<Tile*>(b + L.tiles), reinterpret_cast<uint8_t*>(b + L.act),
+                reinterpret_cast<int32_t*>(b + L.pair_expert), reinterpret_cast<Tile*>(b + L.tiles), reinterpret_cast<uint8_t*>(b + L.act),
                 reinterpret_cast<float*>(b + L.act_scale), reinterpret_cast<float*>(b + L.y)};
 }
 

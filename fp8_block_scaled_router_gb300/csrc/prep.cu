@@ -22,7 +22,8 @@ constexpr int kMaxExperts = 256;
 
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const uint16_t* __restrict__ hidden,
                                                             const int32_t* __restrict__ ids, int M,
-                                                            int H, int E, int K, WsPtrs ws) {
+                                                            int H, int E, int K, int pair_mode,
+                                                            WsPtrs ws) {
   const int tid = threadIdx.x;
   if (blockIdx.x > 0) {
     // ---- quantise hidden: warp per (token, 128-group) ----
@@ -45,6 +46,27 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const uint16_t* __re
       const uint32_t hi = e4m3x2_encode(__fdiv_rn(x2, s), __fdiv_rn(x3, s));
       *reinterpret_cast<uint32_t*>(ws.qa + t * H + g * 128 + lane * 4) = lo | (hi << 16);
       if (lane == 0) ws.sa[t * ngroups_row + g] = s;
+    }
+    return;
+  }
+
+  if (pair_mode) {
+    // ---- block 0, pair mode: each routed pair is its own unit (identity permutation) ----
+    __shared__ int bad_pair;
+    if (tid == 0) bad_pair = 0;
+    __syncthreads();
+    for (int i = tid; i < M * K; i += kPrepThreads) {
+      const int e = ids[i];
+      const bool valid = e >= 0 && e < E;
+      ws.pair_expert[i] = valid ? e : -1;
+      ws.perm_row[i] = valid ? i : -1;
+      ws.row_src[i] = i;
+      if (!valid) bad_pair = 1;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      ws.hdr->n_tiles = 0;
+      if (bad_pair) set_status(ws.hdr, MOE_STATUS_BAD_EXPERT_ID);
     }
     return;
   }
@@ -88,7 +110,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const uint16_t* __re
       ws.tiles[tb] = Tile{e, base[e] + j, min(kTileRows, n - j), 0};
   }
   for (int r0 = 0; r0 < R; r0 += kPrepThreads) {
-    for (int i = tid; i < (kPrepThreads / 32) * E; i += kPrepThreads) (&wcnt[0][0])[i] = 0;
+    for (int i = tid; i < (kPrepThreads / 32) * E; i += kPrepThreads) wcnt[i / E][i % E] = 0;
     __syncthreads();
     const int i = r0 + tid;
     const int e = i < R ? ids[i] : -1;
@@ -119,10 +141,11 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const uint16_t* __re
 
 cudaError_t launch_prep(const uint16_t* hidden, const int32_t* ids, int M, int H, int E, int K,
                         const WsPtrs& ws, cudaStream_t st) {
+  const int pair_mode = use_pair_mode((int64_t)M * K) ? 1 : 0;
   const int64_t groups = (int64_t)M * (H / 128);
   int64_t qblocks = (groups + (kPrepThreads / 32) - 1) / (kPrepThreads / 32);
   if (qblocks > 4 * 152) qblocks = 4 * 152;
-  prep_kernel<<<(unsigned)(1 + qblocks), kPrepThreads, 0, st>>>(hidden, ids, M, H, E, K, ws);
+  prep_kernel<<<(unsigned)(1 + qblocks), kPrepThreads, 0, st>>>(hidden, ids, M, H, E, K, pair_mode, ws);
   return cudaGetLastError();
 }
 

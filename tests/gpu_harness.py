@@ -170,11 +170,22 @@ def check_act(ws, dbg, K, what=""):
     return int(mism.sum()), int(mism.size)
 
 
+# Up to this many routed rows the library runs every (token, slot) pair as its own unit
+# (identity permutation); above it the pairs are sorted into expert-contiguous tiles.
+PAIR_MAX_ROWS = 256
+
+
 def check_permutation(ws, ids, E):
-    """Stable expert-sorted order: row_src is a permutation of the valid pairs, increasing
-    inside each expert segment, offsets match the histogram, perm_row inverts row_src."""
+    """Pair mode: perm_row is the identity on valid pairs and -1 on skipped ones.
+    Sorted mode: stable expert-sorted order -- row_src is a permutation of the valid pairs,
+    increasing inside each expert segment, offsets match the histogram, perm_row inverts
+    row_src."""
     flat = ids.ravel()
     valid = (flat >= 0) & (flat < E)
+    if flat.size <= PAIR_MAX_ROWS:
+        pr = ws["perm_row"][: flat.size]
+        assert np.array_equal(pr, np.where(valid, np.arange(flat.size), -1))
+        return
     counts = np.bincount(flat[valid], minlength=E)
     offs = ws["offsets"]
     assert offs[0] == 0 and np.array_equal(np.diff(offs), counts)
