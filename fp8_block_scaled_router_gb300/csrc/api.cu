@@ -19,10 +19,12 @@ cudaError_t launch_gateup_gemv(const uint8_t* w13, const float* s13, int H, int 
                                int64_t max_tiles, const WsPtrs& ws, cudaStream_t st);
 cudaError_t launch_down_gemv(const uint8_t* w2, const float* s2w, int H, int I, int64_t max_tiles,
                              const WsPtrs& ws, cudaStream_t st);
-cudaError_t launch_pair_gateup(const uint8_t* w13, const float* s13, const int32_t* ids, int M, int H,
-                               int I, int E, int K, const WsPtrs& ws, cudaStream_t st);
-cudaError_t launch_pair_down(const uint8_t* w2, const float* s2w, const int32_t* ids, int M, int H, int I,
-                             int E, int K, const WsPtrs& ws, cudaStream_t st);
+cudaError_t launch_pair_gateup(const uint8_t* w13, const float* s13, const int32_t* ids,
+                               const uint16_t* hidden, int M, int H, int I, int E, int K,
+                               const WsPtrs& ws, cudaStream_t st);
+cudaError_t launch_pair_down(const uint8_t* w2, const float* s2w, const int32_t* ids, const float* topk_w,
+                             uint16_t* out, int M, int H, int I, int E, int K, const WsPtrs& ws,
+                             cudaStream_t st);
 cudaError_t launch_combine(const float* topk_w, int M, int H, int K, uint16_t* out, const WsPtrs& ws,
                            cudaStream_t st);
 }  // namespace moe
@@ -120,8 +122,8 @@ moe_status_t moe_fp8_gate_up(const uint8_t* w13, const float* w13_scale, int32_t
   const WsPtrs ws = ws_ptrs(workspace, L);
   const int64_t R = (int64_t)M * shape->top_k;
   if (use_pair_mode(R))
-    return launched(launch_pair_gateup(w13, w13_scale, ws.pair_expert, M, shape->hidden, shape->inter,
-                                       shape->num_experts, shape->top_k, ws, stream));
+    return launched(launch_pair_gateup(w13, w13_scale, ws.pair_expert, nullptr, M, shape->hidden,
+                                       shape->inter, shape->num_experts, shape->top_k, ws, stream));
   return launched(launch_gateup_gemv(w13, w13_scale, shape->hidden, shape->inter, shape->top_k,
                                      max_tiles_for(R, shape->num_experts, kTileRows), ws, stream));
 }
@@ -137,8 +139,8 @@ moe_status_t moe_fp8_down(const uint8_t* w2, const float* w2_scale, int32_t M, v
   const WsPtrs ws = ws_ptrs(workspace, L);
   const int64_t R = (int64_t)M * shape->top_k;
   if (use_pair_mode(R))
-    return launched(launch_pair_down(w2, w2_scale, ws.pair_expert, M, shape->hidden, shape->inter,
-                                     shape->num_experts, shape->top_k, ws, stream));
+    return launched(launch_pair_down(w2, w2_scale, ws.pair_expert, nullptr, nullptr, M, shape->hidden,
+                                     shape->inter, shape->num_experts, shape->top_k, ws, stream));
   return launched(launch_down_gemv(w2, w2_scale, shape->hidden, shape->inter,
                                    max_tiles_for(R, shape->num_experts, kTileRows), ws, stream));
 }
@@ -170,6 +172,17 @@ moe_status_t moe_fp8_forward(const void* hidden, const int32_t* topk_ids, const 
   Layout L;
   if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
   if (M == 0) return MOE_OK;
+  if (use_pair_mode((int64_t)M * shape->top_k)) {
+    // few routed rows: two launches -- gate/up quantises its own hidden row, down is fused
+    // with the combine (same arithmetic as the four stage calls)
+    const WsPtrs ws = ws_ptrs(workspace, L);
+    const int H = shape->hidden, I = shape->inter, E = shape->num_experts, K = shape->top_k;
+    if (cudaError_t e = launch_pair_gateup(w13, w13_scale, topk_ids, static_cast<const uint16_t*>(hidden),
+                                           M, H, I, E, K, ws, stream))
+      return launched(e);
+    return launched(launch_pair_down(w2, w2_scale, topk_ids, topk_w, static_cast<uint16_t*>(out), M, H, I,
+                                     E, K, ws, stream));
+  }
   if (moe_status_t st = moe_fp8_prepare(hidden, topk_ids, M, workspace, workspace_bytes, shape, stream))
     return st;
   if (moe_status_t st = moe_fp8_gate_up(w13, w13_scale, M, workspace, workspace_bytes, shape, stream))

@@ -21,15 +21,31 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-  for (int j = 0; j < K; ++j) {
-    const int p = ws.perm_row[t * K + j];
-    if (p < 0) continue;
-    const float w = topk_w[t * K + j];
-    const float4 y0 = *reinterpret_cast<const float4*>(ws.y + (size_t)p * H + h);
-    const float4 y1 = *reinterpret_cast<const float4*>(ws.y + (size_t)p * H + h + 4);
-    const float y[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+  // four slots at a time: their indices and weights first, then all their row loads, so
+  // the dependent loads of different slots overlap; the adds stay in slot order
+  for (int j0 = 0; j0 < K; j0 += 4) {
+    int pj[4];
+    float wj[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(w, y[i]));
+    for (int u = 0; u < 4; ++u) {
+      pj[u] = j0 + u < K ? ws.perm_row[t * K + j0 + u] : -1;
+      wj[u] = j0 + u < K ? topk_w[t * K + j0 + u] : 0.0f;
+    }
+    float4 ya[4], yb[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (pj[u] >= 0) {
+        ya[u] = *reinterpret_cast<const float4*>(ws.y + (size_t)pj[u] * H + h);
+        yb[u] = *reinterpret_cast<const float4*>(ws.y + (size_t)pj[u] * H + h + 4);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (pj[u] < 0) continue;
+      const float y[8] = {ya[u].x, ya[u].y, ya[u].z, ya[u].w, yb[u].x, yb[u].y, yb[u].z, yb[u].w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(wj[u], y[i]));
+    }
   }
   uint32_t packed[4];
 #pragma unroll

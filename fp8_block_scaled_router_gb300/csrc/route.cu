@@ -3,13 +3,15 @@
 // Source: "NetraRuntime/netra-kernel" README, capability table (BF16 routing) and the
 // prefill-pair build section (the routed MoE producer starts with a routing stage).
 //
-// GB300 design. A thread-block cluster of CL CTAs covers one block of TB tokens; CTA r of
-// the cluster owns 128-wide hidden chunks [r*nC, (r+1)*nC) and computes, for every token of
-// the block and every expert, one FP32 fma chain per chunk (k ascending, from 0). The chunk
-// partials stay in each CTA's shared memory; after a cluster barrier CTA 0 reads them over
-// distributed shared memory and sums them in ascending chunk order, so the logits -- and
-// hence the top-k ids -- do not depend on the launch shape. No workspace, no atomics and
-// no spin-waits: the only synchronisation is the hardware cluster barrier.
+// GB300 design. A thread-block cluster of CL CTAs covers one block of TB tokens; CTA r
+// owns experts [r*EC, (r+1)*EC). Its threads compute, for every token of the block, one
+// FP32 fma chain per (expert, 128-wide hidden chunk) over the chunk's k ascending from 0,
+// then sum the chunk partials in ascending chunk order -- so each logit is formed inside
+// one CTA in the contract order and the top-k ids do not depend on the launch shape. The
+// CTA stores its logits straight into CTA 0's shared memory (distributed shared memory
+// stores: no round trips), one cluster barrier later CTA 0 holds all E logits of every
+// token and a warp per token selects the top K (ties to the lower expert index) and forms
+// the softmax weights. No workspace, no atomics, no spin-waits.
 #include <cooperative_groups.h>
 
 #include <climits>
@@ -21,111 +23,114 @@ namespace cg = cooperative_groups;
 
 namespace moe {
 
+constexpr int kRouteThreads = 256;
+constexpr int kRouteChunksPerRound = 16;  // hidden chunks staged in shared memory at once
+
 struct RouteSmem {
-  int TB, nC, E;
-  size_t xs, ws, part, logits, total;
+  size_t ws, xs, part, logits, total;
 };
 
-__host__ __device__ inline RouteSmem route_smem(int TB, int nC, int E) {
-  RouteSmem s{TB, nC, E, 0, 0, 0, 0, 0};
+// ws: router slab [16 chunks * 128 rows][EC] bf16; xs: hidden [TB][16*128] bf16;
+// part: chunk partials [nchunks][TB][EC] f32; logits: [TB][E] f32 (filled on CTA 0).
+__host__ __device__ inline RouteSmem route_smem(int TB, int EC, int E, int nchunks) {
+  RouteSmem s{};
   size_t o = 0;
-  s.xs = o;     o += (size_t)TB * 128 * 4;
-  s.ws = o;     o += (size_t)128 * E * 2;
-  s.part = o;   o += (size_t)nC * TB * E * 4;
+  s.ws = o;     o += (size_t)kRouteChunksPerRound * 128 * EC * 2;
+  s.xs = o;     o += (size_t)TB * kRouteChunksPerRound * 128 * 2;
+  s.part = o;   o += (size_t)nchunks * TB * EC * 4;
   s.logits = o; o += (size_t)TB * E * 4;
   s.total = o;
   return s;
 }
 
-// TPT tokens per thread; each thread owns 4 consecutive experts.
-template <int TPT>
-__global__ void __launch_bounds__(256) route_kernel(const uint16_t* __restrict__ hidden,
-                                                    const uint16_t* __restrict__ router_w,
-                                                    const float* __restrict__ bias, int M, int H,
-                                                    int E, int K, int renorm, int nC,
-                                                    int32_t* __restrict__ ids,
-                                                    float* __restrict__ wts) {
+template <int TB>
+__global__ void __launch_bounds__(kRouteThreads)
+    route_kernel(const uint16_t* __restrict__ hidden, const uint16_t* __restrict__ router_w,
+                 const float* __restrict__ bias, int M, int H, int E, int K, int renorm,
+                 int32_t* __restrict__ ids, float* __restrict__ wts) {
   extern __shared__ __align__(16) unsigned char smem[];
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int CL = (int)cluster.num_blocks();
-  const int EG = E / 4, TG = 256 / EG, TB = TG * TPT;
-  const RouteSmem L = route_smem(TB, nC, E);
-  float* xs = reinterpret_cast<float*>(smem + L.xs);
+  const int EC = E / CL;
+  const int nchunks = H / 128;
+  const RouteSmem L = route_smem(TB, EC, E, nchunks);
   uint16_t* wsm = reinterpret_cast<uint16_t*>(smem + L.ws);
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem + L.xs);
   float* part = reinterpret_cast<float*>(smem + L.part);
   float* logits = reinterpret_cast<float*>(smem + L.logits);
-
   const int tid = threadIdx.x;
-  const int eg = tid % EG, tg = tid / EG;
   const int tok0 = blockIdx.y * TB;
+  const int e0 = rank * EC;
 
-  for (int cl = 0; cl < nC; ++cl) {
-    const int c = rank * nC + cl;
-    // stage the chunk: hidden [TB][128] as float, router rows [128][E]
-    for (int i = tid; i < TB * 32; i += 256) {
-      const int t = i / 32, k4 = (i % 32) * 4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (tok0 + t < M) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(hidden + (size_t)(tok0 + t) * H + c * 128 + k4);
-        v = make_float4(bf16_bits_to_float(raw.x & 0xFFFF), bf16_bits_to_float(raw.x >> 16),
-                        bf16_bits_to_float(raw.y & 0xFFFF), bf16_bits_to_float(raw.y >> 16));
+  // inputs may be written by the previous kernel in the stream (programmatic launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+
+  // thread <-> (expert el, chunk lane cgl); chunks cgl, cgl + TPE, ... of each round.
+  // Consecutive lanes take consecutive experts (one 2-byte router value each).
+  const int TPE = kRouteThreads / EC;
+  const int el = tid % EC, cgl = tid / EC;
+  for (int c0 = 0; c0 < nchunks; c0 += kRouteChunksPerRound) {
+    const int nc = min(kRouteChunksPerRound, nchunks - c0);
+    // stage router rows [c0*128, (c0+nc)*128) x experts [e0, e0+EC) and the hidden chunk
+    const int segs = EC * 2 / 16;  // 16-byte pieces per router row slice
+    const int n16 = nc * 128 * segs;
+    for (int i0 = tid; i0 < n16; i0 += kRouteThreads * 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * kRouteThreads;
+        if (i < n16)
+          v[u] = *reinterpret_cast<const uint4*>(router_w + (size_t)(c0 * 128 + i / segs) * E + e0 +
+                                                 (i % segs) * 8);
       }
-      *reinterpret_cast<float4*>(xs + t * 128 + k4) = v;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (i0 + u * kRouteThreads < n16) reinterpret_cast<uint4*>(wsm)[i0 + u * kRouteThreads] = v[u];
     }
-    const uint4* wsrc = reinterpret_cast<const uint4*>(router_w + (size_t)c * 128 * E);
-    for (int i = tid; i < 128 * E / 8; i += 256) reinterpret_cast<uint4*>(wsm)[i] = wsrc[i];
+    for (int i = tid; i < TB * nc * 16; i += kRouteThreads) {
+      const int t = i / (nc * 16), k8 = (i % (nc * 16)) * 8;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (tok0 + t < M) v = *reinterpret_cast<const uint4*>(hidden + (size_t)(tok0 + t) * H + c0 * 128 + k8);
+      *reinterpret_cast<uint4*>(xs + t * kRouteChunksPerRound * 128 + k8) = v;
+    }
     __syncthreads();
-
-    if (tg < TG) {
-      float acc[TPT][4];
+    {
+      for (int cc = cgl; cc < nc; cc += TPE) {
+        float acc[TB];
 #pragma unroll
-      for (int t = 0; t < TPT; ++t)
+        for (int t = 0; t < TB; ++t) acc[t] = 0.0f;
+#pragma unroll 8
+        for (int k = 0; k < 128; ++k) {
+          const float w = bf16_bits_to_float(wsm[(cc * 128 + k) * EC + el]);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc[t][i] = 0.0f;
-#pragma unroll 4
-      for (int k = 0; k < 128; ++k) {
-        const uint2 w4 = *reinterpret_cast<const uint2*>(wsm + k * E + 4 * eg);
-        const float w0 = bf16_bits_to_float(w4.x & 0xFFFF), w1 = bf16_bits_to_float(w4.x >> 16);
-        const float w2 = bf16_bits_to_float(w4.y & 0xFFFF), w3 = bf16_bits_to_float(w4.y >> 16);
-#pragma unroll
-        for (int t = 0; t < TPT; ++t) {
-          const float x = xs[(tg * TPT + t) * 128 + k];
-          acc[t][0] = __fmaf_rn(x, w0, acc[t][0]);
-          acc[t][1] = __fmaf_rn(x, w1, acc[t][1]);
-          acc[t][2] = __fmaf_rn(x, w2, acc[t][2]);
-          acc[t][3] = __fmaf_rn(x, w3, acc[t][3]);
+          for (int t = 0; t < TB; ++t)
+            acc[t] = __fmaf_rn(bf16_bits_to_float(xs[t * kRouteChunksPerRound * 128 + cc * 128 + k]), w, acc[t]);
         }
-      }
 #pragma unroll
-      for (int t = 0; t < TPT; ++t)
-        *reinterpret_cast<float4*>(part + ((size_t)cl * TB + tg * TPT + t) * E + 4 * eg) =
-            make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
+        for (int t = 0; t < TB; ++t) part[((size_t)(c0 + cc) * TB + t) * EC + el] = acc[t];
+      }
     }
     __syncthreads();
   }
-
-  cluster.sync();  // every CTA's chunk partials are complete and visible cluster-wide
-  if (rank == 0) {
-    for (int i = tid; i < TB * E; i += 256) {
-      const int t = i / E, e = i % E;
-      float l = 0.0f;
-      for (int r = 0; r < CL; ++r) {
-        const float* pr = cluster.map_shared_rank(part, r);
-        for (int cl = 0; cl < nC; ++cl) l = __fadd_rn(l, pr[((size_t)cl * TB + t) * E + e]);
-      }
-      if (bias != nullptr) l = __fadd_rn(l, bias[e]);
-      logits[t * E + e] = l;
-    }
+  // logits of this CTA's experts, chunk partials summed in ascending chunk order, pushed
+  // into CTA 0's shared memory
+  float* logits0 = cluster.map_shared_rank(logits, 0);
+  for (int i = tid; i < TB * EC; i += kRouteThreads) {
+    const int t = i / EC, e = i % EC;
+    float l = 0.0f;
+    for (int c = 0; c < nchunks; ++c) l = __fadd_rn(l, part[((size_t)c * TB + t) * EC + e]);
+    if (bias != nullptr) l = __fadd_rn(l, bias[e0 + e]);
+    logits0[t * E + e0 + e] = l;
   }
-  cluster.sync();  // CTA 0 is done reading the other CTAs' shared memory
+  cluster.sync();  // all logits are in CTA 0's shared memory
   if (rank != 0) return;
-  __syncthreads();
 
   // top-k: one warp per token; lane holds experts lane, lane+32, ...
   const int warp = tid / 32, lane = tid % 32;
   constexpr int kMaxPerLane = 8;  // E <= 256
-  for (int t = warp; t < TB; t += 8) {
+  for (int t = warp; t < TB; t += kRouteThreads / 32) {
     if (tok0 + t >= M) break;
     float v[kMaxPerLane];
     bool taken[kMaxPerLane];
@@ -186,51 +191,44 @@ __global__ void __launch_bounds__(256) route_kernel(const uint16_t* __restrict__
   }
 }
 
-template <int TPT>
-static cudaError_t launch_route_t(const uint16_t* hidden, const uint16_t* router_w, const float* bias,
-                                  int M, int H, int E, int K, int renorm, int32_t* ids, float* wts,
-                                  cudaStream_t st) {
-  const int nchunks = H / 128;
-  int CL = 1;
-  for (int c = 8; c >= 1; --c)
-    if (nchunks % c == 0) { CL = c; break; }
-  const int nC = nchunks / CL;
-  const int TB = (256 / (E / 4)) * TPT;
-  const RouteSmem L = route_smem(TB, nC, E);
+namespace {
+
+// CL CTAs per cluster, E/CL >= 8 experts each (a 16-byte router row slice)
+int route_cluster(int E) { return E >= 64 ? 8 : E / 8; }
+
+template <int TB>
+cudaError_t launch_route_t(const uint16_t* hidden, const uint16_t* router_w, const float* bias, int M,
+                           int H, int E, int K, int renorm, int32_t* ids, float* wts, cudaStream_t st) {
+  const int CL = route_cluster(E);
+  const RouteSmem L = route_smem(TB, E / CL, E, H / 128);
   static std::once_flag once;
   std::call_once(once, [] {
-    cudaFuncSetAttribute(route_kernel<TPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaFuncSetAttribute(route_kernel<TB>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
   });
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(CL, (M + TB - 1) / TB, 1);
-  cfg.blockDim = dim3(256, 1, 1);
+  cfg.blockDim = dim3(kRouteThreads, 1, 1);
   cfg.dynamicSmemBytes = L.total;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, route_kernel<TPT>, hidden, router_w, bias, M, H, E, K, renorm, nC,
-                            ids, wts);
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, route_kernel<TB>, hidden, router_w, bias, M, H, E, K, renorm, ids, wts);
 }
 
-size_t route_smem_bytes(int M, int H, int E) {
-  const int TPT = (M >= 256 && E >= 64) ? 4 : 1;
-  const int nchunks = H / 128;
-  int CL = 1;
-  for (int c = 8; c >= 1; --c)
-    if (nchunks % c == 0) { CL = c; break; }
-  return route_smem((256 / (E / 4)) * TPT, nchunks / CL, E).total;
-}
+}  // namespace
 
 cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const float* bias, int M,
                          int H, int E, int K, int renorm, int32_t* ids, float* wts, cudaStream_t st) {
-  if (M >= 256 && E >= 64)
-    return launch_route_t<4>(hidden, router_w, bias, M, H, E, K, renorm, ids, wts, st);
-  return launch_route_t<1>(hidden, router_w, bias, M, H, E, K, renorm, ids, wts, st);
+  if (M <= 2) return launch_route_t<1>(hidden, router_w, bias, M, H, E, K, renorm, ids, wts, st);
+  if (M <= 32) return launch_route_t<2>(hidden, router_w, bias, M, H, E, K, renorm, ids, wts, st);
+  return launch_route_t<8>(hidden, router_w, bias, M, H, E, K, renorm, ids, wts, st);
 }
 
 }  // namespace moe

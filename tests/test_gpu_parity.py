@@ -91,7 +91,12 @@ def run_forward_case(x, M, max_tokens=None, zero_rows=None):
     else:
         import oracle
         ids_o, w_o = oracle.route(hidden, x.router_w, x.bias, x.shape.top_k)
-    out = g.forward(to_dev(hidden), to_dev(ids_o), to_dev(w_o), M)
+    hid_d, ids_d = to_dev(hidden), to_dev(ids_o)
+    out = g.forward(hid_d, ids_d, to_dev(w_o), M)
+    # the few-row forward quantises hidden inside gate/up and writes no permutation; the
+    # prepare stage fills those workspace views (it does not touch the activation codes)
+    from fp8_block_scaled_router_gb300 import _lib as L
+    L.moe_fp8_prepare(hid_d, ids_d, M, g.ws, g.shape)
     torch.cuda.synchronize()
     ws = g.ws_arrays(M)
     out_o, dbg = oracle_forward(x, hidden, ids_o, w_o, debug=True)
