@@ -24,7 +24,8 @@ STATUS_WAIT_TIMEOUT = 0x2
 
 EXPORTS = ("moe_fp8_version", "moe_fp8_workspace_bytes", "moe_fp8_workspace_init", "moe_route",
            "moe_fp8_forward", "moe_fp8_prepare", "moe_fp8_gate_up", "moe_fp8_down",
-           "moe_fp8_combine", "moe_fp8_workspace_view", "moe_fp8_read_status")
+           "moe_fp8_combine", "moe_fp8_workspace_view", "moe_fp8_read_status",
+           "moe_fp8_forward_noalloc")
 
 
 class MoEError(RuntimeError):
@@ -66,6 +67,7 @@ def load(path: str = LIB):
             lib.moe_fp8_combine.argtypes = [vp, i32, vp, vp, sz, sp, vp]
             lib.moe_fp8_workspace_view.argtypes = [vp, sz, sp, ctypes.POINTER(WsView)]
             lib.moe_fp8_read_status.argtypes = [vp, vp, vp]
+            lib.moe_fp8_forward_noalloc.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, sp, vp]
             for f in EXPORTS[2:]:
                 if f != "moe_fp8_workspace_bytes":
                     getattr(lib, f).restype = i32
@@ -174,3 +176,12 @@ def moe_fp8_read_status(workspace, host_dst, stream=None, check=True):
     """host_dst: a pinned torch uint32/int32 CPU tensor of >= 1 element (or a host pointer)."""
     return _check("moe_fp8_read_status", load().moe_fp8_read_status(
         _ptr(workspace), _ptr(host_dst), _stream(stream)), check)
+
+
+def moe_fp8_forward_noalloc(hidden, topk_ids, topk_w, M, w13, w13_scale, w2, w2_scale, out,
+                            shape: Shape, stream=None, check=True):
+    """moe_fp8_forward without a workspace (scratch compiled into the library; see
+    include/moe_fp8.h for its limits and sharing rules)."""
+    return _check("moe_fp8_forward_noalloc", load().moe_fp8_forward_noalloc(
+        _ptr(hidden), _ptr(topk_ids), _ptr(topk_w), int(M), _ptr(w13), _ptr(w13_scale), _ptr(w2),
+        _ptr(w2_scale), _ptr(out), ctypes.byref(shape), _stream(stream)), check)

@@ -157,6 +157,26 @@ typedef struct {
 moe_status_t moe_fp8_workspace_view(void* workspace, size_t workspace_bytes,
                                     const moe_fp8_shape_t* shape, moe_fp8_ws_view_t* view);
 
+/* moe_fp8_forward for callers that cannot allocate device memory where they run the layer
+ * (for example while a memory pool is locked or being resized, inside callbacks that must
+ * not enter the allocator, or in integrations without a device allocator): the same
+ * arguments as moe_fp8_forward minus the workspace. No counterpart in the paper: this is
+ * an addition of this library. The intermediate activation lives in a 1 MiB scratch array
+ * compiled into the library (a file-scope __device__ array that every GPU loading the
+ * library keeps until process exit), so this call allocates nothing.
+ * Limits: only the few-routed-row path (M * top_k <= 256) and M * top_k * (inter + inter/32)
+ * + 512 <= 1 MiB; anything larger returns MOE_ERR_UNSUPPORTED.
+ * Set-up: the first call on a device (made with that device current) looks up the array's
+ * device address; make that first call before any stream capture.
+ * Sharing: all calls on a device share the array, which keeps the last call's contents;
+ * calls whose GPU work overlaps (unordered streams) race on it. Each call clears the
+ * array's status word on `stream`; device status bits are not readable through this call.
+ * Numerics and outputs are identical to moe_fp8_forward. */
+moe_status_t moe_fp8_forward_noalloc(const void* hidden, const int32_t* topk_ids, const float* topk_w,
+                                     int32_t M, const uint8_t* w13, const float* w13_scale,
+                                     const uint8_t* w2, const float* w2_scale, void* out,
+                                     const moe_fp8_shape_t* shape, cudaStream_t stream);
+
 /* Copy the workspace's status word to host memory `host_dst` (asynchronous on `stream`;
  * the caller synchronises before reading it). */
 moe_status_t moe_fp8_read_status(const void* workspace, uint32_t* host_dst, cudaStream_t stream);
