@@ -25,7 +25,7 @@ STATUS_WAIT_TIMEOUT = 0x2
 EXPORTS = ("moe_fp8_version", "moe_fp8_workspace_bytes", "moe_fp8_workspace_init", "moe_route",
            "moe_fp8_forward", "moe_fp8_prepare", "moe_fp8_gate_up", "moe_fp8_down",
            "moe_fp8_combine", "moe_fp8_workspace_view", "moe_fp8_read_status",
-           "moe_fp8_forward_noalloc")
+           "moe_fp8_forward_noalloc", "moe_fp8_gate_up_direct", "moe_fp8_down_combine")
 
 
 class MoEError(RuntimeError):
@@ -68,6 +68,8 @@ def load(path: str = LIB):
             lib.moe_fp8_workspace_view.argtypes = [vp, sz, sp, ctypes.POINTER(WsView)]
             lib.moe_fp8_read_status.argtypes = [vp, vp, vp]
             lib.moe_fp8_forward_noalloc.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, sp, vp]
+            lib.moe_fp8_gate_up_direct.argtypes = [vp, vp, i32, vp, vp, vp, sz, sp, vp]
+            lib.moe_fp8_down_combine.argtypes = [vp, vp, i32, vp, vp, vp, vp, sz, sp, vp]
             for f in EXPORTS[2:]:
                 if f != "moe_fp8_workspace_bytes":
                     getattr(lib, f).restype = i32
@@ -162,6 +164,22 @@ def moe_fp8_combine(topk_w, M, out, workspace, shape: Shape, stream=None, ws_byt
     return _check("moe_fp8_combine", load().moe_fp8_combine(
         _ptr(topk_w), int(M), _ptr(out), _ptr(workspace), nb, ctypes.byref(shape), _stream(stream)),
         check)
+
+
+def moe_fp8_gate_up_direct(hidden, topk_ids, M, w13, w13_scale, workspace, shape: Shape, stream=None,
+                           ws_bytes=None, check=True):
+    nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return _check("moe_fp8_gate_up_direct", load().moe_fp8_gate_up_direct(
+        _ptr(hidden), _ptr(topk_ids), int(M), _ptr(w13), _ptr(w13_scale), _ptr(workspace), nb,
+        ctypes.byref(shape), _stream(stream)), check)
+
+
+def moe_fp8_down_combine(topk_ids, topk_w, M, w2, w2_scale, out, workspace, shape: Shape, stream=None,
+                         ws_bytes=None, check=True):
+    nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return _check("moe_fp8_down_combine", load().moe_fp8_down_combine(
+        _ptr(topk_ids), _ptr(topk_w), int(M), _ptr(w2), _ptr(w2_scale), _ptr(out), _ptr(workspace), nb,
+        ctypes.byref(shape), _stream(stream)), check)
 
 
 def moe_fp8_workspace_view(workspace, shape: Shape, ws_bytes=None) -> WsView:

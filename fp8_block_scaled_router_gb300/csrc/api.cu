@@ -175,13 +175,11 @@ moe_status_t moe_fp8_forward(const void* hidden, const int32_t* topk_ids, const 
   if (use_pair_mode((int64_t)M * shape->top_k)) {
     // few routed rows: two launches -- gate/up quantises its own hidden row, down is fused
     // with the combine (same arithmetic as the four stage calls)
-    const WsPtrs ws = ws_ptrs(workspace, L);
-    const int H = shape->hidden, I = shape->inter, E = shape->num_experts, K = shape->top_k;
-    if (cudaError_t e = launch_pair_gateup(w13, w13_scale, topk_ids, static_cast<const uint16_t*>(hidden),
-                                           M, H, I, E, K, ws, stream))
-      return launched(e);
-    return launched(launch_pair_down(w2, w2_scale, topk_ids, topk_w, static_cast<uint16_t*>(out), M, H, I,
-                                     E, K, ws, stream));
+    if (moe_status_t st = moe_fp8_gate_up_direct(hidden, topk_ids, M, w13, w13_scale, workspace,
+                                                 workspace_bytes, shape, stream))
+      return st;
+    return moe_fp8_down_combine(topk_ids, topk_w, M, w2, w2_scale, out, workspace, workspace_bytes, shape,
+                                stream);
   }
   if (moe_status_t st = moe_fp8_prepare(hidden, topk_ids, M, workspace, workspace_bytes, shape, stream))
     return st;
@@ -190,6 +188,41 @@ moe_status_t moe_fp8_forward(const void* hidden, const int32_t* topk_ids, const 
   if (moe_status_t st = moe_fp8_down(w2, w2_scale, M, workspace, workspace_bytes, shape, stream))
     return st;
   return moe_fp8_combine(topk_w, M, out, workspace, workspace_bytes, shape, stream);
+}
+
+moe_status_t moe_fp8_gate_up_direct(const void* hidden, const int32_t* topk_ids, int32_t M,
+                                    const uint8_t* w13, const float* w13_scale, void* workspace,
+                                    size_t workspace_bytes, const moe_fp8_shape_t* shape,
+                                    cudaStream_t stream) {
+  if (moe_status_t st = check_common(shape, M)) return st;
+  for (const void* p : {hidden, (const void*)topk_ids, (const void*)w13, (const void*)w13_scale})
+    if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  if (M == 0) return MOE_OK;
+  if (!use_pair_mode((int64_t)M * shape->top_k)) return MOE_ERR_UNSUPPORTED;
+  const WsPtrs ws = ws_ptrs(workspace, L);
+  return launched(launch_pair_gateup(w13, w13_scale, topk_ids, static_cast<const uint16_t*>(hidden), M,
+                                     shape->hidden, shape->inter, shape->num_experts, shape->top_k, ws,
+                                     stream));
+}
+
+moe_status_t moe_fp8_down_combine(const int32_t* topk_ids, const float* topk_w, int32_t M,
+                                  const uint8_t* w2, const float* w2_scale, void* out, void* workspace,
+                                  size_t workspace_bytes, const moe_fp8_shape_t* shape,
+                                  cudaStream_t stream) {
+  if (moe_status_t st = check_common(shape, M)) return st;
+  for (const void* p : {(const void*)topk_ids, (const void*)topk_w, (const void*)w2, (const void*)w2_scale,
+                        (const void*)out})
+    if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  if (M == 0) return MOE_OK;
+  if (!use_pair_mode((int64_t)M * shape->top_k)) return MOE_ERR_UNSUPPORTED;
+  const WsPtrs ws = ws_ptrs(workspace, L);
+  return launched(launch_pair_down(w2, w2_scale, topk_ids, topk_w, static_cast<uint16_t*>(out), M,
+                                   shape->hidden, shape->inter, shape->num_experts, shape->top_k, ws,
+                                   stream));
 }
 
 moe_status_t moe_fp8_workspace_view(void* workspace, size_t workspace_bytes,

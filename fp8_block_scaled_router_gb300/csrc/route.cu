@@ -193,8 +193,9 @@ __global__ void __launch_bounds__(kRouteThreads)
 
 namespace {
 
-// CL CTAs per cluster, E/CL >= 8 experts each (a 16-byte router row slice)
-int route_cluster(int E) { return E >= 64 ? 8 : E / 8; }
+// CL CTAs per cluster, E/CL >= 8 experts each (a 16-byte router row slice); 16-CTA
+// clusters (a non-portable size) for E >= 128 spread the router weights over more SMs
+int route_cluster(int E) { return E >= 128 ? 16 : E / 8; }
 
 template <int TB>
 cudaError_t launch_route_t(const uint16_t* hidden, const uint16_t* router_w, const float* bias, int M,
@@ -204,6 +205,7 @@ cudaError_t launch_route_t(const uint16_t* hidden, const uint16_t* router_w, con
   static std::once_flag once;
   std::call_once(once, [] {
     cudaFuncSetAttribute(route_kernel<TB>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaFuncSetAttribute(route_kernel<TB>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   });
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(CL, (M + TB - 1) / TB, 1);

@@ -47,6 +47,7 @@ namespace cg = cooperative_groups;
 namespace moe {
 
 constexpr int kPairN = 16;  // B rows per MMA (row 0 is the unit's pair)
+constexpr int kMaxSplitTerms = 8;  // K blocks per CTA when a unit's K blocks are split
 constexpr int kPairThreads = 192;
 
 enum PairMode { kGateUpWs = 0, kGateUpFused = 1, kDownY = 2, kDownCombine = 3 };
@@ -79,20 +80,23 @@ struct PairParams {
   Header* hdr;
 };
 
+// Split-K terms [kATiles][nkb][128] f32 and combine rows [K][128] f32 are gathered in CTA
+// 0's stage buffers once every CTA of the cluster has drained its pipeline, so they need
+// no shared memory of their own (the host keeps kATiles * nkb * 512 and K * 512 bytes within
+// the stage buffers).
 template <int MODE>
 struct PairSmem {
-  size_t stages, xterm, bq, sas, bars, total;
+  size_t stages, bq, sas, bars, total;
 };
 
 template <int MODE>
 __host__ __device__ inline PairSmem<MODE> pair_smem(int nkb, int nkb_cta, int K) {
   using C = PairCfg<MODE>;
   PairSmem<MODE> s{};
+  (void)nkb;
+  (void)K;
   size_t o = 0;
   s.stages = o; o += (size_t)C::kStages * C::kStageBytes;
-  s.xterm = o;  // split-K terms [kATiles][nkb][128] or combine rows [K][128] (on CTA 0)
-  if (MODE == kDownCombine) o += (size_t)K * 128 * 4;
-  else if (nkb_cta < nkb) o += (size_t)C::kATiles * nkb * 128 * 4;
   s.bq = o;  o += MODE == kGateUpFused ? (size_t)nkb_cta * 128 : 0;  // hidden codes
   s.sas = o; o += (size_t)nkb_cta * 4;                             // hidden scales
   o = (o + 15) & ~size_t(15);
@@ -102,7 +106,7 @@ __host__ __device__ inline PairSmem<MODE> pair_smem(int nkb, int nkb_cta, int K)
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kPairThreads)
+__global__ void __launch_bounds__(kPairThreads, 3)
     pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const PairParams p) {
   using C = PairCfg<MODE>;
@@ -112,7 +116,7 @@ __global__ void __launch_bounds__(kPairThreads)
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
   const PairSmem<MODE> SL = pair_smem<MODE>(p.nkb, p.nkb_cta, p.K);
   unsigned char* stages = base + SL.stages;
-  float* xterm = reinterpret_cast<float*>(base + SL.xterm);
+  float* xterm = reinterpret_cast<float*>(stages);  // reused after the pipeline drains
   uint8_t* bq = base + SL.bq;
   float* sas = reinterpret_cast<float*>(base + SL.sas);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + SL.bars);
@@ -128,6 +132,24 @@ __global__ void __launch_bounds__(kPairThreads)
   const int S = (int)cluster.num_blocks();
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
+  // set-up that touches no global memory overlaps the previous kernel's tail
+  if (warp == 0 && lane == 0) {
+    tc::prefetch_tmap(&tmA);
+    if (MODE != kGateUpFused) tc::prefetch_tmap(&tmB);
+    for (int s = 0; s < C::kStages; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&accf[b], 1);
+      tc::mbar_init(&acce[b], 4);
+    }
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, C::kTmemCols);
+    tc::tmem_relinquish();
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
 
@@ -142,67 +164,52 @@ __global__ void __launch_bounds__(kPairThreads)
     cb = unit % p.ncb;
     tok = pr / p.K;
   }
-  const int e = p.ids[pr];
-  const bool valid = e >= 0 && e < p.E;
-  if (MODE != kDownCombine && !valid) {  // skipped pair: the whole cluster leaves together
-    if (MODE == kGateUpFused && cb == 0 && rank == 0 && threadIdx.x == 0)
-      set_status(p.hdr, MOE_STATUS_BAD_EXPERT_ID);
-    return;
-  }
   const int split = MODE == kDownCombine ? 1 : S;  // CTAs sharing one unit's K blocks
   const int kb0 = MODE == kDownCombine ? 0 : rank * p.nkb_cta;
   const int brow = MODE == kGateUpWs ? tok : pr;  // B row (qa row or act row)
-
-  if (valid) {
-    if (warp == 0 && lane == 0) {
-      tc::prefetch_tmap(&tmA);
-      if (MODE != kGateUpFused) tc::prefetch_tmap(&tmB);
-      for (int s = 0; s < C::kStages; ++s) {
-        tc::mbar_init(&full[s], 1);
-        tc::mbar_init(&empty[s], 1);
-      }
-      for (int b = 0; b < 2; ++b) {
-        tc::mbar_init(&accf[b], 1);
-        tc::mbar_init(&acce[b], 4);
-      }
-      tc::fence_mbar_init();
+  if (MODE == kGateUpFused) {
+    // zero the B tiles (rows 1..15 stay zero) and quantise the pair's hidden row for this
+    // CTA's K blocks (warp w takes blocks w, w+6, ...); independent of the expert id, so
+    // these loads overlap the id load below
+    for (int i = threadIdx.x; i < C::kStages * (C::kBBytes / 16); i += kPairThreads) {
+      const int s = i / (C::kBBytes / 16), c = i % (C::kBBytes / 16);
+      reinterpret_cast<uint4*>(stages + s * C::kStageBytes + C::kTxA)[c] = make_uint4(0, 0, 0, 0);
     }
-    if (warp == 1) {
-      tc::tmem_alloc(tmem_slot, C::kTmemCols);
-      tc::tmem_relinquish();
-    }
-    if (MODE == kGateUpFused) {
-      // zero the B tiles (rows 1..15 stay zero) and quantise the pair's hidden row for
-      // this CTA's K blocks: warp w takes blocks w, w+6, ...
-      for (int i = threadIdx.x; i < C::kStages * (C::kBBytes / 16); i += kPairThreads) {
-        const int s = i / (C::kBBytes / 16), c = i % (C::kBBytes / 16);
-        reinterpret_cast<uint4*>(stages + s * C::kStageBytes + C::kTxA)[c] = make_uint4(0, 0, 0, 0);
-      }
-      for (int i = warp; i < p.nkb_cta; i += kPairThreads / 32) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(p.hidden + (size_t)tok * p.H + (kb0 + i) * 128 + lane * 4);
-        const float x0 = bf16_bits_to_float(raw.x & 0xFFFF), x1 = bf16_bits_to_float(raw.x >> 16);
-        const float x2 = bf16_bits_to_float(raw.y & 0xFFFF), x3 = bf16_bits_to_float(raw.y >> 16);
-        float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
+    for (int i = warp; i < p.nkb_cta; i += kPairThreads / 32) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(p.hidden + (size_t)tok * p.H + (kb0 + i) * 128 + lane * 4);
+      const float x0 = bf16_bits_to_float(raw.x & 0xFFFF), x1 = bf16_bits_to_float(raw.x >> 16);
+      const float x2 = bf16_bits_to_float(raw.y & 0xFFFF), x3 = bf16_bits_to_float(raw.y >> 16);
+      float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        const float s = quant_scale(amax);
-        const uint32_t lo = e4m3x2_encode(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
-        const uint32_t hi = e4m3x2_encode(__fdiv_rn(x2, s), __fdiv_rn(x3, s));
-        reinterpret_cast<uint32_t*>(bq + i * 128)[lane] = lo | (hi << 16);
-        if (lane == 0) sas[i] = s;
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    } else {
-      for (int i = threadIdx.x; i < p.nkb_cta; i += kPairThreads) sas[i] = p.a_scale[(size_t)brow * p.nkb + kb0 + i];
+      for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      const float sc = quant_scale(amax);
+      const uint32_t lo = e4m3x2_encode(__fdiv_rn(x0, sc), __fdiv_rn(x1, sc));
+      const uint32_t hi = e4m3x2_encode(__fdiv_rn(x2, sc), __fdiv_rn(x3, sc));
+      reinterpret_cast<uint32_t*>(bq + i * 128)[lane] = lo | (hi << 16);
+      if (lane == 0) sas[i] = sc;
     }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  } else {
+    for (int i = threadIdx.x; i < p.nkb_cta; i += kPairThreads) sas[i] = p.a_scale[(size_t)brow * p.nkb + kb0 + i];
   }
+  const int e = p.ids[pr];
+  const bool valid = e >= 0 && e < p.E;
+  if (MODE == kGateUpFused && !valid && cb == 0 && rank == 0 && threadIdx.x == 0)
+    set_status(p.hdr, MOE_STATUS_BAD_EXPERT_ID);
+  // a skipped pair (not kDownCombine): the whole cluster shares the unit and leaves together
+  const bool skip_unit = MODE != kDownCombine && !valid;
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  if (skip_unit) {
+    if (warp == 1) tc::tmem_dealloc(tmem, C::kTmemCols);
+    return;
+  }
 
   bool ok = true;
   float chain0 = 0.0f, chain1 = 0.0f;
+  float term0[kMaxSplitTerms], term1[kMaxSplitTerms];
   if (valid && warp == 0) {
     const int yA0 = kGateUp ? e * 2 * p.I + cb * 128 : e * p.H + cb * 128;
     const int yA1 = e * 2 * p.I + p.I + cb * 128;
@@ -257,7 +264,6 @@ __global__ void __launch_bounds__(kPairThreads)
     const int r = q * 32 + lane;
     const float* sw0 = p.w_scale + ((size_t)e * (kGateUp ? 2 * p.I / 128 : p.H / 128) + cb) * p.nkb;
     const float* sw1 = p.w_scale + ((size_t)e * (2 * p.I / 128) + p.I / 128 + cb) * p.nkb;
-    float* x0 = split > 1 ? cluster.map_shared_rank(xterm, 0) : xterm;
     for (int i = 0; i < p.nkb_cta; ++i) {
       const int buf = i & 1;
       if (!tc::mbar_wait(&accf[buf], (i >> 1) & 1)) { ok = false; break; }
@@ -277,16 +283,34 @@ __global__ void __launch_bounds__(kPairThreads)
       if (split == 1) {  // the whole chain is local: kb ascending
         chain0 = __fadd_rn(chain0, t0);
         if (kGateUp) chain1 = __fadd_rn(chain1, t1);
-      } else {           // terms go to CTA 0 at their global K-block index
-        x0[kb * 128 + r] = t0;
-        if (kGateUp) x0[(p.nkb + kb) * 128 + r] = t1;
+      } else {           // kept until CTA 0's stage buffers are free (<= kMaxSplitTerms)
+#pragma unroll
+        for (int j = 0; j < kMaxSplitTerms; ++j)
+          if (j == i) { term0[j] = t0; term1[j] = t1; }
       }
     }
-    if (MODE == kDownCombine) cluster.map_shared_rank(xterm, 0)[rank * 128 + r] = chain0;
   }
   if (!ok) set_status(p.hdr, MOE_STATUS_WAIT_TIMEOUT);
   __syncthreads();
-  if (split > 1 || MODE == kDownCombine) cluster.sync();  // CTA 0 holds every term / row
+  if (split > 1 || MODE == kDownCombine) {
+    cluster.sync();  // every CTA's pipeline has drained: CTA 0's stage buffers are free
+    if (valid && warp >= 2) {
+      const int r = (warp & 3) * 32 + lane;
+      float* x0 = cluster.map_shared_rank(xterm, 0);
+      if (MODE == kDownCombine) {
+        x0[rank * 128 + r] = chain0;
+      } else {
+#pragma unroll
+        for (int j = 0; j < kMaxSplitTerms; ++j) {
+          if (j < p.nkb_cta) {
+            x0[(kb0 + j) * 128 + r] = term0[j];
+            if (kGateUp) x0[(p.nkb + kb0 + j) * 128 + r] = term1[j];
+          }
+        }
+      }
+    }
+    cluster.sync();  // CTA 0 holds every term / row
+  }
 
   if (rank == 0 && warp >= 2) {
     const int q = warp & 3;
@@ -324,9 +348,8 @@ __global__ void __launch_bounds__(kPairThreads)
       p.out[(size_t)tok * p.H + cb * 128 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
     }
   }
-  if (split > 1 || MODE == kDownCombine) cluster.sync();  // keep CTA 0's buffers alive
   __syncthreads();
-  if (valid && warp == 1) {
+  if (warp == 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, C::kTmemCols);
   }
@@ -377,6 +400,9 @@ int pick_split(int nkb, int64_t units, int K) {
   int best = 1;
   for (int s = 1; s <= 8; ++s) {
     if (nkb % s) continue;
+    if (s > 1 && (nkb / s > kMaxSplitTerms ||
+                  (size_t)PairCfg<MODE>::kATiles * nkb * 512 > (size_t)PairCfg<MODE>::kStages * PairCfg<MODE>::kStageBytes))
+      continue;
     const size_t smem = pair_smem<MODE>(nkb, nkb / s, K).total + 1024;
     const int64_t wave = (int64_t)kNumSMs * (int64_t)(kSmemPerSM / smem);
     if (units * s <= wave) best = s;

@@ -9,7 +9,8 @@
  *              at one scale per routed row per 128 columns          (moe_fp8_gate_up)
  *   down       block-scaled grouped GEMM                            (moe_fp8_down)
  *   combine    top-k weighted sum in slot order, no atomics         (moe_fp8_combine)
- * moe_fp8_forward runs prepare -> gate/up -> down -> combine.
+ * moe_fp8_forward runs prepare -> gate/up -> down -> combine, or, for few routed rows,
+ * gate/up (quantising hidden itself) -> down fused with the combine.
  *
  * Sources (web pages; each entry point names the passage that defines it):
  *   [NK]   "NetraRuntime/netra-kernel" README
@@ -137,6 +138,21 @@ moe_status_t moe_fp8_down(const uint8_t* w2, const float* w2_scale, int32_t M, v
 moe_status_t moe_fp8_combine(const float* topk_w, int32_t M, void* out, void* workspace,
                              size_t workspace_bytes, const moe_fp8_shape_t* shape,
                              cudaStream_t stream);
+
+/* The few-routed-row path (M * top_k <= 256) as its two kernels, the layout of the
+ * accepted M=1 MoE objects of [ARCH] (gate/up + SiLU + quantisation, then down/reduce);
+ * moe_fp8_forward runs exactly these two calls for such M. MOE_ERR_UNSUPPORTED above the
+ * limit. moe_fp8_gate_up_direct quantises hidden itself and writes the activation codes
+ * and scales (pair order) to the workspace; moe_fp8_down_combine reads them and writes out
+ * with the combine of moe_fp8_combine (slot order, FP32 multiply then add, from 0). */
+moe_status_t moe_fp8_gate_up_direct(const void* hidden, const int32_t* topk_ids, int32_t M,
+                                    const uint8_t* w13, const float* w13_scale, void* workspace,
+                                    size_t workspace_bytes, const moe_fp8_shape_t* shape,
+                                    cudaStream_t stream);
+moe_status_t moe_fp8_down_combine(const int32_t* topk_ids, const float* topk_w, int32_t M,
+                                  const uint8_t* w2, const float* w2_scale, void* out, void* workspace,
+                                  size_t workspace_bytes, const moe_fp8_shape_t* shape,
+                                  cudaStream_t stream);
 
 /* Debug view of the workspace (device pointers into it, valid after moe_fp8_prepare /
  * moe_fp8_gate_up / moe_fp8_down of the same M): hidden codes qa u8 [M][H], hidden scales
