@@ -4,17 +4,17 @@
 // prefill-pair build section (the routed MoE producer starts with a routing stage).
 //
 // GB300 design. A thread-block cluster of CL CTAs covers one block of TB tokens; CTA r
-// owns experts [r*EC, (r+1)*EC). Its threads compute, for every token of the block, one
-// FP32 fma chain per (expert, 128-wide hidden chunk) over the chunk's k ascending from 0,
-// then sum the chunk partials in ascending chunk order -- so each logit is formed inside
-// one CTA in the contract order and the top-k ids do not depend on the launch shape. The
-// CTA stores its logits straight into CTA 0's shared memory (distributed shared memory
-// stores: no round trips), one cluster barrier later CTA 0 holds all E logits of every
-// token and a warp per token selects the top K (ties to the lower expert index) and forms
-// the softmax weights. No workspace, no atomics, no spin-waits.
+// owns the 128-wide hidden chunks [r*CPC, (r+1)*CPC) for every expert, so it reads whole,
+// contiguous rows of the router matrix. Thread e forms, for each token of the block and each
+// of its chunks, the FP32 fma chain over the chunk's k ascending from 0 (the token values of
+// one k are one 16-byte shared-memory load). The chunk partials are stored straight into
+// CTA 0's shared memory (distributed shared memory stores); after one cluster barrier CTA 0
+// adds them in ascending chunk order, adds the bias, and selects the top K by rank: expert
+// e takes slot #{e' : l[e'] > l[e] or (l[e'] == l[e] and e' < e)} when that is below K
+// (ties to the lower index). Weights: softmax over the K selected logits (renormalised) or
+// over all E. No workspace, no atomics, no spin-waits.
 #include <cooperative_groups.h>
 
-#include <climits>
 #include <mutex>
 
 #include "common.cuh"
@@ -24,21 +24,24 @@ namespace cg = cooperative_groups;
 namespace moe {
 
 constexpr int kRouteThreads = 256;
-constexpr int kRouteChunksPerRound = 16;  // hidden chunks staged in shared memory at once
+constexpr int kRouteMaxCluster = 16;
 
 struct RouteSmem {
-  size_t ws, xs, part, logits, total;
+  size_t ws, xs, part, logits, sel, total;
 };
 
-// ws: router slab [16 chunks * 128 rows][EC] bf16; xs: hidden [TB][16*128] bf16;
-// part: chunk partials [nchunks][TB][EC] f32; logits: [TB][E] f32 (filled on CTA 0).
-__host__ __device__ inline RouteSmem route_smem(int TB, int EC, int E, int nchunks) {
+// ws: router rows [CPC*128][E] bf16; xs: hidden [CPC*128][TB] bf16 (token-minor);
+// part (CTA 0): chunk partials [nchunks][TB][E] f32; logits [TB][E] f32;
+// sel: selected logits [TB][16] f32 + ids [TB][16] i32.
+__host__ __device__ inline RouteSmem route_smem(int TB, int CPC, int E, int nchunks) {
   RouteSmem s{};
   size_t o = 0;
-  s.ws = o;     o += (size_t)kRouteChunksPerRound * 128 * EC * 2;
-  s.xs = o;     o += (size_t)TB * kRouteChunksPerRound * 128 * 2;
-  s.part = o;   o += (size_t)nchunks * TB * EC * 4;
+  s.ws = o;     o += (size_t)CPC * 128 * E * 2;
+  s.xs = o;     o += (size_t)CPC * 128 * TB * 2;
+  o = (o + 15) & ~size_t(15);
+  s.part = o;   o += (size_t)nchunks * TB * E * 4;
   s.logits = o; o += (size_t)TB * E * 4;
+  s.sel = o;    o += (size_t)TB * 16 * 8;
   s.total = o;
   return s;
 }
@@ -52,156 +55,139 @@ __global__ void __launch_bounds__(kRouteThreads)
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int CL = (int)cluster.num_blocks();
-  const int EC = E / CL;
   const int nchunks = H / 128;
-  const RouteSmem L = route_smem(TB, EC, E, nchunks);
+  const int CPC = nchunks / CL;
+  const RouteSmem L = route_smem(TB, CPC, E, nchunks);
   uint16_t* wsm = reinterpret_cast<uint16_t*>(smem + L.ws);
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem + L.xs);
   float* part = reinterpret_cast<float*>(smem + L.part);
   float* logits = reinterpret_cast<float*>(smem + L.logits);
+  float* sel_v = reinterpret_cast<float*>(smem + L.sel);
+  int* sel_i = reinterpret_cast<int*>(sel_v + TB * 16);
   const int tid = threadIdx.x;
   const int tok0 = blockIdx.y * TB;
-  const int e0 = rank * EC;
+  const int c0 = rank * CPC;
 
   // inputs may be written by the previous kernel in the stream (programmatic launch)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
 
-  // thread <-> (expert el, chunk lane cgl); chunks cgl, cgl + TPE, ... of each round.
-  // Consecutive lanes take consecutive experts (one 2-byte router value each).
-  const int TPE = kRouteThreads / EC;
-  const int el = tid % EC, cgl = tid / EC;
-  for (int c0 = 0; c0 < nchunks; c0 += kRouteChunksPerRound) {
-    const int nc = min(kRouteChunksPerRound, nchunks - c0);
-    // stage router rows [c0*128, (c0+nc)*128) x experts [e0, e0+EC) and the hidden chunk
-    const int segs = EC * 2 / 16;  // 16-byte pieces per router row slice
-    const int n16 = nc * 128 * segs;
+  // stage router rows [c0*128, (c0+CPC)*128) (contiguous) and the tokens' hidden values
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(router_w + (size_t)c0 * 128 * E);
+    uint4* dst = reinterpret_cast<uint4*>(wsm);
+    const int n16 = CPC * 128 * E / 8;
     for (int i0 = tid; i0 < n16; i0 += kRouteThreads * 8) {
       uint4 v[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = i0 + u * kRouteThreads;
-        if (i < n16)
-          v[u] = *reinterpret_cast<const uint4*>(router_w + (size_t)(c0 * 128 + i / segs) * E + e0 +
-                                                 (i % segs) * 8);
-      }
+      for (int u = 0; u < 8; ++u)
+        if (i0 + u * kRouteThreads < n16) v[u] = src[i0 + u * kRouteThreads];
 #pragma unroll
       for (int u = 0; u < 8; ++u)
-        if (i0 + u * kRouteThreads < n16) reinterpret_cast<uint4*>(wsm)[i0 + u * kRouteThreads] = v[u];
+        if (i0 + u * kRouteThreads < n16) dst[i0 + u * kRouteThreads] = v[u];
     }
-    for (int i = tid; i < TB * nc * 16; i += kRouteThreads) {
-      const int t = i / (nc * 16), k8 = (i % (nc * 16)) * 8;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (tok0 + t < M) v = *reinterpret_cast<const uint4*>(hidden + (size_t)(tok0 + t) * H + c0 * 128 + k8);
-      *reinterpret_cast<uint4*>(xs + t * kRouteChunksPerRound * 128 + k8) = v;
+    for (int i = tid; i < TB * CPC * 128; i += kRouteThreads) {
+      const int t = i / (CPC * 128), k = i % (CPC * 128);
+      xs[k * TB + t] = tok0 + t < M ? hidden[(size_t)(tok0 + t) * H + c0 * 128 + k] : (uint16_t)0;
     }
-    __syncthreads();
-    {
-      for (int cc = cgl; cc < nc; cc += TPE) {
-        float acc[TB];
+  }
+  __syncthreads();
+
+  float* part0 = cluster.map_shared_rank(part, 0);
+  for (int e = tid; e < E; e += kRouteThreads) {
+    for (int cl = 0; cl < CPC; ++cl) {
+      float acc[TB];
 #pragma unroll
-        for (int t = 0; t < TB; ++t) acc[t] = 0.0f;
-#pragma unroll 8
-        for (int k = 0; k < 128; ++k) {
-          const float w = bf16_bits_to_float(wsm[(cc * 128 + k) * EC + el]);
-#pragma unroll
-          for (int t = 0; t < TB; ++t)
-            acc[t] = __fmaf_rn(bf16_bits_to_float(xs[t * kRouteChunksPerRound * 128 + cc * 128 + k]), w, acc[t]);
+      for (int t = 0; t < TB; ++t) acc[t] = 0.0f;
+      const uint16_t* wcol = wsm + (size_t)cl * 128 * E + e;
+      const uint16_t* xk = xs + (size_t)cl * 128 * TB;
+#pragma unroll 16
+      for (int k = 0; k < 128; ++k) {
+        const float w = bf16_bits_to_float(wcol[k * E]);
+        uint32_t xw[(TB + 1) / 2];
+        if constexpr (TB == 8) {
+          const uint4 q = *reinterpret_cast<const uint4*>(xk + k * TB);
+          xw[0] = q.x; xw[1] = q.y; xw[2] = q.z; xw[3] = q.w;
+        } else if constexpr (TB == 2) {
+          xw[0] = *reinterpret_cast<const uint32_t*>(xk + k * TB);
+        } else {
+          xw[0] = xk[k * TB];
         }
 #pragma unroll
-        for (int t = 0; t < TB; ++t) part[((size_t)(c0 + cc) * TB + t) * EC + el] = acc[t];
+        for (int t = 0; t < TB; ++t) {
+          const uint16_t b = (uint16_t)((t & 1) ? (xw[t / 2] >> 16) : (xw[t / 2] & 0xFFFF));
+          acc[t] = __fmaf_rn(bf16_bits_to_float(b), w, acc[t]);
+        }
       }
+#pragma unroll
+      for (int t = 0; t < TB; ++t) part0[((size_t)(c0 + cl) * TB + t) * E + e] = acc[t];
     }
-    __syncthreads();
   }
-  // logits of this CTA's experts, chunk partials summed in ascending chunk order, pushed
-  // into CTA 0's shared memory
-  float* logits0 = cluster.map_shared_rank(logits, 0);
-  for (int i = tid; i < TB * EC; i += kRouteThreads) {
-    const int t = i / EC, e = i % EC;
-    float l = 0.0f;
-    for (int c = 0; c < nchunks; ++c) l = __fadd_rn(l, part[((size_t)c * TB + t) * EC + e]);
-    if (bias != nullptr) l = __fadd_rn(l, bias[e0 + e]);
-    logits0[t * E + e0 + e] = l;
-  }
-  cluster.sync();  // all logits are in CTA 0's shared memory
+  cluster.sync();  // CTA 0 holds every chunk partial
   if (rank != 0) return;
 
-  // top-k: one warp per token; lane holds experts lane, lane+32, ...
+  for (int i = tid; i < TB * E; i += kRouteThreads) {
+    const int t = i / E, e = i % E;
+    float l = 0.0f;
+    for (int c = 0; c < nchunks; ++c) l = __fadd_rn(l, part[((size_t)c * TB + t) * E + e]);
+    if (bias != nullptr) l = __fadd_rn(l, bias[e]);
+    logits[t * E + e] = l;
+  }
+  __syncthreads();
+  // rank selection: expert e goes to slot rank(e) if rank(e) < K
+  for (int i = tid; i < TB * E; i += kRouteThreads) {
+    const int t = i / E, e = i % E;
+    const float* lt = logits + t * E;
+    const float v = lt[e];
+    int rk = 0;
+    for (int e2 = 0; e2 < E; ++e2) {
+      const float v2 = lt[e2];
+      rk += (v2 > v) || (v2 == v && e2 < e);
+    }
+    if (rk < K) {
+      sel_v[t * 16 + rk] = v;
+      sel_i[t * 16 + rk] = e;
+    }
+  }
+  __syncthreads();
+  // weights: one warp per token
   const int warp = tid / 32, lane = tid % 32;
-  constexpr int kMaxPerLane = 8;  // E <= 256
   for (int t = warp; t < TB; t += kRouteThreads / 32) {
     if (tok0 + t >= M) break;
-    float v[kMaxPerLane];
-    bool taken[kMaxPerLane];
-#pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = e < E ? logits[t * E + e] : -INFINITY;
-      taken[i] = !(e < E);
-    }
-    float sel_v[16];
-    int sel_i[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      if (j >= K) break;
-      float bv = -INFINITY;
-      int bi = INT_MAX;
-#pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i) {
-        const int e = lane + 32 * i;
-        if (!taken[i] && (v[i] > bv || (v[i] == bv && e < bi))) { bv = v[i]; bi = e; }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-      }
-#pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i)
-        if (lane + 32 * i == bi) taken[i] = true;
-      sel_v[j] = bv;
-      sel_i[j] = bi;
-    }
-    const float lmax = sel_v[0];
+    const float lmax = sel_v[t * 16];
     float den = 0.0f;
     if (renorm) {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        if (j >= K) break;
-        den = __fadd_rn(den, expf(__fsub_rn(sel_v[j], lmax)));
-      }
+      for (int j = 0; j < K; ++j) den = __fadd_rn(den, expf(__fsub_rn(sel_v[t * 16 + j], lmax)));
     } else {
-#pragma unroll
-      for (int i = 0; i < kMaxPerLane; ++i)
-        if (lane + 32 * i < E) den = __fadd_rn(den, expf(__fsub_rn(v[i], lmax)));
+      for (int e = lane; e < E; e += 32) den = __fadd_rn(den, expf(__fsub_rn(logits[t * E + e], lmax)));
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) den = __fadd_rn(den, __shfl_xor_sync(0xffffffffu, den, off));
     }
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      if (j >= K) break;
-      if (lane == j) {
-        const size_t o = (size_t)(tok0 + t) * K + j;
-        ids[o] = sel_i[j] == INT_MAX ? -1 : sel_i[j];
-        wts[o] = __fdiv_rn(expf(__fsub_rn(sel_v[j], lmax)), den);
-      }
+    if (lane < K) {
+      const size_t o = (size_t)(tok0 + t) * K + lane;
+      ids[o] = sel_i[t * 16 + lane];
+      wts[o] = __fdiv_rn(expf(__fsub_rn(sel_v[t * 16 + lane], lmax)), den);
     }
   }
 }
 
 namespace {
 
-// CL CTAs per cluster, E/CL >= 8 experts each (a 16-byte router row slice); 16-CTA
-// clusters (a non-portable size) for E >= 128 spread the router weights over more SMs
-int route_cluster(int E) { return E >= 128 ? 16 : E / 8; }
+// CL CTAs per cluster (<= 16, a divisor of the chunk count): one 128-row chunk per CTA
+// whenever the chunk count allows
+int route_cluster(int nchunks) {
+  for (int c = kRouteMaxCluster; c >= 1; --c)
+    if (nchunks % c == 0) return c;
+  return 1;
+}
 
 template <int TB>
 cudaError_t launch_route_t(const uint16_t* hidden, const uint16_t* router_w, const float* bias, int M,
                            int H, int E, int K, int renorm, int32_t* ids, float* wts, cudaStream_t st) {
-  const int CL = route_cluster(E);
-  const RouteSmem L = route_smem(TB, E / CL, E, H / 128);
+  const int nchunks = H / 128;
+  const int CL = route_cluster(nchunks);
+  const RouteSmem L = route_smem(TB, nchunks / CL, E, nchunks);
+  if (L.total > 227 * 1024) return cudaErrorInvalidConfiguration;
   static std::once_flag once;
   std::call_once(once, [] {
     cudaFuncSetAttribute(route_kernel<TB>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
@@ -226,11 +212,16 @@ cudaError_t launch_route_t(const uint16_t* hidden, const uint16_t* router_w, con
 
 }  // namespace
 
+// Tokens per cluster: 1 for a token or two, 8 (one 16-byte load of token values per k)
+// when there are many and CTA 0's chunk partials [nchunks][8][E] still fit.
 cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const float* bias, int M,
                          int H, int E, int K, int renorm, int32_t* ids, float* wts, cudaStream_t st) {
-  if (M <= 2) return launch_route_t<1>(hidden, router_w, bias, M, H, E, K, renorm, ids, wts, st);
-  if (M <= 32) return launch_route_t<2>(hidden, router_w, bias, M, H, E, K, renorm, ids, wts, st);
-  return launch_route_t<8>(hidden, router_w, bias, M, H, E, K, renorm, ids, wts, st);
+  const int nchunks = H / 128;
+  if (M >= 16 && route_smem(8, nchunks / route_cluster(nchunks), E, nchunks).total <= 227 * 1024)
+    return launch_route_t<8>(hidden, router_w, bias, M, H, E, K, renorm, ids, wts, st);
+  if (M >= 4 && route_smem(2, nchunks / route_cluster(nchunks), E, nchunks).total <= 227 * 1024)
+    return launch_route_t<2>(hidden, router_w, bias, M, H, E, K, renorm, ids, wts, st);
+  return launch_route_t<1>(hidden, router_w, bias, M, H, E, K, renorm, ids, wts, st);
 }
 
 }  // namespace moe

@@ -259,9 +259,8 @@ __global__ void __launch_bounds__(kPairThreads, 3)
       }
     }
   } else if (valid) {
-    // epilogue: thread <-> weight row r of the 128-row tile
+    // epilogue: thread <-> weight row (warp % 4) * 32 + lane of the 128-row tile
     const int q = warp & 3;
-    const int r = q * 32 + lane;
     const float* sw0 = p.w_scale + ((size_t)e * (kGateUp ? 2 * p.I / 128 : p.H / 128) + cb) * p.nkb;
     const float* sw1 = p.w_scale + ((size_t)e * (2 * p.I / 128) + p.I / 128 + cb) * p.nkb;
     for (int i = 0; i < p.nkb_cta; ++i) {
