@@ -15,10 +15,11 @@ cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const
                          int H, int E, int K, int renorm, int32_t* ids, float* wts, cudaStream_t st);
 cudaError_t launch_prep(const uint16_t* hidden, const int32_t* ids, int M, int H, int E, int K,
                         const WsPtrs& ws, cudaStream_t st);
-cudaError_t launch_gateup_gemv(const uint8_t* w13, const float* s13, int H, int I, int K,
-                               int64_t max_tiles, const WsPtrs& ws, cudaStream_t st);
-cudaError_t launch_down_gemv(const uint8_t* w2, const float* s2w, int H, int I, int64_t max_tiles,
-                             const WsPtrs& ws, cudaStream_t st);
+cudaError_t launch_gather(int R, int H, int E, int K, const WsPtrs& ws, cudaStream_t st);
+cudaError_t launch_grouped_gateup(const uint8_t* w13, const float* s13, int64_t R, int H, int I, int E,
+                                  int64_t max_tiles, const WsPtrs& ws, cudaStream_t st);
+cudaError_t launch_grouped_down(const uint8_t* w2, const float* s2w, int64_t R, int H, int I, int E,
+                                int64_t max_tiles, const WsPtrs& ws, cudaStream_t st);
 cudaError_t launch_pair_gateup(const uint8_t* w13, const float* s13, const int32_t* ids,
                                const uint16_t* hidden, int M, int H, int I, int E, int K,
                                const WsPtrs& ws, cudaStream_t st);
@@ -39,7 +40,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool shape_supported(const moe_fp8_shape_t* s) {
   if (!s) return false;
   const int H = s->hidden, I = s->inter, E = s->num_experts, K = s->top_k;
-  if (H < 128 || H > 8192 || H % 128) return false;
+  if (H < 256 || H > 8192 || H % 256) return false;
   if (I < 128 || I > 4096 || I % 128) return false;
   if (!(E == 8 || E == 16 || E == 32 || E == 64 || E == 128 || E == 256)) return false;
   if (K < 1 || K > 16 || K > E) return false;
@@ -107,8 +108,12 @@ moe_status_t moe_fp8_prepare(const void* hidden, const int32_t* topk_ids, int32_
   if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
   if (M == 0) return MOE_OK;
   const WsPtrs ws = ws_ptrs(workspace, L);
-  return launched(launch_prep(static_cast<const uint16_t*>(hidden), topk_ids, M, shape->hidden,
-                              shape->num_experts, shape->top_k, ws, stream));
+  const int64_t R = (int64_t)M * shape->top_k;
+  if (cudaError_t e = launch_prep(static_cast<const uint16_t*>(hidden), topk_ids, M, shape->hidden,
+                                  shape->num_experts, shape->top_k, ws, stream))
+    return launched(e);
+  if (use_pair_mode(R)) return MOE_OK;
+  return launched(launch_gather((int)R, shape->hidden, shape->num_experts, shape->top_k, ws, stream));
 }
 
 moe_status_t moe_fp8_gate_up(const uint8_t* w13, const float* w13_scale, int32_t M,
@@ -124,8 +129,8 @@ moe_status_t moe_fp8_gate_up(const uint8_t* w13, const float* w13_scale, int32_t
   if (use_pair_mode(R))
     return launched(launch_pair_gateup(w13, w13_scale, ws.pair_expert, nullptr, M, shape->hidden,
                                        shape->inter, shape->num_experts, shape->top_k, ws, stream));
-  return launched(launch_gateup_gemv(w13, w13_scale, shape->hidden, shape->inter, shape->top_k,
-                                     max_tiles_for(R, shape->num_experts, kTileRows), ws, stream));
+  return launched(launch_grouped_gateup(w13, w13_scale, R, shape->hidden, shape->inter, shape->num_experts,
+                                        max_tiles_for(R, shape->num_experts, kTileRows), ws, stream));
 }
 
 moe_status_t moe_fp8_down(const uint8_t* w2, const float* w2_scale, int32_t M, void* workspace,
@@ -141,8 +146,8 @@ moe_status_t moe_fp8_down(const uint8_t* w2, const float* w2_scale, int32_t M, v
   if (use_pair_mode(R))
     return launched(launch_pair_down(w2, w2_scale, ws.pair_expert, nullptr, nullptr, M, shape->hidden,
                                      shape->inter, shape->num_experts, shape->top_k, ws, stream));
-  return launched(launch_down_gemv(w2, w2_scale, shape->hidden, shape->inter,
-                                   max_tiles_for(R, shape->num_experts, kTileRows), ws, stream));
+  return launched(launch_grouped_down(w2, w2_scale, R, shape->hidden, shape->inter, shape->num_experts,
+                                      max_tiles_for(R, shape->num_experts, kTileRows), ws, stream));
 }
 
 moe_status_t moe_fp8_combine(const float* topk_w, int32_t M, void* out, void* workspace,

@@ -139,6 +139,34 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const uint16_t* __re
   }
 }
 
+// Gather the hidden codes and scales of every routed row into expert-sorted order (the A
+// operand rows of the grouped GEMM): xp[r] = qa[row_src[r] / K], sa_p[r] = sa[row_src[r] / K].
+// One warp per sorted row; rows past the valid count (skipped pairs) are left untouched.
+__global__ void __launch_bounds__(256) gather_kernel(int R, int H, int E, int K, WsPtrs ws) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int r = blockIdx.x * 8 + threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (r >= R || r >= ws.offsets[E]) return;
+  const int t = ws.row_src[r] / K;
+  const uint4* src = reinterpret_cast<const uint4*>(ws.qa + (size_t)t * H);
+  uint4* dst = reinterpret_cast<uint4*>(ws.xp + (size_t)r * H);
+  for (int i = lane; i < H / 16; i += 32) dst[i] = src[i];
+  for (int i = lane; i < H / 128; i += 32) ws.sa_p[(size_t)r * (H / 128) + i] = ws.sa[(size_t)t * (H / 128) + i];
+}
+
+cudaError_t launch_gather(int R, int H, int E, int K, const WsPtrs& ws, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((R + 7) / 8), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gather_kernel, R, H, E, K, ws);
+}
+
 cudaError_t launch_prep(const uint16_t* hidden, const int32_t* ids, int M, int H, int E, int K,
                         const WsPtrs& ws, cudaStream_t st) {
   const int pair_mode = use_pair_mode((int64_t)M * K) ? 1 : 0;

@@ -1,0 +1,303 @@
+// tc_grouped.cu -- block-scaled grouped expert GEMMs on tcgen05 for many routed rows
+// (prefill): expert-sorted tiles of up to 128 routed rows.
+//
+// Sources: "NetraRuntime/netra-kernel" README, prefill-pair build section (the routed MoE
+// producer: gate/up, SiLU and quantisation, down-partial); older lab README, supported
+// targets (FP8 E4M3 weights with 128x128 FP32 block scales); docs/compiler/architecture.md
+// (FP8 activation and activation-scale intermediates between gate/up and down).
+//
+// One CTA per (tile, 256-wide output block). A = the tile's 128 activation rows (FP8,
+// expert-sorted: the gathered hidden codes for gate/up, the activation codes for down),
+// B = 256 weight rows of the tile's expert -- for gate/up the 128 gate rows of an output
+// block followed by the matching 128 up rows, for down 256 rows of w2. Per 128-wide K block
+// the TMA warp loads A (16 KB) and B (32 KB) into a four-stage ring (128-byte swizzle), the
+// MMA warp issues four 128x256x32 FP8 MMAs into a fresh accumulator (double-buffered:
+// 2 x 256 TMEM columns), and eight epilogue warps promote the block sum into FP32 chains,
+//   acc = acc + P_kb * (sa[row][kb] * sw[block][kb])     kb ascending, from 0,
+// thread = (accumulator row, half of the 256 columns); a thread holds 128 running chains.
+// gate/up epilogue: act = silu(g) * u for the thread's 64 columns, the row's amax over 128
+// columns (the partner warp's half via shared memory), scale = amax/448, RNE saturating
+// E4M3 codes -> act [row][I] and act_scale [row][I/128]. down epilogue: y [row][H] FP32.
+// Rows of a tile past its length are computed on zero/neighbour rows and never stored.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "tc.cuh"
+
+namespace moe {
+
+constexpr int kGrpThreads = 320;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2..9 epilogue
+constexpr int kGrpStages = 4;
+constexpr int kGrpABytes = 128 * 128;
+constexpr int kGrpBBytes = 256 * 128;
+constexpr int kGrpStageBytes = kGrpABytes + kGrpBBytes;
+constexpr int kGrpTmemCols = 512;
+
+struct GrpParams {
+  int H, I, E;
+  int nkb;                 // K blocks
+  int nnb;                 // 256-wide output blocks per tile
+  const Tile* tiles;
+  const float* w_scale;    // s13 [E][2I/128][H/128] or s2w [E][H/128][I/128]
+  const float* a_scale;    // sa_p [R][H/128] (gate/up) or act_scale [R][I/128] (down)
+  uint8_t* act_out;        // [R][I]
+  float* act_scale_out;    // [R][I/128]
+  float* y_out;            // [R][H]
+  Header* hdr;
+};
+
+__host__ __device__ constexpr size_t grp_smem_bytes() {
+  return 1024 + (size_t)kGrpStages * kGrpStageBytes + 256 + 128 * 2 * 4;
+}
+
+template <bool GATEUP>
+__global__ void __launch_bounds__(kGrpThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const GrpParams p) {
+  extern __shared__ __align__(1024) unsigned char dsm_raw[];
+  unsigned char* base =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* stages = base;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kGrpStages * kGrpStageBytes);
+  uint64_t* full = bars;                      // [kGrpStages]
+  uint64_t* empty = bars + kGrpStages;        // [kGrpStages]
+  uint64_t* accf = bars + 2 * kGrpStages;     // [2]
+  uint64_t* acce = bars + 2 * kGrpStages + 2; // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kGrpStages + 4);
+  float* red = reinterpret_cast<float*>(base + kGrpStages * kGrpStageBytes + 256);  // [128][2]
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (warp == 0 && lane == 0) {
+    tc::prefetch_tmap(&tmA);
+    tc::prefetch_tmap(&tmB);
+    for (int s = 0; s < kGrpStages; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&accf[b], 1);
+      tc::mbar_init(&acce[b], 8);
+    }
+    tc::fence_mbar_init();
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+
+  const int tile_idx = blockIdx.x / p.nnb, nb = blockIdx.x % p.nnb;
+  if (tile_idx >= (int)*reinterpret_cast<volatile const uint32_t*>(&p.hdr->n_tiles)) return;
+  const Tile tl = p.tiles[tile_idx];
+  const int e = tl.expert, row0 = tl.row0, nrows = tl.nrows;
+
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, kGrpTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  bool ok = true;
+  if (warp == 0) {
+    if (lane == 0) {
+      const int yb0 = GATEUP ? e * 2 * p.I + nb * 128 : e * p.H + nb * 256;
+      const int yb1 = GATEUP ? e * 2 * p.I + p.I + nb * 128 : yb0 + 128;
+      for (int i = 0; i < p.nkb; ++i) {
+        const int s = i % kGrpStages;
+        const uint32_t ph = (i / kGrpStages) & 1;
+        if (!tc::mbar_wait(&empty[s], ph ^ 1)) { ok = false; break; }
+        unsigned char* st = stages + s * kGrpStageBytes;
+        tc::mbar_arrive_expect_tx(&full[s], kGrpStageBytes);
+        const int x = i * 128;
+        tc::tma_load_2d(st, &tmA, &full[s], x, row0);
+        tc::tma_load_2d(st + kGrpABytes, &tmB, &full[s], x, yb0);
+        tc::tma_load_2d(st + kGrpABytes + 128 * 128, &tmB, &full[s], x, yb1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_e4m3(128, 256);
+      for (int i = 0; i < p.nkb; ++i) {
+        const int s = i % kGrpStages;
+        const uint32_t ph = (i / kGrpStages) & 1;
+        const int buf = i & 1;
+        if (!tc::mbar_wait(&full[s], ph)) { ok = false; break; }
+        if (!tc::mbar_wait(&acce[buf], ((i >> 1) & 1) ^ 1)) { ok = false; break; }
+        tc::fence_after_sync();
+        const uint32_t sa = tc::smem_u32(stages + s * kGrpStageBytes);
+        const uint64_t da = tc::sdesc_sw128(sa);
+        const uint64_t db = tc::sdesc_sw128(sa + kGrpABytes);
+        const uint32_t d = tmem + buf * 256;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) tc::mma_e4m3(d, da + 2 * k, db + 2 * k, idesc, k > 0);
+        tc::mma_commit(&empty[s]);
+        tc::mma_commit(&accf[buf]);
+      }
+    }
+  } else {
+    const int q = warp & 3;            // TMEM lane quadrant (hardware: warp % 4)
+    const int hc = (warp - 2) >> 2;    // which half of the 256 accumulator columns
+    const int row = q * 32 + lane;
+    const bool live = row < nrows;
+    const float* sarow = p.a_scale + (size_t)(row0 + (live ? row : 0)) * p.nkb;
+    if (GATEUP) {
+      const float* swg = p.w_scale + ((size_t)e * (2 * p.I / 128) + nb) * p.nkb;
+      const float* swu = p.w_scale + ((size_t)e * (2 * p.I / 128) + p.I / 128 + nb) * p.nkb;
+      float g[64], u[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) { g[c] = 0.0f; u[c] = 0.0f; }
+      for (int i = 0; i < p.nkb; ++i) {
+        const int buf = i & 1;
+        if (!tc::mbar_wait(&accf[buf], (i >> 1) & 1)) { ok = false; break; }
+        tc::fence_after_sync();
+        const float a = live ? sarow[i] : 0.0f;
+        const float scg = __fmul_rn(a, swg[i]), scu = __fmul_rn(a, swu[i]);
+        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + buf * 256 + hc * 64;
+        float P[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          tc::tmem_ld32(ta + h * 32, P);  // gate columns
+#pragma unroll
+          for (int c = 0; c < 32; ++c) g[h * 32 + c] = __fadd_rn(g[h * 32 + c], __fmul_rn(P[c], scg));
+          tc::tmem_ld32(ta + 128 + h * 32, P);  // up columns
+#pragma unroll
+          for (int c = 0; c < 32; ++c) u[h * 32 + c] = __fadd_rn(u[h * 32 + c], __fmul_rn(P[c], scu));
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&acce[buf]);
+      }
+      // act = silu(g) * u; row amax over the 128 columns of this output block
+      float amax = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        g[c] = silu_mul(g[c], u[c]);
+        amax = fmaxf(amax, fabsf(g[c]));
+      }
+      red[row * 2 + hc] = amax;
+      tc::named_bar(1, 256);
+      amax = fmaxf(red[row * 2], red[row * 2 + 1]);
+      const float s2 = quant_scale(amax);
+      if (live) {
+        uint8_t* dst = p.act_out + (size_t)(row0 + row) * p.I + nb * 128 + hc * 64;
+#pragma unroll
+        for (int c16 = 0; c16 < 4; ++c16) {
+          uint32_t w4[4];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int c = c16 * 16 + q4 * 4;
+            const uint32_t lo = e4m3x2_encode(__fdiv_rn(g[c], s2), __fdiv_rn(g[c + 1], s2));
+            const uint32_t hi = e4m3x2_encode(__fdiv_rn(g[c + 2], s2), __fdiv_rn(g[c + 3], s2));
+            w4[q4] = lo | (hi << 16);
+          }
+          reinterpret_cast<uint4*>(dst)[c16] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+        if (hc == 0) p.act_scale_out[(size_t)(row0 + row) * (p.I / 128) + nb] = s2;
+      }
+    } else {
+      const int hblk = nb * 2 + hc;  // 128-row block of w2 this thread's columns belong to
+      const float* sw = p.w_scale + ((size_t)e * (p.H / 128) + hblk) * p.nkb;
+      float y[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) y[c] = 0.0f;
+      for (int i = 0; i < p.nkb; ++i) {
+        const int buf = i & 1;
+        if (!tc::mbar_wait(&accf[buf], (i >> 1) & 1)) { ok = false; break; }
+        tc::fence_after_sync();
+        const float sc = __fmul_rn(live ? sarow[i] : 0.0f, sw[i]);
+        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + buf * 256 + hc * 128;
+        float P[32];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          tc::tmem_ld32(ta + h * 32, P);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) y[h * 32 + c] = __fadd_rn(y[h * 32 + c], __fmul_rn(P[c], sc));
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&acce[buf]);
+      }
+      if (live) {
+        float4* dst = reinterpret_cast<float4*>(p.y_out + (size_t)(row0 + row) * p.H + hblk * 128);
+#pragma unroll
+        for (int c4 = 0; c4 < 32; ++c4) dst[c4] = make_float4(y[4 * c4], y[4 * c4 + 1], y[4 * c4 + 2], y[4 * c4 + 3]);
+      }
+    }
+  }
+  if (!ok) set_status(p.hdr, MOE_STATUS_WAIT_TIMEOUT);
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kGrpTmemCols);
+  }
+}
+
+bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
+
+namespace {
+
+template <bool GATEUP>
+cudaError_t launch_grouped(const CUtensorMap& tA, const CUtensorMap& tB, const GrpParams& prm,
+                           int64_t max_tiles, cudaStream_t st) {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(grouped_gemm_kernel<GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)grp_smem_bytes());
+  });
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(max_tiles * prm.nnb), 1, 1);
+  cfg.blockDim = dim3(kGrpThreads, 1, 1);
+  cfg.dynamicSmemBytes = grp_smem_bytes();
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<GATEUP>, tA, tB, prm);
+}
+
+}  // namespace
+
+// gate/up over the expert tiles: A = gathered hidden codes xp [R][H] with scales sa_p.
+cudaError_t launch_grouped_gateup(const uint8_t* w13, const float* s13, int64_t R, int H, int I, int E,
+                                  int64_t max_tiles, const WsPtrs& ws, cudaStream_t st) {
+  CUtensorMap tA, tB;
+  if (!make_tmap_u8(&tA, ws.xp, (uint64_t)H, (uint64_t)R, 128)) return cudaErrorInvalidValue;
+  if (!make_tmap_u8(&tB, w13, (uint64_t)H, (uint64_t)E * 2 * I, 128)) return cudaErrorInvalidValue;
+  GrpParams prm{};
+  prm.H = H; prm.I = I; prm.E = E;
+  prm.nkb = H / 128;
+  prm.nnb = I / 128;
+  prm.tiles = ws.tiles;
+  prm.w_scale = s13;
+  prm.a_scale = ws.sa_p;
+  prm.act_out = ws.act;
+  prm.act_scale_out = ws.act_scale;
+  prm.y_out = ws.y;
+  prm.hdr = ws.hdr;
+  return launch_grouped<true>(tA, tB, prm, max_tiles, st);
+}
+
+// down over the expert tiles: A = activation codes act [R][I], y [R][H] (H % 256 == 0).
+cudaError_t launch_grouped_down(const uint8_t* w2, const float* s2w, int64_t R, int H, int I, int E,
+                                int64_t max_tiles, const WsPtrs& ws, cudaStream_t st) {
+  CUtensorMap tA, tB;
+  if (!make_tmap_u8(&tA, ws.act, (uint64_t)I, (uint64_t)R, 128)) return cudaErrorInvalidValue;
+  if (!make_tmap_u8(&tB, w2, (uint64_t)I, (uint64_t)E * H, 128)) return cudaErrorInvalidValue;
+  GrpParams prm{};
+  prm.H = H; prm.I = I; prm.E = E;
+  prm.nkb = I / 128;
+  prm.nnb = H / 256;
+  prm.tiles = ws.tiles;
+  prm.w_scale = s2w;
+  prm.a_scale = ws.act_scale;
+  prm.act_out = ws.act;
+  prm.act_scale_out = ws.act_scale;
+  prm.y_out = ws.y;
+  prm.hdr = ws.hdr;
+  return launch_grouped<false>(tA, tB, prm, max_tiles, st);
+}
+
+}  // namespace moe

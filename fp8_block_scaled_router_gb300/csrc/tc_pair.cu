@@ -269,9 +269,7 @@ __global__ void __launch_bounds__(kPairThreads, 3)
       tc::fence_after_sync();
       const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + buf * C::kAccCols;
       float v0[16], v1[16];
-      tc::tmem_ld16(ta, v0);
-      if (kGateUp) tc::tmem_ld16(ta + kPairN, v1);
-      tc::tmem_wait_ld();
+      tc::tmem_ld16x2(ta, kGateUp ? ta + kPairN : ta, v0, v1);
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&acce[buf]);

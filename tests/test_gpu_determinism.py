@@ -22,9 +22,15 @@ def _build_lib():
     build.build()
 
 
-@pytest.mark.parametrize("name,M", [("decode", 1), ("verify", 12), ("tiny", 4)])
+def _workload(name, M):
+    if name == "grouped":  # 64 tokens x top-8 over 16 experts: the sorted-tile path
+        return inputs.make("decode", E=16, tokens=M)
+    return inputs.make(name, tokens=M) if name == "decode" else inputs.make(name)
+
+
+@pytest.mark.parametrize("name,M", [("decode", 1), ("verify", 12), ("tiny", 4), ("grouped", 64)])
 def test_100_launches_bitwise_identical(name, M):
-    x = inputs.make(name, tokens=M) if name == "decode" else inputs.make(name)
+    x = _workload(name, M)
     g = GpuMoE(x, M)
     hid = to_dev(x.hidden[:M])
     ref = None
@@ -67,12 +73,12 @@ def test_graph_capture_replay_matches_eager():
         assert torch.equal(ids2, ids_eager) and torch.equal(w2, w_eager)
 
 
-@pytest.mark.parametrize("name,M", [("decode", 1), ("verify_skewed", 12), ("tiny", 4)])
+@pytest.mark.parametrize("name,M", [("decode", 1), ("verify_skewed", 12), ("tiny", 4), ("grouped", 64)])
 def test_forward_equals_stage_calls(name, M):
     """moe_fp8_forward (which may fuse stages) and the four stage calls give bitwise equal
     outputs: the fused kernels use the same arithmetic in the same order."""
     from fp8_block_scaled_router_gb300 import _lib as L
-    x = inputs.make(name, tokens=M) if name == "decode" else inputs.make(name)
+    x = _workload(name, M)
     g = GpuMoE(x, M)
     hid = to_dev(x.hidden[:M])
     ids, w = g.route(hid, M)
