@@ -6,13 +6,14 @@
 // targets (FP8 E4M3 weights with 128x128 FP32 block scales); docs/compiler/architecture.md
 // (FP8 activation and activation-scale intermediates between gate/up and down).
 //
-// One CTA per (tile, 256-wide output block). A = the tile's 128 activation rows (FP8,
+// Persistent: one CTA per SM walks the (tile, 256-wide output block) units. A = the tile's 128 activation rows (FP8,
 // expert-sorted: the gathered hidden codes for gate/up, the activation codes for down),
 // B = 256 weight rows of the tile's expert -- for gate/up the 128 gate rows of an output
 // block followed by the matching 128 up rows, for down 256 rows of w2. Per 128-wide K block
 // the TMA warp loads A (16 KB) and B (32 KB) into a four-stage ring (128-byte swizzle), the
 // MMA warp issues four 128x256x32 FP8 MMAs into a fresh accumulator (double-buffered:
-// 2 x 256 TMEM columns), and eight epilogue warps promote the block sum into FP32 chains,
+// 2 x 256 TMEM columns), and eight epilogue warps promote the block sum into FP32 chains
+// (packed FP32x2 multiply, then add: bit-identical to the scalar operations),
 //   acc = acc + P_kb * (sa[row][kb] * sw[block][kb])     kb ascending, from 0,
 // thread = (accumulator row, half of the 256 columns); a thread holds 128 running chains.
 // gate/up epilogue: act = silu(g) * u for the thread's 64 columns, the row's amax over 128
@@ -84,10 +85,11 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
 
-  const int tile_idx = blockIdx.x / p.nnb, nb = blockIdx.x % p.nnb;
-  if (tile_idx >= (int)*reinterpret_cast<volatile const uint32_t*>(&p.hdr->n_tiles)) return;
-  const Tile tl = p.tiles[tile_idx];
-  const int e = tl.expert, row0 = tl.row0, nrows = tl.nrows;
+  // persistent: CTA b takes units b, b + gridDim.x, ... (a unit = one tile x one 256-wide
+  // output block); every role walks the same (unit, K block) sequence, so the stage ring
+  // and the TMEM double buffer run on across unit boundaries
+  const int n_units = (int)*reinterpret_cast<volatile const uint32_t*>(&p.hdr->n_tiles) * p.nnb;
+  if ((int)blockIdx.x >= n_units) return;
 
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, kGrpTmemCols);
@@ -97,131 +99,165 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  const int nkb = p.nkb;
 
   bool ok = true;
   if (warp == 0) {
     if (lane == 0) {
-      const int yb0 = GATEUP ? e * 2 * p.I + nb * 128 : e * p.H + nb * 256;
-      const int yb1 = GATEUP ? e * 2 * p.I + p.I + nb * 128 : yb0 + 128;
-      for (int i = 0; i < p.nkb; ++i) {
-        const int s = i % kGrpStages;
-        const uint32_t ph = (i / kGrpStages) & 1;
-        if (!tc::mbar_wait(&empty[s], ph ^ 1)) { ok = false; break; }
-        unsigned char* st = stages + s * kGrpStageBytes;
-        tc::mbar_arrive_expect_tx(&full[s], kGrpStageBytes);
-        const int x = i * 128;
-        tc::tma_load_2d(st, &tmA, &full[s], x, row0);
-        tc::tma_load_2d(st + kGrpABytes, &tmB, &full[s], x, yb0);
-        tc::tma_load_2d(st + kGrpABytes + 128 * 128, &tmB, &full[s], x, yb1);
+      int it = 0;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const int nb = u % p.nnb;
+        const Tile tl = p.tiles[u / p.nnb];
+        const int yb0 = GATEUP ? tl.expert * 2 * p.I + nb * 128 : tl.expert * p.H + nb * 256;
+        const int yb1 = GATEUP ? tl.expert * 2 * p.I + p.I + nb * 128 : yb0 + 128;
+        for (int i = 0; i < nkb; ++i, ++it) {
+          const int s = it % kGrpStages;
+          const uint32_t ph = (it / kGrpStages) & 1;
+          if (!tc::mbar_wait(&empty[s], ph ^ 1)) { ok = false; break; }
+          unsigned char* st = stages + s * kGrpStageBytes;
+          tc::mbar_arrive_expect_tx(&full[s], kGrpStageBytes);
+          const int x = i * 128;
+          tc::tma_load_2d(st, &tmA, &full[s], x, tl.row0);
+          tc::tma_load_2d(st + kGrpABytes, &tmB, &full[s], x, yb0);
+          tc::tma_load_2d(st + kGrpABytes + 128 * 128, &tmB, &full[s], x, yb1);
+        }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_e4m3(128, 256);
-      for (int i = 0; i < p.nkb; ++i) {
-        const int s = i % kGrpStages;
-        const uint32_t ph = (i / kGrpStages) & 1;
-        const int buf = i & 1;
-        if (!tc::mbar_wait(&full[s], ph)) { ok = false; break; }
-        if (!tc::mbar_wait(&acce[buf], ((i >> 1) & 1) ^ 1)) { ok = false; break; }
-        tc::fence_after_sync();
-        const uint32_t sa = tc::smem_u32(stages + s * kGrpStageBytes);
-        const uint64_t da = tc::sdesc_sw128(sa);
-        const uint64_t db = tc::sdesc_sw128(sa + kGrpABytes);
-        const uint32_t d = tmem + buf * 256;
+      int it = 0;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        for (int i = 0; i < nkb; ++i, ++it) {
+          const int s = it % kGrpStages;
+          const uint32_t ph = (it / kGrpStages) & 1;
+          const int buf = it & 1;
+          if (!tc::mbar_wait(&full[s], ph)) { ok = false; break; }
+          if (!tc::mbar_wait(&acce[buf], ((it >> 1) & 1) ^ 1)) { ok = false; break; }
+          tc::fence_after_sync();
+          const uint32_t sa = tc::smem_u32(stages + s * kGrpStageBytes);
+          const uint64_t da = tc::sdesc_sw128(sa);
+          const uint64_t db = tc::sdesc_sw128(sa + kGrpABytes);
+          const uint32_t d = tmem + buf * 256;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) tc::mma_e4m3(d, da + 2 * k, db + 2 * k, idesc, k > 0);
-        tc::mma_commit(&empty[s]);
-        tc::mma_commit(&accf[buf]);
+          for (int k = 0; k < 4; ++k) tc::mma_e4m3(d, da + 2 * k, db + 2 * k, idesc, k > 0);
+          tc::mma_commit(&empty[s]);
+          tc::mma_commit(&accf[buf]);
+        }
       }
     }
   } else {
     const int q = warp & 3;            // TMEM lane quadrant (hardware: warp % 4)
     const int hc = (warp - 2) >> 2;    // which half of the 256 accumulator columns
     const int row = q * 32 + lane;
-    const bool live = row < nrows;
-    const float* sarow = p.a_scale + (size_t)(row0 + (live ? row : 0)) * p.nkb;
-    if (GATEUP) {
-      const float* swg = p.w_scale + ((size_t)e * (2 * p.I / 128) + nb) * p.nkb;
-      const float* swu = p.w_scale + ((size_t)e * (2 * p.I / 128) + p.I / 128 + nb) * p.nkb;
-      float g[64], u[64];
+    // every epilogue warp walks every unit (the named barriers below need all 8); after
+    // a wait has run out the remaining waits are skipped, so the kernel still ends
+    int it = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      const int nb = u % p.nnb;
+      const Tile tl = p.tiles[u / p.nnb];
+      const int e = tl.expert, row0 = tl.row0;
+      const bool live = row < tl.nrows;
+      const float* sarow = p.a_scale + (size_t)(row0 + (live ? row : 0)) * nkb;
+      if (GATEUP) {
+        const float* swg = p.w_scale + ((size_t)e * (2 * p.I / 128) + nb) * nkb;
+        const float* swu = p.w_scale + ((size_t)e * (2 * p.I / 128) + p.I / 128 + nb) * nkb;
+        uint64_t g2[32], u2[32];  // 64 gate and 64 up running chains, packed in pairs
 #pragma unroll
-      for (int c = 0; c < 64; ++c) { g[c] = 0.0f; u[c] = 0.0f; }
-      for (int i = 0; i < p.nkb; ++i) {
-        const int buf = i & 1;
-        if (!tc::mbar_wait(&accf[buf], (i >> 1) & 1)) { ok = false; break; }
-        tc::fence_after_sync();
-        const float a = live ? sarow[i] : 0.0f;
-        const float scg = __fmul_rn(a, swg[i]), scu = __fmul_rn(a, swu[i]);
-        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + buf * 256 + hc * 64;
-        float P[32];
+        for (int c = 0; c < 32; ++c) { g2[c] = 0; u2[c] = 0; }
+        for (int i = 0; i < nkb; ++i, ++it) {
+          const int buf = it & 1;
+          if (ok && !tc::mbar_wait(&accf[buf], (it >> 1) & 1)) ok = false;
+          tc::fence_after_sync();
+          const float a = live ? sarow[i] : 0.0f;
+          const float scg = __fmul_rn(a, swg[i]), scu = __fmul_rn(a, swu[i]);
+          const uint64_t scg2 = tc::f2pack(__float_as_uint(scg), __float_as_uint(scg));
+          const uint64_t scu2 = tc::f2pack(__float_as_uint(scu), __float_as_uint(scu));
+          const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + buf * 256 + hc * 64;
+          uint32_t P[32];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          tc::tmem_ld32(ta + h * 32, P);  // gate columns
+          for (int h = 0; h < 2; ++h) {
+            tc::tmem_ld32u(ta + h * 32, P);  // gate columns
 #pragma unroll
-          for (int c = 0; c < 32; ++c) g[h * 32 + c] = __fadd_rn(g[h * 32 + c], __fmul_rn(P[c], scg));
-          tc::tmem_ld32(ta + 128 + h * 32, P);  // up columns
+            for (int c = 0; c < 16; ++c)
+              g2[h * 16 + c] = tc::f2add(g2[h * 16 + c], tc::f2mul(tc::f2pack(P[2 * c], P[2 * c + 1]), scg2));
+            tc::tmem_ld32u(ta + 128 + h * 32, P);  // up columns
 #pragma unroll
-          for (int c = 0; c < 32; ++c) u[h * 32 + c] = __fadd_rn(u[h * 32 + c], __fmul_rn(P[c], scu));
-        }
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&acce[buf]);
-      }
-      // act = silu(g) * u; row amax over the 128 columns of this output block
-      float amax = 0.0f;
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        g[c] = silu_mul(g[c], u[c]);
-        amax = fmaxf(amax, fabsf(g[c]));
-      }
-      red[row * 2 + hc] = amax;
-      tc::named_bar(1, 256);
-      amax = fmaxf(red[row * 2], red[row * 2 + 1]);
-      const float s2 = quant_scale(amax);
-      if (live) {
-        uint8_t* dst = p.act_out + (size_t)(row0 + row) * p.I + nb * 128 + hc * 64;
-#pragma unroll
-        for (int c16 = 0; c16 < 4; ++c16) {
-          uint32_t w4[4];
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int c = c16 * 16 + q4 * 4;
-            const uint32_t lo = e4m3x2_encode(__fdiv_rn(g[c], s2), __fdiv_rn(g[c + 1], s2));
-            const uint32_t hi = e4m3x2_encode(__fdiv_rn(g[c + 2], s2), __fdiv_rn(g[c + 3], s2));
-            w4[q4] = lo | (hi << 16);
+            for (int c = 0; c < 16; ++c)
+              u2[h * 16 + c] = tc::f2add(u2[h * 16 + c], tc::f2mul(tc::f2pack(P[2 * c], P[2 * c + 1]), scu2));
           }
-          reinterpret_cast<uint4*>(dst)[c16] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&acce[buf]);
         }
-        if (hc == 0) p.act_scale_out[(size_t)(row0 + row) * (p.I / 128) + nb] = s2;
-      }
-    } else {
-      const int hblk = nb * 2 + hc;  // 128-row block of w2 this thread's columns belong to
-      const float* sw = p.w_scale + ((size_t)e * (p.H / 128) + hblk) * p.nkb;
-      float y[128];
+        // act = silu(g) * u; row amax over the 128 columns of this output block
+        float act[64];
+        float amax = 0.0f;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) y[c] = 0.0f;
-      for (int i = 0; i < p.nkb; ++i) {
-        const int buf = i & 1;
-        if (!tc::mbar_wait(&accf[buf], (i >> 1) & 1)) { ok = false; break; }
-        tc::fence_after_sync();
-        const float sc = __fmul_rn(live ? sarow[i] : 0.0f, sw[i]);
-        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + buf * 256 + hc * 128;
-        float P[32];
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          tc::tmem_ld32(ta + h * 32, P);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) y[h * 32 + c] = __fadd_rn(y[h * 32 + c], __fmul_rn(P[c], sc));
+        for (int c = 0; c < 32; ++c) {
+          float g0, g1, u0, u1;
+          tc::f2unpack(g2[c], g0, g1);
+          tc::f2unpack(u2[c], u0, u1);
+          act[2 * c] = silu_mul(g0, u0);
+          act[2 * c + 1] = silu_mul(g1, u1);
+          amax = fmaxf(amax, fmaxf(fabsf(act[2 * c]), fabsf(act[2 * c + 1])));
         }
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&acce[buf]);
-      }
-      if (live) {
-        float4* dst = reinterpret_cast<float4*>(p.y_out + (size_t)(row0 + row) * p.H + hblk * 128);
+        red[row * 2 + hc] = amax;
+        tc::named_bar(1, 256);
+        amax = fmaxf(red[row * 2], red[row * 2 + 1]);
+        tc::named_bar(1, 256);  // red is rewritten by the next unit
+        const float s2 = quant_scale(amax);
+        if (live) {
+          uint8_t* dst = p.act_out + (size_t)(row0 + row) * p.I + nb * 128 + hc * 64;
 #pragma unroll
-        for (int c4 = 0; c4 < 32; ++c4) dst[c4] = make_float4(y[4 * c4], y[4 * c4 + 1], y[4 * c4 + 2], y[4 * c4 + 3]);
+          for (int c16 = 0; c16 < 4; ++c16) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const int c = c16 * 16 + q4 * 4;
+              const uint32_t lo = e4m3x2_encode(__fdiv_rn(act[c], s2), __fdiv_rn(act[c + 1], s2));
+              const uint32_t hi = e4m3x2_encode(__fdiv_rn(act[c + 2], s2), __fdiv_rn(act[c + 3], s2));
+              w4[q4] = lo | (hi << 16);
+            }
+            reinterpret_cast<uint4*>(dst)[c16] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+          if (hc == 0) p.act_scale_out[(size_t)(row0 + row) * (p.I / 128) + nb] = s2;
+        }
+      } else {
+        const int hblk = nb * 2 + hc;  // 128-row block of w2 this thread's columns belong to
+        const float* sw = p.w_scale + ((size_t)e * (p.H / 128) + hblk) * nkb;
+        uint64_t y2[64];  // 128 running chains, packed in pairs
+#pragma unroll
+        for (int c = 0; c < 64; ++c) y2[c] = 0;
+        for (int i = 0; i < nkb; ++i, ++it) {
+          const int buf = it & 1;
+          if (ok && !tc::mbar_wait(&accf[buf], (it >> 1) & 1)) ok = false;
+          tc::fence_after_sync();
+          const float sc = __fmul_rn(live ? sarow[i] : 0.0f, sw[i]);
+          const uint64_t sc2 = tc::f2pack(__float_as_uint(sc), __float_as_uint(sc));
+          const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + buf * 256 + hc * 128;
+          uint32_t P[32];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            tc::tmem_ld32u(ta + h * 32, P);
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+              y2[h * 16 + c] = tc::f2add(y2[h * 16 + c], tc::f2mul(tc::f2pack(P[2 * c], P[2 * c + 1]), sc2));
+          }
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&acce[buf]);
+        }
+        if (live) {
+          float4* dst = reinterpret_cast<float4*>(p.y_out + (size_t)(row0 + row) * p.H + hblk * 128);
+#pragma unroll
+          for (int c4 = 0; c4 < 32; ++c4) {
+            float a0, a1, a2, a3;
+            tc::f2unpack(y2[2 * c4], a0, a1);
+            tc::f2unpack(y2[2 * c4 + 1], a2, a3);
+            dst[c4] = make_float4(a0, a1, a2, a3);
+          }
+        }
       }
     }
   }
@@ -245,8 +281,16 @@ cudaError_t launch_grouped(const CUtensorMap& tA, const CUtensorMap& tB, const G
     cudaFuncSetAttribute(grouped_gemm_kernel<GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)grp_smem_bytes());
   });
+  static int num_sms = 0;
+  static std::once_flag sm_once;
+  std::call_once(sm_once, [] {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+  });
+  const int64_t units = max_tiles * prm.nnb;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(max_tiles * prm.nnb), 1, 1);
+  cfg.gridDim = dim3((unsigned)(units < num_sms ? units : num_sms), 1, 1);
   cfg.blockDim = dim3(kGrpThreads, 1, 1);
   cfg.dynamicSmemBytes = grp_smem_bytes();
   cfg.stream = st;
