@@ -28,7 +28,8 @@
 
 namespace moe {
 
-constexpr int kGrpThreads = 320;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2..9 epilogue
+constexpr int kGrpEpiWarps = 16;
+constexpr int kGrpThreads = 32 * (2 + kGrpEpiWarps);  // warp 0 TMA, warp 1 MMA + TMEM, 2.. epilogue
 constexpr int kGrpStages = 4;
 constexpr int kGrpABytes = 128 * 128;
 constexpr int kGrpBBytes = 256 * 128;
@@ -49,7 +50,7 @@ struct GrpParams {
 };
 
 __host__ __device__ constexpr size_t grp_smem_bytes() {
-  return 1024 + (size_t)kGrpStages * kGrpStageBytes + 256 + 128 * 2 * 4;
+  return 1024 + (size_t)kGrpStages * kGrpStageBytes + 256 + 128 * 4 * 4;
 }
 
 template <bool GATEUP>
@@ -66,7 +67,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
   uint64_t* accf = bars + 2 * kGrpStages;     // [2]
   uint64_t* acce = bars + 2 * kGrpStages + 2; // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kGrpStages + 4);
-  float* red = reinterpret_cast<float*>(base + kGrpStages * kGrpStageBytes + 256);  // [128][2]
+  float* red = reinterpret_cast<float*>(base + kGrpStages * kGrpStageBytes + 256);  // [128][4]
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   if (warp == 0 && lane == 0) {
@@ -78,7 +79,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&accf[b], 1);
-      tc::mbar_init(&acce[b], 8);
+      tc::mbar_init(&acce[b], kGrpEpiWarps);
     }
     tc::fence_mbar_init();
   }
@@ -147,11 +148,14 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
       }
     }
   } else {
-    const int q = warp & 3;            // TMEM lane quadrant (hardware: warp % 4)
-    const int hc = (warp - 2) >> 2;    // which half of the 256 accumulator columns
+    // epilogue: thread = (accumulator row, quarter cq of the 256 columns): gate/up holds 32
+    // gate + 32 up chains (act columns cq*32 .. +32), down holds 64 output columns
+    const int q = warp & 3;               // TMEM lane quadrant (hardware: warp % 4)
+    const int cq = (warp - 2) >> 2;       // column quarter
     const int row = q * 32 + lane;
-    // every epilogue warp walks every unit (the named barriers below need all 8); after
-    // a wait has run out the remaining waits are skipped, so the kernel still ends
+    constexpr int kEpiThreads = 32 * kGrpEpiWarps;
+    // every epilogue warp walks every unit (the named barriers below need all of them);
+    // after a wait has run out the remaining waits are skipped, so the kernel still ends
     int it = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
       const int nb = u % p.nnb;
@@ -159,58 +163,69 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
       const int e = tl.expert, row0 = tl.row0;
       const bool live = row < tl.nrows;
       const float* sarow = p.a_scale + (size_t)(row0 + (live ? row : 0)) * nkb;
-      if (GATEUP) {
-        const float* swg = p.w_scale + ((size_t)e * (2 * p.I / 128) + nb) * nkb;
-        const float* swu = p.w_scale + ((size_t)e * (2 * p.I / 128) + p.I / 128 + nb) * nkb;
-        uint64_t g2[32], u2[32];  // 64 gate and 64 up running chains, packed in pairs
+      // weight-block scales of this thread's columns: gate/up -> (gate block, up block),
+      // down -> the 128-row block of w2 (nb*2 + cq/2) for both
+      const float* sw0 = GATEUP ? p.w_scale + ((size_t)e * (2 * p.I / 128) + nb) * nkb
+                                : p.w_scale + ((size_t)e * (p.H / 128) + nb * 2 + (cq >> 1)) * nkb;
+      const float* sw1 = GATEUP ? p.w_scale + ((size_t)e * (2 * p.I / 128) + p.I / 128 + nb) * nkb : sw0;
+      // column offsets of the two 32-column runs this thread reads per K block
+      const uint32_t c0 = GATEUP ? cq * 32 : cq * 64;
+      const uint32_t c1 = GATEUP ? 128 + cq * 32 : cq * 64 + 32;
+      uint64_t acc[32];  // 64 running chains, packed in pairs: [0,16) run 0, [16,32) run 1
 #pragma unroll
-        for (int c = 0; c < 32; ++c) { g2[c] = 0; u2[c] = 0; }
-        for (int i = 0; i < nkb; ++i, ++it) {
-          const int buf = it & 1;
-          if (ok && !tc::mbar_wait(&accf[buf], (it >> 1) & 1)) ok = false;
-          tc::fence_after_sync();
-          const float a = live ? sarow[i] : 0.0f;
-          const float scg = __fmul_rn(a, swg[i]), scu = __fmul_rn(a, swu[i]);
-          const uint64_t scg2 = tc::f2pack(__float_as_uint(scg), __float_as_uint(scg));
-          const uint64_t scu2 = tc::f2pack(__float_as_uint(scu), __float_as_uint(scu));
-          const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + buf * 256 + hc * 64;
-          uint32_t P[32];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            tc::tmem_ld32u(ta + h * 32, P);  // gate columns
-#pragma unroll
-            for (int c = 0; c < 16; ++c)
-              g2[h * 16 + c] = tc::f2add(g2[h * 16 + c], tc::f2mul(tc::f2pack(P[2 * c], P[2 * c + 1]), scg2));
-            tc::tmem_ld32u(ta + 128 + h * 32, P);  // up columns
-#pragma unroll
-            for (int c = 0; c < 16; ++c)
-              u2[h * 16 + c] = tc::f2add(u2[h * 16 + c], tc::f2mul(tc::f2pack(P[2 * c], P[2 * c + 1]), scu2));
-          }
-          tc::fence_before_sync();
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&acce[buf]);
+      for (int c = 0; c < 32; ++c) acc[c] = 0;
+      float a_n = live ? sarow[0] : 0.0f, s0_n = sw0[0], s1_n = sw1[0];  // scales of block i
+      for (int i = 0; i < nkb; ++i, ++it) {
+        const float a = a_n, s0 = s0_n, s1 = s1_n;
+        if (i + 1 < nkb) {  // prefetch the next block's scales
+          a_n = live ? sarow[i + 1] : 0.0f;
+          s0_n = sw0[i + 1];
+          s1_n = sw1[i + 1];
         }
-        // act = silu(g) * u; row amax over the 128 columns of this output block
-        float act[64];
+        const int buf = it & 1;
+        if (ok && !tc::mbar_wait(&accf[buf], (it >> 1) & 1)) ok = false;
+        tc::fence_after_sync();
+        const float sc0 = __fmul_rn(a, s0), sc1 = __fmul_rn(a, s1);
+        const uint64_t sc0_2 = tc::f2pack(__float_as_uint(sc0), __float_as_uint(sc0));
+        const uint64_t sc1_2 = tc::f2pack(__float_as_uint(sc1), __float_as_uint(sc1));
+        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + buf * 256;
+        uint32_t P[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          tc::tmem_ld16x2u(ta + c0 + h * 16, ta + c1 + h * 16, P);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            acc[h * 8 + c] = tc::f2add(acc[h * 8 + c], tc::f2mul(tc::f2pack(P[2 * c], P[2 * c + 1]), sc0_2));
+            acc[16 + h * 8 + c] =
+                tc::f2add(acc[16 + h * 8 + c], tc::f2mul(tc::f2pack(P[16 + 2 * c], P[16 + 2 * c + 1]), sc1_2));
+          }
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&acce[buf]);
+      }
+      if (GATEUP) {
+        // act = silu(g) * u for 32 columns; row amax over the 128 columns of the block
+        float act[32];
         float amax = 0.0f;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
+        for (int c = 0; c < 16; ++c) {
           float g0, g1, u0, u1;
-          tc::f2unpack(g2[c], g0, g1);
-          tc::f2unpack(u2[c], u0, u1);
+          tc::f2unpack(acc[c], g0, g1);
+          tc::f2unpack(acc[16 + c], u0, u1);
           act[2 * c] = silu_mul(g0, u0);
           act[2 * c + 1] = silu_mul(g1, u1);
           amax = fmaxf(amax, fmaxf(fabsf(act[2 * c]), fabsf(act[2 * c + 1])));
         }
-        red[row * 2 + hc] = amax;
-        tc::named_bar(1, 256);
-        amax = fmaxf(red[row * 2], red[row * 2 + 1]);
-        tc::named_bar(1, 256);  // red is rewritten by the next unit
+        red[row * 4 + cq] = amax;
+        tc::named_bar(1, kEpiThreads);
+        amax = fmaxf(fmaxf(red[row * 4], red[row * 4 + 1]), fmaxf(red[row * 4 + 2], red[row * 4 + 3]));
+        tc::named_bar(1, kEpiThreads);  // red is rewritten by the next unit
         const float s2 = quant_scale(amax);
         if (live) {
-          uint8_t* dst = p.act_out + (size_t)(row0 + row) * p.I + nb * 128 + hc * 64;
+          uint8_t* dst = p.act_out + (size_t)(row0 + row) * p.I + nb * 128 + cq * 32;
 #pragma unroll
-          for (int c16 = 0; c16 < 4; ++c16) {
+          for (int c16 = 0; c16 < 2; ++c16) {
             uint32_t w4[4];
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
@@ -221,42 +236,16 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
             }
             reinterpret_cast<uint4*>(dst)[c16] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
-          if (hc == 0) p.act_scale_out[(size_t)(row0 + row) * (p.I / 128) + nb] = s2;
+          if (cq == 0) p.act_scale_out[(size_t)(row0 + row) * (p.I / 128) + nb] = s2;
         }
-      } else {
-        const int hblk = nb * 2 + hc;  // 128-row block of w2 this thread's columns belong to
-        const float* sw = p.w_scale + ((size_t)e * (p.H / 128) + hblk) * nkb;
-        uint64_t y2[64];  // 128 running chains, packed in pairs
+      } else if (live) {
+        float4* dst = reinterpret_cast<float4*>(p.y_out + (size_t)(row0 + row) * p.H + nb * 256 + cq * 64);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) y2[c] = 0;
-        for (int i = 0; i < nkb; ++i, ++it) {
-          const int buf = it & 1;
-          if (ok && !tc::mbar_wait(&accf[buf], (it >> 1) & 1)) ok = false;
-          tc::fence_after_sync();
-          const float sc = __fmul_rn(live ? sarow[i] : 0.0f, sw[i]);
-          const uint64_t sc2 = tc::f2pack(__float_as_uint(sc), __float_as_uint(sc));
-          const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + buf * 256 + hc * 128;
-          uint32_t P[32];
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            tc::tmem_ld32u(ta + h * 32, P);
-#pragma unroll
-            for (int c = 0; c < 16; ++c)
-              y2[h * 16 + c] = tc::f2add(y2[h * 16 + c], tc::f2mul(tc::f2pack(P[2 * c], P[2 * c + 1]), sc2));
-          }
-          tc::fence_before_sync();
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&acce[buf]);
-        }
-        if (live) {
-          float4* dst = reinterpret_cast<float4*>(p.y_out + (size_t)(row0 + row) * p.H + hblk * 128);
-#pragma unroll
-          for (int c4 = 0; c4 < 32; ++c4) {
-            float a0, a1, a2, a3;
-            tc::f2unpack(y2[2 * c4], a0, a1);
-            tc::f2unpack(y2[2 * c4 + 1], a2, a3);
-            dst[c4] = make_float4(a0, a1, a2, a3);
-          }
+        for (int c4 = 0; c4 < 16; ++c4) {
+          float a0, a1, a2, a3;
+          tc::f2unpack(acc[2 * c4], a0, a1);
+          tc::f2unpack(acc[2 * c4 + 1], a2, a3);
+          dst[c4] = make_float4(a0, a1, a2, a3);
         }
       }
     }
