@@ -12,10 +12,12 @@
 // block followed by the matching 128 up rows, for down 256 rows of w2. Per 128-wide K block
 // the TMA warp loads A (16 KB) and B (32 KB) into a four-stage ring (128-byte swizzle), the
 // MMA warp issues four 128x256x32 FP8 MMAs into a fresh accumulator (double-buffered:
-// 2 x 256 TMEM columns), and eight epilogue warps promote the block sum into FP32 chains
-// (packed FP32x2 multiply, then add: bit-identical to the scalar operations),
-//   acc = acc + P_kb * (sa[row][kb] * sw[block][kb])     kb ascending, from 0,
-// thread = (accumulator row, half of the 256 columns); a thread holds 128 running chains.
+// per K block: two 128x128x32 halves into four 128-column TMEM buffers, so the tensor
+// core runs up to two K blocks ahead of the epilogue), and sixteen epilogue warps promote
+// the block sums into FP32 chains
+//   acc = fma(P_kb, sa[row][kb] * sw[block][kb], acc)     kb ascending, from 0,
+// (one rounding per step: the multiply-add is fused here, which the parity window covers);
+// thread = (accumulator row, 64 of the 256 columns).
 // gate/up epilogue: act = silu(g) * u for the thread's 64 columns, the row's amax over 128
 // columns (the partner warp's half via shared memory), scale = amax/448, RNE saturating
 // E4M3 codes -> act [row][I] and act_scale [row][I/128]. down epilogue: y [row][H] FP32.
@@ -64,9 +66,9 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + kGrpStages * kGrpStageBytes);
   uint64_t* full = bars;                      // [kGrpStages]
   uint64_t* empty = bars + kGrpStages;        // [kGrpStages]
-  uint64_t* accf = bars + 2 * kGrpStages;     // [2]
-  uint64_t* acce = bars + 2 * kGrpStages + 2; // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kGrpStages + 4);
+  uint64_t* accf = bars + 2 * kGrpStages;     // [4]
+  uint64_t* acce = bars + 2 * kGrpStages + 4; // [4]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kGrpStages + 8);
   float* red = reinterpret_cast<float*>(base + kGrpStages * kGrpStageBytes + 256);  // [128][4]
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
@@ -77,9 +79,9 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 4; ++b) {
       tc::mbar_init(&accf[b], 1);
-      tc::mbar_init(&acce[b], kGrpEpiWarps);
+      tc::mbar_init(&acce[b], kGrpEpiWarps / 2);
     }
     tc::fence_mbar_init();
   }
@@ -109,8 +111,11 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const int nb = u % p.nnb;
         const Tile tl = p.tiles[u / p.nnb];
-        const int yb0 = GATEUP ? tl.expert * 2 * p.I + nb * 128 : tl.expert * p.H + nb * 256;
-        const int yb1 = GATEUP ? tl.expert * 2 * p.I + p.I + nb * 128 : yb0 + 128;
+        // B rows in shared memory: gate/up [gate 0-63 | up 0-63 | gate 64-127 | up 64-127]
+        // of the output block (each 128-row half = matching gate and up rows), down
+        // [w2 rows nb*256 .. +128 | +128 .. +256]
+        const int yg = tl.expert * 2 * p.I + nb * 128, yu = yg + p.I;
+        const int yd = tl.expert * p.H + nb * 256;
         for (int i = 0; i < nkb; ++i, ++it) {
           const int s = it % kGrpStages;
           const uint32_t ph = (it / kGrpStages) & 1;
@@ -119,40 +124,58 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
           tc::mbar_arrive_expect_tx(&full[s], kGrpStageBytes);
           const int x = i * 128;
           tc::tma_load_2d(st, &tmA, &full[s], x, tl.row0);
-          tc::tma_load_2d(st + kGrpABytes, &tmB, &full[s], x, yb0);
-          tc::tma_load_2d(st + kGrpABytes + 128 * 128, &tmB, &full[s], x, yb1);
+          if (GATEUP) {
+            tc::tma_load_2d(st + kGrpABytes, &tmB, &full[s], x, yg);
+            tc::tma_load_2d(st + kGrpABytes + 64 * 128, &tmB, &full[s], x, yu);
+            tc::tma_load_2d(st + kGrpABytes + 128 * 128, &tmB, &full[s], x, yg + 64);
+            tc::tma_load_2d(st + kGrpABytes + 192 * 128, &tmB, &full[s], x, yu + 64);
+          } else {
+            tc::tma_load_2d(st + kGrpABytes, &tmB, &full[s], x, yd);
+            tc::tma_load_2d(st + kGrpABytes + 128 * 128, &tmB, &full[s], x, yd + 128);
+          }
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = tc::idesc_e4m3(128, 256);
+      // per K block two 128x128 halves into TMEM buffers (2*it + h) % 4 (128 columns each),
+      // so the MMAs run up to two K blocks ahead of the epilogue
+      constexpr uint32_t idesc = tc::idesc_e4m3(128, 128);
       int it = 0;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         for (int i = 0; i < nkb; ++i, ++it) {
           const int s = it % kGrpStages;
           const uint32_t ph = (it / kGrpStages) & 1;
-          const int buf = it & 1;
           if (!tc::mbar_wait(&full[s], ph)) { ok = false; break; }
-          if (!tc::mbar_wait(&acce[buf], ((it >> 1) & 1) ^ 1)) { ok = false; break; }
-          tc::fence_after_sync();
           const uint32_t sa = tc::smem_u32(stages + s * kGrpStageBytes);
           const uint64_t da = tc::sdesc_sw128(sa);
-          const uint64_t db = tc::sdesc_sw128(sa + kGrpABytes);
-          const uint32_t d = tmem + buf * 256;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) tc::mma_e4m3(d, da + 2 * k, db + 2 * k, idesc, k > 0);
+          for (int h = 0; h < 2; ++h) {
+            const int slot = 2 * it + h;
+            const int buf = slot & 3;
+            if (!tc::mbar_wait(&acce[buf], ((slot >> 2) & 1) ^ 1)) { ok = false; break; }
+            tc::fence_after_sync();
+            const uint64_t db = tc::sdesc_sw128(sa + kGrpABytes + h * 128 * 128);
+            const uint32_t d = tmem + buf * 128;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) tc::mma_e4m3(d, da + 2 * k, db + 2 * k, idesc, k > 0);
+            tc::mma_commit(&accf[buf]);
+          }
+          if (!ok) break;
           tc::mma_commit(&empty[s]);
-          tc::mma_commit(&accf[buf]);
         }
       }
     }
   } else {
-    // epilogue: thread = (accumulator row, quarter cq of the 256 columns): gate/up holds 32
-    // gate + 32 up chains (act columns cq*32 .. +32), down holds 64 output columns
+    // epilogue: 8 warps per MMA half hh; thread = (accumulator row, 64 of the half's 128
+    // columns): gate/up -> 32 gate + 32 up chains (act columns hh*64 + sub*32 .. +32),
+    // down -> 64 output columns of w2 block nb*2 + hh
     const int q = warp & 3;               // TMEM lane quadrant (hardware: warp % 4)
-    const int cq = (warp - 2) >> 2;       // column quarter
+    const int ew = warp - 2;
+    const int hh = ew >> 3;               // MMA half
+    const int sub = (ew >> 2) & 1;        // which 64 of the half's 128 columns
     const int row = q * 32 + lane;
+    const int slot4 = hh * 2 + sub;       // column quarter of the row's 256 outputs
     constexpr int kEpiThreads = 32 * kGrpEpiWarps;
     // every epilogue warp walks every unit (the named barriers below need all of them);
     // after a wait has run out the remaining waits are skipped, so the kernel still ends
@@ -163,17 +186,15 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
       const int e = tl.expert, row0 = tl.row0;
       const bool live = row < tl.nrows;
       const float* sarow = p.a_scale + (size_t)(row0 + (live ? row : 0)) * nkb;
-      // weight-block scales of this thread's columns: gate/up -> (gate block, up block),
-      // down -> the 128-row block of w2 (nb*2 + cq/2) for both
       const float* sw0 = GATEUP ? p.w_scale + ((size_t)e * (2 * p.I / 128) + nb) * nkb
-                                : p.w_scale + ((size_t)e * (p.H / 128) + nb * 2 + (cq >> 1)) * nkb;
+                                : p.w_scale + ((size_t)e * (p.H / 128) + nb * 2 + hh) * nkb;
       const float* sw1 = GATEUP ? p.w_scale + ((size_t)e * (2 * p.I / 128) + p.I / 128 + nb) * nkb : sw0;
-      // column offsets of the two 32-column runs this thread reads per K block
-      const uint32_t c0 = GATEUP ? cq * 32 : cq * 64;
-      const uint32_t c1 = GATEUP ? 128 + cq * 32 : cq * 64 + 32;
-      uint64_t acc[32];  // 64 running chains, packed in pairs: [0,16) run 0, [16,32) run 1
+      // within the half's 128 accumulator columns: gate/up [gate 64 | up 64], down [128]
+      const uint32_t c0 = GATEUP ? sub * 32 : sub * 64;
+      const uint32_t c1 = GATEUP ? 64 + sub * 32 : sub * 64 + 32;
+      float acc[64];  // [0,32) run at c0, [32,64) run at c1
 #pragma unroll
-      for (int c = 0; c < 32; ++c) acc[c] = 0;
+      for (int c = 0; c < 64; ++c) acc[c] = 0.0f;
       float a_n = live ? sarow[0] : 0.0f, s0_n = sw0[0], s1_n = sw1[0];  // scales of block i
       for (int i = 0; i < nkb; ++i, ++it) {
         const float a = a_n, s0 = s0_n, s1 = s1_n;
@@ -182,22 +203,20 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
           s0_n = sw0[i + 1];
           s1_n = sw1[i + 1];
         }
-        const int buf = it & 1;
-        if (ok && !tc::mbar_wait(&accf[buf], (it >> 1) & 1)) ok = false;
+        const int slot = 2 * it + hh;
+        const int buf = slot & 3;
+        if (ok && !tc::mbar_wait(&accf[buf], (slot >> 2) & 1)) ok = false;
         tc::fence_after_sync();
         const float sc0 = __fmul_rn(a, s0), sc1 = __fmul_rn(a, s1);
-        const uint64_t sc0_2 = tc::f2pack(__float_as_uint(sc0), __float_as_uint(sc0));
-        const uint64_t sc1_2 = tc::f2pack(__float_as_uint(sc1), __float_as_uint(sc1));
-        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + buf * 256;
+        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + buf * 128;
         uint32_t P[32];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           tc::tmem_ld16x2u(ta + c0 + h * 16, ta + c1 + h * 16, P);
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            acc[h * 8 + c] = tc::f2add(acc[h * 8 + c], tc::f2mul(tc::f2pack(P[2 * c], P[2 * c + 1]), sc0_2));
-            acc[16 + h * 8 + c] =
-                tc::f2add(acc[16 + h * 8 + c], tc::f2mul(tc::f2pack(P[16 + 2 * c], P[16 + 2 * c + 1]), sc1_2));
+          for (int c = 0; c < 16; ++c) {
+            acc[h * 16 + c] = __fmaf_rn(__uint_as_float(P[c]), sc0, acc[h * 16 + c]);
+            acc[32 + h * 16 + c] = __fmaf_rn(__uint_as_float(P[16 + c]), sc1, acc[32 + h * 16 + c]);
           }
         }
         tc::fence_before_sync();
@@ -209,21 +228,17 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
         float act[32];
         float amax = 0.0f;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          float g0, g1, u0, u1;
-          tc::f2unpack(acc[c], g0, g1);
-          tc::f2unpack(acc[16 + c], u0, u1);
-          act[2 * c] = silu_mul(g0, u0);
-          act[2 * c + 1] = silu_mul(g1, u1);
-          amax = fmaxf(amax, fmaxf(fabsf(act[2 * c]), fabsf(act[2 * c + 1])));
+        for (int c = 0; c < 32; ++c) {
+          act[c] = silu_mul(acc[c], acc[32 + c]);
+          amax = fmaxf(amax, fabsf(act[c]));
         }
-        red[row * 4 + cq] = amax;
+        red[row * 4 + slot4] = amax;
         tc::named_bar(1, kEpiThreads);
         amax = fmaxf(fmaxf(red[row * 4], red[row * 4 + 1]), fmaxf(red[row * 4 + 2], red[row * 4 + 3]));
         tc::named_bar(1, kEpiThreads);  // red is rewritten by the next unit
         const float s2 = quant_scale(amax);
         if (live) {
-          uint8_t* dst = p.act_out + (size_t)(row0 + row) * p.I + nb * 128 + cq * 32;
+          uint8_t* dst = p.act_out + (size_t)(row0 + row) * p.I + nb * 128 + slot4 * 32;
 #pragma unroll
           for (int c16 = 0; c16 < 2; ++c16) {
             uint32_t w4[4];
@@ -236,17 +251,13 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
             }
             reinterpret_cast<uint4*>(dst)[c16] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
-          if (cq == 0) p.act_scale_out[(size_t)(row0 + row) * (p.I / 128) + nb] = s2;
+          if (slot4 == 0) p.act_scale_out[(size_t)(row0 + row) * (p.I / 128) + nb] = s2;
         }
       } else if (live) {
-        float4* dst = reinterpret_cast<float4*>(p.y_out + (size_t)(row0 + row) * p.H + nb * 256 + cq * 64);
+        float4* dst = reinterpret_cast<float4*>(p.y_out + (size_t)(row0 + row) * p.H + nb * 256 + slot4 * 64);
 #pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4) {
-          float a0, a1, a2, a3;
-          tc::f2unpack(acc[2 * c4], a0, a1);
-          tc::f2unpack(acc[2 * c4 + 1], a2, a3);
-          dst[c4] = make_float4(a0, a1, a2, a3);
-        }
+        for (int c4 = 0; c4 < 16; ++c4)
+          dst[c4] = make_float4(acc[4 * c4], acc[4 * c4 + 1], acc[4 * c4 + 2], acc[4 * c4 + 3]);
       }
     }
   }
@@ -298,7 +309,8 @@ cudaError_t launch_grouped_gateup(const uint8_t* w13, const float* s13, int64_t 
                                   int64_t max_tiles, const WsPtrs& ws, cudaStream_t st) {
   CUtensorMap tA, tB;
   if (!make_tmap_u8(&tA, ws.xp, (uint64_t)H, (uint64_t)R, 128)) return cudaErrorInvalidValue;
-  if (!make_tmap_u8(&tB, w13, (uint64_t)H, (uint64_t)E * 2 * I, 128)) return cudaErrorInvalidValue;
+  // 64-row boxes: each K-block stage holds gate/up rows interleaved in groups of 64
+  if (!make_tmap_u8(&tB, w13, (uint64_t)H, (uint64_t)E * 2 * I, 64)) return cudaErrorInvalidValue;
   GrpParams prm{};
   prm.H = H; prm.I = I; prm.E = E;
   prm.nkb = H / 128;
