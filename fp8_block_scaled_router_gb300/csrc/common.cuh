@@ -130,6 +130,12 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
   return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
 }
 
+// silu(g) * u with one correctly rounded reciprocal instead of a division (within one
+// ulp of silu_mul; used where the epilogue's instruction count bounds the GEMM)
+__device__ __forceinline__ float silu_mul_rcp(float g, float u) {
+  return __fmul_rn(__fmul_rn(g, __frcp_rn(__fadd_rn(1.0f, expf(-g)))), u);
+}
+
 __device__ __forceinline__ void set_status(Header* hdr, uint32_t bits) {
   atomicOr(&hdr->status, bits);  // a flag word, never a value accumulation
 }

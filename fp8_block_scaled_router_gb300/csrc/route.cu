@@ -171,6 +171,163 @@ __global__ void __launch_bounds__(kRouteThreads)
   }
 }
 
+// ---------------------------------------------------------------------------------------
+// Many tokens: one CTA per block of kBigTB tokens covers all E experts over the whole hidden
+// dimension, so every logit's chunk chains and their ascending chunk sum stay inside one
+// thread. The router's 128-row chunks (128 * E * 2 contiguous bytes) stream through a
+// two-slot shared-memory ring with bulk asynchronous copies; thread (e, token group) holds
+// kBigTB/2 chain accumulators and the running logits of its tokens.
+// ---------------------------------------------------------------------------------------
+constexpr int kBigTB = 16;
+
+__host__ __device__ inline size_t route_big_smem(int E) {
+  return 16 + (size_t)2 * 128 * E * 2 + (size_t)2 * 128 * kBigTB * 2 + (size_t)kBigTB * E * 4 +
+         (size_t)kBigTB * 16 * 8 + 64;
+}
+
+__global__ void __launch_bounds__(256)
+    route_big_kernel(const uint16_t* __restrict__ hidden, const uint16_t* __restrict__ router_w,
+                     const float* __restrict__ bias, int M, int H, int E, int K, int renorm,
+                     int32_t* __restrict__ ids, float* __restrict__ wts) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem);                 // [2] ring barriers
+  uint16_t* wring = reinterpret_cast<uint16_t*>(smem + 16);          // [2][128][E]
+  uint16_t* xring = wring + (size_t)2 * 128 * E;                     // [2][128][kBigTB]
+  float* logits = reinterpret_cast<float*>(xring + (size_t)2 * 128 * kBigTB);  // [kBigTB][E]
+  float* sel_v = logits + kBigTB * E;                                // [kBigTB][16]
+  int* sel_i = reinterpret_cast<int*>(sel_v + kBigTB * 16);          // [kBigTB][16]
+  const int tid = threadIdx.x;
+  const int tok0 = blockIdx.x * kBigTB;
+  const int nchunks = H / 128;
+  const uint32_t wbytes = 128u * (uint32_t)E * 2u;
+
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (tid == 0) {
+    for (int b = 0; b < 2; ++b)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"((uint32_t)__cvta_generic_to_shared(&bar[b])));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  auto issue = [&](int c) {  // router chunk c -> slot c & 1 (thread 0)
+    const uint32_t b = (uint32_t)__cvta_generic_to_shared(&bar[c & 1]);
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(wring + (size_t)(c & 1) * 128 * E);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(wbytes) : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(d),
+                 "l"(router_w + (size_t)c * 128 * E), "r"(wbytes), "r"(b)
+                 : "memory");
+  };
+  if (tid == 0) {
+    issue(0);
+    if (nchunks > 1) issue(1);
+  }
+  // thread <-> expert e, token group g (tokens g*8 .. g*8+7)
+  const int e = tid % E, g = tid / E;
+  const int ngroups = 256 / E;  // >= 2 for E <= 128
+  constexpr int kTPG = kBigTB / 2;
+  float logit[kTPG];
+#pragma unroll
+  for (int t = 0; t < kTPG; ++t) logit[t] = 0.0f;
+  bool ok = true;
+  for (int c = 0; c < nchunks; ++c) {
+    // this chunk's hidden values, token-minor: xring[slot][k][t]
+    uint16_t* xs = xring + (size_t)(c & 1) * 128 * kBigTB;
+    for (int i = tid; i < 128 * kBigTB; i += 256) {
+      const int t = i / 128, k = i % 128;
+      xs[k * kBigTB + t] = tok0 + t < M ? hidden[(size_t)(tok0 + t) * H + c * 128 + k] : (uint16_t)0;
+    }
+    __syncthreads();
+    {  // bounded wait for the router chunk
+      const uint32_t b = (uint32_t)__cvta_generic_to_shared(&bar[c & 1]);
+      const uint32_t par = (c >> 1) & 1;
+      uint32_t done = 0;
+      const uint64_t t0 = globaltimer_ns();
+      while (ok) {
+        asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                     : "=r"(done) : "r"(b), "r"(par) : "memory");
+        if (done) break;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) ok = false;
+      }
+    }
+    if (g < 2 && ok) {
+      const uint16_t* wcol = wring + (size_t)(c & 1) * 128 * E + e;
+      const uint16_t* xk = xs + g * kTPG;
+      float acc[kTPG];
+#pragma unroll
+      for (int t = 0; t < kTPG; ++t) acc[t] = 0.0f;
+#pragma unroll 8
+      for (int k = 0; k < 128; ++k) {
+        const float w = bf16_bits_to_float(wcol[k * E]);
+        const uint4 q = *reinterpret_cast<const uint4*>(xk + k * kBigTB);
+        const uint32_t xw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int t = 0; t < kTPG; ++t) {
+          const uint16_t xb = (uint16_t)((t & 1) ? (xw[t / 2] >> 16) : (xw[t / 2] & 0xFFFF));
+          acc[t] = __fmaf_rn(bf16_bits_to_float(xb), w, acc[t]);
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kTPG; ++t) logit[t] = __fadd_rn(logit[t], acc[t]);
+    }
+    __syncthreads();  // slot c & 1 is free again
+    if (tid == 0 && c + 2 < nchunks) issue(c + 2);
+  }
+  (void)ngroups;
+  // a router chunk that never arrived (bounded wait ran out): the block's tokens get id -1,
+  // which the expert FFN skips and reports as MOE_STATUS_BAD_EXPERT_ID
+  ok = __syncthreads_and(ok);
+  if (!ok) {
+    for (int i = tid; i < kBigTB * K; i += 256)
+      if (tok0 + i / K < M) {
+        ids[(size_t)tok0 * K + i] = -1;
+        wts[(size_t)tok0 * K + i] = 0.0f;
+      }
+    return;
+  }
+  if (g < 2) {
+#pragma unroll
+    for (int t = 0; t < kTPG; ++t) {
+      float l = logit[t];
+      if (bias != nullptr) l = __fadd_rn(l, bias[e]);
+      logits[(g * kTPG + t) * E + e] = l;
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < kBigTB * E; i += 256) {  // rank selection, ties to the lower index
+    const int t = i / E, ee = i % E;
+    const float* lt = logits + t * E;
+    const float v = lt[ee];
+    int rk = 0;
+    for (int e2 = 0; e2 < E; ++e2) {
+      const float v2 = lt[e2];
+      rk += (v2 > v) || (v2 == v && e2 < ee);
+    }
+    if (rk < K) {
+      sel_v[t * 16 + rk] = v;
+      sel_i[t * 16 + rk] = ee;
+    }
+  }
+  __syncthreads();
+  const int warp = tid / 32, lane = tid % 32;
+  for (int t = warp; t < kBigTB; t += 8) {
+    if (tok0 + t >= M) break;
+    const float lmax = sel_v[t * 16];
+    float den = 0.0f;
+    if (renorm) {
+      for (int j = 0; j < K; ++j) den = __fadd_rn(den, expf(__fsub_rn(sel_v[t * 16 + j], lmax)));
+    } else {
+      for (int ee = lane; ee < E; ee += 32) den = __fadd_rn(den, expf(__fsub_rn(logits[t * E + ee], lmax)));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) den = __fadd_rn(den, __shfl_xor_sync(0xffffffffu, den, off));
+    }
+    if (lane < K) {
+      const size_t o = (size_t)(tok0 + t) * K + lane;
+      ids[o] = sel_i[t * 16 + lane];
+      wts[o] = __fdiv_rn(expf(__fsub_rn(sel_v[t * 16 + lane], lmax)), den);
+    }
+  }
+}
+
 namespace {
 
 // CL CTAs per cluster (<= 16, a divisor of the chunk count): one 128-row chunk per CTA
@@ -217,6 +374,23 @@ cudaError_t launch_route_t(const uint16_t* hidden, const uint16_t* router_w, con
 cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const float* bias, int M,
                          int H, int E, int K, int renorm, int32_t* ids, float* wts, cudaStream_t st) {
   const int nchunks = H / 128;
+  if (M >= 512 && E <= 128) {
+    static std::once_flag once;
+    std::call_once(once, [] {
+      cudaFuncSetAttribute(route_big_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    });
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((M + kBigTB - 1) / kBigTB), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = route_big_smem(E);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, route_big_kernel, hidden, router_w, bias, M, H, E, K, renorm, ids, wts);
+  }
   if (M >= 16 && route_smem(8, nchunks / route_cluster(nchunks), E, nchunks).total <= 227 * 1024)
     return launch_route_t<8>(hidden, router_w, bias, M, H, E, K, renorm, ids, wts, st);
   if (M >= 4 && route_smem(2, nchunks / route_cluster(nchunks), E, nchunks).total <= 227 * 1024)
