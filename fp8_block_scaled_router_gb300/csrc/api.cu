@@ -15,7 +15,8 @@ cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const
                          int H, int E, int K, int renorm, int32_t* ids, float* wts, cudaStream_t st);
 cudaError_t launch_prep(const uint16_t* hidden, const int32_t* ids, int M, int H, int E, int K,
                         const WsPtrs& ws, cudaStream_t st);
-cudaError_t launch_gather(int R, int H, int E, int K, const WsPtrs& ws, cudaStream_t st);
+cudaError_t launch_sort_gather(const uint16_t* hidden, const int32_t* ids, int M, int H, int E, int K,
+                               const WsPtrs& ws, cudaStream_t st);
 cudaError_t launch_grouped_gateup(const uint8_t* w13, const float* s13, int64_t R, int H, int I, int E,
                                   int64_t max_tiles, const WsPtrs& ws, cudaStream_t st);
 cudaError_t launch_grouped_down(const uint8_t* w2, const float* s2w, int64_t R, int H, int I, int E,
@@ -109,11 +110,11 @@ moe_status_t moe_fp8_prepare(const void* hidden, const int32_t* topk_ids, int32_
   if (M == 0) return MOE_OK;
   const WsPtrs ws = ws_ptrs(workspace, L);
   const int64_t R = (int64_t)M * shape->top_k;
-  if (cudaError_t e = launch_prep(static_cast<const uint16_t*>(hidden), topk_ids, M, shape->hidden,
-                                  shape->num_experts, shape->top_k, ws, stream))
-    return launched(e);
-  if (use_pair_mode(R)) return MOE_OK;
-  return launched(launch_gather((int)R, shape->hidden, shape->num_experts, shape->top_k, ws, stream));
+  if (use_pair_mode(R))
+    return launched(launch_prep(static_cast<const uint16_t*>(hidden), topk_ids, M, shape->hidden,
+                                shape->num_experts, shape->top_k, ws, stream));
+  return launched(launch_sort_gather(static_cast<const uint16_t*>(hidden), topk_ids, M, shape->hidden,
+                                     shape->num_experts, shape->top_k, ws, stream));
 }
 
 moe_status_t moe_fp8_gate_up(const uint8_t* w13, const float* w13_scale, int32_t M,

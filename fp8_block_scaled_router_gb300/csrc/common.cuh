@@ -31,7 +31,7 @@ struct Tile {               // a run of up to `tile_rows` expert-sorted rows of 
 };
 
 struct Layout {
-  size_t header, qa, sa, offsets, row_src, perm_row, pair_expert, tiles, xp, sa_p, act, act_scale, y, total;
+  size_t header, qa, sa, offsets, row_src, perm_row, pair_expert, blk_counts, tiles, xp, sa_p, act, act_scale, y, total;
   int64_t R, max_tiles;
 };
 
@@ -39,6 +39,9 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Routed rows per tile of the grouped GEMMs (the MMA's M).
 constexpr int kTileRows = 128;
+
+// Routed pairs per block of the multi-block counting sort.
+constexpr int kSortBlock = 256;
 
 // Up to this many routed rows (M*K) every (token, slot) pair is its own GEMM unit ("pair
 // mode": no sort, weights of an expert chosen by several pairs are re-read from L2);
@@ -64,6 +67,7 @@ inline Layout make_layout(const moe_fp8_shape_t& s) {
   L.row_src = o;   o = align256(o + (size_t)L.R * 4);
   L.perm_row = o;  o = align256(o + (size_t)L.R * 4);
   L.pair_expert = o; o = align256(o + (size_t)L.R * 4);
+  L.blk_counts = o; o = align256(o + (size_t)((L.R + kSortBlock - 1) / kSortBlock) * E * 4);
   L.tiles = o;     o = align256(o + (size_t)L.max_tiles * sizeof(Tile));
   L.xp = o;        o = align256(o + (size_t)(L.R * H));
   L.sa_p = o;      o = align256(o + (size_t)(L.R * (H / kBlock)) * 4);
@@ -83,6 +87,7 @@ struct WsPtrs {
   int32_t* row_src;
   int32_t* perm_row;
   int32_t* pair_expert;  // [R] expert of each routed pair, -1 if skipped (pair mode)
+  int32_t* blk_counts;   // [R/kSortBlock][E] per-block expert histograms (sorted mode)
   Tile* tiles;
   uint8_t* xp;      // [R][H] hidden codes gathered into expert-sorted row order
   float* sa_p;      // [R][H/128] their scales
@@ -96,7 +101,8 @@ inline WsPtrs ws_ptrs(void* ws, const Layout& L) {
   return WsPtrs{reinterpret_cast<Header*>(b + L.header), reinterpret_cast<uint8_t*>(b + L.qa),
                 reinterpret_cast<float*>(b + L.sa), reinterpret_cast<int32_t*>(b + L.offsets),
                 reinterpret_cast<int32_t*>(b + L.row_src), reinterpret_cast<int32_t*>(b + L.perm_row),
-                reinterpret_cast<int32_t*>(b + L.pair_expert), reinterpret_cast<Tile*>(b + L.tiles),
+                reinterpret_cast<int32_t*>(b + L.pair_expert), reinterpret_cast<int32_t*>(b + L.blk_counts),
+                reinterpret_cast<Tile*>(b + L.tiles),
                 reinterpret_cast<uint8_t*>(b + L.xp), reinterpret_cast<float*>(b + L.sa_p),
                 reinterpret_cast<uint8_t*>(b + L.act),
                 reinterpret_cast<float*>(b + L.act_scale), reinterpret_cast<float*>(b + L.y)};

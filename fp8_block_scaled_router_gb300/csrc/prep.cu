@@ -5,14 +5,10 @@
 // repository layout (MoE "activation packing"); the per-token-per-128 FP8 activation
 // format of docs/compiler/architecture.md (FP8 activation plus activation-scale tensors).
 //
-// One launch. Block 0 (1024 threads) runs a stable counting sort of the R = M*K (token,
-// slot) pairs by expert: a shared-memory histogram, an exclusive scan, then a scatter in
-// rounds of 1024 pairs where each pair's position is its expert's base + the pairs of the
-// same expert in earlier warps of the round (per-warp counts) + its rank inside its warp
-// (__match_any_sync). Within an expert, rows therefore keep ascending flat pair order
-// t*K + j. It also cuts each expert's rows into tiles of at most kTileRows rows.
-// Blocks 1.. quantise hidden: one warp per (token, 128-column group), amax by a warp max
-// reduction, scale = amax/448, RNE saturating E4M3 codes.
+// Quantisation: one warp per (token, 128-column group), amax by a warp max reduction,
+// scale = amax/448 (IEEE division; 1.0 for an all-zero group), RNE saturating E4M3 codes.
+// Few routed rows (pair mode): block 0 records each pair's expert (-1 if out of range) and
+// the identity permutation. Many routed rows: the two-launch counting sort below.
 #include "common.cuh"
 
 namespace moe {
@@ -22,8 +18,7 @@ constexpr int kMaxExperts = 256;
 
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const uint16_t* __restrict__ hidden,
                                                             const int32_t* __restrict__ ids, int M,
-                                                            int H, int E, int K, int pair_mode,
-                                                            WsPtrs ws) {
+                                                            int H, int E, int K, WsPtrs ws) {
   const int tid = threadIdx.x;
   if (blockIdx.x > 0) {
     // ---- quantise hidden: warp per (token, 128-group) ----
@@ -50,7 +45,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const uint16_t* __re
     return;
   }
 
-  if (pair_mode) {
+  {
     // ---- block 0, pair mode: each routed pair is its own unit (identity permutation) ----
     __shared__ int bad_pair;
     if (tid == 0) bad_pair = 0;
@@ -70,93 +65,157 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const uint16_t* __re
     }
     return;
   }
+}
 
-  // ---- block 0: stable counting sort of the routed pairs by expert ----
-  __shared__ int cnt[kMaxExperts];
-  __shared__ int base[kMaxExperts + 1];
-  __shared__ int tile_base[kMaxExperts + 1];
-  __shared__ int wcnt[kPrepThreads / 32][kMaxExperts];
-  __shared__ int bad;
+// ---------------------------------------------------------------------------------------
+// Many routed rows: a counting sort over blocks of kSortBlock pairs in two launches.
+//   count:   blocks [0, NB) histogram their pairs by expert into blk_counts[b][E]; the
+//            remaining blocks quantise hidden (as above).
+//   scatter: block b forms, for every expert, tot[e] = sum over all blocks and
+//            pre[e] = sum over blocks before b, the exclusive scan base[e] over experts, and
+//            places its pairs at base[e] + pre[e] + (earlier pairs of e in this block), so
+//            rows keep ascending flat pair order t*K + j within each expert; it then gathers
+//            each placed pair's hidden codes and scales into xp / sa_p. Block 0 also writes
+//            the expert offsets and the 128-row tile list.
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) count_quant_kernel(const uint16_t* __restrict__ hidden,
+                                                          const int32_t* __restrict__ ids, int M, int H,
+                                                          int E, int K, int nblk, WsPtrs ws) {
+  const int tid = threadIdx.x;
   const int R = M * K;
-  const int warp = tid / 32, lane = tid % 32;
-  for (int e = tid; e < E; e += kPrepThreads) cnt[e] = 0;
-  if (tid == 0) bad = 0;
-  __syncthreads();
-  for (int i = tid; i < R; i += kPrepThreads) {
-    const int e = ids[i];
-    if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);  // integer count: order-independent
-    else bad = 1;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    // E <= 256: a serial scan is a few hundred cycles, off the critical path of the quant blocks
-    int acc = 0, tacc = 0;
-    for (int e = 0; e < E; ++e) {
-      base[e] = acc;
-      tile_base[e] = tacc;
-      acc += cnt[e];
-      tacc += (cnt[e] + kTileRows - 1) / kTileRows;
-    }
-    base[E] = acc;
-    tile_base[E] = tacc;
-    ws.hdr->n_tiles = (uint32_t)tacc;
-    if (bad) set_status(ws.hdr, MOE_STATUS_BAD_EXPERT_ID);
-  }
-  __syncthreads();
-  for (int e = tid; e <= E; e += kPrepThreads) ws.offsets[e] = base[e];
-  for (int e = tid; e < E; e += kPrepThreads) {
-    const int n = cnt[e];
-    for (int j = 0, tb = tile_base[e]; j < n; j += kTileRows, ++tb)
-      ws.tiles[tb] = Tile{e, base[e] + j, min(kTileRows, n - j), 0};
-  }
-  for (int r0 = 0; r0 < R; r0 += kPrepThreads) {
-    for (int i = tid; i < (kPrepThreads / 32) * E; i += kPrepThreads) wcnt[i / E][i % E] = 0;
+  if ((int)blockIdx.x < nblk) {
+    __shared__ int hist[kMaxExperts];
+    __shared__ int bad;
+    for (int e = tid; e < E; e += 256) hist[e] = 0;
+    if (tid == 0) bad = 0;
     __syncthreads();
-    const int i = r0 + tid;
-    const int e = i < R ? ids[i] : -1;
-    const bool valid = i < R && e >= 0 && e < E;
-    const unsigned mask = __match_any_sync(0xffffffffu, valid ? e : -1);
-    const int rank = __popc(mask & ((1u << lane) - 1u));
-    if (valid && rank == 0) wcnt[warp][e] = __popc(mask);
-    __syncthreads();
+    const int i = blockIdx.x * kSortBlock + tid;
     if (i < R) {
-      if (valid) {
-        int pos = base[e] + rank;
-        for (int w = 0; w < warp; ++w) pos += wcnt[w][e];
-        ws.row_src[pos] = i;
-        ws.perm_row[i] = pos;
-      } else {
-        ws.perm_row[i] = -1;
-      }
+      const int e = ids[i];
+      if (e >= 0 && e < E) atomicAdd(&hist[e], 1);  // integer count: order-independent
+      else bad = 1;
     }
     __syncthreads();
-    for (int e2 = tid; e2 < E; e2 += kPrepThreads) {
-      int s = 0;
-      for (int w = 0; w < kPrepThreads / 32; ++w) s += wcnt[w][e2];
-      base[e2] += s;
-    }
-    __syncthreads();
+    for (int e = tid; e < E; e += 256) ws.blk_counts[(size_t)blockIdx.x * E + e] = hist[e];
+    if (tid == 0 && bad) set_status(ws.hdr, MOE_STATUS_BAD_EXPERT_ID);
+    return;
+  }
+  const int warp = tid / 32, lane = tid % 32;
+  const int ngroups_row = H / 128;
+  const int64_t ngroups = (int64_t)M * ngroups_row;
+  const int64_t nwarps = (int64_t)(gridDim.x - nblk) * 8;
+  for (int64_t gidx = (int64_t)(blockIdx.x - nblk) * 8 + warp; gidx < ngroups; gidx += nwarps) {
+    const int64_t t = gidx / ngroups_row;
+    const int g = (int)(gidx % ngroups_row);
+    const uint2 raw = *reinterpret_cast<const uint2*>(hidden + t * H + g * 128 + lane * 4);
+    const float x0 = bf16_bits_to_float(raw.x & 0xFFFF), x1 = bf16_bits_to_float(raw.x >> 16);
+    const float x2 = bf16_bits_to_float(raw.y & 0xFFFF), x3 = bf16_bits_to_float(raw.y >> 16);
+    float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float s = quant_scale(amax);
+    const uint32_t lo = e4m3x2_encode(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
+    const uint32_t hi = e4m3x2_encode(__fdiv_rn(x2, s), __fdiv_rn(x3, s));
+    *reinterpret_cast<uint32_t*>(ws.qa + t * H + g * 128 + lane * 4) = lo | (hi << 16);
+    if (lane == 0) ws.sa[t * ngroups_row + g] = s;
   }
 }
 
-// Gather the hidden codes and scales of every routed row into expert-sorted order (the A
-// operand rows of the grouped GEMM): xp[r] = qa[row_src[r] / K], sa_p[r] = sa[row_src[r] / K].
-// One warp per sorted row; rows past the valid count (skipped pairs) are left untouched.
-__global__ void __launch_bounds__(256) gather_kernel(int R, int H, int E, int K, WsPtrs ws) {
+__global__ void __launch_bounds__(256) scatter_gather_kernel(const int32_t* __restrict__ ids, int M, int H,
+                                                             int E, int K, int nblk, WsPtrs ws) {
+  __shared__ int start[kMaxExperts];
+  __shared__ int scan[kMaxExperts];
+  __shared__ int wcnt[8][kMaxExperts];
+  __shared__ int pos_s[kSortBlock];
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int R = M * K;
+  const int b = blockIdx.x;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
-  const int r = blockIdx.x * 8 + threadIdx.x / 32, lane = threadIdx.x % 32;
-  if (r >= R || r >= ws.offsets[E]) return;
-  const int t = ws.row_src[r] / K;
-  const uint4* src = reinterpret_cast<const uint4*>(ws.qa + (size_t)t * H);
-  uint4* dst = reinterpret_cast<uint4*>(ws.xp + (size_t)r * H);
-  for (int i = lane; i < H / 16; i += 32) dst[i] = src[i];
-  for (int i = lane; i < H / 128; i += 32) ws.sa_p[(size_t)r * (H / 128) + i] = ws.sa[(size_t)t * (H / 128) + i];
+  // per expert: total over all blocks and the count in blocks before this one
+  int tot = 0, pre = 0;
+  if (tid < E) {
+    for (int bb = 0; bb < nblk; ++bb) {
+      const int c = ws.blk_counts[(size_t)bb * E + tid];
+      tot += c;
+      pre += bb < b ? c : 0;
+    }
+  }
+  // exclusive scan of tot over experts (Hillis-Steele on 256 entries)
+  scan[tid] = tid < E ? tot : 0;
+  __syncthreads();
+  for (int off = 1; off < 256; off <<= 1) {
+    const int v = tid >= off ? scan[tid - off] : 0;
+    __syncthreads();
+    scan[tid] += v;
+    __syncthreads();
+  }
+  const int base_e = tid < E ? scan[tid] - tot : 0;  // exclusive
+  if (tid < E) start[tid] = base_e + pre;
+  if (b == 0) {
+    if (tid < E) ws.offsets[tid] = base_e;
+    if (tid == E - 1) ws.offsets[E] = scan[tid];
+  }
+  // per-warp counts of each expert in this block (stable order: warp, then lane)
+  for (int i = tid; i < 8 * E; i += 256) wcnt[i / E][i % E] = 0;
+  __syncthreads();
+  const int i = b * kSortBlock + tid;
+  const int e = i < R ? ids[i] : -1;
+  const bool valid = i < R && e >= 0 && e < E;
+  const unsigned mask = __match_any_sync(0xffffffffu, valid ? e : -1);
+  const int rank = __popc(mask & ((1u << lane) - 1u));
+  if (valid && rank == 0) wcnt[warp][e] = __popc(mask);
+  __syncthreads();
+  int pos = -1;
+  if (valid) {
+    pos = start[e] + rank;
+    for (int w = 0; w < warp; ++w) pos += wcnt[w][e];
+    ws.row_src[pos] = i;
+  }
+  if (i < R) ws.perm_row[i] = pos;
+  pos_s[tid] = pos;
+  // block 0: the 128-row tile list (expert counts are the totals)
+  if (b == 0) {
+    __syncthreads();
+    const int ntile = tid < E ? (tot + kTileRows - 1) / kTileRows : 0;
+    scan[tid] = ntile;
+    __syncthreads();
+    for (int off = 1; off < 256; off <<= 1) {
+      const int v = tid >= off ? scan[tid - off] : 0;
+      __syncthreads();
+      scan[tid] += v;
+      __syncthreads();
+    }
+    if (tid < E) {
+      int tb = scan[tid] - ntile;
+      for (int j = 0; j < tot; j += kTileRows, ++tb) ws.tiles[tb] = Tile{tid, base_e + j, min(kTileRows, tot - j), 0};
+    }
+    if (tid == 255) ws.hdr->n_tiles = (uint32_t)scan[255];
+  }
+  __syncthreads();
+  // gather: warp w copies the hidden codes (H bytes) and scales of rows w, w+8, ...
+  for (int r = warp; r < kSortBlock; r += 8) {
+    const int p = pos_s[r];
+    if (p < 0) continue;
+    const int t = (b * kSortBlock + r) / K;
+    const uint4* src = reinterpret_cast<const uint4*>(ws.qa + (size_t)t * H);
+    uint4* dst = reinterpret_cast<uint4*>(ws.xp + (size_t)p * H);
+    for (int c = lane; c < H / 16; c += 32) dst[c] = src[c];
+    for (int c = lane; c < H / 128; c += 32) ws.sa_p[(size_t)p * (H / 128) + c] = ws.sa[(size_t)t * (H / 128) + c];
+  }
 }
 
-cudaError_t launch_gather(int R, int H, int E, int K, const WsPtrs& ws, cudaStream_t st) {
+cudaError_t launch_sort_gather(const uint16_t* hidden, const int32_t* ids, int M, int H, int E, int K,
+                               const WsPtrs& ws, cudaStream_t st) {
+  const int R = M * K;
+  const int nblk = (R + kSortBlock - 1) / kSortBlock;
+  const int64_t groups = (int64_t)M * (H / 128);
+  int64_t qblocks = (groups + 7) / 8;
+  if (qblocks > 8 * 152) qblocks = 8 * 152;
+  count_quant_kernel<<<(unsigned)(nblk + qblocks), 256, 0, st>>>(hidden, ids, M, H, E, K, nblk, ws);
+  if (cudaError_t e = cudaGetLastError()) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((R + 7) / 8), 1, 1);
+  cfg.gridDim = dim3((unsigned)nblk, 1, 1);
   cfg.blockDim = dim3(256, 1, 1);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -164,16 +223,15 @@ cudaError_t launch_gather(int R, int H, int E, int K, const WsPtrs& ws, cudaStre
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gather_kernel, R, H, E, K, ws);
+  return cudaLaunchKernelEx(&cfg, scatter_gather_kernel, ids, M, H, E, K, nblk, ws);
 }
 
 cudaError_t launch_prep(const uint16_t* hidden, const int32_t* ids, int M, int H, int E, int K,
                         const WsPtrs& ws, cudaStream_t st) {
-  const int pair_mode = use_pair_mode((int64_t)M * K) ? 1 : 0;
   const int64_t groups = (int64_t)M * (H / 128);
   int64_t qblocks = (groups + (kPrepThreads / 32) - 1) / (kPrepThreads / 32);
   if (qblocks > 4 * 152) qblocks = 4 * 152;
-  prep_kernel<<<(unsigned)(1 + qblocks), kPrepThreads, 0, st>>>(hidden, ids, M, H, E, K, pair_mode, ws);
+  prep_kernel<<<(unsigned)(1 + qblocks), kPrepThreads, 0, st>>>(hidden, ids, M, H, E, K, ws);
   return cudaGetLastError();
 }
 
