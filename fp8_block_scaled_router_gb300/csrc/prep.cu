@@ -130,12 +130,14 @@ __global__ void __launch_bounds__(256) scatter_gather_kernel(const int32_t* __re
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int R = M * K;
   const int b = blockIdx.x;
+  (void)lane;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   // per expert: total over all blocks and the count in blocks before this one
   int tot = 0, pre = 0;
   if (tid < E) {
-    for (int bb = 0; bb < nblk; ++bb) {
+#pragma unroll 16
+    for (int bb = 0; bb < nblk; ++bb) {  // independent loads: unrolled so they overlap
       const int c = ws.blk_counts[(size_t)bb * E + tid];
       tot += c;
       pre += bb < b ? c : 0;
@@ -193,15 +195,25 @@ __global__ void __launch_bounds__(256) scatter_gather_kernel(const int32_t* __re
     if (tid == 255) ws.hdr->n_tiles = (uint32_t)scan[255];
   }
   __syncthreads();
-  // gather: warp w copies the hidden codes (H bytes) and scales of rows w, w+8, ...
-  for (int r = warp; r < kSortBlock; r += 8) {
+  // gather: the block's placed rows, hidden codes (H bytes) and scales, as one flat loop
+  // over (row, 16-byte piece) so that many independent copies are in flight
+  const int per_row = H / 16;
+  const int n16 = kSortBlock * per_row;
+#pragma unroll 8
+  for (int idx = tid; idx < n16; idx += 256) {
+    const int r = idx / per_row, c = idx % per_row;
     const int p = pos_s[r];
     if (p < 0) continue;
     const int t = (b * kSortBlock + r) / K;
-    const uint4* src = reinterpret_cast<const uint4*>(ws.qa + (size_t)t * H);
-    uint4* dst = reinterpret_cast<uint4*>(ws.xp + (size_t)p * H);
-    for (int c = lane; c < H / 16; c += 32) dst[c] = src[c];
-    for (int c = lane; c < H / 128; c += 32) ws.sa_p[(size_t)p * (H / 128) + c] = ws.sa[(size_t)t * (H / 128) + c];
+    reinterpret_cast<uint4*>(ws.xp + (size_t)p * H)[c] = reinterpret_cast<const uint4*>(ws.qa + (size_t)t * H)[c];
+  }
+  const int nsc = H / 128;
+  for (int idx = tid; idx < kSortBlock * nsc; idx += 256) {
+    const int r = idx / nsc, c = idx % nsc;
+    const int p = pos_s[r];
+    if (p < 0) continue;
+    const int t = (b * kSortBlock + r) / K;
+    ws.sa_p[(size_t)p * nsc + c] = ws.sa[(size_t)t * nsc + c];
   }
 }
 

@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kRouteThreads)
 constexpr int kBigTB = 16;
 
 __host__ __device__ inline size_t route_big_smem(int E) {
-  return 16 + (size_t)2 * 128 * E * 2 + (size_t)2 * 128 * kBigTB * 2 + (size_t)kBigTB * E * 4 +
+  return 16 + (size_t)2 * 128 * E * 2 + (size_t)2 * 128 * kBigTB * 4 + (size_t)kBigTB * E * 4 +
          (size_t)kBigTB * 16 * 8 + 64;
 }
 
@@ -192,8 +192,8 @@ __global__ void __launch_bounds__(256)
   extern __shared__ __align__(16) unsigned char smem[];
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem);                 // [2] ring barriers
   uint16_t* wring = reinterpret_cast<uint16_t*>(smem + 16);          // [2][128][E]
-  uint16_t* xring = wring + (size_t)2 * 128 * E;                     // [2][128][kBigTB]
-  float* logits = reinterpret_cast<float*>(xring + (size_t)2 * 128 * kBigTB);  // [kBigTB][E]
+  float* xring = reinterpret_cast<float*>(wring + (size_t)2 * 128 * E);  // [2][128][kBigTB] f32
+  float* logits = xring + (size_t)2 * 128 * kBigTB;                  // [kBigTB][E]
   float* sel_v = logits + kBigTB * E;                                // [kBigTB][16]
   int* sel_i = reinterpret_cast<int*>(sel_v + kBigTB * 16);          // [kBigTB][16]
   const int tid = threadIdx.x;
@@ -231,10 +231,10 @@ __global__ void __launch_bounds__(256)
   bool ok = true;
   for (int c = 0; c < nchunks; ++c) {
     // this chunk's hidden values, token-minor: xring[slot][k][t]
-    uint16_t* xs = xring + (size_t)(c & 1) * 128 * kBigTB;
+    float* xs = xring + (size_t)(c & 1) * 128 * kBigTB;
     for (int i = tid; i < 128 * kBigTB; i += 256) {
       const int t = i / 128, k = i % 128;
-      xs[k * kBigTB + t] = tok0 + t < M ? hidden[(size_t)(tok0 + t) * H + c * 128 + k] : (uint16_t)0;
+      xs[k * kBigTB + t] = tok0 + t < M ? bf16_bits_to_float(hidden[(size_t)(tok0 + t) * H + c * 128 + k]) : 0.0f;
     }
     __syncthreads();
     {  // bounded wait for the router chunk
@@ -251,20 +251,18 @@ __global__ void __launch_bounds__(256)
     }
     if (g < 2 && ok) {
       const uint16_t* wcol = wring + (size_t)(c & 1) * 128 * E + e;
-      const uint16_t* xk = xs + g * kTPG;
+      const float* xk = xs + g * kTPG;
       float acc[kTPG];
 #pragma unroll
       for (int t = 0; t < kTPG; ++t) acc[t] = 0.0f;
 #pragma unroll 8
       for (int k = 0; k < 128; ++k) {
         const float w = bf16_bits_to_float(wcol[k * E]);
-        const uint4 q = *reinterpret_cast<const uint4*>(xk + k * kBigTB);
-        const uint32_t xw[4] = {q.x, q.y, q.z, q.w};
+        const float4 x0 = *reinterpret_cast<const float4*>(xk + k * kBigTB);
+        const float4 x1 = *reinterpret_cast<const float4*>(xk + k * kBigTB + 4);
+        const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-        for (int t = 0; t < kTPG; ++t) {
-          const uint16_t xb = (uint16_t)((t & 1) ? (xw[t / 2] >> 16) : (xw[t / 2] & 0xFFFF));
-          acc[t] = __fmaf_rn(bf16_bits_to_float(xb), w, acc[t]);
-        }
+        for (int t = 0; t < kTPG; ++t) acc[t] = __fmaf_rn(xv[t], w, acc[t]);
       }
 #pragma unroll
       for (int t = 0; t < kTPG; ++t) logit[t] = __fadd_rn(logit[t], acc[t]);
