@@ -23,7 +23,8 @@ cudaError_t launch_grouped_down(const uint8_t* w2, const float* s2w, int64_t R, 
                                 int64_t max_tiles, const WsPtrs& ws, cudaStream_t st);
 cudaError_t launch_pair_gateup(const uint8_t* w13, const float* s13, const int32_t* ids,
                                const uint16_t* hidden, int M, int H, int I, int E, int K,
-                               const WsPtrs& ws, cudaStream_t st);
+                               const WsPtrs& ws, cudaStream_t st, const uint8_t* w2 = nullptr,
+                               const float* s2w = nullptr);
 cudaError_t launch_pair_down(const uint8_t* w2, const float* s2w, const int32_t* ids, const float* topk_w,
                              uint16_t* out, int M, int H, int I, int E, int K, const WsPtrs& ws,
                              cudaStream_t st);
@@ -179,13 +180,16 @@ moe_status_t moe_fp8_forward(const void* hidden, const int32_t* topk_ids, const 
   if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
   if (M == 0) return MOE_OK;
   if (use_pair_mode((int64_t)M * shape->top_k)) {
-    // few routed rows: two launches -- gate/up quantises its own hidden row, down is fused
-    // with the combine (same arithmetic as the four stage calls)
-    if (moe_status_t st = moe_fp8_gate_up_direct(hidden, topk_ids, M, w13, w13_scale, workspace,
-                                                 workspace_bytes, shape, stream))
+    // few routed rows: two launches -- gate/up quantises its own hidden row and prefetches
+    // the routed experts' down weights into L2, down is fused with the combine (same
+    // arithmetic as the four stage calls)
+    const WsPtrs ws = ws_ptrs(workspace, L);
+    const int H = shape->hidden, I = shape->inter, E = shape->num_experts, K = shape->top_k;
+    if (moe_status_t st = launched(launch_pair_gateup(w13, w13_scale, topk_ids, static_cast<const uint16_t*>(hidden),
+                                                      M, H, I, E, K, ws, stream, w2, w2_scale)))
       return st;
-    return moe_fp8_down_combine(topk_ids, topk_w, M, w2, w2_scale, out, workspace, workspace_bytes, shape,
-                                stream);
+    return launched(launch_pair_down(w2, w2_scale, topk_ids, topk_w, static_cast<uint16_t*>(out), M, H, I, E, K,
+                                     ws, stream));
   }
   if (moe_status_t st = moe_fp8_prepare(hidden, topk_ids, M, workspace, workspace_bytes, shape, stream))
     return st;

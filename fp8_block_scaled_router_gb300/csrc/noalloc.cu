@@ -23,7 +23,8 @@
 namespace moe {
 cudaError_t launch_pair_gateup(const uint8_t* w13, const float* s13, const int32_t* ids,
                                const uint16_t* hidden, int M, int H, int I, int E, int K,
-                               const WsPtrs& ws, cudaStream_t st);
+                               const WsPtrs& ws, cudaStream_t st, const uint8_t* w2 = nullptr,
+                               const float* s2w = nullptr);
 cudaError_t launch_pair_down(const uint8_t* w2, const float* s2w, const int32_t* ids, const float* topk_w,
                              uint16_t* out, int M, int H, int I, int E, int K, const WsPtrs& ws,
                              cudaStream_t st);
@@ -86,7 +87,7 @@ extern "C" moe_status_t moe_fp8_forward_noalloc(const void* hidden, const int32_
   ws.act_scale = reinterpret_cast<float*>(b + 256 + align256((size_t)(R * I)));
   if (cudaMemsetAsync(ws.hdr, 0, sizeof(Header), stream) != cudaSuccess) return MOE_ERR_LAUNCH;
   if (launch_pair_gateup(w13, w13_scale, topk_ids, static_cast<const uint16_t*>(hidden), M, H, I, E, K, ws,
-                         stream) != cudaSuccess)
+                         stream, w2, w2_scale) != cudaSuccess)
     return MOE_ERR_LAUNCH;
   if (launch_pair_down(w2, w2_scale, topk_ids, topk_w, static_cast<uint16_t*>(out), M, H, I, E, K, ws,
                        stream) != cudaSuccess)

@@ -17,8 +17,15 @@
 // into a fresh accumulator (double-buffered in TMEM), and its epilogue warps read the block
 // sum P back with tcgen05.ld and form the promoted term t_kb = P * (sa_kb * sw_kb). The
 // promotion chain acc = acc + t_kb runs over kb ascending in FP32 from 0 -- in registers
-// when one CTA owns all K blocks, otherwise every CTA of the cluster stores its terms into
-// CTA 0's shared memory and CTA 0 runs the chain after one cluster barrier.
+// when one CTA owns all K blocks, otherwise CTA 0 of the cluster runs it over every CTA's
+// terms.
+//
+// Latency plan (one dependent chain per launch, so every step is taken as early as it can
+// be): warp 0 loads the expert id and issues the TMA loads of the first stages straight
+// after the grid dependency resolves, while the other warps quantise the hidden row (or load
+// the activation scales) and stage the weight scales. The split-K terms and the combine
+// rows cross the cluster as plain distributed-shared-memory stores between hardware cluster
+// barriers (measured faster here than point-to-point mbarrier signalling between CTAs).
 //
 // Modes:
 //   kGateUpWs     gate/up, B rows from the prepared hidden codes in the workspace (TMA)
@@ -30,7 +37,9 @@
 //                 ascending (FP32 multiply then add, from 0) and writes BF16 out.
 // gate/up epilogue: act = silu(g) * u per row, block amax over the 128 rows (warp max +
 // shared memory), scale = amax/448, RNE saturating E4M3 codes into act [p][I] and the
-// scale into act_scale [p][I/128].
+// scale into act_scale [p][I/128]. A gate/up launch may also be given the down weights:
+// each CTA then prefetches its share of its expert's w2 block into L2, so the down launch
+// reads them from L2.
 // Warp roles: warp 0 feeds the stages (TMA), warp 1 owns TMEM and issues MMAs, warps 2..5
 // are the epilogue (TMEM lane quadrant = warp % 4). Every kernel waits on the previous
 // kernel of the stream (griddepcontrol.wait) before touching global memory and then
@@ -38,6 +47,7 @@
 #include <cooperative_groups.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "tc.cuh"
@@ -49,6 +59,7 @@ namespace moe {
 constexpr int kPairN = 16;  // B rows per MMA (row 0 is the unit's pair)
 constexpr int kMaxSplitTerms = 8;  // K blocks per CTA when a unit's K blocks are split
 constexpr int kPairThreads = 192;
+constexpr int kMaxStages = 8;
 
 enum PairMode { kGateUpWs = 0, kGateUpFused = 1, kDownY = 2, kDownCombine = 3 };
 
@@ -56,7 +67,6 @@ template <int MODE>
 struct PairCfg {
   static constexpr bool kGateUp = MODE == kGateUpWs || MODE == kGateUpFused;
   static constexpr int kATiles = kGateUp ? 2 : 1;
-  static constexpr int kStages = kGateUp ? 2 : 4;
   static constexpr int kABytes = 128 * 128;
   static constexpr int kBBytes = kPairN * 128;
   static constexpr int kStageBytes = ((kATiles * kABytes + kBBytes + 1023) / 1024) * 1024;
@@ -68,6 +78,7 @@ struct PairCfg {
 struct PairParams {
   int H, I, K, E;
   int nkb, nkb_cta, ncb;   // K blocks total / per CTA; 128-row output blocks per unit
+  int nst;                 // pipeline stages (<= kMaxStages)
   const int32_t* ids;      // [R] expert of each pair (raw top-k ids or the workspace copy)
   const float* w_scale;    // s13 [E][2I/128][H/128] or s2w [E][H/128][I/128]
   const float* a_scale;    // sa [M][H/128] (kGateUpWs) or act_scale [R][I/128] (down)
@@ -78,28 +89,30 @@ struct PairParams {
   float* act_scale_out;    // [R][I/128]
   float* y_out;            // [R][H]
   Header* hdr;
+  const uint8_t* pf_w2;    // gate/up: w2 [E][H][I] to prefetch into L2, or null
+  const float* pf_s2;      // gate/up: its scales [E][H/128][I/128]
 };
 
-// Split-K terms [kATiles][nkb][128] f32 and combine rows [K][128] f32 are gathered in CTA
-// 0's stage buffers once every CTA of the cluster has drained its pipeline, so they need
-// no shared memory of their own (the host keeps kATiles * nkb * 512 and K * 512 bytes within
-// the stage buffers).
+// Split-K terms [kATiles][nkb][128] f32 arrive in CTA 0's stage buffers once its own MMAs
+// are complete (the host keeps kATiles * nkb * 512 bytes within them); the combine rows
+// [K][128] f32 have a region of their own.
 template <int MODE>
 struct PairSmem {
-  size_t stages, bq, sas, bars, total;
+  size_t stages, bq, sas, sws, comb, cw, bars, total;
 };
 
 template <int MODE>
-__host__ __device__ inline PairSmem<MODE> pair_smem(int nkb, int nkb_cta, int K) {
+__host__ __device__ inline PairSmem<MODE> pair_smem(int nst, int nkb_cta, int K) {
   using C = PairCfg<MODE>;
   PairSmem<MODE> s{};
-  (void)nkb;
-  (void)K;
   size_t o = 0;
-  s.stages = o; o += (size_t)C::kStages * C::kStageBytes;
-  s.bq = o;  o += MODE == kGateUpFused ? (size_t)nkb_cta * 128 : 0;  // hidden codes
-  s.sas = o; o += (size_t)nkb_cta * 4;                             // hidden scales
+  s.stages = o; o += (size_t)nst * C::kStageBytes;
+  s.bq = o;   o += MODE == kGateUpFused ? (size_t)nkb_cta * 128 : 0;  // hidden codes past the stages
+  s.sas = o;  o += (size_t)nkb_cta * 4;                               // activation scales
+  s.sws = o;  o += (size_t)C::kATiles * nkb_cta * 4;                  // weight scales
   o = (o + 15) & ~size_t(15);
+  s.comb = o; o += MODE == kDownCombine ? (size_t)K * 512 : 0;        // combine rows
+  s.cw = o;   o += MODE == kDownCombine ? 16 * 8 : 0;                 // combine weights + ids
   s.bars = o; o += 256;
   s.total = o + 1024;  // + alignment slack of the dynamic shared memory base
   return s;
@@ -114,29 +127,37 @@ __global__ void __launch_bounds__(kPairThreads, 3)
   extern __shared__ __align__(1024) unsigned char dsm_raw[];
   unsigned char* base =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
-  const PairSmem<MODE> SL = pair_smem<MODE>(p.nkb, p.nkb_cta, p.K);
+  const int nst = p.nst;
+  const PairSmem<MODE> SL = pair_smem<MODE>(nst, p.nkb_cta, p.K);
   unsigned char* stages = base + SL.stages;
-  float* xterm = reinterpret_cast<float*>(stages);  // reused after the pipeline drains
+  float* xterm = reinterpret_cast<float*>(stages);  // split-K terms, after CTA 0's MMAs
   uint8_t* bq = base + SL.bq;
   float* sas = reinterpret_cast<float*>(base + SL.sas);
+  float* sws = reinterpret_cast<float*>(base + SL.sws);
+  float* comb = reinterpret_cast<float*>(base + SL.comb);
+  float* cwt = reinterpret_cast<float*>(base + SL.cw);  // [16] combine weights
+  int* cid = reinterpret_cast<int*>(cwt + 16);           // [16] their expert ids
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + SL.bars);
-  uint64_t* full = bars;                        // [kStages]
-  uint64_t* empty = bars + C::kStages;          // [kStages]
-  uint64_t* accf = bars + 2 * C::kStages;       // [2]
-  uint64_t* acce = bars + 2 * C::kStages + 2;   // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 4);
-  float* red = reinterpret_cast<float*>(tmem_slot + 4);  // [4] warp maxima
+  uint64_t* full = bars;                      // [kMaxStages]
+  uint64_t* empty = bars + kMaxStages;        // [kMaxStages]
+  uint64_t* accf = bars + 2 * kMaxStages;     // [2]
+  uint64_t* acce = accf + 2;                  // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
+  float* red = reinterpret_cast<float*>(tmem_slot + 1);  // [4] warp maxima
+  int* e_sh = reinterpret_cast<int*>(red + 4);
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int S = (int)cluster.num_blocks();
+  const bool clustered = S > 1;
+  const int split = MODE == kDownCombine ? 1 : S;  // CTAs sharing one unit's K blocks
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   // set-up that touches no global memory overlaps the previous kernel's tail
   if (warp == 0 && lane == 0) {
     tc::prefetch_tmap(&tmA);
     if (MODE != kGateUpFused) tc::prefetch_tmap(&tmB);
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < nst; ++s) {
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
@@ -149,6 +170,12 @@ __global__ void __launch_bounds__(kPairThreads, 3)
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, C::kTmemCols);
     tc::tmem_relinquish();
+  }
+  if (MODE == kGateUpFused) {  // B tile rows 1..15 stay zero
+    for (int i = threadIdx.x; i < nst * (C::kBBytes / 16); i += kPairThreads) {
+      const int s = i / (C::kBBytes / 16), c = i % (C::kBBytes / 16);
+      reinterpret_cast<uint4*>(stages + s * C::kStageBytes + C::kTxA)[c] = make_uint4(0, 0, 0, 0);
+    }
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
@@ -164,18 +191,33 @@ __global__ void __launch_bounds__(kPairThreads, 3)
     cb = unit % p.ncb;
     tok = pr / p.K;
   }
-  const int split = MODE == kDownCombine ? 1 : S;  // CTAs sharing one unit's K blocks
   const int kb0 = MODE == kDownCombine ? 0 : rank * p.nkb_cta;
   const int brow = MODE == kGateUpWs ? tok : pr;  // B row (qa row or act row)
-  if (MODE == kGateUpFused) {
-    // zero the B tiles (rows 1..15 stay zero) and quantise the pair's hidden row for this
-    // CTA's K blocks (warp w takes blocks w, w+6, ...); independent of the expert id, so
-    // these loads overlap the id load below
-    for (int i = threadIdx.x; i < C::kStages * (C::kBBytes / 16); i += kPairThreads) {
-      const int s = i / (C::kBBytes / 16), c = i % (C::kBBytes / 16);
-      reinterpret_cast<uint4*>(stages + s * C::kStageBytes + C::kTxA)[c] = make_uint4(0, 0, 0, 0);
+  const int npre = min(nst, p.nkb_cta);           // stages issued before the block barrier
+  if (warp == 0) {
+    // the expert id, then the first stages' loads: the first bytes are in flight before the
+    // rest of the prologue runs
+    int e = 0;
+    if (lane == 0) e = p.ids[pr];
+    if (lane == 0) {
+      *e_sh = e;
+      if (e >= 0 && e < p.E) {
+        const int ya = kGateUp ? e * 2 * p.I + cb * 128 : e * p.H + cb * 128;
+        const int yb = e * 2 * p.I + p.I + cb * 128;
+        for (int i = 0; i < npre; ++i) {
+          unsigned char* st = stages + i * C::kStageBytes;
+          const int x = (kb0 + i) * 128;
+          tc::mbar_arrive_expect_tx(&full[i], MODE == kGateUpFused ? C::kTxA : C::kTxA + C::kBBytes);
+          tc::tma_load_2d(st, &tmA, &full[i], x, ya);
+          if (kGateUp) tc::tma_load_2d(st + C::kABytes, &tmA, &full[i], x, yb);
+          if (MODE != kGateUpFused) tc::tma_load_2d(st + C::kTxA, &tmB, &full[i], x, brow);
+        }
+      }
     }
-    for (int i = warp; i < p.nkb_cta; i += kPairThreads / 32) {
+  } else if (MODE == kGateUpFused) {
+    // warps 1..5 quantise the pair's hidden row for this CTA's K blocks straight into the
+    // stage B tiles (row 0; unswizzled in the first 8-row group), the rest into bq
+    for (int i = warp - 1; i < p.nkb_cta; i += kPairThreads / 32 - 1) {
       const uint2 raw = *reinterpret_cast<const uint2*>(p.hidden + (size_t)tok * p.H + (kb0 + i) * 128 + lane * 4);
       const float x0 = bf16_bits_to_float(raw.x & 0xFFFF), x1 = bf16_bits_to_float(raw.x >> 16);
       const float x2 = bf16_bits_to_float(raw.y & 0xFFFF), x3 = bf16_bits_to_float(raw.y >> 16);
@@ -185,24 +227,29 @@ __global__ void __launch_bounds__(kPairThreads, 3)
       const float sc = quant_scale(amax);
       const uint32_t lo = e4m3x2_encode(__fdiv_rn(x0, sc), __fdiv_rn(x1, sc));
       const uint32_t hi = e4m3x2_encode(__fdiv_rn(x2, sc), __fdiv_rn(x3, sc));
-      reinterpret_cast<uint32_t*>(bq + i * 128)[lane] = lo | (hi << 16);
+      uint8_t* dst = i < nst ? stages + i * C::kStageBytes + C::kTxA : bq + i * 128;
+      reinterpret_cast<uint32_t*>(dst)[lane] = lo | (hi << 16);
       if (lane == 0) sas[i] = sc;
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   } else {
-    for (int i = threadIdx.x; i < p.nkb_cta; i += kPairThreads) sas[i] = p.a_scale[(size_t)brow * p.nkb + kb0 + i];
+    for (int i = threadIdx.x - 32; i < p.nkb_cta; i += kPairThreads - 32)
+      sas[i] = p.a_scale[(size_t)brow * p.nkb + kb0 + i];
+    if (MODE == kDownCombine && rank == 0 && warp == 1 && lane < p.K) {
+      cwt[lane] = p.topk_w[tok * p.K + lane];
+      cid[lane] = p.ids[tok * p.K + lane];
+    }
   }
-  const int e = p.ids[pr];
-  const bool valid = e >= 0 && e < p.E;
-  if (MODE == kGateUpFused && !valid && cb == 0 && rank == 0 && threadIdx.x == 0)
-    set_status(p.hdr, MOE_STATUS_BAD_EXPERT_ID);
-  // a skipped pair (not kDownCombine): the whole cluster shares the unit and leaves together
-  const bool skip_unit = MODE != kDownCombine && !valid;
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  const int e = *e_sh;
+  const bool valid = e >= 0 && e < p.E;
+  if (MODE == kGateUpFused && !valid && cb == 0 && rank == 0 && threadIdx.x == 0)
+    set_status(p.hdr, MOE_STATUS_BAD_EXPERT_ID);
   const uint32_t tmem = *tmem_slot;
-  if (skip_unit) {
+  // a skipped pair (not kDownCombine): the whole cluster shares the unit and leaves together
+  if (MODE != kDownCombine && !valid) {
     if (warp == 1) tc::tmem_dealloc(tmem, C::kTmemCols);
     return;
   }
@@ -211,11 +258,11 @@ __global__ void __launch_bounds__(kPairThreads, 3)
   float chain0 = 0.0f, chain1 = 0.0f;
   float term0[kMaxSplitTerms], term1[kMaxSplitTerms];
   if (valid && warp == 0) {
-    const int yA0 = kGateUp ? e * 2 * p.I + cb * 128 : e * p.H + cb * 128;
-    const int yA1 = e * 2 * p.I + p.I + cb * 128;
-    for (int i = 0; i < p.nkb_cta; ++i) {
-      const int s = i % C::kStages;
-      const uint32_t ph = (i / C::kStages) & 1;
+    const int ya = kGateUp ? e * 2 * p.I + cb * 128 : e * p.H + cb * 128;
+    const int yb = e * 2 * p.I + p.I + cb * 128;
+    for (int i = npre; i < p.nkb_cta; ++i) {
+      const int s = i % nst;
+      const uint32_t ph = (i / nst) & 1;
       bool w_ok = true;
       if (lane == 0) w_ok = tc::mbar_wait(&empty[s], ph ^ 1);
       if (!__shfl_sync(0xffffffffu, (int)w_ok, 0)) { ok = false; break; }
@@ -229,8 +276,8 @@ __global__ void __launch_bounds__(kPairThreads, 3)
       if (lane == 0) {
         const int x = (kb0 + i) * 128;
         tc::mbar_arrive_expect_tx(&full[s], MODE == kGateUpFused ? C::kTxA : C::kTxA + C::kBBytes);
-        tc::tma_load_2d(st, &tmA, &full[s], x, yA0);
-        if (kGateUp) tc::tma_load_2d(st + C::kABytes, &tmA, &full[s], x, yA1);
+        tc::tma_load_2d(st, &tmA, &full[s], x, ya);
+        if (kGateUp) tc::tma_load_2d(st + C::kABytes, &tmA, &full[s], x, yb);
         if (MODE != kGateUpFused) tc::tma_load_2d(st + C::kTxA, &tmB, &full[s], x, brow);
       }
     }
@@ -238,8 +285,8 @@ __global__ void __launch_bounds__(kPairThreads, 3)
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_e4m3(128, kPairN);
       for (int i = 0; i < p.nkb_cta; ++i) {
-        const int s = i % C::kStages;
-        const uint32_t ph = (i / C::kStages) & 1;
+        const int s = i % nst;
+        const uint32_t ph = (i / nst) & 1;
         const int buf = i & 1;
         if (!tc::mbar_wait(&full[s], ph)) { ok = false; break; }
         if (!tc::mbar_wait(&acce[buf], ((i >> 1) & 1) ^ 1)) { ok = false; break; }
@@ -257,12 +304,36 @@ __global__ void __launch_bounds__(kPairThreads, 3)
         tc::mma_commit(&empty[s]);
         tc::mma_commit(&accf[buf]);
       }
+      if (kGateUp && ok && p.pf_w2 != nullptr) {
+        // every weight byte of this CTA has landed: spend the idle memory time of the
+        // epilogue on this CTA's share of the expert's down weights (and, once per pair,
+        // their scales)
+        const size_t wbytes = (size_t)p.H * p.I;
+        const int parts = p.ncb * S, part = cb * S + rank;
+        const size_t chunk = ((wbytes + parts - 1) / parts + 15) & ~size_t(15);
+        const size_t off = (size_t)part * chunk;
+        if (off < wbytes)
+          tc::prefetch_l2_bulk(p.pf_w2 + (size_t)e * wbytes + off, (uint32_t)min(chunk, wbytes - off));
+        if (part == 0) {
+          const size_t sb = (size_t)(p.H / 128) * (p.I / 128) * 4;
+          const char* s0 = reinterpret_cast<const char*>(p.pf_s2) + (size_t)e * sb;
+          for (size_t o = 0; o < sb; o += 128) tc::prefetch_l2_line(s0 + o);
+        }
+      }
     }
   } else if (valid) {
-    // epilogue: thread <-> weight row (warp % 4) * 32 + lane of the 128-row tile
+    // epilogue: thread <-> weight row (warp % 4) * 32 + lane of the 128-row tile; the
+    // block's weight scales are staged first, while the loads are in flight
     const int q = warp & 3;
-    const float* sw0 = p.w_scale + ((size_t)e * (kGateUp ? 2 * p.I / 128 : p.H / 128) + cb) * p.nkb;
-    const float* sw1 = p.w_scale + ((size_t)e * (2 * p.I / 128) + p.I / 128 + cb) * p.nkb;
+    {
+      const float* sw0 = p.w_scale + ((size_t)e * (kGateUp ? 2 * p.I / 128 : p.H / 128) + cb) * p.nkb;
+      const float* sw1 = p.w_scale + ((size_t)e * (2 * p.I / 128) + p.I / 128 + cb) * p.nkb;
+      for (int i = threadIdx.x - 64; i < p.nkb_cta; i += 128) {
+        sws[i] = sw0[kb0 + i];
+        if (kGateUp) sws[p.nkb_cta + i] = sw1[kb0 + i];
+      }
+      tc::named_bar(1, 128);
+    }
     for (int i = 0; i < p.nkb_cta; ++i) {
       const int buf = i & 1;
       if (!tc::mbar_wait(&accf[buf], (i >> 1) & 1)) { ok = false; break; }
@@ -273,10 +344,9 @@ __global__ void __launch_bounds__(kPairThreads, 3)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&acce[buf]);
-      const int kb = kb0 + i;
       const float a = sas[i];
-      const float t0 = __fmul_rn(v0[0], __fmul_rn(a, sw0[kb]));
-      const float t1 = kGateUp ? __fmul_rn(v1[0], __fmul_rn(a, sw1[kb])) : 0.0f;
+      const float t0 = __fmul_rn(v0[0], __fmul_rn(a, sws[i]));
+      const float t1 = kGateUp ? __fmul_rn(v1[0], __fmul_rn(a, sws[p.nkb_cta + i])) : 0.0f;
       if (split == 1) {  // the whole chain is local: kb ascending
         chain0 = __fadd_rn(chain0, t0);
         if (kGateUp) chain1 = __fadd_rn(chain1, t1);
@@ -287,16 +357,18 @@ __global__ void __launch_bounds__(kPairThreads, 3)
       }
     }
   }
-  if (!ok) set_status(p.hdr, MOE_STATUS_WAIT_TIMEOUT);
-  __syncthreads();
-  if (split > 1 || MODE == kDownCombine) {
-    cluster.sync();  // every CTA's pipeline has drained: CTA 0's stage buffers are free
-    if (valid && warp >= 2) {
+
+  // ---- cross-CTA exchange: every CTA stores its terms (or its combine row) into CTA 0's
+  // shared memory between two cluster barriers -- the first one guarantees that CTA 0's own
+  // MMAs, and with them every read of its stage buffers, are complete
+  if (clustered) {
+    if (MODE != kDownCombine) cluster.sync();
+    if (warp >= 2) {
       const int r = (warp & 3) * 32 + lane;
-      float* x0 = cluster.map_shared_rank(xterm, 0);
       if (MODE == kDownCombine) {
-        x0[rank * 128 + r] = chain0;
+        cluster.map_shared_rank(comb, 0)[rank * 128 + r] = chain0;
       } else {
+        float* x0 = cluster.map_shared_rank(xterm, 0);
 #pragma unroll
         for (int j = 0; j < kMaxSplitTerms; ++j) {
           if (j < p.nkb_cta) {
@@ -306,8 +378,11 @@ __global__ void __launch_bounds__(kPairThreads, 3)
         }
       }
     }
-    cluster.sync();  // CTA 0 holds every term / row
+    cluster.sync();
+  } else if (MODE == kDownCombine && warp >= 2) {
+    comb[(warp & 3) * 32 + lane] = chain0;
   }
+  if (!ok) set_status(p.hdr, MOE_STATUS_WAIT_TIMEOUT);
 
   if (rank == 0 && warp >= 2) {
     const int q = warp & 3;
@@ -338,13 +413,14 @@ __global__ void __launch_bounds__(kPairThreads, 3)
     } else {
       float acc = 0.0f;
       for (int j = 0; j < p.K; ++j) {
-        const int ej = p.ids[tok * p.K + j];
+        const int ej = cid[j];
         if (ej < 0 || ej >= p.E) continue;
-        acc = __fadd_rn(acc, __fmul_rn(p.topk_w[tok * p.K + j], xterm[j * 128 + r]));
+        acc = __fadd_rn(acc, __fmul_rn(cwt[j], comb[j * 128 + r]));
       }
       p.out[(size_t)tok * p.H + cb * 128 + r] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
     }
   }
+  tc::fence_before_sync();
   __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
@@ -387,22 +463,56 @@ bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t row
 
 namespace {
 
+struct PairPlan {
+  int split, nst;
+};
+
+template <int MODE>
+void set_pair_attrs() {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(pair_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaFuncSetAttribute(pair_gemm_kernel<MODE>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  });
+}
+
 constexpr int kNumSMs = 152;
 constexpr size_t kSmemPerSM = 228 * 1024;
 
-// Largest divisor S of nkb (S <= 8, the cluster size) such that units * S CTAs fit in one
-// wave at the occupancy their shared memory allows; at least 1.
+// CTAs of `smem` bytes resident at once in clusters of `cluster`: SMs x CTAs per SM, less a
+// tenth for clusters that a GPC cannot place whole. Clusters of two or more CTAs at one CTA
+// per SM are counted as not fitting (a GPC's SM count is not a multiple of the cluster).
+inline int64_t resident_ctas(int cluster, size_t smem) {
+  const int64_t per_sm = (int64_t)(kSmemPerSM / (smem + 1024));
+  if (per_sm == 0 || (cluster > 1 && per_sm < 2)) return 0;
+  return cluster > 1 ? kNumSMs * per_sm * 9 / 10 : kNumSMs * per_sm;
+}
+
+// The largest K split S (a divisor of nkb, S <= 8) whose units * S CTAs are all resident at
+// once, with the most pipeline stages (<= the CTA's K blocks, <= kMaxStages) that keep them
+// resident; `fixed_cluster` (down fused with the combine) is the cluster size when the mode
+// fixes it. When nothing fits one wave: no split, 2 stages for gate/up and 4 for down.
 template <int MODE>
-int pick_split(int nkb, int64_t units, int K) {
-  int best = 1;
-  for (int s = 1; s <= 8; ++s) {
+PairPlan plan_pair(int nkb, int64_t units, int K, bool allow_split, int fixed_cluster = 0) {
+  using C = PairCfg<MODE>;
+  PairPlan best{1, std::min(nkb, C::kGateUp ? 2 : 4)};
+  for (int s = 1; s <= (allow_split ? 8 : 1); ++s) {
     if (nkb % s) continue;
-    if (s > 1 && (nkb / s > kMaxSplitTerms ||
-                  (size_t)PairCfg<MODE>::kATiles * nkb * 512 > (size_t)PairCfg<MODE>::kStages * PairCfg<MODE>::kStageBytes))
-      continue;
-    const size_t smem = pair_smem<MODE>(nkb, nkb / s, K).total + 1024;
-    const int64_t wave = (int64_t)kNumSMs * (int64_t)(kSmemPerSM / smem);
-    if (units * s <= wave) best = s;
+    const int per = nkb / s;
+    if (s > 1 && per > kMaxSplitTerms) continue;
+    const int cluster = fixed_cluster ? fixed_cluster : s;
+    int chosen = 0;
+    for (int n = std::min(per, kMaxStages); n >= std::min(per, 2); --n) {
+      // split-K terms land in CTA 0's stage buffers
+      if (s > 1 && (size_t)C::kATiles * nkb * 512 > (size_t)n * C::kStageBytes) break;
+      const size_t smem = pair_smem<MODE>(n, per, K).total;
+      if (smem > 227 * 1024) continue;
+      if (units * cluster <= resident_ctas(cluster, smem)) {
+        chosen = n;
+        break;
+      }
+    }
+    if (chosen) best = {s, chosen};
   }
   return best;
 }
@@ -410,12 +520,8 @@ int pick_split(int nkb, int64_t units, int K) {
 template <int MODE>
 cudaError_t launch_pair(const CUtensorMap& tA, const CUtensorMap& tB, PairParams prm, int cluster_x,
                         int64_t units, cudaStream_t st) {
-  const PairSmem<MODE> SL = pair_smem<MODE>(prm.nkb, prm.nkb_cta, prm.K);
-  static std::once_flag once;
-  std::call_once(once, [] {
-    cudaFuncSetAttribute(pair_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    cudaFuncSetAttribute(pair_gemm_kernel<MODE>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  });
+  const PairSmem<MODE> SL = pair_smem<MODE>(prm.nst, prm.nkb_cta, prm.K);
+  set_pair_attrs<MODE>();
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cluster_x, (unsigned)units, 1);
   cfg.blockDim = dim3(kPairThreads, 1, 1);
@@ -445,10 +551,11 @@ PairParams base_params(int M, int H, int I, int E, int K, const WsPtrs& ws) {
 
 // gate/up for R = M*K pairs: act [R][I] + act_scale [R][I/128] in pair order. fused: the
 // hidden row is quantised inside the kernel (ids = raw top-k ids); otherwise B comes from
-// the prepared codes ws.qa / ws.sa and ids = ws.pair_expert.
+// the prepared codes ws.qa / ws.sa and ids = ws.pair_expert. w2 / s2w (optional): the down
+// weights the next launch will read; each routed expert's block is prefetched into L2.
 cudaError_t launch_pair_gateup(const uint8_t* w13, const float* s13, const int32_t* ids,
                                const uint16_t* hidden, int M, int H, int I, int E, int K,
-                               const WsPtrs& ws, cudaStream_t st) {
+                               const WsPtrs& ws, cudaStream_t st, const uint8_t* w2, const float* s2w) {
   CUtensorMap tA, tB;
   if (!make_tmap_u8(&tA, w13, (uint64_t)H, (uint64_t)E * 2 * I, 128)) return cudaErrorInvalidValue;
   PairParams prm = base_params(M, H, I, E, K, ws);
@@ -458,15 +565,19 @@ cudaError_t launch_pair_gateup(const uint8_t* w13, const float* s13, const int32
   prm.w_scale = s13;
   prm.a_scale = ws.sa;
   prm.hidden = hidden;
+  prm.pf_w2 = w2;
+  prm.pf_s2 = s2w;
   const int64_t units = (int64_t)M * K * prm.ncb;
-  const int S = hidden ? pick_split<kGateUpFused>(prm.nkb, units, K) : pick_split<kGateUpWs>(prm.nkb, units, K);
-  prm.nkb_cta = prm.nkb / S;
+  const PairPlan pl = hidden ? plan_pair<kGateUpFused>(prm.nkb, units, K, true)
+                             : plan_pair<kGateUpWs>(prm.nkb, units, K, true);
+  prm.nkb_cta = prm.nkb / pl.split;
+  prm.nst = pl.nst;
   if (hidden) {
     tB = tA;  // unused: the B tile is written by the kernel
-    return launch_pair<kGateUpFused>(tA, tB, prm, S, units, st);
+    return launch_pair<kGateUpFused>(tA, tB, prm, pl.split, units, st);
   }
   if (!make_tmap_u8(&tB, ws.qa, (uint64_t)H, (uint64_t)M, kPairN)) return cudaErrorInvalidValue;
-  return launch_pair<kGateUpWs>(tA, tB, prm, S, units, st);
+  return launch_pair<kGateUpWs>(tA, tB, prm, pl.split, units, st);
 }
 
 // down for R pairs. combine: fused with the top-k combine into out (cluster of K CTAs per
@@ -488,12 +599,14 @@ cudaError_t launch_pair_down(const uint8_t* w2, const float* s2w, const int32_t*
     prm.topk_w = topk_w;
     prm.out = out;
     prm.nkb_cta = prm.nkb;
+    prm.nst = plan_pair<kDownCombine>(prm.nkb, (int64_t)M * prm.ncb, K, false, K).nst;
     return launch_pair<kDownCombine>(tA, tB, prm, K, (int64_t)M * prm.ncb, st);
   }
   const int64_t units = (int64_t)R * prm.ncb;
-  const int S = pick_split<kDownY>(prm.nkb, units, K);
-  prm.nkb_cta = prm.nkb / S;
-  return launch_pair<kDownY>(tA, tB, prm, S, units, st);
+  const PairPlan pl = plan_pair<kDownY>(prm.nkb, units, K, true);
+  prm.nkb_cta = prm.nkb / pl.split;
+  prm.nst = pl.nst;
+  return launch_pair<kDownY>(tA, tB, prm, pl.split, units, st);
 }
 
 }  // namespace moe
