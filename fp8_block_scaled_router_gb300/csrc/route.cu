@@ -27,7 +27,7 @@ constexpr int kRouteThreads = 256;
 constexpr int kRouteMaxCluster = 16;
 
 struct RouteSmem {
-  size_t ws, xs, part, logits, sel, total;
+  size_t ws, xs, part, logits, sel, bias, total;
 };
 
 // ws: router rows [CPC*128][E] bf16; xs: hidden [CPC*128][TB] bf16 (token-minor);
@@ -42,6 +42,7 @@ __host__ __device__ inline RouteSmem route_smem(int TB, int CPC, int E, int nchu
   s.part = o;   o += (size_t)nchunks * TB * E * 4;
   s.logits = o; o += (size_t)TB * E * 4;
   s.sel = o;    o += (size_t)TB * 16 * 8;
+  s.bias = o;   o += (size_t)E * 4;
   s.total = o;
   return s;
 }
@@ -64,15 +65,14 @@ __global__ void __launch_bounds__(kRouteThreads)
   float* logits = reinterpret_cast<float*>(smem + L.logits);
   float* sel_v = reinterpret_cast<float*>(smem + L.sel);
   int* sel_i = reinterpret_cast<int*>(sel_v + TB * 16);
+  float* bias_s = reinterpret_cast<float*>(smem + L.bias);
   const int tid = threadIdx.x;
   const int tok0 = blockIdx.y * TB;
   const int c0 = rank * CPC;
 
-  // inputs may be written by the previous kernel in the stream (programmatic launch)
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;");
-
-  // stage router rows [c0*128, (c0+CPC)*128) (contiguous) and the tokens' hidden values
+  // The router rows [c0*128, (c0+CPC)*128) (contiguous) and the bias are layer parameters:
+  // they are staged while the previous kernel of the stream finishes (programmatic launch);
+  // the hidden rows, which it may have written, only after the grid dependency resolves.
   {
     const uint4* src = reinterpret_cast<const uint4*>(router_w + (size_t)c0 * 128 * E);
     uint4* dst = reinterpret_cast<uint4*>(wsm);
@@ -86,6 +86,12 @@ __global__ void __launch_bounds__(kRouteThreads)
       for (int u = 0; u < 8; ++u)
         if (i0 + u * kRouteThreads < n16) dst[i0 + u * kRouteThreads] = v[u];
     }
+    if (rank == 0)
+      for (int e = tid; e < E; e += kRouteThreads) bias_s[e] = bias != nullptr ? bias[e] : 0.0f;
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  {
     for (int i = tid; i < TB * CPC * 128; i += kRouteThreads) {
       const int t = i / (CPC * 128), k = i % (CPC * 128);
       xs[k * TB + t] = tok0 + t < M ? hidden[(size_t)(tok0 + t) * H + c0 * 128 + k] : (uint16_t)0;
@@ -128,22 +134,32 @@ __global__ void __launch_bounds__(kRouteThreads)
 
   for (int i = tid; i < TB * E; i += kRouteThreads) {
     const int t = i / E, e = i % E;
+    const float* pc = part + (size_t)t * E + e;
+    const size_t cstride = (size_t)TB * E;
     float l = 0.0f;
-    for (int c = 0; c < nchunks; ++c) l = __fadd_rn(l, part[((size_t)c * TB + t) * E + e]);
-    if (bias != nullptr) l = __fadd_rn(l, bias[e]);
+#pragma unroll 8
+    for (int c = 0; c < nchunks; ++c) l = __fadd_rn(l, pc[c * cstride]);
+    if (bias != nullptr) l = __fadd_rn(l, bias_s[e]);
     logits[t * E + e] = l;
   }
   __syncthreads();
-  // rank selection: expert e goes to slot rank(e) if rank(e) < K
+  // rank selection: expert e goes to slot rank(e) if rank(e) < K (four independent counts
+  // over 16-byte loads of the token's logits)
   for (int i = tid; i < TB * E; i += kRouteThreads) {
     const int t = i / E, e = i % E;
-    const float* lt = logits + t * E;
-    const float v = lt[e];
-    int rk = 0;
-    for (int e2 = 0; e2 < E; ++e2) {
-      const float v2 = lt[e2];
-      rk += (v2 > v) || (v2 == v && e2 < e);
+    const float4* lt4 = reinterpret_cast<const float4*>(logits + t * E);
+    const float v = logits[t * E + e];
+    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+#pragma unroll 8
+    for (int q = 0; q < E / 4; ++q) {
+      const float4 w = lt4[q];
+      const int e2 = 4 * q;
+      r0 += (w.x > v) || (w.x == v && e2 < e);
+      r1 += (w.y > v) || (w.y == v && e2 + 1 < e);
+      r2 += (w.z > v) || (w.z == v && e2 + 2 < e);
+      r3 += (w.w > v) || (w.w == v && e2 + 3 < e);
     }
+    const int rk = r0 + r1 + r2 + r3;
     if (rk < K) {
       sel_v[t * 16 + rk] = v;
       sel_i[t * 16 + rk] = e;

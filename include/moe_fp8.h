@@ -95,7 +95,10 @@ moe_status_t moe_fp8_workspace_init(void* workspace, size_t workspace_bytes,
  *             else the softmax over all E logits read at the selected experts
  * logit[t][e] = sum over 128-wide chunks c ascending of an FP32 fma chain over the
  * chunk's k ascending (from 0), then + bias[e]. Top-k ids are a pure function of these
- * logits. M = 0 is a no-op. Needs no workspace. */
+ * logits. M = 0 is a no-op. Needs no workspace.
+ * router_w and bias are layer parameters: they are read while the kernel launched just
+ * before this call on `stream` may still be running (programmatic dependent launch), so
+ * that kernel must not write them. hidden is read only after it has completed. */
 moe_status_t moe_route(const void* hidden, const void* router_w, const float* bias, int32_t M,
                        const moe_fp8_shape_t* shape, int32_t renormalize, int32_t* topk_ids,
                        float* topk_w, cudaStream_t stream);
