@@ -238,6 +238,7 @@ def ours_arm(args, wl, world, rank, local):
     from fp8_block_scaled_router_gb300 import _lib as L
     from fp8_block_scaled_router_gb300 import build as B
     from fp8_block_scaled_router_gb300 import inputs
+    from fp8_block_scaled_router_gb300 import replicas
 
     B.build()
     torch.cuda.set_device(local)
@@ -255,7 +256,7 @@ def ours_arm(args, wl, world, rank, local):
     H, I, E, K = x.shape.hidden, x.shape.inter, x.shape.num_experts, x.shape.top_k
     # each rank steps through its own token stream (a different slice of the seeded rows)
     if decode and world > 1:
-        x.hidden = np.roll(x.hidden, -rank * (ntok // world), axis=0)
+        x.hidden = np.roll(x.hidden, -replicas.token_offset(rank, world, ntok), axis=0)
 
     def dev(a):
         a = np.ascontiguousarray(a)
@@ -343,11 +344,9 @@ def ours_arm(args, wl, world, rank, local):
     elapsed = ev0.elapsed_time(ev1) / 1e3
     clocks = sampler.stop() if sampler else None
     if dist:
-        t = torch.tensor([elapsed], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+        elapsed = replicas.slowest(elapsed, dist, "cuda")
         dist.barrier()
-    value = world * steps * M / elapsed
+    value = replicas.throughput(world, steps, M, elapsed)
     ms_per_step = 1e3 * elapsed / steps
 
     # ---- dominant kernel alone: gate/up, back to back in a CUDA graph on its own stream
@@ -424,10 +423,8 @@ def ours_arm(args, wl, world, rank, local):
     torch.cuda.synchronize()
     e2e_t = a0.elapsed_time(a1) / 1e3
     if dist:
-        t = torch.tensor([e2e_t], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_t = float(t.item())
-    e2e = {"value": world * e2e_steps * M / e2e_t, "unit": "tokens/s",
+        e2e_t = replicas.slowest(e2e_t, dist, "cuda")
+    e2e = {"value": replicas.throughput(world, e2e_steps, M, e2e_t), "unit": "tokens/s",
            "h2d_bytes_per_step": M * H * 2, "d2h_bytes_per_step": M * H * 2, "steps": e2e_steps}
 
     cpu = None
