@@ -188,156 +188,234 @@ __global__ void __launch_bounds__(kRouteThreads)
 }
 
 // ---------------------------------------------------------------------------------------
-// Many tokens: one CTA per block of kBigTB tokens covers all E experts over the whole hidden
-// dimension, so every logit's chunk chains and their ascending chunk sum stay inside one
-// thread. The router's 128-row chunks (128 * E * 2 contiguous bytes) stream through a
-// two-slot shared-memory ring with bulk asynchronous copies; thread (e, token group) holds
-// kBigTB/2 chain accumulators and the running logits of its tokens.
+// Many tokens (E = 32 * EPT experts, EPT in {1, 2, 4}): one CTA per kBigTok = 32 tokens
+// covers all experts over the whole hidden dimension, so every logit's chunk chains and
+// their ascending chunk sum stay inside the CTA. Thread (lane, warp) owns experts
+// lane*EPT .. lane*EPT+EPT-1 of the 8 tokens of group (warp % 4): 8*EPT independent fma
+// chains, one 8*EPT-byte router load and two broadcast 16-byte hidden loads per k. Warps
+// 0-3 take the even chunks, warps 4-7 the odd ones; after each pair of chunks the odd
+// partials pass through shared memory and warps 0-3 add them to the running logits in chunk
+// order ((l + acc_2p) + acc_2p+1). The router's chunks (128 * E * 2 contiguous bytes) stream
+// four ahead through a shared-memory ring with bulk asynchronous copies; the next pair's
+// hidden values are prefetched into registers while the current pair is computed.
+// Top-k: one warp per token, K rounds of a warp argmax over 64-bit keys (order-preserving
+// bits of the logit, then the complement of the expert index: the larger logit wins, ties
+// go to the lower index).
 // ---------------------------------------------------------------------------------------
-constexpr int kBigTB = 16;
+constexpr int kBigTok = 32;
+constexpr int kBigSlots = 4;
 
 __host__ __device__ inline size_t route_big_smem(int E) {
-  return 16 + (size_t)2 * 128 * E * 2 + (size_t)2 * 128 * kBigTB * 4 + (size_t)kBigTB * E * 4 +
-         (size_t)kBigTB * 16 * 8 + 64;
+  return 64 + (size_t)kBigSlots * 128 * E * 2 + (size_t)2 * 128 * kBigTok * 4 + (size_t)128 * 8 * (E / 32) * 4 +
+         (size_t)kBigTok * E * 4;
 }
 
-__global__ void __launch_bounds__(256)
-    route_big_kernel(const uint16_t* __restrict__ hidden, const uint16_t* __restrict__ router_w,
-                     const float* __restrict__ bias, int M, int H, int E, int K, int renorm,
-                     int32_t* __restrict__ ids, float* __restrict__ wts) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem);                 // [2] ring barriers
-  uint16_t* wring = reinterpret_cast<uint16_t*>(smem + 16);          // [2][128][E]
-  float* xring = reinterpret_cast<float*>(wring + (size_t)2 * 128 * E);  // [2][128][kBigTB] f32
-  float* logits = xring + (size_t)2 * 128 * kBigTB;                  // [kBigTB][E]
-  float* sel_v = logits + kBigTB * E;                                // [kBigTB][16]
-  int* sel_i = reinterpret_cast<int*>(sel_v + kBigTB * 16);          // [kBigTB][16]
-  const int tid = threadIdx.x;
-  const int tok0 = blockIdx.x * kBigTB;
-  const int nchunks = H / 128;
-  const uint32_t wbytes = 128u * (uint32_t)E * 2u;
+__device__ __forceinline__ uint64_t logit_key(float v, int e) {
+  uint32_t u = __float_as_uint(v);
+  if (v == 0.0f) u = 0u;  // -0 and +0 are one value
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((uint64_t)u << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)e);
+}
 
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;");
-  if (tid == 0) {
-    for (int b = 0; b < 2; ++b)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"((uint32_t)__cvta_generic_to_shared(&bar[b])));
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
-  auto issue = [&](int c) {  // router chunk c -> slot c & 1 (thread 0)
-    const uint32_t b = (uint32_t)__cvta_generic_to_shared(&bar[c & 1]);
-    const uint32_t d = (uint32_t)__cvta_generic_to_shared(wring + (size_t)(c & 1) * 128 * E);
+template <int EPT>
+__global__ void __launch_bounds__(256, 1)
+    route_big_kernel(const uint16_t* __restrict__ hidden, const uint16_t* __restrict__ router_w,
+                     const float* __restrict__ bias, int M, int H, int K, int renorm,
+                     int32_t* __restrict__ ids, float* __restrict__ wts) {
+  constexpr int E = 32 * EPT;
+  constexpr int NA = 8 * EPT;  // accumulators per thread
+  extern __shared__ __align__(16) unsigned char smem[];
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem);                         // [kBigSlots]
+  uint16_t* wring = reinterpret_cast<uint16_t*>(smem + 64);                  // [slots][128][E]
+  float* xring = reinterpret_cast<float*>(wring + (size_t)kBigSlots * 128 * E);  // [2][128][32]
+  float* xch = xring + 2 * 128 * kBigTok;                                    // [NA][128]
+  float* logits = xch + NA * 128;                                            // [32][E]
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int grp = warp & 3, par = warp >> 2;
+  const int tok0 = blockIdx.x * kBigTok;
+  const int nchunks = H / 128, npairs = nchunks / 2;
+  constexpr uint32_t wbytes = 128u * E * 2u;
+
+  // layer parameters first (router chunks, bias), while the previous kernel finishes
+  auto issue = [&](int c) {
+    const int slot = c % kBigSlots;
+    const uint32_t b = (uint32_t)__cvta_generic_to_shared(&bar[slot]);
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(wring + (size_t)slot * 128 * E);
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(wbytes) : "memory");
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(d),
                  "l"(router_w + (size_t)c * 128 * E), "r"(wbytes), "r"(b)
                  : "memory");
   };
   if (tid == 0) {
-    issue(0);
-    if (nchunks > 1) issue(1);
+    for (int b = 0; b < kBigSlots; ++b)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"((uint32_t)__cvta_generic_to_shared(&bar[b])));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int c = 0; c < kBigSlots && c < nchunks; ++c) issue(c);
   }
-  // thread <-> expert e, token group g (tokens g*8 .. g*8+7)
-  const int e = tid % E, g = tid / E;
-  const int ngroups = 256 / E;  // >= 2 for E <= 128
-  constexpr int kTPG = kBigTB / 2;
-  float logit[kTPG];
+  float bias_r[EPT];
 #pragma unroll
-  for (int t = 0; t < kTPG; ++t) logit[t] = 0.0f;
-  bool ok = true;
-  for (int c = 0; c < nchunks; ++c) {
-    // this chunk's hidden values, token-minor: xring[slot][k][t]
-    float* xs = xring + (size_t)(c & 1) * 128 * kBigTB;
-    for (int i = tid; i < 128 * kBigTB; i += 256) {
-      const int t = i / 128, k = i % 128;
-      xs[k * kBigTB + t] = tok0 + t < M ? bf16_bits_to_float(hidden[(size_t)(tok0 + t) * H + c * 128 + k]) : 0.0f;
+  for (int j = 0; j < EPT; ++j) bias_r[j] = bias != nullptr ? bias[lane * EPT + j] : 0.0f;
+
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+
+  // hidden values of one pair of chunks: 2 x 128 x 32 BF16, four 16-byte loads per thread;
+  // element (cc, k, t) lands at xring[cc][k][t] as FP32
+  uint4 xr[4];
+  auto load_pair = [&](int p) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int idx = j * 256 + tid, t = idx & 31, g8 = idx >> 5;
+      const int cc = g8 >> 4, k8 = (g8 & 15) * 8;
+      xr[j] = tok0 + t < M ? *reinterpret_cast<const uint4*>(hidden + (size_t)(tok0 + t) * H + (2 * p + cc) * 128 + k8)
+                           : make_uint4(0, 0, 0, 0);
     }
-    __syncthreads();
-    {  // bounded wait for the router chunk
-      const uint32_t b = (uint32_t)__cvta_generic_to_shared(&bar[c & 1]);
-      const uint32_t par = (c >> 1) & 1;
+  };
+  auto store_pair = [&]() {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int idx = j * 256 + tid, t = idx & 31, g8 = idx >> 5;
+      const int cc = g8 >> 4, k8 = (g8 & 15) * 8;
+      const uint32_t w4[4] = {xr[j].x, xr[j].y, xr[j].z, xr[j].w};
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        xring[((size_t)cc * 128 + k8 + u) * kBigTok + t] =
+            bf16_bits_to_float((uint16_t)((u & 1) ? (w4[u / 2] >> 16) : (w4[u / 2] & 0xFFFF)));
+    }
+  };
+  load_pair(0);
+  store_pair();
+  __syncthreads();
+
+  float logit[NA];
+#pragma unroll
+  for (int i = 0; i < NA; ++i) logit[i] = 0.0f;
+  bool ok = true;
+  for (int p = 0; p < npairs; ++p) {
+    if (p + 1 < npairs) load_pair(p + 1);
+    const int c = 2 * p + par, slot = c % kBigSlots;
+    {  // bounded wait for this warp's router chunk
+      const uint32_t b = (uint32_t)__cvta_generic_to_shared(&bar[slot]);
+      const uint32_t ph = (uint32_t)(c / kBigSlots) & 1u;
       uint32_t done = 0;
       const uint64_t t0 = globaltimer_ns();
       while (ok) {
-        asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-                     : "=r"(done) : "r"(b), "r"(par) : "memory");
+        asm volatile("{\n\t.reg .pred q;\n\tmbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                     : "=r"(done) : "r"(b), "r"(ph) : "memory");
         if (done) break;
         if (globaltimer_ns() - t0 > kWaitLimitNs) ok = false;
       }
     }
-    if (g < 2 && ok) {
-      const uint16_t* wcol = wring + (size_t)(c & 1) * 128 * E + e;
-      const float* xk = xs + g * kTPG;
-      float acc[kTPG];
+    float acc[NA];
 #pragma unroll
-      for (int t = 0; t < kTPG; ++t) acc[t] = 0.0f;
-#pragma unroll 8
+    for (int i = 0; i < NA; ++i) acc[i] = 0.0f;
+    if (ok) {
+      const uint16_t* wk = wring + (size_t)slot * 128 * E + lane * EPT;
+      const float* xk = xring + (size_t)par * 128 * kBigTok + grp * 8;
+#pragma unroll 4
       for (int k = 0; k < 128; ++k) {
-        const float w = bf16_bits_to_float(wcol[k * E]);
-        const float4 x0 = *reinterpret_cast<const float4*>(xk + k * kBigTB);
-        const float4 x1 = *reinterpret_cast<const float4*>(xk + k * kBigTB + 4);
+        float w[EPT];
+        if constexpr (EPT == 4) {
+          const uint2 q = *reinterpret_cast<const uint2*>(wk + k * E);
+          w[0] = bf16_bits_to_float(q.x & 0xFFFF); w[1] = bf16_bits_to_float(q.x >> 16);
+          w[2] = bf16_bits_to_float(q.y & 0xFFFF); w[3] = bf16_bits_to_float(q.y >> 16);
+        } else if constexpr (EPT == 2) {
+          const uint32_t q = *reinterpret_cast<const uint32_t*>(wk + k * E);
+          w[0] = bf16_bits_to_float(q & 0xFFFF); w[1] = bf16_bits_to_float(q >> 16);
+        } else {
+          w[0] = bf16_bits_to_float(wk[k * E]);
+        }
+        const float4 x0 = *reinterpret_cast<const float4*>(xk + k * kBigTok);
+        const float4 x1 = *reinterpret_cast<const float4*>(xk + k * kBigTok + 4);
         const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-        for (int t = 0; t < kTPG; ++t) acc[t] = __fmaf_rn(xv[t], w, acc[t]);
-      }
+        for (int j = 0; j < EPT; ++j)
 #pragma unroll
-      for (int t = 0; t < kTPG; ++t) logit[t] = __fadd_rn(logit[t], acc[t]);
+          for (int t = 0; t < 8; ++t) acc[j * 8 + t] = __fmaf_rn(xv[t], w[j], acc[j * 8 + t]);
+      }
     }
-    __syncthreads();  // slot c & 1 is free again
-    if (tid == 0 && c + 2 < nchunks) issue(c + 2);
+    if (par == 1) {
+#pragma unroll
+      for (int i = 0; i < NA; ++i) xch[i * 128 + grp * 32 + lane] = acc[i];
+    }
+    __syncthreads();
+    if (par == 0) {
+#pragma unroll
+      for (int i = 0; i < NA; ++i) logit[i] = __fadd_rn(__fadd_rn(logit[i], acc[i]), xch[i * 128 + grp * 32 + lane]);
+    }
+    __syncthreads();  // the pair's ring slots, hidden values and exchange buffer are free
+    if (tid == 0) {
+      if (2 * p + kBigSlots < nchunks) issue(2 * p + kBigSlots);
+      if (2 * p + 1 + kBigSlots < nchunks) issue(2 * p + 1 + kBigSlots);
+    }
+    if (p + 1 < npairs) {
+      store_pair();
+      __syncthreads();
+    }
   }
-  (void)ngroups;
   // a router chunk that never arrived (bounded wait ran out): the block's tokens get id -1,
   // which the expert FFN skips and reports as MOE_STATUS_BAD_EXPERT_ID
   ok = __syncthreads_and(ok);
   if (!ok) {
-    for (int i = tid; i < kBigTB * K; i += 256)
+    for (int i = tid; i < kBigTok * K; i += 256)
       if (tok0 + i / K < M) {
         ids[(size_t)tok0 * K + i] = -1;
         wts[(size_t)tok0 * K + i] = 0.0f;
       }
     return;
   }
-  if (g < 2) {
+  if (par == 0) {
 #pragma unroll
-    for (int t = 0; t < kTPG; ++t) {
-      float l = logit[t];
-      if (bias != nullptr) l = __fadd_rn(l, bias[e]);
-      logits[(g * kTPG + t) * E + e] = l;
-    }
+    for (int j = 0; j < EPT; ++j)
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        float l = logit[j * 8 + t];
+        if (bias != nullptr) l = __fadd_rn(l, bias_r[j]);
+        logits[(grp * 8 + t) * E + lane * EPT + j] = l;
+      }
   }
   __syncthreads();
-  for (int i = tid; i < kBigTB * E; i += 256) {  // rank selection, ties to the lower index
-    const int t = i / E, ee = i % E;
-    const float* lt = logits + t * E;
-    const float v = lt[ee];
-    int rk = 0;
-    for (int e2 = 0; e2 < E; ++e2) {
-      const float v2 = lt[e2];
-      rk += (v2 > v) || (v2 == v && e2 < ee);
-    }
-    if (rk < K) {
-      sel_v[t * 16 + rk] = v;
-      sel_i[t * 16 + rk] = ee;
-    }
-  }
-  __syncthreads();
-  const int warp = tid / 32, lane = tid % 32;
-  for (int t = warp; t < kBigTB; t += 8) {
+  // top-k per token: warp `warp` takes tokens warp, warp + 8, ...
+  for (int t = warp; t < kBigTok; t += 8) {
     if (tok0 + t >= M) break;
-    const float lmax = sel_v[t * 16];
+    const float* lt = logits + t * E;
+    uint64_t key[EPT];
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) key[j] = logit_key(lt[lane * EPT + j], lane * EPT + j);
+    int my_e = -1;   // lane r < K: the expert of slot r
+    float my_v = 0.0f;
+    for (int r = 0; r < K; ++r) {
+      uint64_t best = key[0];
+#pragma unroll
+      for (int j = 1; j < EPT; ++j) best = key[j] > best ? key[j] : best;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
+        best = o > best ? o : best;
+      }
+      const int e = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFu));
+#pragma unroll
+      for (int j = 0; j < EPT; ++j)
+        if (lane * EPT + j == e) key[j] = 0;  // taken
+      if (lane == r) {
+        my_e = e;
+        my_v = lt[e];
+      }
+    }
+    const float lmax = __shfl_sync(0xffffffffu, my_v, 0);
     float den = 0.0f;
     if (renorm) {
-      for (int j = 0; j < K; ++j) den = __fadd_rn(den, expf(__fsub_rn(sel_v[t * 16 + j], lmax)));
+      for (int j = 0; j < K; ++j) den = __fadd_rn(den, expf(__fsub_rn(__shfl_sync(0xffffffffu, my_v, j), lmax)));
     } else {
-      for (int ee = lane; ee < E; ee += 32) den = __fadd_rn(den, expf(__fsub_rn(logits[t * E + ee], lmax)));
+#pragma unroll
+      for (int j = 0; j < EPT; ++j) den = __fadd_rn(den, expf(__fsub_rn(lt[lane * EPT + j], lmax)));
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) den = __fadd_rn(den, __shfl_xor_sync(0xffffffffu, den, off));
     }
     if (lane < K) {
       const size_t o = (size_t)(tok0 + t) * K + lane;
-      ids[o] = sel_i[t * 16 + lane];
-      wts[o] = __fdiv_rn(expf(__fsub_rn(sel_v[t * 16 + lane], lmax)), den);
+      ids[o] = my_e;
+      wts[o] = __fdiv_rn(expf(__fsub_rn(my_v, lmax)), den);
     }
   }
 }
@@ -388,13 +466,9 @@ cudaError_t launch_route_t(const uint16_t* hidden, const uint16_t* router_w, con
 cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const float* bias, int M,
                          int H, int E, int K, int renorm, int32_t* ids, float* wts, cudaStream_t st) {
   const int nchunks = H / 128;
-  if (M >= 512 && E <= 128) {
-    static std::once_flag once;
-    std::call_once(once, [] {
-      cudaFuncSetAttribute(route_big_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    });
+  if (M >= 512 && (E == 32 || E == 64 || E == 128) && nchunks % 2 == 0) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((M + kBigTB - 1) / kBigTB), 1, 1);
+    cfg.gridDim = dim3((unsigned)((M + kBigTok - 1) / kBigTok), 1, 1);
     cfg.blockDim = dim3(256, 1, 1);
     cfg.dynamicSmemBytes = route_big_smem(E);
     cfg.stream = st;
@@ -403,7 +477,16 @@ cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, route_big_kernel, hidden, router_w, bias, M, H, E, K, renorm, ids, wts);
+    static std::once_flag once;
+    std::call_once(once, [] {
+      cudaFuncSetAttribute(route_big_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      cudaFuncSetAttribute(route_big_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+      cudaFuncSetAttribute(route_big_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    });
+    auto go = [&](auto kern) { return cudaLaunchKernelEx(&cfg, kern, hidden, router_w, bias, M, H, K, renorm, ids, wts); };
+    if (E == 128) return go(route_big_kernel<4>);
+    if (E == 64) return go(route_big_kernel<2>);
+    return go(route_big_kernel<1>);
   }
   if (M >= 16 && route_smem(8, nchunks / route_cluster(nchunks), E, nchunks).total <= 227 * 1024)
     return launch_route_t<8>(hidden, router_w, bias, M, H, E, K, renorm, ids, wts, st);

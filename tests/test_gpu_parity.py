@@ -59,6 +59,36 @@ def test_route_parity(name, M):
     assert np.all(np.abs(wg - w_o) <= 2e-6 * w_o)
 
 
+# the many-token router (M >= 512, E in {32, 64, 128}): ragged last block, every expert
+# count it covers, the bias of the skewed workload, both softmax domains
+BIG_ROUTE = [("prefill", 128, 1000, True), ("prefill", 64, 512, True), ("prefill", 32, 777, False),
+             ("verify_skewed", 128, 600, True), ("decode", 128, 544, False)]
+
+
+@pytest.mark.parametrize("name,E,M,renorm", BIG_ROUTE, ids=[f"{n}-E{e}-M{m}-{r}" for n, e, m, r in BIG_ROUTE])
+def test_route_many_tokens(name, E, M, renorm):
+    x = workload(name, E=E, tokens=M) if name == "decode" else workload(name, E=E, M=M)
+    g = gpu_for(x, M)
+    ids, w = g.route(to_dev(x.hidden[:M]), M, renorm=renorm)
+    torch.cuda.synchronize()
+    ids_o, w_o = oracle_route(x, rows=slice(0, M), renorm=renorm)
+    assert np.array_equal(ids.cpu().numpy(), ids_o)
+    assert np.all(np.abs(w.cpu().numpy() - w_o) <= 2e-6 * w_o)
+
+
+def test_route_many_tokens_ties():
+    # zero hidden rows: every logit is +0, so the top-k are experts 0..K-1 with equal weights
+    M = 640
+    x = inputs.make("prefill", M=M, zero_rows=np.arange(0, M, 7))
+    g = gpu_for(x, M)
+    ids, w = g.route(to_dev(x.hidden[:M]), M)
+    torch.cuda.synchronize()
+    ids_o, w_o = oracle_route(x, rows=slice(0, M))
+    assert np.array_equal(ids.cpu().numpy(), ids_o)
+    assert np.array_equal(ids_o[0], np.arange(x.shape.top_k))
+    assert np.all(np.abs(w.cpu().numpy() - w_o) <= 2e-6 * w_o)
+
+
 def test_route_not_renormalised():
     x = workload("decode", tokens=64)
     g = gpu_for(x, 64)
