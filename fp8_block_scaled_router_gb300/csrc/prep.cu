@@ -74,9 +74,10 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const uint16_t* __re
 //   scatter: block b forms, for every expert, tot[e] = sum over all blocks and
 //            pre[e] = sum over blocks before b, the exclusive scan base[e] over experts, and
 //            places its pairs at base[e] + pre[e] + (earlier pairs of e in this block), so
-//            rows keep ascending flat pair order t*K + j within each expert; it then gathers
-//            each placed pair's hidden codes and scales into xp / sa_p. Block 0 also writes
-//            the expert offsets and the 128-row tile list.
+//            rows keep ascending flat pair order t*K + j within each expert. Block 0 also
+//            writes the expert offsets and the 128-row tile list.
+//   gather:  one warp per placed row copies the row's hidden codes (H bytes) and scales
+//            into xp / sa_p -- thousands of independent 16-byte copies in flight.
 // ---------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) count_quant_kernel(const uint16_t* __restrict__ hidden,
                                                           const int32_t* __restrict__ ids, int M, int H,
@@ -121,28 +122,39 @@ __global__ void __launch_bounds__(256) count_quant_kernel(const uint16_t* __rest
   }
 }
 
-__global__ void __launch_bounds__(256) scatter_gather_kernel(const int32_t* __restrict__ ids, int M, int H,
+__global__ void __launch_bounds__(256) scatter_kernel(const int32_t* __restrict__ ids, int M, int H,
                                                              int E, int K, int nblk, WsPtrs ws) {
   __shared__ int start[kMaxExperts];
   __shared__ int scan[kMaxExperts];
   __shared__ int wcnt[8][kMaxExperts];
-  __shared__ int pos_s[kSortBlock];
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int R = M * K;
   const int b = blockIdx.x;
   (void)lane;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
-  // per expert: total over all blocks and the count in blocks before this one
-  int tot = 0, pre = 0;
-  if (tid < E) {
-#pragma unroll 16
-    for (int bb = 0; bb < nblk; ++bb) {  // independent loads: unrolled so they overlap
-      const int c = ws.blk_counts[(size_t)bb * E + tid];
-      tot += c;
-      pre += bb < b ? c : 0;
+  // per expert: total over all blocks and the count in blocks before this one; the
+  // 256 / E thread groups each sum a slice of the blocks (independent loads in flight)
+  __shared__ int part_tot[256], part_pre[256];
+  {
+    const int e = tid % E, g = tid / E, ng = 256 / E;
+    int t_ = 0, p_ = 0;
+#pragma unroll 8
+    for (int bb = g; bb < nblk; bb += ng) {
+      const int c = ws.blk_counts[(size_t)bb * E + e];
+      t_ += c;
+      p_ += bb < b ? c : 0;
     }
+    part_tot[tid] = t_;
+    part_pre[tid] = p_;
   }
+  __syncthreads();
+  int tot = 0, pre = 0;
+  if (tid < E)
+    for (int g = 0; g < 256 / E; ++g) {
+      tot += part_tot[g * E + tid];
+      pre += part_pre[g * E + tid];
+    }
   // exclusive scan of tot over experts (Hillis-Steele on 256 entries)
   scan[tid] = tid < E ? tot : 0;
   __syncthreads();
@@ -175,7 +187,6 @@ __global__ void __launch_bounds__(256) scatter_gather_kernel(const int32_t* __re
     ws.row_src[pos] = i;
   }
   if (i < R) ws.perm_row[i] = pos;
-  pos_s[tid] = pos;
   // block 0: the 128-row tile list (expert counts are the totals)
   if (b == 0) {
     __syncthreads();
@@ -194,27 +205,30 @@ __global__ void __launch_bounds__(256) scatter_gather_kernel(const int32_t* __re
     }
     if (tid == 255) ws.hdr->n_tiles = (uint32_t)scan[255];
   }
-  __syncthreads();
-  // gather: the block's placed rows, hidden codes (H bytes) and scales, as one flat loop
-  // over (row, 16-byte piece) so that many independent copies are in flight
-  const int per_row = H / 16;
-  const int n16 = kSortBlock * per_row;
-#pragma unroll 8
-  for (int idx = tid; idx < n16; idx += 256) {
-    const int r = idx / per_row, c = idx % per_row;
-    const int p = pos_s[r];
-    if (p < 0) continue;
-    const int t = (b * kSortBlock + r) / K;
-    reinterpret_cast<uint4*>(ws.xp + (size_t)p * H)[c] = reinterpret_cast<const uint4*>(ws.qa + (size_t)t * H)[c];
-  }
-  const int nsc = H / 128;
-  for (int idx = tid; idx < kSortBlock * nsc; idx += 256) {
-    const int r = idx / nsc, c = idx % nsc;
-    const int p = pos_s[r];
-    if (p < 0) continue;
-    const int t = (b * kSortBlock + r) / K;
-    ws.sa_p[(size_t)p * nsc + c] = ws.sa[(size_t)t * nsc + c];
-  }
+}
+
+// xp[p] = qa[row_src[p] / K], sa_p[p] = sa[row_src[p] / K]: one warp per placed row. Only
+// the first offsets[E] rows are placed (pairs with an invalid id are not); row_src past them
+// is not written by this call and is never read.
+__global__ void __launch_bounds__(256) gather_rows_kernel(int R, int H, int E, int K, WsPtrs ws) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int p = blockIdx.x * 8 + warp;
+  if (p >= R || p >= ws.offsets[E]) return;
+  const int t = ws.row_src[p] / K;
+  const uint4* src = reinterpret_cast<const uint4*>(ws.qa + (size_t)t * H);
+  uint4* dst = reinterpret_cast<uint4*>(ws.xp + (size_t)p * H);
+  const int n16 = H / 16;  // <= 512: at most 16 per lane
+  uint4 v[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if (lane + 32 * j < n16) v[j] = src[lane + 32 * j];
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if (lane + 32 * j < n16) dst[lane + 32 * j] = v[j];
+  const int nsc = H / 128;  // <= 64
+  for (int c = lane; c < nsc; c += 32) ws.sa_p[(size_t)p * nsc + c] = ws.sa[(size_t)t * nsc + c];
 }
 
 cudaError_t launch_sort_gather(const uint16_t* hidden, const int32_t* ids, int M, int H, int E, int K,
@@ -235,7 +249,9 @@ cudaError_t launch_sort_gather(const uint16_t* hidden, const int32_t* ids, int M
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, scatter_gather_kernel, ids, M, H, E, K, nblk, ws);
+  if (cudaError_t e = cudaLaunchKernelEx(&cfg, scatter_kernel, ids, M, H, E, K, nblk, ws)) return e;
+  cfg.gridDim = dim3((unsigned)((R + 7) / 8), 1, 1);  // one warp per row, R rows at most
+  return cudaLaunchKernelEx(&cfg, gather_rows_kernel, R, H, E, K, ws);
 }
 
 cudaError_t launch_prep(const uint16_t* hidden, const int32_t* ids, int M, int H, int E, int K,

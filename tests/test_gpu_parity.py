@@ -245,6 +245,26 @@ def test_invalid_ids_flagged_and_skipped():
     assert g2.status() == 0
 
 
+def test_invalid_ids_grouped_path():
+    # 48 tokens x 8 slots = 384 routed rows: expert-sorted tiles; invalid pairs are never
+    # placed, so fewer rows than M*K are gathered and the GEMM tiles cover only valid rows
+    M = 48
+    x = workload("decode", tokens=M)
+    g = gpu_for(x, M)
+    g.ws.fill_(0xFF)  # stale workspace contents must not matter
+    from fp8_block_scaled_router_gb300 import _lib as L
+    L.moe_fp8_workspace_init(g.ws, g.shape)
+    import oracle
+    ids_o, w_o = oracle.route(x.hidden[:M], x.router_w, None, 8)
+    bad = ids_o.copy()
+    bad[0, 1] = -1
+    bad[5, 0] = 128
+    bad[47, 7] = -5
+    out = u16(g.forward(to_dev(x.hidden[:M]), to_dev(bad), to_dev(w_o), M))
+    assert g.status() & 0x1
+    check_out(out, oracle_forward(x, x.hidden[:M], bad, w_o), "invalid ids (grouped)")
+
+
 def test_end_to_end_gpu_route_feeds_forward():
     x = workload("verify_skewed")
     g = gpu_for(x, 12)
