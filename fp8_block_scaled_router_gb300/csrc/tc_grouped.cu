@@ -16,7 +16,8 @@
 // core runs up to two K blocks ahead of the epilogue), and sixteen epilogue warps promote
 // the block sums into FP32 chains
 //   acc = fma(P_kb, sa[row][kb] * sw[block][kb], acc)     kb ascending, from 0,
-// (one rounding per step: the multiply-add is fused here, which the parity window covers);
+// (one rounding per step: the multiply-add is fused here, which the parity window covers;
+// two adjacent columns per packed fma.rn.f32x2);
 // thread = (accumulator row, 64 of the 256 columns).
 // gate/up epilogue: act = silu(g) * u for the thread's 64 columns, the row's amax over 128
 // columns (the partner warp's half via shared memory), scale = amax/448, RNE saturating
@@ -192,9 +193,11 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
       // within the half's 128 accumulator columns: gate/up [gate 64 | up 64], down [128]
       const uint32_t c0 = GATEUP ? sub * 32 : sub * 64;
       const uint32_t c1 = GATEUP ? 64 + sub * 32 : sub * 64 + 32;
-      float acc[64];  // [0,32) run at c0, [32,64) run at c1
+      // promoted chains as FP32 pairs (adjacent columns share a scale): [0,16) the run at
+      // c0, [16,32) the run at c1; fma.rn.f32x2 is two IEEE fmas, bit-identical to fmaf
+      uint64_t acc2[32];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) acc[c] = 0.0f;
+      for (int c = 0; c < 32; ++c) acc2[c] = 0ull;
       float a_n = live ? sarow[0] : 0.0f, s0_n = sw0[0], s1_n = sw1[0];  // scales of block i
       for (int i = 0; i < nkb; ++i, ++it) {
         const float a = a_n, s0 = s0_n, s1 = s1_n;
@@ -207,22 +210,26 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
         const int buf = slot & 3;
         if (ok && !tc::mbar_wait(&accf[buf], (slot >> 2) & 1)) ok = false;
         tc::fence_after_sync();
-        const float sc0 = __fmul_rn(a, s0), sc1 = __fmul_rn(a, s1);
+        const uint32_t sc0 = __float_as_uint(__fmul_rn(a, s0)), sc1 = __float_as_uint(__fmul_rn(a, s1));
+        const uint64_t sc0x2 = tc::f2pack(sc0, sc0), sc1x2 = tc::f2pack(sc1, sc1);
         const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + buf * 128;
         uint32_t P[32];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           tc::tmem_ld16x2u(ta + c0 + h * 16, ta + c1 + h * 16, P);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            acc[h * 16 + c] = __fmaf_rn(__uint_as_float(P[c]), sc0, acc[h * 16 + c]);
-            acc[32 + h * 16 + c] = __fmaf_rn(__uint_as_float(P[16 + c]), sc1, acc[32 + h * 16 + c]);
+          for (int c = 0; c < 8; ++c) {
+            acc2[h * 8 + c] = tc::f2fma(tc::f2pack(P[2 * c], P[2 * c + 1]), sc0x2, acc2[h * 8 + c]);
+            acc2[16 + h * 8 + c] = tc::f2fma(tc::f2pack(P[16 + 2 * c], P[16 + 2 * c + 1]), sc1x2, acc2[16 + h * 8 + c]);
           }
         }
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&acce[buf]);
       }
+      float acc[64];  // [0,32) run at c0, [32,64) run at c1
+#pragma unroll
+      for (int c = 0; c < 32; ++c) tc::f2unpack(acc2[c], acc[2 * c], acc[2 * c + 1]);
       if (GATEUP) {
         // act = silu(g) * u for 32 columns; row amax over the 128 columns of the block
         float act[32];

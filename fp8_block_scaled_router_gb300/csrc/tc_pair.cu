@@ -177,9 +177,6 @@ __global__ void __launch_bounds__(kPairThreads, 3)
       reinterpret_cast<uint4*>(stages + s * C::kStageBytes + C::kTxA)[c] = make_uint4(0, 0, 0, 0);
     }
   }
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;");
-
   const int unit = blockIdx.y;
   int pr, cb, tok;
   if (MODE == kDownCombine) {
@@ -194,7 +191,35 @@ __global__ void __launch_bounds__(kPairThreads, 3)
   const int kb0 = MODE == kDownCombine ? 0 : rank * p.nkb_cta;
   const int brow = MODE == kGateUpWs ? tok : pr;  // B row (qa row or act row)
   const int npre = min(nst, p.nkb_cta);           // stages issued before the block barrier
-  if (warp == 0) {
+  // Down fused with the combine runs right after the gate/up launch, which itself waited
+  // for whatever wrote the top-k ids and weights: those, and the down weights, are complete
+  // before this grid can start, so the weight tiles stream in while gate/up finishes; only
+  // the activation rows (gate/up's output) wait for the grid dependency.
+  constexpr bool kEarly = MODE == kDownCombine;
+  if (kEarly && warp == 0 && lane == 0) {
+    const int e = p.ids[pr];
+    *e_sh = e;
+    if (e >= 0 && e < p.E)
+      for (int i = 0; i < npre; ++i) {
+        tc::mbar_arrive_expect_tx(&full[i], C::kTxA + C::kBBytes);
+        tc::tma_load_2d(stages + i * C::kStageBytes, &tmA, &full[i], (kb0 + i) * 128, e * p.H + cb * 128);
+      }
+  }
+  if (kEarly && rank == 0 && warp == 1 && lane < p.K) {
+    cwt[lane] = p.topk_w[tok * p.K + lane];
+    cid[lane] = p.ids[tok * p.K + lane];
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+
+  if (kEarly && warp == 0) {
+    if (lane == 0) {
+      const int e = *e_sh;
+      if (e >= 0 && e < p.E)
+        for (int i = 0; i < npre; ++i)
+          tc::tma_load_2d(stages + i * C::kStageBytes + C::kTxA, &tmB, &full[i], (kb0 + i) * 128, brow);
+    }
+  } else if (warp == 0) {
     // the expert id, then the first stages' loads: the first bytes are in flight before the
     // rest of the prologue runs
     int e = 0;
@@ -235,10 +260,6 @@ __global__ void __launch_bounds__(kPairThreads, 3)
   } else {
     for (int i = threadIdx.x - 32; i < p.nkb_cta; i += kPairThreads - 32)
       sas[i] = p.a_scale[(size_t)brow * p.nkb + kb0 + i];
-    if (MODE == kDownCombine && rank == 0 && warp == 1 && lane < p.K) {
-      cwt[lane] = p.topk_w[tok * p.K + lane];
-      cid[lane] = p.ids[tok * p.K + lane];
-    }
   }
   tc::fence_before_sync();
   __syncthreads();

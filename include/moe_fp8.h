@@ -144,10 +144,14 @@ moe_status_t moe_fp8_combine(const float* topk_w, int32_t M, void* out, void* wo
 
 /* The few-routed-row path (M * top_k <= 256) as its two kernels, the layout of the
  * accepted M=1 MoE objects of [ARCH] (gate/up + SiLU + quantisation, then down/reduce);
- * moe_fp8_forward runs exactly these two calls for such M. MOE_ERR_UNSUPPORTED above the
- * limit. moe_fp8_gate_up_direct quantises hidden itself and writes the activation codes
+ * moe_fp8_forward runs these two kernels for such M (its gate/up launch also prefetches the
+ * routed experts' w2 blocks into L2; the arithmetic is the same). MOE_ERR_UNSUPPORTED above
+ * the limit. moe_fp8_gate_up_direct quantises hidden itself and writes the activation codes
  * and scales (pair order) to the workspace; moe_fp8_down_combine reads them and writes out
- * with the combine of moe_fp8_combine (slot order, FP32 multiply then add, from 0). */
+ * with the combine of moe_fp8_combine (slot order, FP32 multiply then add, from 0).
+ * moe_fp8_down_combine reads topk_ids, topk_w, w2 and w2_scale while the kernel launched
+ * just before it on `stream` (normally moe_fp8_gate_up_direct) may still be running, so
+ * that kernel must not write them; the activation is read only after it has completed. */
 moe_status_t moe_fp8_gate_up_direct(const void* hidden, const int32_t* topk_ids, int32_t M,
                                     const uint8_t* w13, const float* w13_scale, void* workspace,
                                     size_t workspace_bytes, const moe_fp8_shape_t* shape,
