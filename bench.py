@@ -66,6 +66,8 @@ def parse():
     p.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
     p.add_argument("--m", type=int, default=None, help="tokens per step (wide sweep)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--dominant-only", type=int, default=0, metavar="N",
+                   help="run only N launches of the dominant kernel (gate/up) and exit, for ncu")
     return p.parse_args()
 
 
@@ -289,7 +291,27 @@ def ours_arm(args, wl, world, rank, local):
             ii, ww = ids[b], wts[b]
         L.moe_fp8_forward(hid, ii, ww, M, w13, s13, w2, s2, out[b], ws, shape, stream=stream)
 
-    kernels_per_step = 5  # route, prepare, gate/up, down, combine
+    # our kernels per step: few routed rows -> route, gate/up, down+combine; otherwise route,
+    # count+quantise, scatter, gather, gate/up, down, combine
+    kernels_per_step = 3 if M * K <= 256 else 7
+
+    if args.dominant_only:
+        # only the dominant kernel (the launch the roofline times), for a profiler
+        st = torch.cuda.current_stream()
+        ii0 = given_ids[0] if given_ids is not None else None
+        if ii0 is None:
+            L.moe_route(hidden_all[:M], router, bias, M, shape, True, ids[0], wts[0])
+            ii0 = ids[0]
+        if M * K > 256:
+            L.moe_fp8_prepare(hidden_all[:M], ii0, M, ws, shape)
+        for i in range(args.dominant_only):
+            w13, s13, _, _ = reps[i % n_rep]
+            if M * K <= 256:
+                L.moe_fp8_gate_up_direct(hidden_all[:M], ii0, M, w13, s13, ws, shape, stream=st)
+            else:
+                L.moe_fp8_gate_up(w13, s13, M, ws, shape, stream=st)
+        torch.cuda.synchronize()
+        return
 
     # distinct experts per step (accounting only)
     for i in range(min(nbatches, 64)):
