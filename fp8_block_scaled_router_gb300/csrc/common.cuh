@@ -142,6 +142,13 @@ __device__ __forceinline__ float silu_mul_rcp(float g, float u) {
   return __fmul_rn(__fmul_rn(g, __frcp_rn(__fadd_rn(1.0f, expf(-g)))), u);
 }
 
+// silu(g) * u with the fast exponential and division intrinsics (a few ulp from silu_mul;
+// for the many-row epilogue, where the tail of each 128-row tile is on the critical path).
+// For g below about -88 the exponential overflows to +inf and the quotient is -0.
+__device__ __forceinline__ float silu_mul_fast(float g, float u) {
+  return __fmul_rn(__fdividef(g, __fadd_rn(1.0f, __expf(-g))), u);
+}
+
 __device__ __forceinline__ void set_status(Header* hdr, uint32_t bits) {
   atomicOr(&hdr->status, bits);  // a flag word, never a value accumulation
 }

@@ -19,9 +19,10 @@
 // (one rounding per step: the multiply-add is fused here, which the parity window covers;
 // two adjacent columns per packed fma.rn.f32x2);
 // thread = (accumulator row, 64 of the 256 columns).
-// gate/up epilogue: act = silu(g) * u for the thread's 64 columns, the row's amax over 128
-// columns (the partner warp's half via shared memory), scale = amax/448, RNE saturating
-// E4M3 codes -> act [row][I] and act_scale [row][I/128]. down epilogue: y [row][H] FP32.
+// gate/up epilogue: act = silu(g) * u (fast exponential and division intrinsics, a few ulp)
+// for the thread's columns, the row's amax over 128 columns (the partner warps' parts via
+// shared memory), scale = amax/448, RNE saturating E4M3 codes -> act [row][I] and
+// act_scale [row][I/128]. down epilogue: y [row][H] FP32 in 32-byte stores.
 // Rows of a tile past its length are computed on zero/neighbour rows and never stored.
 #include <cudaTypedefs.h>
 
@@ -236,7 +237,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
         float amax = 0.0f;
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          act[c] = silu_mul_rcp(acc[c], acc[32 + c]);
+          act[c] = silu_mul_fast(acc[c], acc[32 + c]);
           amax = fmaxf(amax, fabsf(act[c]));
         }
         red[row * 4 + slot4] = amax;
@@ -264,10 +265,14 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
           if (slot4 == 0) p.act_scale_out[(size_t)(row0 + row) * (p.I / 128) + nb] = s2;
         }
       } else if (live) {
-        float4* dst = reinterpret_cast<float4*>(p.y_out + (size_t)(row0 + row) * p.H + nb * 256 + slot4 * 64);
+        // 32-byte stores: each one fills a whole L2 sector of the row
+        float* dst = p.y_out + (size_t)(row0 + row) * p.H + nb * 256 + slot4 * 64;
 #pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4)
-          dst[c4] = make_float4(acc[4 * c4], acc[4 * c4 + 1], acc[4 * c4 + 2], acc[4 * c4 + 3]);
+        for (int c8 = 0; c8 < 8; ++c8)
+          asm volatile("st.global.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst + 8 * c8), "f"(acc[8 * c8]),
+                       "f"(acc[8 * c8 + 1]), "f"(acc[8 * c8 + 2]), "f"(acc[8 * c8 + 3]), "f"(acc[8 * c8 + 4]),
+                       "f"(acc[8 * c8 + 5]), "f"(acc[8 * c8 + 6]), "f"(acc[8 * c8 + 7])
+                       : "memory");
       }
     }
   }
