@@ -9,8 +9,10 @@
 // Persistent: one CTA per SM walks the (tile, 256-wide output block) units. A = the tile's 128 activation rows (FP8,
 // expert-sorted: the gathered hidden codes for gate/up, the activation codes for down),
 // B = 256 weight rows of the tile's expert -- for gate/up the 128 gate rows of an output
-// block followed by the matching 128 up rows, for down 256 rows of w2. Per 128-wide K block
-// the TMA warp loads A (16 KB) and B (32 KB) into a four-stage ring (128-byte swizzle), the
+// block and the matching 128 up rows, interleaved in groups of 64 (two boxes of a 3-D view
+// of w13: 64 rows x {gate, up}), for down 256 rows of w2 (one box). Per 128-wide K block
+// three lanes of the TMA warp load A (16 KB) and B (32 KB) -- few, tall boxes stream
+// faster per issue than many short ones -- into a four-stage ring (128-byte swizzle), the
 // MMA warp issues four 128x256x32 FP8 MMAs into a fresh accumulator (double-buffered:
 // per K block: two 128x128x32 halves into four 128-column TMEM buffers, so the tensor
 // core runs up to two K blocks ahead of the epilogue), and sixteen epilogue warps promote
@@ -108,33 +110,32 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
 
   bool ok = true;
   if (warp == 0) {
-    if (lane == 0) {
-      int it = 0;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const int nb = u % p.nnb;
-        const Tile tl = p.tiles[u / p.nnb];
-        // B rows in shared memory: gate/up [gate 0-63 | up 0-63 | gate 64-127 | up 64-127]
-        // of the output block (each 128-row half = matching gate and up rows), down
-        // [w2 rows nb*256 .. +128 | +128 .. +256]
-        const int yg = tl.expert * 2 * p.I + nb * 128, yu = yg + p.I;
-        const int yd = tl.expert * p.H + nb * 256;
-        for (int i = 0; i < nkb; ++i, ++it) {
-          const int s = it % kGrpStages;
-          const uint32_t ph = (it / kGrpStages) & 1;
-          if (!tc::mbar_wait(&empty[s], ph ^ 1)) { ok = false; break; }
-          unsigned char* st = stages + s * kGrpStageBytes;
-          tc::mbar_arrive_expect_tx(&full[s], kGrpStageBytes);
-          const int x = i * 128;
-          tc::tma_load_2d(st, &tmA, &full[s], x, tl.row0);
-          if (GATEUP) {
-            tc::tma_load_2d(st + kGrpABytes, &tmB, &full[s], x, yg);
-            tc::tma_load_2d(st + kGrpABytes + 64 * 128, &tmB, &full[s], x, yu);
-            tc::tma_load_2d(st + kGrpABytes + 128 * 128, &tmB, &full[s], x, yg + 64);
-            tc::tma_load_2d(st + kGrpABytes + 192 * 128, &tmB, &full[s], x, yu + 64);
-          } else {
-            tc::tma_load_2d(st + kGrpABytes, &tmB, &full[s], x, yd);
-            tc::tma_load_2d(st + kGrpABytes + 128 * 128, &tmB, &full[s], x, yd + 128);
+    int it = 0;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const int nb = u % p.nnb;
+      const Tile tl = p.tiles[u / p.nnb];
+      // B rows in shared memory: gate/up [gate 0-63 | up 0-63 | gate 64-127 | up 64-127]
+      // of the output block (each 128-row half = matching gate and up rows), down
+      // [w2 rows nb*256 .. +256]
+      const int yd = tl.expert * p.H + nb * 256;
+      for (int i = 0; i < nkb; ++i, ++it) {
+        const int s = it % kGrpStages;
+        const uint32_t ph = (it / kGrpStages) & 1;
+        bool w_ok = true;
+        if (lane == 0) w_ok = tc::mbar_wait(&empty[s], ph ^ 1);
+        if (!__shfl_sync(0xffffffffu, (int)w_ok, 0)) { ok = false; break; }
+        unsigned char* st = stages + s * kGrpStageBytes;
+        if (lane == 0) tc::mbar_arrive_expect_tx(&full[s], kGrpStageBytes);
+        __syncwarp();
+        const int x = i * 128;
+        if (lane == 0) tc::tma_load_2d(st, &tmA, &full[s], x, tl.row0);
+        if (GATEUP) {
+          if (lane == 1 || lane == 2) {
+            const int h = lane - 1;  // rows nb*128 + h*64 .. +64 of gate (z = 2e) and up (2e+1)
+            tc::tma_load_3d(st + kGrpABytes + h * 128 * 128, &tmB, &full[s], x, nb * 128 + h * 64, 2 * tl.expert);
           }
+        } else if (lane == 1) {
+          tc::tma_load_2d(st + kGrpABytes, &tmB, &full[s], x, yd);
         }
       }
     }
@@ -285,6 +286,8 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
 }
 
 bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
+bool make_tmap_u8_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
+                     uint64_t s2, uint32_t b1, uint32_t b2);
 
 namespace {
 
@@ -324,8 +327,10 @@ cudaError_t launch_grouped_gateup(const uint8_t* w13, const float* s13, int64_t 
                                   int64_t max_tiles, const WsPtrs& ws, cudaStream_t st) {
   CUtensorMap tA, tB;
   if (!make_tmap_u8(&tA, ws.xp, (uint64_t)H, (uint64_t)R, 128)) return cudaErrorInvalidValue;
-  // 64-row boxes: each K-block stage holds gate/up rows interleaved in groups of 64
-  if (!make_tmap_u8(&tB, w13, (uint64_t)H, (uint64_t)E * 2 * I, 64)) return cudaErrorInvalidValue;
+  // w13 viewed as [2E][I][H] (z = 2e gate, 2e + 1 up); a box is 64 rows of gate then the same
+  // 64 rows of up
+  if (!make_tmap_u8_3d(&tB, w13, (uint64_t)H, (uint64_t)I, (uint64_t)E * 2, (uint64_t)H, (uint64_t)I * H, 64, 2))
+    return cudaErrorInvalidValue;
   GrpParams prm{};
   prm.H = H; prm.I = I; prm.E = E;
   prm.nkb = H / 128;
@@ -345,7 +350,8 @@ cudaError_t launch_grouped_down(const uint8_t* w2, const float* s2w, int64_t R, 
                                 int64_t max_tiles, const WsPtrs& ws, cudaStream_t st) {
   CUtensorMap tA, tB;
   if (!make_tmap_u8(&tA, ws.act, (uint64_t)I, (uint64_t)R, 128)) return cudaErrorInvalidValue;
-  if (!make_tmap_u8(&tB, w2, (uint64_t)I, (uint64_t)E * H, 128)) return cudaErrorInvalidValue;
+  // one 256-row box per stage: the w2 rows of the 256-wide output block
+  if (!make_tmap_u8(&tB, w2, (uint64_t)I, (uint64_t)E * H, 256)) return cudaErrorInvalidValue;
   GrpParams prm{};
   prm.H = H; prm.I = I; prm.E = E;
   prm.nkb = I / 128;
