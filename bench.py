@@ -57,6 +57,10 @@ WORKLOADS = {
 }
 
 
+# routed rows up to which moe_fp8_forward runs the two pair kernels
+PAIR_ROWS = 64
+
+
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -291,9 +295,10 @@ def ours_arm(args, wl, world, rank, local):
             ii, ww = ids[b], wts[b]
         L.moe_fp8_forward(hid, ii, ww, M, w13, s13, w2, s2, out[b], ws, shape, stream=stream)
 
-    # our kernels per step: few routed rows -> route, gate/up, down+combine; otherwise route,
+    # our kernels per step: few routed rows (M*K <= PAIR_ROWS, the library's switch to sorted
+    # expert tiles) -> route, gate/up, down+combine; otherwise route,
     # count+quantise, scatter, gather, gate/up, down, combine
-    kernels_per_step = 3 if M * K <= 256 else 7
+    kernels_per_step = 3 if M * K <= PAIR_ROWS else 7
 
     if args.dominant_only:
         # only the dominant kernel (the launch the roofline times), for a profiler
@@ -302,11 +307,11 @@ def ours_arm(args, wl, world, rank, local):
         if ii0 is None:
             L.moe_route(hidden_all[:M], router, bias, M, shape, True, ids[0], wts[0])
             ii0 = ids[0]
-        if M * K > 256:
+        if M * K > PAIR_ROWS:
             L.moe_fp8_prepare(hidden_all[:M], ii0, M, ws, shape)
         for i in range(args.dominant_only):
             w13, s13, _, _ = reps[i % n_rep]
-            if M * K <= 256:
+            if M * K <= PAIR_ROWS:
                 L.moe_fp8_gate_up_direct(hidden_all[:M], ii0, M, w13, s13, ws, shape, stream=st)
             else:
                 L.moe_fp8_gate_up(w13, s13, M, ws, shape, stream=st)
@@ -374,7 +379,7 @@ def ours_arm(args, wl, world, rank, local):
     # ---- dominant kernel alone: gate/up, back to back in a CUDA graph on its own stream
     # (few routed rows: the direct gate/up kernel of the step; otherwise the stage kernel
     # after one prepare), rotating weight replicas and the steps' expert sets
-    pair_mode = M * K <= 256
+    pair_mode = M * K <= PAIR_ROWS
     n_k = 200 if pair_mode else 10
     ks = torch.cuda.Stream()
     ks.wait_stream(torch.cuda.current_stream())

@@ -210,7 +210,7 @@ moe_status_t moe_fp8_gate_up_direct(const void* hidden, const int32_t* topk_ids,
   Layout L;
   if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
   if (M == 0) return MOE_OK;
-  if (!use_pair_mode((int64_t)M * shape->top_k)) return MOE_ERR_UNSUPPORTED;
+  if (!pair_capable((int64_t)M * shape->top_k)) return MOE_ERR_UNSUPPORTED;
   const WsPtrs ws = ws_ptrs(workspace, L);
   return launched(launch_pair_gateup(w13, w13_scale, topk_ids, static_cast<const uint16_t*>(hidden), M,
                                      shape->hidden, shape->inter, shape->num_experts, shape->top_k, ws,
@@ -228,7 +228,7 @@ moe_status_t moe_fp8_down_combine(const int32_t* topk_ids, const float* topk_w, 
   Layout L;
   if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
   if (M == 0) return MOE_OK;
-  if (!use_pair_mode((int64_t)M * shape->top_k)) return MOE_ERR_UNSUPPORTED;
+  if (!pair_capable((int64_t)M * shape->top_k)) return MOE_ERR_UNSUPPORTED;
   const WsPtrs ws = ws_ptrs(workspace, L);
   return launched(launch_pair_down(w2, w2_scale, topk_ids, topk_w, static_cast<uint16_t*>(out), M,
                                    shape->hidden, shape->inter, shape->num_experts, shape->top_k, ws,

@@ -43,11 +43,15 @@ constexpr int kTileRows = 128;
 // Routed pairs per block of the multi-block counting sort.
 constexpr int kSortBlock = 256;
 
-// Up to this many routed rows (M*K) every (token, slot) pair is its own GEMM unit ("pair
-// mode": no sort, weights of an expert chosen by several pairs are re-read from L2);
-// above it the rows are sorted into expert tiles.
+// Pair mode: every (token, slot) pair is its own GEMM unit -- no sort, but the weights of
+// an expert chosen by several pairs are re-read once per pair. The pair kernels take up to
+// kPairMaxRows routed rows (M*K); the layer uses them up to kPairPreferRows, above which
+// sorting the rows into expert tiles (each expert's weights read once per 128 rows) was
+// measured faster on every shape tried (h2048/i768/e128/top8 and h6144/i768/e128/top4).
 constexpr int kPairMaxRows = 256;
-inline bool use_pair_mode(int64_t R) { return R <= kPairMaxRows; }
+constexpr int kPairPreferRows = 64;
+inline bool pair_capable(int64_t R) { return R <= kPairMaxRows; }
+inline bool use_pair_mode(int64_t R) { return R <= kPairPreferRows; }
 
 inline int64_t max_tiles_for(int64_t R, int E, int tile_rows) {
   // sum over experts of ceil(n_e / tile_rows) <= R / tile_rows + (non-empty experts)

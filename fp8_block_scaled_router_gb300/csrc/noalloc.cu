@@ -66,7 +66,7 @@ extern "C" moe_status_t moe_fp8_forward_noalloc(const void* hidden, const int32_
   const int H = shape->hidden, I = shape->inter, E = shape->num_experts, K = shape->top_k;
   const int64_t R = (int64_t)M * K;
   // limits: the few-row path only, and the activation must fit the scratch array
-  if (!use_pair_mode(R) || noalloc_bytes(R, I) > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED;
+  if (!pair_capable(R) || noalloc_bytes(R, I) > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED;
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_LAUNCH;

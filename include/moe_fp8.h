@@ -9,8 +9,8 @@
  *              at one scale per routed row per 128 columns          (moe_fp8_gate_up)
  *   down       block-scaled grouped GEMM                            (moe_fp8_down)
  *   combine    top-k weighted sum in slot order, no atomics         (moe_fp8_combine)
- * moe_fp8_forward runs prepare -> gate/up -> down -> combine, or, for few routed rows,
- * gate/up (quantising hidden itself) -> down fused with the combine.
+ * moe_fp8_forward runs prepare -> gate/up -> down -> combine, or, for at most 64 routed
+ * rows (M * top_k), gate/up (quantising hidden itself) -> down fused with the combine.
  *
  * Sources (web pages; each entry point names the passage that defines it):
  *   [NK]   "NetraRuntime/netra-kernel" README
@@ -142,11 +142,12 @@ moe_status_t moe_fp8_combine(const float* topk_w, int32_t M, void* out, void* wo
                              size_t workspace_bytes, const moe_fp8_shape_t* shape,
                              cudaStream_t stream);
 
-/* The few-routed-row path (M * top_k <= 256) as its two kernels, the layout of the
- * accepted M=1 MoE objects of [ARCH] (gate/up + SiLU + quantisation, then down/reduce);
- * moe_fp8_forward runs these two kernels for such M (its gate/up launch also prefetches the
- * routed experts' w2 blocks into L2; the arithmetic is the same). MOE_ERR_UNSUPPORTED above
- * the limit. moe_fp8_gate_up_direct quantises hidden itself and writes the activation codes
+/* The few-routed-row path as its two kernels (one unit per (token, slot) pair; M * top_k
+ * <= 256), the layout of the accepted M=1 MoE objects of [ARCH] (gate/up + SiLU +
+ * quantisation, then down/reduce). moe_fp8_forward runs these two kernels when M * top_k
+ * <= 64 (its gate/up launch also prefetches the routed experts' w2 blocks into L2; the
+ * arithmetic is the same); above that it sorts the pairs into expert tiles, which re-reads
+ * fewer weights. MOE_ERR_UNSUPPORTED above 256 rows. moe_fp8_gate_up_direct quantises hidden itself and writes the activation codes
  * and scales (pair order) to the workspace; moe_fp8_down_combine reads them and writes out
  * with the combine of moe_fp8_combine (slot order, FP32 multiply then add, from 0).
  * moe_fp8_down_combine reads topk_ids, topk_w, w2 and w2_scale while the kernel launched
@@ -187,14 +188,16 @@ moe_status_t moe_fp8_workspace_view(void* workspace, size_t workspace_bytes,
  * an addition of this library. The intermediate activation lives in a 1 MiB scratch array
  * compiled into the library (a file-scope __device__ array that every GPU loading the
  * library keeps until process exit), so this call allocates nothing.
- * Limits: only the few-routed-row path (M * top_k <= 256) and M * top_k * (inter + inter/32)
- * + 512 <= 1 MiB; anything larger returns MOE_ERR_UNSUPPORTED.
+ * It runs the kernels of moe_fp8_gate_up_direct + moe_fp8_down_combine.
+ * Limits: M * top_k <= 256 and M * top_k * (inter + inter/32) + 512 <= 1 MiB; anything
+ * larger returns MOE_ERR_UNSUPPORTED.
  * Set-up: the first call on a device (made with that device current) looks up the array's
  * device address; make that first call before any stream capture.
  * Sharing: all calls on a device share the array, which keeps the last call's contents;
  * calls whose GPU work overlaps (unordered streams) race on it. Each call clears the
  * array's status word on `stream`; device status bits are not readable through this call.
- * Numerics and outputs are identical to moe_fp8_forward. */
+ * Numerics and outputs are identical to moe_fp8_gate_up_direct + moe_fp8_down_combine, and so
+ * to moe_fp8_forward when M * top_k <= 64. */
 moe_status_t moe_fp8_forward_noalloc(const void* hidden, const int32_t* topk_ids, const float* topk_w,
                                      int32_t M, const uint8_t* w13, const float* w13_scale,
                                      const uint8_t* w2, const float* w2_scale, void* out,

@@ -170,9 +170,9 @@ def check_act(ws, dbg, K, what=""):
     return int(mism.sum()), int(mism.size)
 
 
-# Up to this many routed rows the library runs every (token, slot) pair as its own unit
+# Up to this many routed rows moe_fp8_forward runs every (token, slot) pair as its own unit
 # (identity permutation); above it the pairs are sorted into expert-contiguous tiles.
-PAIR_MAX_ROWS = 256
+PAIR_MAX_ROWS = 64
 
 
 def check_permutation(ws, ids, E):
