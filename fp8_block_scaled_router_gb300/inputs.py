@@ -53,6 +53,11 @@ CONFIGS = {
     "prefill": dict(shape=Shape(2048, 768, 128, 8), M=4096, router_std=None, seed=4),
     "prefill_zipf": dict(shape=Shape(2048, 768, 128, 8), M=4096, router_std=None, seed=5,
                          zipf=1.1),
+    # edges of the supported shape set (parity tests only): the largest hidden and
+    # intermediate sizes, the most experts with the largest top-k, and top-1
+    "max_dims": dict(shape=Shape(8192, 4096, 8, 8), M=16, router_std=0.02, seed=6),
+    "many_experts": dict(shape=Shape(256, 128, 256, 16), M=24, router_std=0.02, seed=7),
+    "top1": dict(shape=Shape(2048, 768, 16, 1), M=100, router_std=0.02, seed=8),
 }
 
 
