@@ -25,7 +25,8 @@ STATUS_WAIT_TIMEOUT = 0x2
 EXPORTS = ("moe_fp8_version", "moe_fp8_workspace_bytes", "moe_fp8_workspace_init", "moe_route",
            "moe_fp8_forward", "moe_fp8_prepare", "moe_fp8_gate_up", "moe_fp8_down",
            "moe_fp8_combine", "moe_fp8_workspace_view", "moe_fp8_read_status",
-           "moe_fp8_forward_noalloc", "moe_fp8_gate_up_direct", "moe_fp8_down_combine")
+           "moe_fp8_forward_noalloc", "moe_fp8_gate_up_direct", "moe_fp8_down_combine",
+           "moe_fp8_route_forward_host")
 
 
 class MoEError(RuntimeError):
@@ -42,7 +43,8 @@ class Shape(ctypes.Structure):
 
 class WsView(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
-                ("qa", "sa", "row_src", "perm_row", "act", "act_scale", "y", "expert_offsets")]
+                ("qa", "sa", "row_src", "perm_row", "act", "act_scale", "y", "expert_offsets", "topk_ids",
+                 "topk_w")]
 
 
 def load(path: str = LIB):
@@ -70,6 +72,7 @@ def load(path: str = LIB):
             lib.moe_fp8_forward_noalloc.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, sp, vp]
             lib.moe_fp8_gate_up_direct.argtypes = [vp, vp, i32, vp, vp, vp, sz, sp, vp]
             lib.moe_fp8_down_combine.argtypes = [vp, vp, i32, vp, vp, vp, vp, sz, sp, vp]
+            lib.moe_fp8_route_forward_host.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, vp, vp, vp, sz, sp, vp]
             for f in EXPORTS[2:]:
                 if f != "moe_fp8_workspace_bytes":
                     getattr(lib, f).restype = i32
@@ -203,3 +206,13 @@ def moe_fp8_forward_noalloc(hidden, topk_ids, topk_w, M, w13, w13_scale, w2, w2_
     return _check("moe_fp8_forward_noalloc", load().moe_fp8_forward_noalloc(
         _ptr(hidden), _ptr(topk_ids), _ptr(topk_w), int(M), _ptr(w13), _ptr(w13_scale), _ptr(w2),
         _ptr(w2_scale), _ptr(out), ctypes.byref(shape), _stream(stream)), check)
+
+
+def moe_fp8_route_forward_host(host_hidden, host_out, M, router_w, bias, renormalize, w13, w13_scale, w2,
+                               w2_scale, workspace, shape: Shape, stream=None, ws_bytes=None, check=True):
+    """moe_route + moe_fp8_forward with hidden and out in (pinned) host memory; see
+    include/moe_fp8.h. Returns at once; synchronise the stream before reading host_out."""
+    nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return _check("moe_fp8_route_forward_host", load().moe_fp8_route_forward_host(
+        _ptr(host_hidden), _ptr(host_out), int(M), _ptr(router_w), _ptr(bias), int(bool(renormalize)), _ptr(w13),
+        _ptr(w13_scale), _ptr(w2), _ptr(w2_scale), _ptr(workspace), nb, ctypes.byref(shape), _stream(stream)), check)

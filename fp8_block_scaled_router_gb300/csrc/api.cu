@@ -250,7 +250,34 @@ moe_status_t moe_fp8_workspace_view(void* workspace, size_t workspace_bytes,
   view->act_scale = ws.act_scale;
   view->y = ws.y;
   view->expert_offsets = ws.offsets;
+  view->topk_ids = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + L.ids_stage);
+  view->topk_w = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.wts_stage);
   return MOE_OK;
+}
+
+moe_status_t moe_fp8_route_forward_host(const void* host_hidden, void* host_out, int32_t M,
+                                        const void* router_w, const float* bias, int32_t renormalize,
+                                        const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
+                                        const float* w2_scale, void* workspace, size_t workspace_bytes,
+                                        const moe_fp8_shape_t* shape, cudaStream_t stream) {
+  if (moe_status_t st = check_common(shape, M)) return st;
+  if (!host_hidden || !host_out) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  if (M == 0) return MOE_OK;
+  char* b = static_cast<char*>(workspace);
+  void* hid = b + L.hid_stage;
+  void* out = b + L.out_stage;
+  int32_t* ids = reinterpret_cast<int32_t*>(b + L.ids_stage);
+  float* wts = reinterpret_cast<float*>(b + L.wts_stage);
+  const size_t bytes = (size_t)M * shape->hidden * 2;
+  if (cudaMemcpyAsync(hid, host_hidden, bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return MOE_ERR_LAUNCH;
+  if (moe_status_t st = moe_route(hid, router_w, bias, M, shape, renormalize, ids, wts, stream)) return st;
+  if (moe_status_t st = moe_fp8_forward(hid, ids, wts, M, w13, w13_scale, w2, w2_scale, out, workspace,
+                                        workspace_bytes, shape, stream))
+    return st;
+  return launched(cudaMemcpyAsync(host_out, out, bytes, cudaMemcpyDeviceToHost, stream));
 }
 
 moe_status_t moe_fp8_read_status(const void* workspace, uint32_t* host_dst, cudaStream_t stream) {

@@ -177,9 +177,30 @@ typedef struct {
   float* act_scale;
   float* y;
   int32_t* expert_offsets; /* i32 [E+1] start of each expert's rows */
+  int32_t* topk_ids;       /* i32 [M][K], f32 [M][K]: the routing of the last */
+  float* topk_w;           /*   moe_fp8_route_forward_host call */
 } moe_fp8_ws_view_t;
 moe_status_t moe_fp8_workspace_view(void* workspace, size_t workspace_bytes,
                                     const moe_fp8_shape_t* shape, moe_fp8_ws_view_t* view);
+
+/* The whole layer for a caller holding the tokens in host memory: one call enqueues on
+ * `stream` the copy of hidden to the device (into the workspace), moe_route, moe_fp8_forward
+ * and the copy of out back to the host, and returns at once; the caller synchronises the
+ * stream before reading host_out. No counterpart in the paper: this is an addition of this
+ * library (a host-facing entry for integrations that keep activations in host memory).
+ *   host_hidden  BF16 [M][H] host memory, read by the first copy
+ *   host_out     BF16 [M][H] host memory, written by the last copy
+ *   the other arguments as for moe_route and moe_fp8_forward (router_w, bias, w13, w13_scale,
+ *   w2, w2_scale are device pointers).
+ * Host buffers should be page-locked (pinned): with pageable memory the copies are staged
+ * by the driver and the call does not return until they are done. The routing is kept in
+ * the workspace (moe_fp8_workspace_view: topk_ids, topk_w). Results equal moe_route then
+ * moe_fp8_forward on the same inputs. */
+moe_status_t moe_fp8_route_forward_host(const void* host_hidden, void* host_out, int32_t M,
+                                        const void* router_w, const float* bias, int32_t renormalize,
+                                        const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
+                                        const float* w2_scale, void* workspace, size_t workspace_bytes,
+                                        const moe_fp8_shape_t* shape, cudaStream_t stream);
 
 /* moe_fp8_forward for callers that cannot allocate device memory where they run the layer
  * (for example while a memory pool is locked or being resized, inside callbacks that must
