@@ -38,6 +38,17 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Device address of page-locked (pinned or registered) host memory, or null for any other
+// pointer (pageable host memory, device memory, unknown).
+const void* device_view(const void* host) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 // The compiled contract set.
 bool shape_supported(const moe_fp8_shape_t* s) {
   if (!s) return false;
@@ -266,18 +277,28 @@ moe_status_t moe_fp8_route_forward_host(const void* host_hidden, void* host_out,
   if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
   if (M == 0) return MOE_OK;
   char* b = static_cast<char*>(workspace);
-  void* hid = b + L.hid_stage;
-  void* out = b + L.out_stage;
   int32_t* ids = reinterpret_cast<int32_t*>(b + L.ids_stage);
   float* wts = reinterpret_cast<float*>(b + L.wts_stage);
   const size_t bytes = (size_t)M * shape->hidden * 2;
-  if (cudaMemcpyAsync(hid, host_hidden, bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
-    return MOE_ERR_LAUNCH;
+  // Page-locked host buffers are device-addressable: the kernels read hidden from and write
+  // out to them directly, with no copies (one fewer round trip per direction). Pageable
+  // buffers go through device copies in the workspace.
+  const void* hid = device_view(host_hidden);
+  void* out = const_cast<void*>(device_view(host_out));
+  const bool copy_in = hid == nullptr, copy_out = out == nullptr;
+  if (copy_in) {
+    hid = b + L.hid_stage;
+    if (cudaMemcpyAsync(const_cast<void*>(hid), host_hidden, bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+      return MOE_ERR_LAUNCH;
+  }
+  if (copy_out) out = b + L.out_stage;
+  if (!aligned16(hid) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
   if (moe_status_t st = moe_route(hid, router_w, bias, M, shape, renormalize, ids, wts, stream)) return st;
   if (moe_status_t st = moe_fp8_forward(hid, ids, wts, M, w13, w13_scale, w2, w2_scale, out, workspace,
                                         workspace_bytes, shape, stream))
     return st;
-  return launched(cudaMemcpyAsync(host_out, out, bytes, cudaMemcpyDeviceToHost, stream));
+  if (copy_out) return launched(cudaMemcpyAsync(host_out, out, bytes, cudaMemcpyDeviceToHost, stream));
+  return MOE_OK;
 }
 
 moe_status_t moe_fp8_read_status(const void* workspace, uint32_t* host_dst, cudaStream_t stream) {

@@ -470,16 +470,44 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 2-D u8 tensor [rows][inner] (row stride = inner bytes), box = 128 bytes x box_rows,
 // 128-byte swizzle, out-of-range rows read as zero.
+// Tensor maps depend only on (base, inner, rows, box_rows): the last few encodings of each
+// host thread are kept, so a call sequence that reuses its weights and workspace encodes
+// them once (the encode is a driver call on the launch path).
+namespace {
+struct TmapEntry {
+  const void* base;
+  uint64_t inner, rows;
+  uint32_t box_rows;
+  CUtensorMap map;
+};
+constexpr int kTmapCache = 32;
+thread_local TmapEntry g_tmap_cache[kTmapCache];
+thread_local int g_tmap_used = 0, g_tmap_next = 0;
+}  // namespace
+
 bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  for (int i = 0; i < g_tmap_used; ++i) {
+    const TmapEntry& c = g_tmap_cache[i];
+    if (c.base == base && c.inner == inner && c.rows == rows && c.box_rows == box_rows) {
+      *m = c.map;
+      return true;
+    }
+  }
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {inner};
   cuuint32_t box[2] = {128, box_rows};
   cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  TmapEntry& c = g_tmap_cache[g_tmap_next];
+  c = TmapEntry{base, inner, rows, box_rows, *m};
+  g_tmap_next = (g_tmap_next + 1) % kTmapCache;
+  if (g_tmap_used < kTmapCache) ++g_tmap_used;
+  return true;
 }
 
 // 3-D u8 tensor [d2][d1][d0] (strides s1, s2 bytes), box 128 bytes x b1 x b2, 128-byte

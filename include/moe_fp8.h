@@ -192,10 +192,11 @@ moe_status_t moe_fp8_workspace_view(void* workspace, size_t workspace_bytes,
  *   host_out     BF16 [M][H] host memory, written by the last copy
  *   the other arguments as for moe_route and moe_fp8_forward (router_w, bias, w13, w13_scale,
  *   w2, w2_scale are device pointers).
- * Host buffers should be page-locked (pinned): with pageable memory the copies are staged
- * by the driver and the call does not return until they are done. The routing is kept in
- * the workspace (moe_fp8_workspace_view: topk_ids, topk_w). Results equal moe_route then
- * moe_fp8_forward on the same inputs. */
+ * Page-locked (pinned or registered) host buffers are read and written by the kernels
+ * directly, without copies. Other host memory goes through device copies in the workspace;
+ * with pageable memory the driver stages those copies and the call returns only when they
+ * are done. The routing is kept in the workspace (moe_fp8_workspace_view: topk_ids,
+ * topk_w). Results equal moe_route then moe_fp8_forward on the same inputs. */
 moe_status_t moe_fp8_route_forward_host(const void* host_hidden, void* host_out, int32_t M,
                                         const void* router_w, const float* bias, int32_t renormalize,
                                         const uint8_t* w13, const float* w13_scale, const uint8_t* w2,

@@ -15,15 +15,22 @@ if torch.cuda.is_available():
     from gpu_harness import GpuMoE, to_dev
 
 
-@pytest.mark.parametrize("name,M", [("decode", 1), ("verify_skewed", 12), ("decode", 300)])
-def test_host_call_equals_device_calls(name, M):
+CASES = [("decode", 1, True), ("verify_skewed", 12, True), ("decode", 300, True), ("decode", 1, False),
+         ("verify_skewed", 12, False)]
+
+
+@pytest.mark.parametrize("name,M,pinned", CASES, ids=[f"{n}-M{m}-{'pinned' if p else 'pageable'}" for n, m, p in CASES])
+def test_host_call_equals_device_calls(name, M, pinned):
+    # pinned buffers are read and written by the kernels in place; pageable ones are copied
     from fp8_block_scaled_router_gb300 import _lib as L
 
     x = inputs.make(name, tokens=M) if name == "decode" else inputs.make(name, M=M)
     g = GpuMoE(x, M)
     hid_np = np.ascontiguousarray(x.hidden[:M]).view(np.int16)
-    host_in = torch.from_numpy(hid_np.copy()).pin_memory()
-    host_out = torch.full((M + 2, g.H), 0x1234, dtype=torch.int16).pin_memory()
+    host_in = torch.from_numpy(hid_np.copy())
+    host_out = torch.full((M + 2, g.H), 0x1234, dtype=torch.int16)
+    if pinned:
+        host_in, host_out = host_in.pin_memory(), host_out.pin_memory()
     L.moe_fp8_route_forward_host(host_in, host_out, M, g.router, g.bias, True, g.w13, g.s13, g.w2, g.s2, g.ws,
                                  g.shape)
     torch.cuda.synchronize()
