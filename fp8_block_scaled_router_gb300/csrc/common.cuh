@@ -136,20 +136,8 @@ __device__ __forceinline__ uint16_t e4m3x2_encode(float a, float b) {
       __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
 }
 
-// Decode two E4M3 codes (low byte first) to float2 (exact: E4M3 is a subset of FP16).
-__device__ __forceinline__ float2 e4m3x2_decode(uint16_t two) {
-  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
-  return __half22float2(*reinterpret_cast<__half2*>(&h));
-}
-
 __device__ __forceinline__ float silu_mul(float g, float u) {
   return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
-}
-
-// silu(g) * u with one correctly rounded reciprocal instead of a division (within one
-// ulp of silu_mul; used where the epilogue's instruction count bounds the GEMM)
-__device__ __forceinline__ float silu_mul_rcp(float g, float u) {
-  return __fmul_rn(__fmul_rn(g, __frcp_rn(__fadd_rn(1.0f, expf(-g)))), u);
 }
 
 // silu(g) * u with the fast exponential and division intrinsics (a few ulp from silu_mul;
