@@ -196,14 +196,14 @@ __global__ void __launch_bounds__(kPairThreads, 3)
   // before this grid can start, so the weight tiles stream in while gate/up finishes; only
   // the activation rows (gate/up's output) wait for the grid dependency.
   constexpr bool kEarly = MODE == kDownCombine;
-  if (kEarly && warp == 0 && lane == 0) {
+  if (kEarly && warp == 0) {
+    // one lane per stage issues its load: several issuers keep more of a CTA's tiles moving
     const int e = p.ids[pr];
-    *e_sh = e;
-    if (e >= 0 && e < p.E)
-      for (int i = 0; i < npre; ++i) {
-        tc::mbar_arrive_expect_tx(&full[i], C::kTxA + C::kBBytes);
-        tc::tma_load_2d(stages + i * C::kStageBytes, &tmA, &full[i], (kb0 + i) * 128, e * p.H + cb * 128);
-      }
+    if (lane == 0) *e_sh = e;
+    if (e >= 0 && e < p.E && lane < npre) {
+      tc::mbar_arrive_expect_tx(&full[lane], C::kTxA + C::kBBytes);
+      tc::tma_load_2d(stages + lane * C::kStageBytes, &tmA, &full[lane], (kb0 + lane) * 128, e * p.H + cb * 128);
+    }
   }
   if (kEarly && rank == 0 && warp == 1 && lane < p.K) {
     cwt[lane] = p.topk_w[tok * p.K + lane];
@@ -222,22 +222,18 @@ __global__ void __launch_bounds__(kPairThreads, 3)
   } else if (warp == 0) {
     // the expert id, then the first stages' loads: the first bytes are in flight before the
     // rest of the prologue runs
-    int e = 0;
-    if (lane == 0) e = p.ids[pr];
-    if (lane == 0) {
-      *e_sh = e;
-      if (e >= 0 && e < p.E) {
-        const int ya = kGateUp ? e * 2 * p.I + cb * 128 : e * p.H + cb * 128;
-        const int yb = e * 2 * p.I + p.I + cb * 128;
-        for (int i = 0; i < npre; ++i) {
-          unsigned char* st = stages + i * C::kStageBytes;
-          const int x = (kb0 + i) * 128;
-          tc::mbar_arrive_expect_tx(&full[i], MODE == kGateUpFused ? C::kTxA : C::kTxA + C::kBBytes);
-          tc::tma_load_2d(st, &tmA, &full[i], x, ya);
-          if (kGateUp) tc::tma_load_2d(st + C::kABytes, &tmA, &full[i], x, yb);
-          if (MODE != kGateUpFused) tc::tma_load_2d(st + C::kTxA, &tmB, &full[i], x, brow);
-        }
-      }
+    const int e = p.ids[pr];
+    if (lane == 0) *e_sh = e;
+    if (e >= 0 && e < p.E && lane < npre) {  // one lane per stage issues its loads
+      const int i = lane;
+      const int ya = kGateUp ? e * 2 * p.I + cb * 128 : e * p.H + cb * 128;
+      const int yb = e * 2 * p.I + p.I + cb * 128;
+      unsigned char* st = stages + i * C::kStageBytes;
+      const int x = (kb0 + i) * 128;
+      tc::mbar_arrive_expect_tx(&full[i], MODE == kGateUpFused ? C::kTxA : C::kTxA + C::kBBytes);
+      tc::tma_load_2d(st, &tmA, &full[i], x, ya);
+      if (kGateUp) tc::tma_load_2d(st + C::kABytes, &tmA, &full[i], x, yb);
+      if (MODE != kGateUpFused) tc::tma_load_2d(st + C::kTxA, &tmB, &full[i], x, brow);
     }
   } else if (MODE == kGateUpFused) {
     // warps 1..5 quantise the pair's hidden row for this CTA's K blocks straight into the
