@@ -55,14 +55,16 @@ struct GrpParams {
   Header* hdr;
 };
 
-__host__ __device__ constexpr size_t grp_smem_bytes() {
-  return 1024 + (size_t)kGrpStages * kGrpStageBytes + 256 + 128 * 4 * 4;
+// stages, barriers, then gate/up: the row-amax exchange [128][4] f32; down: 16 per-warp
+// staging tiles of 32 rows x 16 FP32 for the y stores
+__host__ __device__ constexpr size_t grp_smem_bytes(bool gateup) {
+  return 1024 + (size_t)kGrpStages * kGrpStageBytes + 256 + (gateup ? 128 * 4 * 4 : kGrpEpiWarps * 32 * 16 * 4);
 }
 
 template <bool GATEUP>
 __global__ void __launch_bounds__(kGrpThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const GrpParams p) {
+                        const __grid_constant__ CUtensorMap tmY, const GrpParams p) {
   extern __shared__ __align__(1024) unsigned char dsm_raw[];
   unsigned char* base =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
@@ -74,6 +76,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
   uint64_t* acce = bars + 2 * kGrpStages + 4; // [4]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kGrpStages + 8);
   float* red = reinterpret_cast<float*>(base + kGrpStages * kGrpStageBytes + 256);  // [128][4]
+  float* ystage = red;  // down: [16 warps][32 rows][16] f32
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   if (warp == 0 && lane == 0) {
@@ -265,8 +268,28 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
           }
           if (slot4 == 0) p.act_scale_out[(size_t)(row0 + row) * (p.I / 128) + nb] = s2;
         }
+      } else if (q * 32 + 32 <= tl.nrows) {
+        // all 32 rows of this warp belong to the tile: four 32 x 16 pieces through shared
+        // memory, each written by one TMA store (whole rows of 64 bytes per request)
+        float* stw = ystage + (ew * 32) * 16;
+        for (int ch = 0; ch < 4; ++ch) {
+          if (lane == 0) tc::bulk_wait_read_all();  // the previous piece has left shared memory
+          __syncwarp();
+          float4* d4 = reinterpret_cast<float4*>(stw + lane * 16);
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4)
+            d4[c4] = make_float4(acc[ch * 16 + 4 * c4], acc[ch * 16 + 4 * c4 + 1], acc[ch * 16 + 4 * c4 + 2],
+                                 acc[ch * 16 + 4 * c4 + 3]);
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tc::tma_store_2d(&tmY, stw, nb * 256 + slot4 * 64 + ch * 16, row0 + q * 32);
+            tc::bulk_commit();
+          }
+        }
       } else if (live) {
-        // 32-byte stores: each one fills a whole L2 sector of the row
+        // a warp straddling the tile's end (the next rows belong to another tile): 32-byte
+        // stores of the live rows, each one filling a whole L2 sector
         float* dst = p.y_out + (size_t)(row0 + row) * p.H + nb * 256 + slot4 * 64;
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8)
@@ -278,6 +301,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
     }
   }
   if (!ok) set_status(p.hdr, MOE_STATUS_WAIT_TIMEOUT);
+  if (!GATEUP && warp >= 2 && lane == 0) tc::bulk_wait_all();  // this warp's y stores are done
   __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
@@ -286,18 +310,20 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
 }
 
 bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
+bool make_tmap_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                   uint32_t box_rows);
 bool make_tmap_u8_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
                      uint64_t s2, uint32_t b1, uint32_t b2);
 
 namespace {
 
 template <bool GATEUP>
-cudaError_t launch_grouped(const CUtensorMap& tA, const CUtensorMap& tB, const GrpParams& prm,
-                           int64_t max_tiles, cudaStream_t st) {
+cudaError_t launch_grouped(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tY,
+                           const GrpParams& prm, int64_t max_tiles, cudaStream_t st) {
   static std::once_flag once;
   std::call_once(once, [] {
     cudaFuncSetAttribute(grouped_gemm_kernel<GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)grp_smem_bytes());
+                         (int)grp_smem_bytes(GATEUP));
   });
   static int num_sms = 0;
   static std::once_flag sm_once;
@@ -310,14 +336,14 @@ cudaError_t launch_grouped(const CUtensorMap& tA, const CUtensorMap& tB, const G
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(units < num_sms ? units : num_sms), 1, 1);
   cfg.blockDim = dim3(kGrpThreads, 1, 1);
-  cfg.dynamicSmemBytes = grp_smem_bytes();
+  cfg.dynamicSmemBytes = grp_smem_bytes(GATEUP);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<GATEUP>, tA, tB, prm);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<GATEUP>, tA, tB, tY, prm);
 }
 
 }  // namespace
@@ -342,14 +368,16 @@ cudaError_t launch_grouped_gateup(const uint8_t* w13, const float* s13, int64_t 
   prm.act_scale_out = ws.act_scale;
   prm.y_out = ws.y;
   prm.hdr = ws.hdr;
-  return launch_grouped<true>(tA, tB, prm, max_tiles, st);
+  return launch_grouped<true>(tA, tB, tA, prm, max_tiles, st);  // no y stores
 }
 
 // down over the expert tiles: A = activation codes act [R][I], y [R][H] (H % 256 == 0).
 cudaError_t launch_grouped_down(const uint8_t* w2, const float* s2w, int64_t R, int H, int I, int E,
                                 int64_t max_tiles, const WsPtrs& ws, cudaStream_t st) {
-  CUtensorMap tA, tB;
+  CUtensorMap tA, tB, tY;
   if (!make_tmap_u8(&tA, ws.act, (uint64_t)I, (uint64_t)R, 128)) return cudaErrorInvalidValue;
+  // y [R][H] FP32 written in 32-row x 16-column pieces
+  if (!make_tmap_f32(&tY, ws.y, (uint64_t)H, (uint64_t)R, 16, 32)) return cudaErrorInvalidValue;
   // one 256-row box per stage: the w2 rows of the 256-wide output block
   if (!make_tmap_u8(&tB, w2, (uint64_t)I, (uint64_t)E * H, 256)) return cudaErrorInvalidValue;
   GrpParams prm{};
@@ -363,7 +391,7 @@ cudaError_t launch_grouped_down(const uint8_t* w2, const float* s2w, int64_t R, 
   prm.act_scale_out = ws.act_scale;
   prm.y_out = ws.y;
   prm.hdr = ws.hdr;
-  return launch_grouped<false>(tA, tB, prm, max_tiles, st);
+  return launch_grouped<false>(tA, tB, tY, prm, max_tiles, st);
 }
 
 }  // namespace moe

@@ -506,6 +506,21 @@ bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t row
   return true;
 }
 
+// 2-D FP32 tensor [rows][inner] (row stride inner * 4 bytes), box box_inner x box_rows
+// elements, no swizzle (for stores of row-major shared-memory tiles).
+bool make_tmap_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                   uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 4};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3-D u8 tensor [d2][d1][d0] (strides s1, s2 bytes), box 128 bytes x b1 x b2, 128-byte
 // swizzle; the box lands in shared memory as b2 blocks of b1 rows.
 bool make_tmap_u8_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
