@@ -254,18 +254,18 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
         const float inv = amax == 0.0f ? 1.0f : __fdiv_rn(448.0f, amax);
         if (live) {
           uint8_t* dst = p.act_out + (size_t)(row0 + row) * p.I + nb * 128 + slot4 * 32;
+          uint32_t w8[8];
 #pragma unroll
-          for (int c16 = 0; c16 < 2; ++c16) {
-            uint32_t w4[4];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              const int c = c16 * 16 + q4 * 4;
-              const uint32_t lo = e4m3x2_encode(__fmul_rn(act[c], inv), __fmul_rn(act[c + 1], inv));
-              const uint32_t hi = e4m3x2_encode(__fmul_rn(act[c + 2], inv), __fmul_rn(act[c + 3], inv));
-              w4[q4] = lo | (hi << 16);
-            }
-            reinterpret_cast<uint4*>(dst)[c16] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const int c = q4 * 4;
+            const uint32_t lo = e4m3x2_encode(__fmul_rn(act[c], inv), __fmul_rn(act[c + 1], inv));
+            const uint32_t hi = e4m3x2_encode(__fmul_rn(act[c + 2], inv), __fmul_rn(act[c + 3], inv));
+            w8[q4] = lo | (hi << 16);
           }
+          // the row's 32 codes in one 32-byte store (a whole L2 sector)
+          asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(w8[0]), "r"(w8[1]),
+                       "r"(w8[2]), "r"(w8[3]), "r"(w8[4]), "r"(w8[5]), "r"(w8[6]), "r"(w8[7])
+                       : "memory");
           if (slot4 == 0) p.act_scale_out[(size_t)(row0 + row) * (p.I / 128) + nb] = s2;
         }
       } else if (q * 32 + 32 <= tl.nrows) {
