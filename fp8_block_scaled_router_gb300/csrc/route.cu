@@ -30,13 +30,16 @@ struct RouteSmem {
   size_t ws, xs, part, logits, sel, bias, total;
 };
 
-// ws: router rows [CPC*128][E] bf16; xs: hidden [CPC*128][TB] bf16 (token-minor);
+// ws: router rows [CPC*128][E] bf16 (or one chunk [128][E] at a time when they do not fit);
+// xs: hidden [CPC*128][TB] bf16 (token-minor);
 // part (CTA 0): chunk partials [nchunks][TB][E] f32; logits [TB][E] f32;
 // sel: selected logits [TB][16] f32 + ids [TB][16] i32.
-__host__ __device__ inline RouteSmem route_smem(int TB, int CPC, int E, int nchunks) {
+// stage_all: all CPC router chunks of the CTA are held in shared memory (staged before the
+// grid dependency); otherwise one chunk at a time streams through it.
+__host__ __device__ inline RouteSmem route_smem(int TB, int CPC, int E, int nchunks, bool stage_all) {
   RouteSmem s{};
   size_t o = 0;
-  s.ws = o;     o += (size_t)CPC * 128 * E * 2;
+  s.ws = o;     o += (size_t)(stage_all ? CPC : 1) * 128 * E * 2;
   s.xs = o;     o += (size_t)CPC * 128 * TB * 2;
   o = (o + 15) & ~size_t(15);
   s.part = o;   o += (size_t)nchunks * TB * E * 4;
@@ -47,18 +50,21 @@ __host__ __device__ inline RouteSmem route_smem(int TB, int CPC, int E, int nchu
   return s;
 }
 
-template <int TB>
+// STREAM: the CTA's router chunks do not fit in shared memory together and stream through it
+// one at a time (a separate instantiation, so the common path keeps its register budget).
+template <int TB, bool STREAM>
 __global__ void __launch_bounds__(kRouteThreads)
     route_kernel(const uint16_t* __restrict__ hidden, const uint16_t* __restrict__ router_w,
                  const float* __restrict__ bias, int M, int H, int E, int K, int renorm,
                  int32_t* __restrict__ ids, float* __restrict__ wts) {
+  constexpr bool stage_all = !STREAM;
   extern __shared__ __align__(16) unsigned char smem[];
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int CL = (int)cluster.num_blocks();
   const int nchunks = H / 128;
   const int CPC = nchunks / CL;
-  const RouteSmem L = route_smem(TB, CPC, E, nchunks);
+  const RouteSmem L = route_smem(TB, CPC, E, nchunks, stage_all);
   uint16_t* wsm = reinterpret_cast<uint16_t*>(smem + L.ws);
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem + L.xs);
   float* part = reinterpret_cast<float*>(smem + L.part);
@@ -73,7 +79,10 @@ __global__ void __launch_bounds__(kRouteThreads)
   // The router rows [c0*128, (c0+CPC)*128) (contiguous) and the bias are layer parameters:
   // they are staged while the previous kernel of the stream finishes (programmatic launch);
   // the hidden rows, which it may have written, only after the grid dependency resolves.
-  {
+  if constexpr (STREAM) {
+    if (rank == 0)
+      for (int e = tid; e < E; e += kRouteThreads) bias_s[e] = bias != nullptr ? bias[e] : 0.0f;
+  } else {
     const uint4* src = reinterpret_cast<const uint4*>(router_w + (size_t)c0 * 128 * E);
     uint4* dst = reinterpret_cast<uint4*>(wsm);
     const int n16 = CPC * 128 * E / 8;
@@ -100,13 +109,53 @@ __global__ void __launch_bounds__(kRouteThreads)
   __syncthreads();
 
   float* part0 = cluster.map_shared_rank(part, 0);
+  // one chunk's fma chains over the plain [128][E] layout at w (k ascending, from 0)
+  auto plain_chains = [&](const uint16_t* w, const uint16_t* xk, int e, float (&acc)[TB]) {
+#pragma unroll
+    for (int t = 0; t < TB; ++t) acc[t] = 0.0f;
+    const uint16_t* wcol = w + e;
+#pragma unroll 16
+    for (int k = 0; k < 128; ++k) {
+      const float wv = bf16_bits_to_float(wcol[k * E]);
+      uint32_t xw[(TB + 1) / 2];
+      if constexpr (TB == 8) {
+        const uint4 q = *reinterpret_cast<const uint4*>(xk + k * TB);
+        xw[0] = q.x; xw[1] = q.y; xw[2] = q.z; xw[3] = q.w;
+      } else if constexpr (TB == 2) {
+        xw[0] = *reinterpret_cast<const uint32_t*>(xk + k * TB);
+      } else {
+        xw[0] = xk[k * TB];
+      }
+#pragma unroll
+      for (int t = 0; t < TB; ++t) {
+        const uint16_t b = (uint16_t)((t & 1) ? (xw[t / 2] >> 16) : (xw[t / 2] & 0xFFFF));
+        acc[t] = __fmaf_rn(bf16_bits_to_float(b), wv, acc[t]);
+      }
+    }
+  };
+  if constexpr (STREAM) {
+    // chunks streamed through one staging buffer: stage chunk cl, then every expert's chains
+    for (int cl = 0; cl < CPC; ++cl) {
+      if (cl > 0) __syncthreads();  // the previous chunk's readers are done
+      const uint4* src = reinterpret_cast<const uint4*>(router_w + (size_t)(c0 + cl) * 128 * E);
+      uint4* dst = reinterpret_cast<uint4*>(wsm);
+      for (int i = tid; i < 128 * E / 8; i += kRouteThreads) dst[i] = src[i];
+      __syncthreads();
+      for (int e = tid; e < E; e += kRouteThreads) {
+        float acc[TB];
+        plain_chains(wsm, xs + (size_t)cl * 128 * TB, e, acc);
+#pragma unroll
+        for (int t = 0; t < TB; ++t) part0[((size_t)(c0 + cl) * TB + t) * E + e] = acc[t];
+      }
+    }
+  } else {
   for (int e = tid; e < E; e += kRouteThreads) {
     for (int cl = 0; cl < CPC; ++cl) {
       float acc[TB];
 #pragma unroll
       for (int t = 0; t < TB; ++t) acc[t] = 0.0f;
-      const uint16_t* wcol = wsm + (size_t)cl * 128 * E + e;
       const uint16_t* xk = xs + (size_t)cl * 128 * TB;
+      const uint16_t* wcol = wsm + (size_t)cl * 128 * E + e;
 #pragma unroll 16
       for (int k = 0; k < 128; ++k) {
         const float w = bf16_bits_to_float(wcol[k * E]);
@@ -128,6 +177,7 @@ __global__ void __launch_bounds__(kRouteThreads)
 #pragma unroll
       for (int t = 0; t < TB; ++t) part0[((size_t)(c0 + cl) * TB + t) * E + e] = acc[t];
     }
+  }
   }
   cluster.sync();  // CTA 0 holds every chunk partial
   if (rank != 0) return;
@@ -435,12 +485,19 @@ cudaError_t launch_route_t(const uint16_t* hidden, const uint16_t* router_w, con
                            int H, int E, int K, int renorm, int32_t* ids, float* wts, cudaStream_t st) {
   const int nchunks = H / 128;
   const int CL = route_cluster(nchunks);
-  const RouteSmem L = route_smem(TB, nchunks / CL, E, nchunks);
+  bool stream = false;
+  RouteSmem L = route_smem(TB, nchunks / CL, E, nchunks, true);
+  if (L.total > 227 * 1024) {  // the CTA's router chunks do not all fit: stream them
+    stream = true;
+    L = route_smem(TB, nchunks / CL, E, nchunks, false);
+  }
   if (L.total > 227 * 1024) return cudaErrorInvalidConfiguration;
   static std::once_flag once;
   std::call_once(once, [] {
-    cudaFuncSetAttribute(route_kernel<TB>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    cudaFuncSetAttribute(route_kernel<TB>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaFuncSetAttribute(route_kernel<TB, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaFuncSetAttribute(route_kernel<TB, false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaFuncSetAttribute(route_kernel<TB, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaFuncSetAttribute(route_kernel<TB, true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   });
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(CL, (M + TB - 1) / TB, 1);
@@ -456,7 +513,9 @@ cudaError_t launch_route_t(const uint16_t* hidden, const uint16_t* router_w, con
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, route_kernel<TB>, hidden, router_w, bias, M, H, E, K, renorm, ids, wts);
+  if (stream)
+    return cudaLaunchKernelEx(&cfg, route_kernel<TB, true>, hidden, router_w, bias, M, H, E, K, renorm, ids, wts);
+  return cudaLaunchKernelEx(&cfg, route_kernel<TB, false>, hidden, router_w, bias, M, H, E, K, renorm, ids, wts);
 }
 
 }  // namespace
@@ -488,9 +547,9 @@ cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const
     if (E == 64) return go(route_big_kernel<2>);
     return go(route_big_kernel<1>);
   }
-  if (M >= 16 && route_smem(8, nchunks / route_cluster(nchunks), E, nchunks).total <= 227 * 1024)
+  if (M >= 16 && route_smem(8, nchunks / route_cluster(nchunks), E, nchunks, true).total <= 227 * 1024)
     return launch_route_t<8>(hidden, router_w, bias, M, H, E, K, renorm, ids, wts, st);
-  if (M >= 4 && route_smem(2, nchunks / route_cluster(nchunks), E, nchunks).total <= 227 * 1024)
+  if (M >= 4 && route_smem(2, nchunks / route_cluster(nchunks), E, nchunks, true).total <= 227 * 1024)
     return launch_route_t<2>(hidden, router_w, bias, M, H, E, K, renorm, ids, wts, st);
   return launch_route_t<1>(hidden, router_w, bias, M, H, E, K, renorm, ids, wts, st);
 }

@@ -51,3 +51,25 @@ def test_edge_shape_parity(name, M):
     assert np.all(np.abs(w.cpu().numpy() - w_o) <= 2e-6 * w_o)
     assert ids_o.shape == (M, K)
     check_out(out, oracle_forward(x, x.hidden[:M], ids_o, w_o), f"{name} M={M}")
+
+
+ROUTE_WIDE = [(6144, 256, 1), (8192, 256, 1), (8192, 256, 5), (8192, 256, 40), (8192, 128, 3)]
+
+
+@pytest.mark.parametrize("H,E,M", ROUTE_WIDE, ids=[f"H{h}-E{e}-M{m}" for h, e, m in ROUTE_WIDE])
+def test_route_largest_router_matrices(H, E, M):
+    """Router matrices too large for a CTA's chunks to sit in shared memory at once (they are
+    streamed through it chunk by chunk) against the oracle; the expert FFN is not involved."""
+    import oracle
+    from fp8_block_scaled_router_gb300 import _lib as L
+    K = 8
+    hid = inputs.hidden_states(9, M, H)
+    wr = inputs.router_weights(9, H, E, 0.02)
+    shape = L.make_shape(H, 128, E, K, M)
+    ids = torch.empty((M, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    L.moe_route(to_dev(hid), to_dev(wr), None, M, shape, True, ids, w)
+    torch.cuda.synchronize()
+    ids_o, w_o = oracle.route(hid, wr, None, K)
+    assert np.array_equal(ids.cpu().numpy(), ids_o)
+    assert np.all(np.abs(w.cpu().numpy() - w_o) <= 2e-6 * w_o)
