@@ -104,23 +104,25 @@ def load_peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(files=None):
+    """Hash of the kernel sources (all of csrc, or the named files there)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp8_block_scaled_router_gb300", "csrc")
-    for n in sorted(os.listdir(csrc)):
-        if n.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, n), "rb") as f:
-                h.update(n.encode() + f.read())
+    names = sorted(files) if files else sorted(n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh")))
+    for n in names:
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(n.encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel, workload):
-    """DRAM bytes per launch from a committed ncu summary, if taken on the current sources."""
+    """DRAM bytes per launch from a committed ncu summary, if the sources of that kernel
+    (the files the record lists) are unchanged since the counters were taken."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             d = json.load(f)
         rec = d.get(workload, {}).get(kernel)
-        if rec and rec.get("source_hash") == kernel_source_hash():
+        if rec and rec.get("source_hash") == kernel_source_hash(rec.get("source_files")):
             return rec["dram_bytes_per_launch"]
     except Exception:
         pass
