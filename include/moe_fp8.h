@@ -20,8 +20,10 @@
  *
  * Conventions for every call:
  *   - All tensor pointers are DEVICE pointers owned by the caller, 16-byte aligned, with
- *     the row-major layouts stated below. The library never allocates, frees, copies to
- *     the host or synchronises ([NKL] "Design": the dispatch path avoids allocation,
+ *     the row-major layouts stated below (moe_fp8_route_forward_host takes its hidden and
+ *     out in host memory; moe_fp8_read_status writes a host word). The library never
+ *     allocates, frees or synchronises; host<->device copies happen only in those two calls,
+ *     enqueued on the caller's stream ([NKL] "Design": the dispatch path avoids allocation,
  *     synchronisation, filesystem access, environment parsing and symbol lookup).
  *   - Work is enqueued on `stream` (0 = legacy default stream) and returns at once.
  *     Nothing in the library keeps per-call state between calls: two calls on different
@@ -119,6 +121,10 @@ moe_status_t moe_route(const void* hidden, const void* router_w, const float* bi
  * codes; each GEMM output is sum over 128-blocks kb ascending of P_kb * (sa_kb * sw_kb)
  * in FP32 (P_kb = the block's FP8 dot product on the tensor core or in FP32);
  * act = silu(g) * u in FP32; out = bf16(sum over slots j ascending of w_j * y_j).
+ * With more than 64 routed rows (sorted expert tiles) the promotion is one fused
+ * multiply-add per block, silu uses the fast exponential and division intrinsics and the
+ * requantisation multiplies by 448/amax: a few ulp from the forms above, inside the same
+ * tolerances (activation codes may move one step next to a rounding boundary).
  * 0 <= M <= max_tokens; M = 0 is a no-op. */
 moe_status_t moe_fp8_forward(const void* hidden, const int32_t* topk_ids, const float* topk_w,
                              int32_t M, const uint8_t* w13, const float* w13_scale,
