@@ -203,14 +203,9 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
       uint64_t acc2[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) acc2[c] = 0ull;
-      float a_n = live ? sarow[0] : 0.0f, s0_n = sw0[0], s1_n = sw1[0];  // scales of block i
       for (int i = 0; i < nkb; ++i, ++it) {
-        const float a = a_n, s0 = s0_n, s1 = s1_n;
-        if (i + 1 < nkb) {  // prefetch the next block's scales
-          a_n = live ? sarow[i + 1] : 0.0f;
-          s0_n = sw0[i + 1];
-          s1_n = sw1[i + 1];
-        }
+        // block i's scales, loaded before the accumulator wait that covers their latency
+        const float a = live ? sarow[i] : 0.0f, s0 = sw0[i], s1 = sw1[i];
         const int slot = 2 * it + hh;
         const int buf = slot & 3;
         if (ok && !tc::mbar_wait(&accf[buf], (slot >> 2) & 1)) ok = false;
