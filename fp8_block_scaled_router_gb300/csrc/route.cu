@@ -253,6 +253,21 @@ __global__ void __launch_bounds__(kRouteThreads)
 // go to the lower index).
 // ---------------------------------------------------------------------------------------
 constexpr int kBigTok = 32;
+// packed FP32x2 (sm_100 family): two IEEE round-to-nearest fmas per instruction,
+// bit-identical to two __fmaf_rn
+__device__ __forceinline__ uint64_t rt_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(__float_as_uint(lo)), "r"(__float_as_uint(hi)));
+  return r;
+}
+__device__ __forceinline__ void rt_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t rt_fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
 constexpr int kBigSlots = 4;
 
 __host__ __device__ inline size_t route_big_smem(int E) {
@@ -356,9 +371,10 @@ __global__ void __launch_bounds__(256, 1)
         if (globaltimer_ns() - t0 > kWaitLimitNs) ok = false;
       }
     }
-    float acc[NA];
+    // chains of tokens (2u, 2u + 1) of expert j as one FP32 pair: acc2[j * 4 + u]
+    uint64_t acc2[NA / 2];
 #pragma unroll
-    for (int i = 0; i < NA; ++i) acc[i] = 0.0f;
+    for (int i = 0; i < NA / 2; ++i) acc2[i] = 0ull;
     if (ok) {
       const uint16_t* wk = wring + (size_t)slot * 128 * E + lane * EPT;
       const float* xk = xring + (size_t)par * 128 * kBigTok + grp * 8;
@@ -377,13 +393,18 @@ __global__ void __launch_bounds__(256, 1)
         }
         const float4 x0 = *reinterpret_cast<const float4*>(xk + k * kBigTok);
         const float4 x1 = *reinterpret_cast<const float4*>(xk + k * kBigTok + 4);
-        const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        const uint64_t xp[4] = {rt_pack(x0.x, x0.y), rt_pack(x0.z, x0.w), rt_pack(x1.x, x1.y), rt_pack(x1.z, x1.w)};
 #pragma unroll
-        for (int j = 0; j < EPT; ++j)
+        for (int j = 0; j < EPT; ++j) {
+          const uint64_t wj = rt_pack(w[j], w[j]);
 #pragma unroll
-          for (int t = 0; t < 8; ++t) acc[j * 8 + t] = __fmaf_rn(xv[t], w[j], acc[j * 8 + t]);
+          for (int u = 0; u < 4; ++u) acc2[j * 4 + u] = rt_fma2(xp[u], wj, acc2[j * 4 + u]);
+        }
       }
     }
+    float acc[NA];
+#pragma unroll
+    for (int i = 0; i < NA / 2; ++i) rt_unpack(acc2[i], acc[2 * i], acc[2 * i + 1]);
     if (par == 1) {
 #pragma unroll
       for (int i = 0; i < NA; ++i) xch[i * 128 + grp * 32 + lane] = acc[i];
