@@ -62,9 +62,11 @@ typedef enum {
 #define MOE_STATUS_BAD_EXPERT_ID 0x1u /* an id < 0 or >= E was skipped (contributes 0) */
 #define MOE_STATUS_WAIT_TIMEOUT 0x2u  /* a bounded device wait gave up; outputs invalid */
 
-/* Layer shape. hidden (H) and inter (I) are multiples of 128 (the block-scale grid),
- * H <= 8192, I <= 4096; num_experts (E) in {8,16,32,64,128,256}; 1 <= top_k (K) <= min(E,16).
- * max_tokens bounds M for every call that uses one workspace. */
+/* Layer shape. hidden (H) is a multiple of 256 (the down GEMM's 256-wide output blocks) with
+ * 256 <= H <= 8192; inter (I) is a multiple of 128 (the block-scale grid) with
+ * 128 <= I <= 4096; num_experts (E) in {8,16,32,64,128,256}; 1 <= top_k (K) <= min(E,16).
+ * max_tokens (1 <= max_tokens <= 2^20 / K) bounds M for every call that uses one workspace.
+ * Any other shape is MOE_ERR_UNSUPPORTED (moe_fp8_workspace_bytes returns 0). */
 typedef struct {
   int32_t hidden;
   int32_t inter;
