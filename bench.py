@@ -4,20 +4,23 @@
 A step is one pass of the whole layer -- moe_route then moe_fp8_forward (prepare, gate/up
 + SiLU*up requantisation, down, combine) -- over one batch of synthetic tokens. The default
 workload is decode: hidden 2048, intermediate 768, 128 experts, top-8 renormalised, one
-token per step, stepping through 10,000 seeded tokens. Other workloads (--workload):
-verify, verify_skewed (M=12), wide (M=1..64, h6144/i768/e128/top4), prefill, prefill_zipf
-(M=4096).
+token per step, stepping through 10,000 seeded tokens; the same line carries a "prefill"
+record (M=4096, same shapes), the metric's tensor-bound half. Other workloads
+(--workload): verify, verify_skewed (M=12), wide (M=1..64, h6144/i768/e128/top4),
+prefill, prefill_zipf (M=4096).
 
-value   tokens/s with inputs resident in HBM, timed with CUDA events around CUDA-graph
-        replays of the steps; 8 weight replicas (decode/verify/wide) or 2 (prefill) are
-        rotated step by step so that no step reuses L2-resident weights.
+value   tokens/s with inputs resident in HBM: exactly --steps steps timed with CUDA events
+        around CUDA-graph replays; 8 weight replicas (decode/verify/wide) or 2 (prefill)
+        are rotated step by step so that no step reuses L2-resident weights. Clocks are
+        sampled during about a second of untimed replays of the same steps and the timed
+        region after them.
 e2e     the same metric through the public API with host buffers: per step one
-        moe_fp8_route_forward_host call copies the hidden rows from pinned host memory,
-        routes, runs the forward and copies the output back to pinned host memory, all
+        moe_fp8_route_forward_pinned call -- the kernels read the hidden rows from and write
+        the output to pinned host memory, route and forward enqueued by one call -- all
         inside the timed region (the Zipf workload, whose routing is given, uses a host copy,
         moe_route, moe_fp8_forward and a copy back).
-roofline the dominant kernel (gate/up) timed alone with CUDA events on its stream, its
-        algorithmic bytes (or FLOPs) per launch divided by the mean launch time.
+roofline the dominant kernel timed alone with CUDA events on its stream, its algorithmic
+        bytes (or FLOPs) per launch divided by the mean launch time.
 cpu_baseline the oracle (plain C++ on the host cores) on a bounded sample of the same
         workload (rank 0, N=1 only).
 
@@ -74,6 +77,10 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--dominant-only", type=int, default=0, metavar="N",
                    help="run only N launches of the dominant kernel (gate/up) and exit, for ncu")
+    p.add_argument("--no-prefill", action="store_true",
+                   help="decode only: leave out the prefill record of the same line")
+    p.add_argument("--clock-soak", type=float, default=1.0, metavar="S",
+                   help="seconds of untimed replays before the timed region while clocks are sampled")
     return p.parse_args()
 
 
@@ -243,23 +250,16 @@ def reference_arm(args, wl, world, rank):
 
 
 # ----------------------------------------------------------------------------- our arm
-def ours_arm(args, wl, world, rank, local):
+def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_s):
+    """Measure one workload; returns its record (the JSON line's fields)."""
     import torch
     from fp8_block_scaled_router_gb300 import _lib as L
-    from fp8_block_scaled_router_gb300 import build as B
     from fp8_block_scaled_router_gb300 import inputs
     from fp8_block_scaled_router_gb300 import replicas
 
-    B.build()
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-
     cfg = wl["cfg"]
     decode = cfg == "decode"
-    M = args.m or wl["M"]
+    M = args.m if (args.m and cfg == "wide") else wl["M"]
     prefill = M >= 1024
     ntok = 10000 if decode else M
     x = inputs.make(cfg, tokens=ntok if decode else None, M=M if cfg == "wide" else None)
@@ -304,24 +304,6 @@ def ours_arm(args, wl, world, rank, local):
     # count+quantise, scatter, gather, gate/up, down, combine
     kernels_per_step = 3 if M * K <= PAIR_ROWS else 7
 
-    if args.dominant_only:
-        # only the dominant kernel (the launch the roofline times), for a profiler
-        st = torch.cuda.current_stream()
-        ii0 = given_ids[0] if given_ids is not None else None
-        if ii0 is None:
-            L.moe_route(hidden_all[:M], router, bias, M, shape, True, ids[0], wts[0])
-            ii0 = ids[0]
-        if M * K > PAIR_ROWS:
-            L.moe_fp8_prepare(hidden_all[:M], ii0, M, ws, shape)
-        for i in range(args.dominant_only):
-            w13, s13, _, _ = reps[i % n_rep]
-            if M * K <= PAIR_ROWS:
-                L.moe_fp8_gate_up_direct(hidden_all[:M], ii0, M, w13, s13, ws, shape, stream=st)
-            else:
-                L.moe_fp8_gate_up(w13, s13, M, ws, shape, stream=st)
-        torch.cuda.synchronize()
-        return
-
     # distinct experts per step (accounting only)
     for i in range(min(nbatches, 64)):
         step(i)
@@ -332,14 +314,15 @@ def ours_arm(args, wl, world, rank, local):
     distinct = float(np.mean([len(np.unique(r)) for r in sample]))
     alg_bytes, alg_flops, gu_bytes, gu_flops = algorithmic(H, I, E, K, M, distinct)
 
-    # ---- CUDA graphs of G steps each
-    steps = args.steps or (50000 if decode else (2000 if M <= 64 else 20))
-    warm = max(3, args.warmup if args.warmup is not None else (200 if decode else 5))
-    G = 500 if decode else (50 if M <= 64 else 1)
+    # ---- CUDA graphs: exactly `steps` steps are timed -- `full` replays of a G-step graph
+    # (rotating over a few graphs so that consecutive replays walk different tokens) and one
+    # graph of the remaining steps
+    G = min(steps, 500 if decode else (50 if M <= 64 else 1))
+    full, rem = divmod(steps, G)
     n_graphs = max(1, min(20, nbatches // G)) if decode else 1
-    graphs = []
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
+    graphs = []
     with torch.cuda.stream(s):
         for gi in range(n_graphs):
             g = torch.cuda.CUDAGraph()
@@ -347,28 +330,43 @@ def ours_arm(args, wl, world, rank, local):
                 for j in range(G):
                     step(gi * G + j)
             graphs.append(g)
+        g_rem = None
+        if rem:
+            g_rem = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_rem, stream=s):
+                for j in range(rem):
+                    step(full * G + j)
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
-    reps_needed = max(1, -(-steps // G))
-    steps = reps_needed * G
-    for i in range(max(1, -(-warm // G))):
+    for i in range(max(1, -(-warm // G))):       # >= warm untimed steps
         graphs[i % n_graphs].replay()
     torch.cuda.synchronize()
 
-    props = torch.cuda.get_device_properties(local)
-    uuid = str(getattr(props, "uuid", ""))
-    sel = ("GPU-" + uuid if uuid and not uuid.startswith("GPU-") else uuid) or str(local)
-    sampler = ClockSampler(sel) if rank == 0 else None
+    def replay_timed():
+        for i in range(full):
+            graphs[i % n_graphs].replay()
+        if g_rem is not None:
+            g_rem.replay()
+
+    # clocks are sampled while the same steps run for about a second before the timed region
+    # and during it (a timed region of a few steps is shorter than the sampling period)
+    sampler = ClockSampler(gpu_selector(torch)) if rank == 0 else None
     if sampler:
         sampler.start()
+    t_soak = time.perf_counter()
+    n_soak = 0
+    while time.perf_counter() - t_soak < args.clock_soak:
+        replay_timed()
+        n_soak += 1
+        if n_soak % 8 == 0:
+            torch.cuda.synchronize()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_wall = time.perf_counter()
     ev0.record()
-    for i in range(reps_needed):
-        graphs[i % n_graphs].replay()
+    replay_timed()
     ev1.record()
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
@@ -380,9 +378,74 @@ def ours_arm(args, wl, world, rank, local):
     value = replicas.throughput(world, steps, M, elapsed)
     ms_per_step = 1e3 * elapsed / steps
 
-    # ---- dominant kernel alone: gate/up, back to back in a CUDA graph on its own stream
-    # (few routed rows: the direct gate/up kernel of the step; otherwise the stage kernel
-    # after one prepare), rotating weight replicas and the steps' expert sets
+    roof = dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, given_ids, ids, ws, shape,
+                           prefill, gu_bytes, gu_flops)
+    roof["traffic"] = recorded_traffic("gate_up", "prefill" if prefill else args.workload)
+
+    # ---- end to end through the public API with host buffers
+    e2e_steps = min(steps * max(1, n_soak), 3000 if decode else (500 if M <= 64 else 10))
+    host_in = torch.empty((nbatches, M, H), dtype=torch.int16).pin_memory()
+    host_in.copy_(hidden_all.view(nbatches, M, H).cpu())
+    host_out = torch.empty((nbatches, M, H), dtype=torch.int16).pin_memory()
+    stage = torch.empty((2, M, H), dtype=torch.int16, device="cuda")
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    cs = torch.cuda.current_stream()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record()
+    for i in range(e2e_steps):
+        b = i % nbatches
+        w13, s13, w2, s2 = reps[i % n_rep]
+        if given_ids is None:
+            # the public host-buffer call: hidden read from and out written to pinned host
+            # memory by the kernels, route + forward, enqueued by one call
+            L.moe_fp8_route_forward_pinned(host_in[b], host_out[b], M, router, bias, True, w13, s13, w2, s2,
+                                           ws, shape, stream=cs)
+            continue
+        hid = stage[i % 2]
+        hid.copy_(host_in[b], non_blocking=True)
+        L.moe_route(hid, router, bias, M, shape, True, ids[b], wts[b], stream=cs)
+        ii, ww = given_ids
+        L.moe_fp8_forward(hid, ii, ww, M, w13, s13, w2, s2, out[b], ws, shape, stream=cs)
+        host_out[b].copy_(out[b], non_blocking=True)
+    a1.record()
+    torch.cuda.synchronize()
+    e2e_t = a0.elapsed_time(a1) / 1e3
+    if dist:
+        e2e_t = replicas.slowest(e2e_t, dist, "cuda")
+    e2e = {"value": replicas.throughput(world, e2e_steps, M, e2e_t), "unit": "tokens/s",
+           "h2d_bytes_per_step": M * H * 2, "d2h_bytes_per_step": M * H * 2, "steps": e2e_steps}
+
+    cpu = None
+    if want_cpu:
+        tps, cores, n, dt = oracle_tokens_per_s(x, M, budget_s=cpu_budget_s)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{n} tokens of the same workload (route + expert FFN), {dt:.1f} s, "
+                         f"std::thread over tokens"}
+    rec = {"value": value, "unit": "tokens/s", "steps": steps, "warmup": warm, "ms_per_step": ms_per_step,
+           "config": {"workload": wl["desc"], "M": M, "hidden": H, "inter": I, "experts": E, "top_k": K,
+                      "distinct_experts_per_step": distinct,
+                      "l2": f"inputs larger than L2: {n_rep} weight replicas "
+                            f"({n_rep * (x.w13.nbytes + x.w2.nbytes) / 1e9:.2f} GB) rotated per step",
+                      "timing": f"{steps} steps timed as {full} replays of a {G}-step CUDA graph"
+                                f"{f' + one {rem}-step graph' if rem else ''}, events; wall {t_wall:.4f} s; "
+                                f"{n_soak} untimed replays of the same steps before it while clocks were sampled"},
+           "achieved_gbs": alg_bytes * steps / elapsed / 1e9 * world,
+           "achieved_tflops": alg_flops * steps / elapsed / 1e12 * world,
+           "alg_bytes_per_step": alg_bytes, "alg_flops_per_step": alg_flops,
+           "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": kernels_per_step * steps,
+           "clocks": clocks}
+    del reps, w13_0, s13_0, w2_0, s2_0, hidden_all, ws
+    torch.cuda.empty_cache()
+    return rec
+
+
+def dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, given_ids, ids, ws, shape, prefill,
+                    gu_bytes, gu_flops):
+    """gate/up alone, back to back in a CUDA graph on its own stream (few routed rows: the
+    direct gate/up kernel; otherwise the stage kernel, the same launch the forward makes,
+    after one prepare), rotating weight replicas and the steps' expert sets."""
     pair_mode = M * K <= PAIR_ROWS
     n_k = 200 if pair_mode else 10
     ks = torch.cuda.Stream()
@@ -400,8 +463,7 @@ def ours_arm(args, wl, world, rank, local):
 
     with torch.cuda.stream(ks):
         if not pair_mode:
-            b0 = 0
-            ii0 = given_ids[0] if given_ids is not None else ids[b0]
+            ii0 = given_ids[0] if given_ids is not None else ids[0]
             L.moe_fp8_prepare(hidden_all[:M], ii0, M, ws, shape, stream=ks)
         gu(0, ks)
         kg = torch.cuda.CUDAGraph()
@@ -421,75 +483,95 @@ def ours_arm(args, wl, world, rank, local):
         fp8_peak = 2.0 * bf16  # FP8 dense rate = 2x the measured bf16 rate (nominal ratio)
         roof = {"bound": "tensor", "kernel": "gate_up", "achieved": gu_flops / t_gu / 1e12,
                 "peak": fp8_peak, "unit": "TFLOP/s", "frac": gu_flops / t_gu / 1e12 / fp8_peak,
-                "peak_source": f"{peak_src} bf16 x 2 (fp8/bf16 nominal ratio)"}
+                "peak_source": f"{peak_src} bf16 x 2 (fp8/bf16 nominal ratio), burst"}
     else:
         roof = {"bound": "hbm", "kernel": "gate_up", "achieved": gu_bytes / t_gu / 1e9, "peak": hbm,
                 "unit": "GB/s", "frac": gu_bytes / t_gu / 1e9 / hbm, "peak_source": f"{peak_src} hbm_gbs"}
-    roof["traffic"] = recorded_traffic("gate_up", args.workload)
     roof["alg_per_launch"] = gu_flops if prefill else gu_bytes
     roof["mean_launch_us"] = t_gu * 1e6
+    return roof
 
-    # ---- end to end through the public API with host buffers
-    e2e_steps = min(steps, 3000 if decode else (500 if M <= 64 else 10))
-    host_in = torch.empty((nbatches, M, H), dtype=torch.int16).pin_memory()
-    host_in.copy_(hidden_all.view(nbatches, M, H).cpu())
-    host_out = torch.empty((nbatches, M, H), dtype=torch.int16).pin_memory()
-    stage = torch.empty((2, M, H), dtype=torch.int16, device="cuda")
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    cs = torch.cuda.current_stream()
-    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a0.record()
-    for i in range(e2e_steps):
-        b = i % nbatches
-        w13, s13, w2, s2 = reps[i % n_rep]
-        if given_ids is None:
-            # the public host-buffer call: hidden from pinned host memory, route + forward,
-            # output back to pinned host memory, enqueued by one call
-            L.moe_fp8_route_forward_host(host_in[b], host_out[b], M, router, bias, True, w13, s13, w2, s2, ws,
-                                         shape, stream=cs)
-            continue
-        hid = stage[i % 2]
-        hid.copy_(host_in[b], non_blocking=True)
-        L.moe_route(hid, router, bias, M, shape, True, ids[b], wts[b], stream=cs)
-        ii, ww = given_ids
-        L.moe_fp8_forward(hid, ii, ww, M, w13, s13, w2, s2, out[b], ws, shape, stream=cs)
-        host_out[b].copy_(out[b], non_blocking=True)
-    a1.record()
-    torch.cuda.synchronize()
-    e2e_t = a0.elapsed_time(a1) / 1e3
-    if dist:
-        e2e_t = replicas.slowest(e2e_t, dist, "cuda")
-    e2e = {"value": replicas.throughput(world, e2e_steps, M, e2e_t), "unit": "tokens/s",
-           "h2d_bytes_per_step": M * H * 2, "d2h_bytes_per_step": M * H * 2, "steps": e2e_steps}
 
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tps, cores, n, dt = oracle_tokens_per_s(x, M, budget_s=15.0)
-        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": f"{n} tokens of the same workload (route + expert FFN), {dt:.1f} s, "
-                         f"std::thread over tokens"}
+def gpu_selector(torch):
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    uuid = str(getattr(props, "uuid", ""))
+    return ("GPU-" + uuid if uuid and not uuid.startswith("GPU-") else uuid) or str(torch.cuda.current_device())
 
+
+def ours_arm(args, wl, world, rank, local):
+    import torch
+    from fp8_block_scaled_router_gb300 import build as B
+
+    B.build()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    decode = wl["cfg"] == "decode"
+    M = args.m or wl["M"]
+    steps = args.steps or (50000 if decode else (2000 if M <= 64 else 200))
+    warm = max(3, args.warmup if args.warmup is not None else (200 if decode else 5))
+    if args.dominant_only:
+        dominant_only(args, wl)
+        return
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    rec = run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, 12.0)
+    # the metric's other half: prefill (M=4096) in the same run and the same line
+    pre = None
+    if args.workload == "decode" and not args.no_prefill:
+        pre = run_workload(args, WORKLOADS["prefill"], steps, warm, world, rank, dist, want_cpu, 12.0)
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-                "steps": steps, "warmup": warm, "ms_per_step": ms_per_step, "higher_is_better": True,
+        line = {"metric": METRIC, "value": rec["value"], "unit": "tokens/s", "n_gpus": world,
+                "steps": steps, "warmup": warm, "ms_per_step": rec["ms_per_step"], "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 (f32 accumulate)",
-                "data": "synthetic",
-                "config": {"workload": wl["desc"], "M": M, "hidden": H, "inter": I, "experts": E,
-                           "top_k": K, "distinct_experts_per_step": distinct,
-                           "l2": f"inputs larger than L2: {n_rep} weight replicas "
-                                 f"({n_rep * (x.w13.nbytes + x.w2.nbytes) / 1e9:.2f} GB) rotated per step",
-                           "timing": f"CUDA graphs of {G} steps, events, wall {t_wall:.3f} s"},
-                "achieved_gbs": alg_bytes * steps / elapsed / 1e9 / 1 * world,
-                "achieved_tflops": alg_flops * steps / elapsed / 1e12 * world,
-                "alg_bytes_per_step": alg_bytes, "alg_flops_per_step": alg_flops,
-                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": kernels_per_step * steps, "clocks": clocks}
+                "data": "synthetic"}
+        line.update({k: v for k, v in rec.items() if k not in ("value", "unit", "steps", "warmup", "ms_per_step")})
+        if pre is not None:
+            line["prefill"] = pre
         print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def dominant_only(args, wl):
+    """Only the dominant kernel (the launch the roofline times), for a profiler."""
+    import torch
+    from fp8_block_scaled_router_gb300 import _lib as L
+    from fp8_block_scaled_router_gb300 import inputs
+
+    cfg = wl["cfg"]
+    M = args.m if (args.m and cfg == "wide") else wl["M"]
+    x = inputs.make(cfg, tokens=M if cfg == "decode" else None, M=M if cfg == "wide" else None)
+    H, I, E, K = x.shape.hidden, x.shape.inter, x.shape.num_experts, x.shape.top_k
+
+    def dev(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
+
+    n_rep = 2
+    reps = [(dev(x.w13), dev(x.s13)) for _ in range(n_rep)]
+    shape = L.make_shape(H, I, E, K, M)
+    ws = torch.empty(L.moe_fp8_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
+    L.moe_fp8_workspace_init(ws, shape)
+    hid = dev(x.hidden[:M])
+    if x.ids is not None:
+        ii = dev(x.ids[:M])
+    else:
+        ii = torch.empty((M, K), dtype=torch.int32, device="cuda")
+        w = torch.empty((M, K), dtype=torch.float32, device="cuda")
+        L.moe_route(hid, dev(x.router_w), None if x.bias is None else dev(x.bias), M, shape, True, ii, w)
+    if M * K > PAIR_ROWS:
+        L.moe_fp8_prepare(hid, ii, M, ws, shape)
+    for i in range(args.dominant_only):
+        w13, s13 = reps[i % n_rep]
+        if M * K <= PAIR_ROWS:
+            L.moe_fp8_gate_up_direct(hid, ii, M, w13, s13, ws, shape)
+        else:
+            L.moe_fp8_gate_up(w13, s13, M, ws, shape)
+    torch.cuda.synchronize()
 
 
 def main():

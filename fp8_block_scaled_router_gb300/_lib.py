@@ -26,7 +26,7 @@ EXPORTS = ("moe_fp8_version", "moe_fp8_workspace_bytes", "moe_fp8_workspace_init
            "moe_fp8_forward", "moe_fp8_prepare", "moe_fp8_gate_up", "moe_fp8_down",
            "moe_fp8_combine", "moe_fp8_workspace_view", "moe_fp8_read_status",
            "moe_fp8_forward_noalloc", "moe_fp8_gate_up_direct", "moe_fp8_down_combine",
-           "moe_fp8_route_forward_host")
+           "moe_fp8_route_forward_host", "moe_fp8_route_forward_pinned", "moe_fp8_selftest_wait")
 
 
 class MoEError(RuntimeError):
@@ -73,6 +73,8 @@ def load(path: str = LIB):
             lib.moe_fp8_gate_up_direct.argtypes = [vp, vp, i32, vp, vp, vp, sz, sp, vp]
             lib.moe_fp8_down_combine.argtypes = [vp, vp, i32, vp, vp, vp, vp, sz, sp, vp]
             lib.moe_fp8_route_forward_host.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, vp, vp, vp, sz, sp, vp]
+            lib.moe_fp8_route_forward_pinned.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, vp, vp, vp, sz, sp, vp]
+            lib.moe_fp8_selftest_wait.argtypes = [vp, sz, sp, ctypes.c_uint32, vp]
             for f in EXPORTS[2:]:
                 if f != "moe_fp8_workspace_bytes":
                     getattr(lib, f).restype = i32
@@ -216,3 +218,20 @@ def moe_fp8_route_forward_host(host_hidden, host_out, M, router_w, bias, renorma
     return _check("moe_fp8_route_forward_host", load().moe_fp8_route_forward_host(
         _ptr(host_hidden), _ptr(host_out), int(M), _ptr(router_w), _ptr(bias), int(bool(renormalize)), _ptr(w13),
         _ptr(w13_scale), _ptr(w2), _ptr(w2_scale), _ptr(workspace), nb, ctypes.byref(shape), _stream(stream)), check)
+
+
+def moe_fp8_route_forward_pinned(host_hidden, host_out, M, router_w, bias, renormalize, w13, w13_scale, w2,
+                                 w2_scale, workspace, shape: Shape, stream=None, ws_bytes=None, check=True):
+    """moe_fp8_route_forward_host for page-locked host buffers (no pointer query); see
+    include/moe_fp8.h."""
+    nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return _check("moe_fp8_route_forward_pinned", load().moe_fp8_route_forward_pinned(
+        _ptr(host_hidden), _ptr(host_out), int(M), _ptr(router_w), _ptr(bias), int(bool(renormalize)), _ptr(w13),
+        _ptr(w13_scale), _ptr(w2), _ptr(w2_scale), _ptr(workspace), nb, ctypes.byref(shape), _stream(stream)), check)
+
+
+def moe_fp8_selftest_wait(workspace, shape: Shape, limit_us, stream=None, ws_bytes=None, check=True):
+    """Bounded-wait self-check: sets MOE_STATUS_WAIT_TIMEOUT in the workspace status."""
+    nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return _check("moe_fp8_selftest_wait", load().moe_fp8_selftest_wait(
+        _ptr(workspace), nb, ctypes.byref(shape), int(limit_us), _stream(stream)), check)

@@ -1,5 +1,6 @@
 // api.cu -- the C ABI (include/moe_fp8.h): host-side validation, workspace layout and the
-// launch sequence. No call allocates, frees, synchronises or reads device memory.
+// launch sequence. No call allocates, frees or reads device memory; only the host-buffer
+// call with pageable (not page-locked) buffers blocks, in the driver's staged copies.
 //
 // Sources: "NetraRuntime/netra-kernel" README (stable C ABI that launches on a
 // caller-provided stream; exact profile guards, unsupported contracts are refused) and
@@ -30,6 +31,7 @@ cudaError_t launch_pair_down(const uint8_t* w2, const float* s2w, const int32_t*
                              cudaStream_t st);
 cudaError_t launch_combine(const float* topk_w, int M, int H, int K, uint16_t* out, const WsPtrs& ws,
                            cudaStream_t st);
+cudaError_t launch_wait_selftest(Header* hdr, uint32_t limit_us, cudaStream_t st);
 }  // namespace moe
 
 using namespace moe;
@@ -299,6 +301,35 @@ moe_status_t moe_fp8_route_forward_host(const void* host_hidden, void* host_out,
     return st;
   if (copy_out) return launched(cudaMemcpyAsync(host_out, out, bytes, cudaMemcpyDeviceToHost, stream));
   return MOE_OK;
+}
+
+moe_status_t moe_fp8_route_forward_pinned(const void* host_hidden, void* host_out, int32_t M,
+                                          const void* router_w, const float* bias, int32_t renormalize,
+                                          const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
+                                          const float* w2_scale, void* workspace, size_t workspace_bytes,
+                                          const moe_fp8_shape_t* shape, cudaStream_t stream) {
+  if (moe_status_t st = check_common(shape, M)) return st;
+  if (!host_hidden || !host_out || !aligned16(host_hidden) || !aligned16(host_out)) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  if (M == 0) return MOE_OK;
+  char* b = static_cast<char*>(workspace);
+  int32_t* ids = reinterpret_cast<int32_t*>(b + L.ids_stage);
+  float* wts = reinterpret_cast<float*>(b + L.wts_stage);
+  // page-locked host memory under unified addressing: the host pointers are device-usable
+  if (moe_status_t st = moe_route(host_hidden, router_w, bias, M, shape, renormalize, ids, wts, stream)) return st;
+  return moe_fp8_forward(host_hidden, ids, wts, M, w13, w13_scale, w2, w2_scale, host_out, workspace,
+                         workspace_bytes, shape, stream);
+}
+
+moe_status_t moe_fp8_selftest_wait(void* workspace, size_t workspace_bytes, const moe_fp8_shape_t* shape,
+                                   uint32_t limit_us, cudaStream_t stream) {
+  if (!shape) return MOE_ERR_INVALID_ARG;
+  if (!shape_supported(shape)) return MOE_ERR_UNSUPPORTED;
+  if (limit_us < 1 || limit_us > 1000000) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  return launched(launch_wait_selftest(ws_ptrs(workspace, L).hdr, limit_us, stream));
 }
 
 moe_status_t moe_fp8_read_status(const void* workspace, uint32_t* host_dst, cudaStream_t stream) {

@@ -17,6 +17,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       WsPtrs ws) {
   const int t = blockIdx.x;
   const int h = (blockIdx.y * 256 + threadIdx.x) * 8;
+  // y and perm_row come from the kernels before this one on the stream
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   if (t >= M || h >= H) return;
   float acc[8];
 #pragma unroll
@@ -59,9 +62,16 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 
 cudaError_t launch_combine(const float* topk_w, int M, int H, int K, uint16_t* out, const WsPtrs& ws,
                            cudaStream_t st) {
-  dim3 grid(M, (H + 2047) / 2048);
-  combine_kernel<<<grid, 256, 0, st>>>(topk_w, M, H, K, out, ws);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)M, (unsigned)((H + 2047) / 2048), 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, topk_w, M, H, K, out, ws);
 }
 
 }  // namespace moe

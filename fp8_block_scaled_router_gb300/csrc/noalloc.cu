@@ -9,13 +9,16 @@
 // file-scope __device__ array of kNoAllocScratchBytes (1 MiB) that every GPU which loads
 // this library keeps until the process exits.
 //
-// Set-up: the first call on each device (with that device current) looks up the array's
-// device address with cudaGetSymbolAddress and caches it; make that first call before any
-// stream capture. Host code never passes the array's host-side symbol to a kernel.
+// Set-up: the first call in each CUDA context (with that context current) looks up the
+// array's device address with cudaGetSymbolAddress and caches it under (device, context);
+// make that first call before any stream capture. Host code never passes the array's
+// host-side symbol to a kernel.
 // Sharing: every call on a device uses the same array and leaves its contents behind; calls
 // whose GPU work overlaps (different streams, no ordering between them) race on it. The
 // status word at the start of the array is cleared on every call (an asynchronous memset
 // on the caller's stream); no other part of the array needs to start at zero.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -35,12 +38,32 @@ using namespace moe;
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;
-constexpr int kMaxDevices = 64;
+constexpr int kMaxContexts = 64;
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
+// The array's device address per (device, context) seen so far.
+struct ScratchEntry {
+  int dev;
+  CUcontext ctx;
+  void* ptr;
+};
 std::mutex g_scratch_mu;
-void* g_scratch_dev[kMaxDevices] = {};
+ScratchEntry g_scratch[kMaxContexts] = {};
+int g_scratch_used = 0;
+
+PFN_cuCtxGetCurrent_v4000 ctx_get_current() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+  });
+  return fn;
+}
 
 // Layout inside the scratch array: header (256 B), act [R][I], act_scale [R][I/128].
 size_t noalloc_bytes(int64_t R, int I) {
@@ -69,16 +92,27 @@ extern "C" moe_status_t moe_fp8_forward_noalloc(const void* hidden, const int32_
   if (!pair_capable(R) || noalloc_bytes(R, I) > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED;
 
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_LAUNCH;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return MOE_ERR_LAUNCH;
   void* base = nullptr;
   {
+    CUcontext ctx = nullptr;
+    auto get_ctx = ctx_get_current();
+    if (!get_ctx || get_ctx(&ctx) != CUDA_SUCCESS) return MOE_ERR_LAUNCH;
+    if (!ctx) {  // no context current yet: the runtime's first symbol lookup creates the primary one
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || get_ctx(&ctx) != CUDA_SUCCESS || !ctx)
+        return MOE_ERR_LAUNCH;
+    }
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_dev[dev]) {
+    for (int i = 0; i < g_scratch_used; ++i)
+      if (g_scratch[i].dev == dev && g_scratch[i].ctx == ctx) base = g_scratch[i].ptr;
+    if (!base) {
+      if (g_scratch_used == kMaxContexts) return MOE_ERR_LAUNCH;
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MOE_ERR_LAUNCH;
-      g_scratch_dev[dev] = p;
+      g_scratch[g_scratch_used++] = ScratchEntry{dev, ctx, p};
+      base = p;
     }
-    base = g_scratch_dev[dev];
   }
   char* b = static_cast<char*>(base);
   WsPtrs ws{};

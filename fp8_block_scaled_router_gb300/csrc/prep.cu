@@ -10,6 +10,7 @@
 // Few routed rows (pair mode): block 0 records each pair's expert (-1 if out of range) and
 // the identity permutation. Many routed rows: the two-launch counting sort below.
 #include "common.cuh"
+#include "device.h"
 
 namespace moe {
 
@@ -237,7 +238,8 @@ cudaError_t launch_sort_gather(const uint16_t* hidden, const int32_t* ids, int M
   const int nblk = (R + kSortBlock - 1) / kSortBlock;
   const int64_t groups = (int64_t)M * (H / 128);
   int64_t qblocks = (groups + 7) / 8;
-  if (qblocks > 8 * 152) qblocks = 8 * 152;
+  const int64_t cap8 = 8 * (int64_t)(device_info().sms > 0 ? device_info().sms : 1);  // 8 CTAs per SM
+  if (qblocks > cap8) qblocks = cap8;
   count_quant_kernel<<<(unsigned)(nblk + qblocks), 256, 0, st>>>(hidden, ids, M, H, E, K, nblk, ws);
   if (cudaError_t e = cudaGetLastError()) return e;
   cudaLaunchConfig_t cfg = {};
@@ -258,7 +260,8 @@ cudaError_t launch_prep(const uint16_t* hidden, const int32_t* ids, int M, int H
                         const WsPtrs& ws, cudaStream_t st) {
   const int64_t groups = (int64_t)M * (H / 128);
   int64_t qblocks = (groups + (kPrepThreads / 32) - 1) / (kPrepThreads / 32);
-  if (qblocks > 4 * 152) qblocks = 4 * 152;
+  const int64_t cap4 = 4 * (int64_t)(device_info().sms > 0 ? device_info().sms : 1);  // 4 CTAs per SM
+  if (qblocks > cap4) qblocks = cap4;
   prep_kernel<<<(unsigned)(1 + qblocks), kPrepThreads, 0, st>>>(hidden, ids, M, H, E, K, ws);
   return cudaGetLastError();
 }

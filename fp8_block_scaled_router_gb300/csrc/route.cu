@@ -18,6 +18,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "device.h"
 
 namespace cg = cooperative_groups;
 
@@ -506,18 +507,20 @@ cudaError_t launch_route_t(const uint16_t* hidden, const uint16_t* router_w, con
                            int H, int E, int K, int renorm, int32_t* ids, float* wts, cudaStream_t st) {
   const int nchunks = H / 128;
   const int CL = route_cluster(nchunks);
+  const DeviceInfo d = device_info();
+  if (d.sms == 0) return cudaErrorInvalidDevice;
   bool stream = false;
   RouteSmem L = route_smem(TB, nchunks / CL, E, nchunks, true);
-  if (L.total > 227 * 1024) {  // the CTA's router chunks do not all fit: stream them
+  if (L.total > d.smem_optin) {  // the CTA's router chunks do not all fit: stream them
     stream = true;
     L = route_smem(TB, nchunks / CL, E, nchunks, false);
   }
-  if (L.total > 227 * 1024) return cudaErrorInvalidConfiguration;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    cudaFuncSetAttribute(route_kernel<TB, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (L.total > d.smem_optin) return cudaErrorInvalidConfiguration;
+  static PerDeviceOnce once;
+  once_per_device(once, [&] {
+    cudaFuncSetAttribute(route_kernel<TB, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)d.smem_optin);
     cudaFuncSetAttribute(route_kernel<TB, false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    cudaFuncSetAttribute(route_kernel<TB, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaFuncSetAttribute(route_kernel<TB, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)d.smem_optin);
     cudaFuncSetAttribute(route_kernel<TB, true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   });
   cudaLaunchConfig_t cfg = {};
@@ -557,20 +560,22 @@ cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    static std::once_flag once;
-    std::call_once(once, [] {
-      cudaFuncSetAttribute(route_big_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-      cudaFuncSetAttribute(route_big_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-      cudaFuncSetAttribute(route_big_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    static PerDeviceOnce once;
+    once_per_device(once, [] {
+      const int bytes = (int)route_big_smem(128);
+      cudaFuncSetAttribute(route_big_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+      cudaFuncSetAttribute(route_big_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+      cudaFuncSetAttribute(route_big_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     });
     auto go = [&](auto kern) { return cudaLaunchKernelEx(&cfg, kern, hidden, router_w, bias, M, H, K, renorm, ids, wts); };
     if (E == 128) return go(route_big_kernel<4>);
     if (E == 64) return go(route_big_kernel<2>);
     return go(route_big_kernel<1>);
   }
-  if (M >= 16 && route_smem(8, nchunks / route_cluster(nchunks), E, nchunks, true).total <= 227 * 1024)
+  const size_t optin = device_info().smem_optin;
+  if (M >= 16 && route_smem(8, nchunks / route_cluster(nchunks), E, nchunks, true).total <= optin)
     return launch_route_t<8>(hidden, router_w, bias, M, H, E, K, renorm, ids, wts, st);
-  if (M >= 4 && route_smem(2, nchunks / route_cluster(nchunks), E, nchunks, true).total <= 227 * 1024)
+  if (M >= 4 && route_smem(2, nchunks / route_cluster(nchunks), E, nchunks, true).total <= optin)
     return launch_route_t<2>(hidden, router_w, bias, M, H, E, K, renorm, ids, wts, st);
   return launch_route_t<1>(hidden, router_w, bias, M, H, E, K, renorm, ids, wts, st);
 }

@@ -46,12 +46,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Wait for the phase with the given parity to complete; false if kWaitLimitNs elapsed.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
+// Wait for the phase with the given parity to complete; false if `limit_ns` elapsed first.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(b, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(b, parity))
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   return true;
 }
 

@@ -21,15 +21,16 @@
 // (one rounding per step: the multiply-add is fused here, which the parity window covers;
 // two adjacent columns per packed fma.rn.f32x2);
 // thread = (accumulator row, 64 of the 256 columns).
-// gate/up epilogue: act = silu(g) * u (fast exponential and division intrinsics, a few ulp)
-// for the thread's columns, the row's amax over 128 columns (the partner warps' parts via
-// shared memory), scale = amax/448, RNE saturating E4M3 codes -> act [row][I] and
+// gate/up epilogue: act = silu(g) * u (expf and IEEE division) for the thread's columns,
+// the row's amax over 128 columns (the partner warps' parts via shared memory),
+// scale = amax/448, RNE saturating E4M3 codes of act / scale -> act [row][I] and
 // act_scale [row][I/128]. down epilogue: y [row][H] FP32 in 32-byte stores.
 // Rows of a tile past its length are computed on zero/neighbour rows and never stored.
 #include <cudaTypedefs.h>
 
 #include <mutex>
 
+#include "device.h"
 #include "tc.cuh"
 
 namespace moe {
@@ -236,7 +237,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
         float amax = 0.0f;
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          act[c] = silu_mul_fast(acc[c], acc[32 + c]);
+          act[c] = silu_mul(acc[c], acc[32 + c]);
           amax = fmaxf(amax, fabsf(act[c]));
         }
         red[row * 4 + slot4] = amax;
@@ -244,17 +245,15 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
         amax = fmaxf(fmaxf(red[row * 4], red[row * 4 + 1]), fmaxf(red[row * 4 + 2], red[row * 4 + 3]));
         tc::named_bar(1, kEpiThreads);  // red is rewritten by the next unit
         const float s2 = quant_scale(amax);
-        // codes = RNE_E4M3(act * (448 / amax)): one reciprocal per row instead of 32
-        // divisions; within one ulp of act / s2 before rounding to E4M3
-        const float inv = amax == 0.0f ? 1.0f : __fdiv_rn(448.0f, amax);
+        // codes = RNE_E4M3(act / s2), IEEE division as in the few-row path
         if (live) {
           uint8_t* dst = p.act_out + (size_t)(row0 + row) * p.I + nb * 128 + slot4 * 32;
           uint32_t w8[8];
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
             const int c = q4 * 4;
-            const uint32_t lo = e4m3x2_encode(__fmul_rn(act[c], inv), __fmul_rn(act[c + 1], inv));
-            const uint32_t hi = e4m3x2_encode(__fmul_rn(act[c + 2], inv), __fmul_rn(act[c + 3], inv));
+            const uint32_t lo = e4m3x2_encode(__fdiv_rn(act[c], s2), __fdiv_rn(act[c + 1], s2));
+            const uint32_t hi = e4m3x2_encode(__fdiv_rn(act[c + 2], s2), __fdiv_rn(act[c + 3], s2));
             w8[q4] = lo | (hi << 16);
           }
           // the row's 32 codes in one 32-byte store (a whole L2 sector)
@@ -315,18 +314,13 @@ namespace {
 template <bool GATEUP>
 cudaError_t launch_grouped(const CUtensorMap& tA, const CUtensorMap& tB, const CUtensorMap& tY,
                            const GrpParams& prm, int64_t max_tiles, cudaStream_t st) {
-  static std::once_flag once;
-  std::call_once(once, [] {
+  static PerDeviceOnce once;
+  once_per_device(once, [] {
     cudaFuncSetAttribute(grouped_gemm_kernel<GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)grp_smem_bytes(GATEUP));
   });
-  static int num_sms = 0;
-  static std::once_flag sm_once;
-  std::call_once(sm_once, [] {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
-  });
+  const int num_sms = device_info().sms;
+  if (num_sms == 0) return cudaErrorInvalidDevice;
   const int64_t units = max_tiles * prm.nnb;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(units < num_sms ? units : num_sms), 1, 1);

@@ -50,30 +50,13 @@
 #include <algorithm>
 #include <mutex>
 
+#include "device.h"
+#include "pair_plan.h"
 #include "tc.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace moe {
-
-constexpr int kPairN = 16;  // B rows per MMA (row 0 is the unit's pair)
-constexpr int kMaxSplitTerms = 8;  // K blocks per CTA when a unit's K blocks are split
-constexpr int kPairThreads = 192;
-constexpr int kMaxStages = 8;
-
-enum PairMode { kGateUpWs = 0, kGateUpFused = 1, kDownY = 2, kDownCombine = 3 };
-
-template <int MODE>
-struct PairCfg {
-  static constexpr bool kGateUp = MODE == kGateUpWs || MODE == kGateUpFused;
-  static constexpr int kATiles = kGateUp ? 2 : 1;
-  static constexpr int kABytes = 128 * 128;
-  static constexpr int kBBytes = kPairN * 128;
-  static constexpr int kStageBytes = ((kATiles * kABytes + kBBytes + 1023) / 1024) * 1024;
-  static constexpr uint32_t kTxA = kATiles * kABytes;
-  static constexpr int kAccCols = kATiles * kPairN;  // one K block's accumulators
-  static constexpr int kTmemCols = 2 * kAccCols < 32 ? 32 : 2 * kAccCols;
-};
 
 struct PairParams {
   int H, I, K, E;
@@ -91,32 +74,9 @@ struct PairParams {
   Header* hdr;
   const uint8_t* pf_w2;    // gate/up: w2 [E][H][I] to prefetch into L2, or null
   const float* pf_s2;      // gate/up: its scales [E][H/128][I/128]
+  uint8_t* qa_out;         // kGateUpFused: the hidden codes it quantised [M][H] (slot 0's
+  float* sa_out;           //   CTAs of the first output block write them), scales [M][H/128]
 };
-
-// Split-K terms [kATiles][nkb][128] f32 arrive in CTA 0's stage buffers once its own MMAs
-// are complete (the host keeps kATiles * nkb * 512 bytes within them); the combine rows
-// [K][128] f32 have a region of their own.
-template <int MODE>
-struct PairSmem {
-  size_t stages, bq, sas, sws, comb, cw, bars, total;
-};
-
-template <int MODE>
-__host__ __device__ inline PairSmem<MODE> pair_smem(int nst, int nkb_cta, int K) {
-  using C = PairCfg<MODE>;
-  PairSmem<MODE> s{};
-  size_t o = 0;
-  s.stages = o; o += (size_t)nst * C::kStageBytes;
-  s.bq = o;   o += MODE == kGateUpFused ? (size_t)nkb_cta * 128 : 0;  // hidden codes past the stages
-  s.sas = o;  o += (size_t)nkb_cta * 4;                               // activation scales
-  s.sws = o;  o += (size_t)C::kATiles * nkb_cta * 4;                  // weight scales
-  o = (o + 15) & ~size_t(15);
-  s.comb = o; o += MODE == kDownCombine ? (size_t)K * 512 : 0;        // combine rows
-  s.cw = o;   o += MODE == kDownCombine ? 16 * 8 : 0;                 // combine weights + ids
-  s.bars = o; o += 256;
-  s.total = o + 1024;  // + alignment slack of the dynamic shared memory base
-  return s;
-}
 
 template <int MODE>
 __global__ void __launch_bounds__(kPairThreads, 3)
@@ -251,6 +211,10 @@ __global__ void __launch_bounds__(kPairThreads, 3)
       uint8_t* dst = i < nst ? stages + i * C::kStageBytes + C::kTxA : bq + i * 128;
       reinterpret_cast<uint32_t*>(dst)[lane] = lo | (hi << 16);
       if (lane == 0) sas[i] = sc;
+      if (p.qa_out != nullptr && cb == 0 && pr % p.K == 0) {  // one copy of the token's codes (view)
+        reinterpret_cast<uint32_t*>(p.qa_out + (size_t)tok * p.H + (kb0 + i) * 128)[lane] = lo | (hi << 16);
+        if (lane == 0) p.sa_out[(size_t)tok * p.nkb + kb0 + i] = sc;
+      }
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   } else {
@@ -538,65 +502,25 @@ bool make_tmap_u8_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
 
 namespace {
 
-struct PairPlan {
-  int split, nst;
-};
-
 template <int MODE>
-void set_pair_attrs() {
-  static std::once_flag once;
-  std::call_once(once, [] {
-    cudaFuncSetAttribute(pair_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+void set_pair_attrs(const DeviceInfo& d) {
+  static PerDeviceOnce once;
+  once_per_device(once, [&] {
+    cudaFuncSetAttribute(pair_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)d.smem_optin);
     cudaFuncSetAttribute(pair_gemm_kernel<MODE>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   });
 }
 
-constexpr int kNumSMs = 152;
-constexpr size_t kSmemPerSM = 228 * 1024;
-
-// CTAs of `smem` bytes resident at once in clusters of `cluster`: SMs x CTAs per SM, less a
-// tenth for clusters that a GPC cannot place whole. Clusters of two or more CTAs at one CTA
-// per SM are counted as not fitting (a GPC's SM count is not a multiple of the cluster).
-inline int64_t resident_ctas(int cluster, size_t smem) {
-  const int64_t per_sm = (int64_t)(kSmemPerSM / (smem + 1024));
-  if (per_sm == 0 || (cluster > 1 && per_sm < 2)) return 0;
-  return cluster > 1 ? kNumSMs * per_sm * 9 / 10 : kNumSMs * per_sm;
-}
-
-// The largest K split S (a divisor of nkb, S <= 8) whose units * S CTAs are all resident at
-// once, with the most pipeline stages (<= the CTA's K blocks, <= kMaxStages) that keep them
-// resident; `fixed_cluster` (down fused with the combine) is the cluster size when the mode
-// fixes it. When nothing fits one wave: no split, 2 stages for gate/up and 4 for down.
-template <int MODE>
-PairPlan plan_pair(int nkb, int64_t units, int K, bool allow_split, int fixed_cluster = 0) {
-  using C = PairCfg<MODE>;
-  PairPlan best{1, std::min(nkb, C::kGateUp ? 2 : 4)};
-  for (int s = 1; s <= (allow_split ? 8 : 1); ++s) {
-    if (nkb % s) continue;
-    const int per = nkb / s;
-    if (s > 1 && per > kMaxSplitTerms) continue;
-    const int cluster = fixed_cluster ? fixed_cluster : s;
-    int chosen = 0;
-    for (int n = std::min(per, kMaxStages); n >= std::min(per, 2); --n) {
-      // split-K terms land in CTA 0's stage buffers
-      if (s > 1 && (size_t)C::kATiles * nkb * 512 > (size_t)n * C::kStageBytes) break;
-      const size_t smem = pair_smem<MODE>(n, per, K).total;
-      if (smem > 227 * 1024) continue;
-      if (units * cluster <= resident_ctas(cluster, smem)) {
-        chosen = n;
-        break;
-      }
-    }
-    if (chosen) best = {s, chosen};
-  }
-  return best;
-}
+PlanDevice plan_device(const DeviceInfo& d) { return PlanDevice{d.sms, d.smem_per_sm, d.smem_optin}; }
 
 template <int MODE>
 cudaError_t launch_pair(const CUtensorMap& tA, const CUtensorMap& tB, PairParams prm, int cluster_x,
                         int64_t units, cudaStream_t st) {
   const PairSmem<MODE> SL = pair_smem<MODE>(prm.nst, prm.nkb_cta, prm.K);
-  set_pair_attrs<MODE>();
+  const DeviceInfo d = device_info();
+  if (d.sms == 0) return cudaErrorInvalidDevice;
+  if (SL.total > d.smem_optin) return cudaErrorInvalidConfiguration;
+  set_pair_attrs<MODE>(d);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cluster_x, (unsigned)units, 1);
   cfg.blockDim = dim3(kPairThreads, 1, 1);
@@ -643,8 +567,11 @@ cudaError_t launch_pair_gateup(const uint8_t* w13, const float* s13, const int32
   prm.pf_w2 = w2;
   prm.pf_s2 = s2w;
   const int64_t units = (int64_t)M * K * prm.ncb;
-  const PairPlan pl = hidden ? plan_pair<kGateUpFused>(prm.nkb, units, K, true)
-                             : plan_pair<kGateUpWs>(prm.nkb, units, K, true);
+  prm.qa_out = ws.qa;
+  prm.sa_out = ws.sa;
+  const PlanDevice dv = plan_device(device_info());
+  const PairPlan pl = hidden ? plan_pair<kGateUpFused>(dv, prm.nkb, units, K, true)
+                             : plan_pair<kGateUpWs>(dv, prm.nkb, units, K, true);
   prm.nkb_cta = prm.nkb / pl.split;
   prm.nst = pl.nst;
   if (hidden) {
@@ -674,11 +601,11 @@ cudaError_t launch_pair_down(const uint8_t* w2, const float* s2w, const int32_t*
     prm.topk_w = topk_w;
     prm.out = out;
     prm.nkb_cta = prm.nkb;
-    prm.nst = plan_pair<kDownCombine>(prm.nkb, (int64_t)M * prm.ncb, K, false, K).nst;
+    prm.nst = plan_pair<kDownCombine>(plan_device(device_info()), prm.nkb, (int64_t)M * prm.ncb, K, false, K).nst;
     return launch_pair<kDownCombine>(tA, tB, prm, K, (int64_t)M * prm.ncb, st);
   }
   const int64_t units = (int64_t)R * prm.ncb;
-  const PairPlan pl = plan_pair<kDownY>(prm.nkb, units, K, true);
+  const PairPlan pl = plan_pair<kDownY>(plan_device(device_info()), prm.nkb, units, K, true);
   prm.nkb_cta = prm.nkb / pl.split;
   prm.nst = pl.nst;
   return launch_pair<kDownY>(tA, tB, prm, pl.split, units, st);

@@ -124,8 +124,7 @@ moe_status_t moe_route(const void* hidden, const void* router_w, const float* bi
  * in FP32 (P_kb = the block's FP8 dot product on the tensor core or in FP32);
  * act = silu(g) * u in FP32; out = bf16(sum over slots j ascending of w_j * y_j).
  * With more than 64 routed rows (sorted expert tiles) the promotion is one fused
- * multiply-add per block, silu uses the fast exponential and division intrinsics and the
- * requantisation multiplies by 448/amax: a few ulp from the forms above, inside the same
+ * multiply-add per block (one rounding instead of two per step), inside the same
  * tolerances (activation codes may move one step next to a rounding boundary).
  * 0 <= M <= max_tokens; M = 0 is a no-op. */
 moe_status_t moe_fp8_forward(const void* hidden, const int32_t* topk_ids, const float* topk_w,
@@ -211,6 +210,18 @@ moe_status_t moe_fp8_route_forward_host(const void* host_hidden, void* host_out,
                                         const float* w2_scale, void* workspace, size_t workspace_bytes,
                                         const moe_fp8_shape_t* shape, cudaStream_t stream);
 
+/* moe_fp8_route_forward_host for host buffers the caller guarantees are page-locked and
+ * mapped (cudaMallocHost / cudaHostAlloc, or cudaHostRegister on a device that can use host
+ * pointers for registered memory): the kernels read host_hidden and write host_out in place
+ * through unified addressing, with no pointer-type query and no copy on the call's path.
+ * host_hidden and host_out must be 16-byte aligned. Passing pageable memory is a caller
+ * error (the kernels' accesses to it fail). No counterpart in the paper (as above). */
+moe_status_t moe_fp8_route_forward_pinned(const void* host_hidden, void* host_out, int32_t M,
+                                          const void* router_w, const float* bias, int32_t renormalize,
+                                          const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
+                                          const float* w2_scale, void* workspace, size_t workspace_bytes,
+                                          const moe_fp8_shape_t* shape, cudaStream_t stream);
+
 /* moe_fp8_forward for callers that cannot allocate device memory where they run the layer
  * (for example while a memory pool is locked or being resized, inside callbacks that must
  * not enter the allocator, or in integrations without a device allocator): the same
@@ -221,8 +232,10 @@ moe_status_t moe_fp8_route_forward_host(const void* host_hidden, void* host_out,
  * It runs the kernels of moe_fp8_gate_up_direct + moe_fp8_down_combine.
  * Limits: M * top_k <= 256 and M * top_k * (inter + inter/32) + 512 <= 1 MiB; anything
  * larger returns MOE_ERR_UNSUPPORTED.
- * Set-up: the first call on a device (made with that device current) looks up the array's
- * device address; make that first call before any stream capture.
+ * Set-up: the first call in a CUDA context (made with that context current) looks up the
+ * array's device address; make that first call before any stream capture. The address is
+ * kept per (device, context) for the life of the process, so a process that calls
+ * cudaDeviceReset must not call this entry point on that device again.
  * Sharing: all calls on a device share the array, which keeps the last call's contents;
  * calls whose GPU work overlaps (unordered streams) race on it. Each call clears the
  * array's status word on `stream`; device status bits are not readable through this call.
@@ -232,6 +245,14 @@ moe_status_t moe_fp8_forward_noalloc(const void* hidden, const int32_t* topk_ids
                                      int32_t M, const uint8_t* w13, const float* w13_scale,
                                      const uint8_t* w2, const float* w2_scale, void* out,
                                      const moe_fp8_shape_t* shape, cudaStream_t stream);
+
+/* Self-check of the bounded device wait that every kernel uses ([NKL] "Development
+ * expectations": a focused correctness entry point per kernel contract). One thread waits on a barrier phase
+ * that nothing completes, gives up after limit_us microseconds (1 .. 10^6), sets
+ * MOE_STATUS_WAIT_TIMEOUT in the workspace's status word and returns; the context stays
+ * usable. Clear the status afterwards with moe_fp8_workspace_init. */
+moe_status_t moe_fp8_selftest_wait(void* workspace, size_t workspace_bytes, const moe_fp8_shape_t* shape,
+                                   uint32_t limit_us, cudaStream_t stream);
 
 /* Copy the workspace's status word to host memory `host_dst` (asynchronous on `stream`;
  * the caller synchronises before reading it). */

@@ -1,0 +1,36 @@
+// Host-only client of the pair-kernel launch planner (csrc/pair_plan.h), built and run by
+// tests/test_plan_host.py with the host C++ compiler: no CUDA, no GPU. For each case it
+// prints the plan and the facts the test checks it against, one line per case:
+//   sms smem_per_sm mode nkb units K split nst smem_total resident
+#include <cstdio>
+
+#include "pair_plan.h"
+
+using namespace moe;
+
+template <int MODE>
+void show(const PlanDevice& d, int nkb, long long units, int K, bool allow_split, int fixed_cluster) {
+  const PairPlan p = plan_pair<MODE>(d, nkb, units, K, allow_split, fixed_cluster);
+  const size_t smem = pair_smem<MODE>(p.nst, nkb / p.split, K).total;
+  const int cluster = fixed_cluster ? fixed_cluster : p.split;
+  std::printf("%d %zu %d %d %lld %d %d %d %zu %lld\n", d.sms, d.smem_per_sm, MODE, nkb, units, K, p.split, p.nst,
+              smem, (long long)resident_ctas(d, cluster, smem));
+}
+
+int main() {
+  const PlanDevice devs[] = {{152, 233472, 232448}, {148, 233472, 232448}, {132, 233472, 232448},
+                             {76, 233472, 232448}, {38, 233472, 232448}, {8, 233472, 232448},
+                             {152, 102400, 101376}};
+  for (const PlanDevice& d : devs) {
+    // decode gate/up (h2048: 16 K blocks, 8 pairs x 6 output blocks), verify (96 pairs),
+    // wide (h6144: 48 K blocks, 4 pairs x 6), down+combine (6 K blocks, cluster of K)
+    show<kGateUpFused>(d, 16, 48, 8, true, 0);
+    show<kGateUpFused>(d, 16, 576, 8, true, 0);
+    show<kGateUpFused>(d, 48, 24, 4, true, 0);
+    show<kGateUpWs>(d, 16, 48, 8, true, 0);
+    show<kDownY>(d, 6, 128, 8, true, 0);
+    show<kDownCombine>(d, 6, 16, 8, false, 8);
+    show<kDownCombine>(d, 6, 192, 8, false, 8);
+  }
+  return 0;
+}

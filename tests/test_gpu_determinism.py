@@ -25,27 +25,41 @@ def _build_lib():
 def _workload(name, M):
     if name == "grouped":  # 64 tokens x top-8 over 16 experts: the sorted-tile path
         return inputs.make("decode", E=16, tokens=M)
-    return inputs.make(name, tokens=M) if name == "decode" else inputs.make(name)
+    if name == "decode":
+        return inputs.make(name, tokens=M)
+    return inputs.make(name, M=M)
 
 
-@pytest.mark.parametrize("name,M", [("decode", 1), ("verify", 12), ("tiny", 4), ("grouped", 64)])
+DET_CASES = [("decode", 1), ("verify", 12), ("tiny", 4), ("grouped", 64), ("wide", 1), ("wide", 64),
+             ("prefill", 4096), ("prefill_zipf", 4096)]
+
+
+@pytest.mark.parametrize("name,M", DET_CASES, ids=[f"{n}-M{m}" for n, m in DET_CASES])
 def test_100_launches_bitwise_identical(name, M):
+    """Route + forward 100 times on the same inputs: ids, weights, the activation codes and
+    scales and the output are bitwise identical every time (compared on the device)."""
+    from fp8_block_scaled_router_gb300 import _lib as L
     x = _workload(name, M)
     g = GpuMoE(x, M)
     hid = to_dev(x.hidden[:M])
+    given = None if x.ids is None else (to_dev(x.ids[:M]), to_dev(x.weights[:M]))
+    v = L.moe_fp8_workspace_view(g.ws, g.shape)
+    base = g.ws.data_ptr()
+    R = M * g.K
+    act = g.ws[v.act - base: v.act - base + R * g.I]
+    act_s = g.ws[v.act_scale - base: v.act_scale - base + R * (g.I // 128) * 4]
     ref = None
     for it in range(100):
         ids, w = g.route(hid, M)
-        out = g.forward(hid, ids, w, M)
-        ws = g.ws_arrays(M) if it % 25 == 0 else None
-        cur = (ids.cpu().numpy(), w.cpu().numpy().view(np.uint32), out.cpu().numpy())
+        fi, fw = given if given is not None else (ids, w)
+        out = g.forward(hid, fi, fw, M)
+        cur = (ids.clone(), w.view(torch.int32).clone(), out.clone(), act.clone(), act_s.clone())
         if ref is None:
-            ref, ref_act = cur, ws["act"].copy()
+            ref = cur
         else:
-            for a, b in zip(ref, cur):
-                assert np.array_equal(a, b), f"launch {it} differs"
-            if ws is not None:
-                assert np.array_equal(ws["act"], ref_act)
+            for k, (a, b) in enumerate(zip(ref, cur)):
+                assert torch.equal(a, b), f"launch {it} differs (output {k})"
+    assert g.status() == 0
 
 
 def test_graph_capture_replay_matches_eager():

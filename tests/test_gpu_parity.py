@@ -111,8 +111,16 @@ def test_route_rows_beyond_m_untouched():
 
 
 # ------------------------------------------------------------------ forward
+def poison_workspace(g):
+    """Stale contents must not matter: every value a test reads must be written by the call."""
+    g.ws.fill_(0xFF)
+    from fp8_block_scaled_router_gb300 import _lib as L
+    L.moe_fp8_workspace_init(g.ws, g.shape)
+
+
 def run_forward_case(x, M, max_tokens=None, zero_rows=None):
     g = gpu_for(x, max_tokens or M)
+    poison_workspace(g)
     hidden = x.hidden[:M].copy()
     if zero_rows is not None:
         hidden[zero_rows] = 0
@@ -123,12 +131,18 @@ def run_forward_case(x, M, max_tokens=None, zero_rows=None):
         ids_o, w_o = oracle.route(hidden, x.router_w, x.bias, x.shape.top_k)
     hid_d, ids_d = to_dev(hidden), to_dev(ids_o)
     out = g.forward(hid_d, ids_d, to_dev(w_o), M)
-    # the few-row forward quantises hidden inside gate/up and writes no permutation; the
-    # prepare stage fills those workspace views (it does not touch the activation codes)
+    torch.cuda.synchronize()
+    # the hidden codes and scales as the forward's own quantiser wrote them (the few-row
+    # gate/up kernel quantises in its prologue; the sorted path in its count+quantise pass)
+    ws = g.ws_arrays(M)
+    qa, sa = ws["qa"].copy(), ws["sa"].copy()
+    # the few-row forward writes no permutation; the prepare stage fills those views (it
+    # does not touch the activation codes)
     from fp8_block_scaled_router_gb300 import _lib as L
     L.moe_fp8_prepare(hid_d, ids_d, M, g.ws, g.shape)
     torch.cuda.synchronize()
     ws = g.ws_arrays(M)
+    ws["qa"], ws["sa"] = qa, sa
     out_o, dbg = oracle_forward(x, hidden, ids_o, w_o, debug=True)
     return g, ids_o, ws, u16(out), out_o, dbg
 
@@ -187,33 +201,41 @@ def test_many_tiles_with_ragged_tails():
 
 
 @pytest.mark.parametrize("name", ["prefill", "prefill_zipf"])
-def test_prefill_full_size_sampled(name):
-    """Full M=4096 launch; the oracle evaluates 40 sampled tokens one by one (each token's
-    output depends only on its own row, ids and weights)."""
+def test_prefill_full_size(name):
+    """The full M=4096 launch against the oracle on every token: hidden codes and scales,
+    the permutation, all 32768 routed rows' activation codes and scales, and the output."""
     x = workload(name)
     M = 4096
+    _, ids_o, ws, out, out_o, dbg = run_forward_case(x, M)
+    check_all(x, M, ids_o, ws, out, out_o, dbg, name)
+
+
+PAIR_DIRECT = [("verify_skewed", 12), ("decode", 32)]  # 96 and 256 routed rows
+
+
+@pytest.mark.parametrize("name,M", PAIR_DIRECT, ids=[f"{n}-R{m * 8}" for n, m in PAIR_DIRECT])
+def test_pair_kernels_against_oracle(name, M):
+    """The two few-row kernels as direct calls (one unit per routed pair) above the 64 rows
+    at which moe_fp8_forward switches to sorted tiles: hidden codes from the gate/up kernel's
+    own quantiser, activation codes and scales in pair order, and the output."""
+    from fp8_block_scaled_router_gb300 import _lib as L
+    x = workload(name) if name != "decode" else workload(name, tokens=M)
     g = gpu_for(x, M)
-    if x.ids is not None:
-        ids_o, w_o = x.ids, x.weights
-    else:
-        import oracle
-        ids_o, w_o = oracle.route(x.hidden, x.router_w, None, 8)
-    out = u16(g.forward(to_dev(x.hidden), to_dev(ids_o), to_dev(w_o), M))
+    poison_workspace(g)
+    import oracle
+    ids_o, w_o = oracle.route(x.hidden[:M], x.router_w, x.bias, x.shape.top_k)
+    hid, ids, w = to_dev(x.hidden[:M]), to_dev(ids_o), to_dev(w_o)
+    out = torch.empty((M, g.H), dtype=torch.int16, device="cuda")
+    L.moe_fp8_gate_up_direct(hid, ids, M, g.w13, g.s13, g.ws, g.shape)
+    L.moe_fp8_down_combine(ids, w, M, g.w2, g.s2, out, g.ws, g.shape)
+    torch.cuda.synchronize()
+    assert g.status() == 0
     ws = g.ws_arrays(M)
-    check_permutation(ws, ids_o, x.shape.num_experts)
-    rng = np.random.default_rng(99)
-    rows = np.sort(rng.choice(M, 40, replace=False))
-    out_o, dbg = oracle_forward(x, x.hidden[rows], ids_o[rows], w_o[rows], debug=True)
-    assert np.array_equal(ws["qa"][rows], dbg["qa"]) and np.array_equal(ws["sa"][rows], dbg["sa"])
-    check_out(out[rows], out_o, name)
-    # activation codes of the sampled tokens' routed rows
-    K = 8
-    sub = dict(row_src=np.array([t * K + j for t in range(len(rows)) for j in range(K)]))
-    pr = ws["perm_row"]
-    src_rows = np.array([pr[r * K + j] for r in rows for j in range(K)])
-    sub["act"] = ws["act"][src_rows]
-    sub["act_scale"] = ws["act_scale"][src_rows]
-    check_act(sub, dbg, K, name)
+    out_o, dbg = oracle_forward(x, x.hidden[:M], ids_o, w_o, debug=True)
+    assert np.array_equal(ws["qa"], dbg["qa"]) and np.array_equal(ws["sa"], dbg["sa"])
+    ws["row_src"] = np.arange(M * g.K, dtype=np.int32)  # pair order
+    check_act(ws, dbg, g.K, f"{name} direct R={M * g.K}")
+    check_out(u16(out), out_o, f"{name} direct")
 
 
 def test_output_rows_beyond_m_untouched():

@@ -44,6 +44,25 @@ def test_noalloc_matches_workspace_forward_twice(name, M):
         assert torch.equal(out, ref), f"call {call}"
 
 
+@pytest.mark.parametrize("name,M", [("verify_skewed", 12), ("decode", 32)], ids=["R96", "R256"])
+def test_noalloc_against_oracle(name, M):
+    """The no-workspace call above the 64 routed rows where moe_fp8_forward sorts rows into
+    expert tiles (the range only the pair kernels serve), against the oracle's output."""
+    import oracle
+    from fp8_block_scaled_router_gb300 import _lib as L
+    from gpu_harness import GpuMoE, check_out, oracle_forward, to_dev, u16
+
+    oracle.build()
+    x = inputs.make(name, tokens=M) if name == "decode" else inputs.make(name, M=M)
+    g = GpuMoE(x, M)
+    ids_o, w_o = oracle.route(x.hidden[:M], x.router_w, x.bias, g.K)
+    out = torch.full((M, g.H), 0x7ABC, dtype=torch.int16, device="cuda")
+    L.moe_fp8_forward_noalloc(to_dev(x.hidden[:M]), to_dev(ids_o), to_dev(w_o), M, g.w13, g.s13, g.w2, g.s2,
+                              out, g.shape)
+    torch.cuda.synchronize()
+    check_out(u16(out), oracle_forward(x, x.hidden[:M], ids_o, w_o), f"noalloc {name} R={M * g.K}")
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     from fp8_block_scaled_router_gb300 import _lib as L
     fake = 0x10000
