@@ -140,11 +140,30 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
   return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
 }
 
-// silu(g) * u with the fast exponential and division intrinsics (a few ulp from silu_mul;
-// for the many-row epilogue, where the tail of each 128-row tile is on the critical path).
-// For g below about -88 the exponential overflows to +inf and the quotient is -0.
+// exp(-g) from the hardware base-2 exponential with a split argument, accurate to a few
+// ulp for every g. -g*log2(e) is carried as an unevaluated sum hi + lo: hi = fl(-g * L2E_HI),
+// lo = its exact rounding error (one fma, the TwoProduct of Dekker / Ogita-Rump-Oishi) plus
+// -g * L2E_LO, the product with the low part of log2(e) (Cody-Waite style argument
+// splitting). Then exp(-g) = 2^hi * 2^lo with 2^lo = 1 + lo*ln2 to first order (|lo| is a
+// few ulp of hi). A single rounded product -g*log2(e) would instead lose about |g| ulp.
+__device__ __forceinline__ float exp_neg_split(float g) {
+  constexpr float kL2eHi = 1.4426950216293335f;    // float32 nearest to log2(e)
+  constexpr float kL2eLo = 1.925963033500011e-08f; // log2(e) - kL2eHi
+  constexpr float kLn2 = 0.6931471805599453f;
+  const float x = -g;
+  const float hi = __fmul_rn(x, kL2eHi);
+  const float lo = __fadd_rn(__fmaf_rn(x, kL2eHi, -hi), __fmul_rn(x, kL2eLo));
+  float p;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(p) : "f"(hi));
+  return __fmaf_rn(p, __fmul_rn(lo, kLn2), p);
+}
+
+// silu(g) * u with the split-argument exponential and the fast division intrinsic: within a
+// few ulp of silu_mul for every g (for the many-row epilogue, where the tail of each 128-row
+// tile is on the tensor core's critical path). For g below about -88 the exponential
+// overflows to +inf and the quotient is -0, as in silu_mul.
 __device__ __forceinline__ float silu_mul_fast(float g, float u) {
-  return __fmul_rn(__fdividef(g, __fadd_rn(1.0f, __expf(-g))), u);
+  return __fmul_rn(__fdividef(g, __fadd_rn(1.0f, exp_neg_split(g))), u);
 }
 
 __device__ __forceinline__ void set_status(Header* hdr, uint32_t bits) {

@@ -21,9 +21,10 @@
 // (one rounding per step: the multiply-add is fused here, which the parity window covers;
 // two adjacent columns per packed fma.rn.f32x2);
 // thread = (accumulator row, 64 of the 256 columns).
-// gate/up epilogue: act = silu(g) * u (expf and IEEE division) for the thread's columns,
-// the row's amax over 128 columns (the partner warps' parts via shared memory),
-// scale = amax/448, RNE saturating E4M3 codes of act / scale -> act [row][I] and
+// gate/up epilogue: act = silu(g) * u (split-argument base-2 exponential and the fast
+// division, a few ulp for every g) for the thread's columns, the row's amax over 128
+// columns (the partner warps' parts via shared memory), scale = amax/448, RNE saturating
+// E4M3 codes of act * (448/amax) -> act [row][I] and
 // act_scale [row][I/128]. down epilogue: y [row][H] FP32 in 32-byte stores.
 // Rows of a tile past its length are computed on zero/neighbour rows and never stored.
 #include <cudaTypedefs.h>
@@ -237,7 +238,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
         float amax = 0.0f;
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          act[c] = silu_mul(acc[c], acc[32 + c]);
+          act[c] = silu_mul_fast(acc[c], acc[32 + c]);
           amax = fmaxf(amax, fabsf(act[c]));
         }
         red[row * 4 + slot4] = amax;
@@ -245,15 +246,17 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
         amax = fmaxf(fmaxf(red[row * 4], red[row * 4 + 1]), fmaxf(red[row * 4 + 2], red[row * 4 + 3]));
         tc::named_bar(1, kEpiThreads);  // red is rewritten by the next unit
         const float s2 = quant_scale(amax);
-        // codes = RNE_E4M3(act / s2), IEEE division as in the few-row path
+        // codes = RNE_E4M3(act * (448 / amax)): one reciprocal per row instead of 32
+        // divisions; within one ulp of act / s2 before rounding to E4M3
+        const float inv = amax == 0.0f ? 1.0f : __fdiv_rn(448.0f, amax);
         if (live) {
           uint8_t* dst = p.act_out + (size_t)(row0 + row) * p.I + nb * 128 + slot4 * 32;
           uint32_t w8[8];
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
             const int c = q4 * 4;
-            const uint32_t lo = e4m3x2_encode(__fdiv_rn(act[c], s2), __fdiv_rn(act[c + 1], s2));
-            const uint32_t hi = e4m3x2_encode(__fdiv_rn(act[c + 2], s2), __fdiv_rn(act[c + 3], s2));
+            const uint32_t lo = e4m3x2_encode(__fmul_rn(act[c], inv), __fmul_rn(act[c + 1], inv));
+            const uint32_t hi = e4m3x2_encode(__fmul_rn(act[c + 2], inv), __fmul_rn(act[c + 3], inv));
             w8[q4] = lo | (hi << 16);
           }
           // the row's 32 codes in one 32-byte store (a whole L2 sector)

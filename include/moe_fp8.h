@@ -124,8 +124,10 @@ moe_status_t moe_route(const void* hidden, const void* router_w, const float* bi
  * in FP32 (P_kb = the block's FP8 dot product on the tensor core or in FP32);
  * act = silu(g) * u in FP32; out = bf16(sum over slots j ascending of w_j * y_j).
  * With more than 64 routed rows (sorted expert tiles) the promotion is one fused
- * multiply-add per block (one rounding instead of two per step), inside the same
- * tolerances (activation codes may move one step next to a rounding boundary).
+ * multiply-add per block (one rounding instead of two per step), silu's exponential is the
+ * hardware base-2 exponential of a split argument with a fast division (a few ulp for every
+ * g) and the requantisation multiplies by 448/amax (within one ulp of the division): inside
+ * the same tolerances (activation codes may move one step next to a rounding boundary).
  * 0 <= M <= max_tokens; M = 0 is a no-op. */
 moe_status_t moe_fp8_forward(const void* hidden, const int32_t* topk_ids, const float* topk_w,
                              int32_t M, const uint8_t* w13, const float* w13_scale,

@@ -65,6 +65,8 @@ def _load():
             lib.orc_moe_forward.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp,
                                             vp, ctypes.POINTER(_Debug), i32]
             lib.orc_moe_forward.restype = i32
+            lib.orc_down_combine.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i32]
+            lib.orc_down_combine.restype = i32
             _lib = lib
     return _lib
 
@@ -157,3 +159,21 @@ def moe_forward(hidden, ids, weights, w13, s13, w2, s2w, debug: bool = False, nt
     if rc != 0:
         raise ValueError("oracle forward: unsupported sizes")
     return (out, arrays) if debug else out
+
+
+def down_combine(qact, s2, ids, weights, w2, s2w, nthreads: int = 1):
+    """Steps 6-7 from given activation codes qact uint8 [M][K][I] and scales s2 f32
+    [M][K][I/128]: the down projection of every routed pair and the slot-order combine.
+    Returns out uint16(BF16) [M][H]."""
+    qact, s2 = _c(qact, np.uint8), _c(s2, np.float32)
+    ids, weights = _c(ids, np.int32), _c(weights, np.float32)
+    w2, s2w = _c(w2, np.uint8), _c(s2w, np.float32)
+    M, K, I = qact.shape
+    E, H, I2 = w2.shape
+    assert I2 == I and s2.shape == (M, K, I // 128) and ids.shape == weights.shape == (M, K)
+    out = np.empty((M, H), np.uint16)
+    rc = _load().orc_down_combine(_p(qact), _p(s2), _p(ids), _p(weights), M, H, I, E, K, _p(w2), _p(s2w), _p(out),
+                                  int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle down_combine: unsupported sizes")
+    return out

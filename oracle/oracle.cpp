@@ -233,6 +233,32 @@ float scaled_row(const uint8_t* a, const float* sa, const uint8_t* w, const floa
   return acc;
 }
 
+// Down projection of one routed pair (step 6): y[h] for every row h of w2[e] ([H][I], K
+// contiguous), from the pair's activation codes and scales.
+void down_row(const uint8_t* qact, const float* s2, int e, const Dims d, const uint8_t* w2, const float* s2w,
+              float* y) {
+  const int H = d.H, I = d.I, nki = I / 128;
+  for (int h = 0; h < H; ++h) {
+    const uint8_t* wrow = w2 + ((int64_t)e * H + h) * I;
+    const float* srow = s2w + ((int64_t)e * (H / 128) + h / 128) * nki;
+    y[h] = scaled_row(qact, s2, wrow, srow, nki, nullptr);
+  }
+}
+
+// Combine (step 7, the route reducer): slots j ascending, FP32 multiply then add, from 0;
+// a skipped slot contributes nothing; BF16 round to nearest even.
+void combine_token(const float* Y, const float* w_t, const char* valid, int K, int H, uint16_t* out_t) {
+  for (int h = 0; h < H; ++h) {
+    float acc = 0.0f;
+    for (int j = 0; j < K; ++j) {
+      if (!valid[j]) continue;
+      const float p = w_t[j] * Y[(size_t)j * H + h];
+      acc = acc + p;
+    }
+    out_t[h] = f32_to_bf16(acc);
+  }
+}
+
 void forward_tokens(const uint16_t* hidden, const int32_t* ids, const float* w, const Dims d,
                     const uint8_t* w13, const float* s13, const uint8_t* w2, const float* s2w,
                     uint16_t* out, const orc_debug_t* dbg, int t0, int t1) {
@@ -264,13 +290,8 @@ void forward_tokens(const uint16_t* hidden, const int32_t* ids, const float* w, 
         act[i] = (float)(g / (1.0 + std::exp(-g)) * u);
       }
       for (int kb = 0; kb < nki; ++kb) s2[kb] = quantise_group(&act[kb * 128], 128, &qact[kb * 128]);
-      // down: rows h of w2[e] ([H][I], K contiguous)
       float* y = &Y[(size_t)j * H];
-      for (int h = 0; h < H; ++h) {
-        const uint8_t* wrow = w2 + ((int64_t)e * H + h) * I;
-        const float* srow = s2w + ((int64_t)e * (H / 128) + h / 128) * nki;
-        y[h] = scaled_row(qact.data(), s2.data(), wrow, srow, nki, nullptr);
-      }
+      down_row(qact.data(), s2.data(), e, d, w2, s2w, y);
       if (dbg) {
         if (dbg->g) std::memcpy(dbg->g + pj * I, G.data(), I * 4);
         if (dbg->u) std::memcpy(dbg->u + pj * I, G.data() + I, I * 4);
@@ -282,16 +303,25 @@ void forward_tokens(const uint16_t* hidden, const int32_t* ids, const float* w, 
         if (dbg->y) std::memcpy(dbg->y + pj * H, y, (size_t)H * 4);
       }
     }
-    // combine (route reducer): slots j ascending, FP32 multiply then add, from 0
-    for (int h = 0; h < H; ++h) {
-      float acc = 0.0f;
-      for (int j = 0; j < K; ++j) {
-        if (!valid[j]) continue;
-        const float p = w[(int64_t)t * K + j] * Y[(size_t)j * H + h];
-        acc = acc + p;
-      }
-      out[(int64_t)t * H + h] = f32_to_bf16(acc);
+    combine_token(Y.data(), w + (int64_t)t * K, valid.data(), K, H, out + (int64_t)t * H);
+  }
+}
+
+// Steps 6 and 7 for M tokens from given activation codes and scales (per routed pair).
+void down_combine_tokens(const uint8_t* qact, const float* s2, const int32_t* ids, const float* w, const Dims d,
+                         const uint8_t* w2, const float* s2w, uint16_t* out, int t0, int t1) {
+  const int H = d.H, I = d.I, E = d.E, K = d.K, nki = I / 128;
+  std::vector<float> Y((size_t)K * H);
+  std::vector<char> valid(K);
+  for (int t = t0; t < t1; ++t) {
+    for (int j = 0; j < K; ++j) {
+      const int e = ids[(int64_t)t * K + j];
+      valid[j] = (e >= 0 && e < E);
+      if (!valid[j]) continue;
+      const int64_t pj = (int64_t)t * K + j;
+      down_row(qact + pj * I, s2 + pj * nki, e, d, w2, s2w, &Y[(size_t)j * H]);
     }
+    combine_token(Y.data(), w + (int64_t)t * K, valid.data(), K, H, out + (int64_t)t * H);
   }
 }
 
@@ -319,6 +349,29 @@ int orc_moe_forward(const uint16_t* hidden, const int32_t* ids, const float* w, 
   for (int i = 0; i < nthreads; ++i) {
     const int t0 = (int)((int64_t)M * i / nthreads), t1 = (int)((int64_t)M * (i + 1) / nthreads);
     th.emplace_back(forward_tokens, hidden, ids, w, d, w13, s13, w2, s2w, out, dbg, t0, t1);
+  }
+  for (auto& x : th) x.join();
+  return 0;
+}
+
+// Steps 6 and 7 alone: the down projection of every routed pair from GIVEN activation
+// codes qact [M][K][I] and scales s2 [M][K][I/128], then the slot-order combine into BF16
+// out [M][H] -- the same arithmetic as the tail of orc_moe_forward, so that the output of
+// a path whose activation codes are known can be checked on its own. Returns 0 or -1.
+int orc_down_combine(const uint8_t* qact, const float* s2, const int32_t* ids, const float* w, int M, int H,
+                     int I, int E, int K, const uint8_t* w2, const float* s2w, uint16_t* out, int nthreads) {
+  if (M < 0 || H <= 0 || I <= 0 || H % 128 || I % 128 || E <= 0 || K <= 0) return -1;
+  const Dims d{M, H, I, E, K};
+  table();
+  if (nthreads <= 1 || M <= 1) {
+    down_combine_tokens(qact, s2, ids, w, d, w2, s2w, out, 0, M);
+    return 0;
+  }
+  nthreads = std::min(nthreads, M);
+  std::vector<std::thread> th;
+  for (int i = 0; i < nthreads; ++i) {
+    const int t0 = (int)((int64_t)M * i / nthreads), t1 = (int)((int64_t)M * (i + 1) / nthreads);
+    th.emplace_back(down_combine_tokens, qact, s2, ids, w, d, w2, s2w, out, t0, t1);
   }
   for (auto& x : th) x.join();
   return 0;

@@ -14,8 +14,8 @@ from fp8_block_scaled_router_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
-    from gpu_harness import (GpuMoE, check_act, check_out, check_permutation, oracle_forward,
-                             oracle_route, to_dev, u16)
+    from gpu_harness import (GpuMoE, check_act, check_out, check_out_given_act, check_permutation,
+                             oracle_forward, oracle_route, to_dev, u16)
 
 _CACHE = {}
 
@@ -144,6 +144,7 @@ def run_forward_case(x, M, max_tokens=None, zero_rows=None):
     ws = g.ws_arrays(M)
     ws["qa"], ws["sa"] = qa, sa
     out_o, dbg = oracle_forward(x, hidden, ids_o, w_o, debug=True)
+    dbg["w"] = w_o
     return g, ids_o, ws, u16(out), out_o, dbg
 
 
@@ -152,7 +153,7 @@ def check_all(x, M, ids_o, ws, out, out_o, dbg, what):
     assert np.array_equal(ws["sa"], dbg["sa"]), f"{what}: hidden scales"
     check_permutation(ws, ids_o, x.shape.num_experts)
     check_act(ws, dbg, x.shape.top_k, what)
-    check_out(out, out_o, what)
+    check_out_given_act(out, out_o, ws, dbg, ids_o, dbg["w"], x, what)
 
 
 FWD_CASES = [("tiny", 4), ("verify", 12), ("verify_skewed", 12)]
@@ -210,6 +211,18 @@ def test_prefill_full_size(name):
     check_all(x, M, ids_o, ws, out, out_o, dbg, name)
 
 
+def test_large_gate_values_sorted_tiles():
+    """Gate/up values of tens (w13 block scales x 16, a power of two, so the codes are
+    unchanged): the sorted-tile epilogue's SiLU must hold the activation-code window where
+    exp(-g) is far from 1 in either direction. 300 tokens over 16 experts (sorted tiles)."""
+    import dataclasses
+    x = workload("decode", E=16, tokens=300)
+    x = dataclasses.replace(x, s13=(x.s13 * np.float32(16.0)).astype(np.float32))
+    _, ids_o, ws, out, out_o, dbg = run_forward_case(x, 300)
+    assert np.abs(dbg["g"]).max() > 20 and dbg["g"].min() < -20
+    check_all(x, 300, ids_o, ws, out, out_o, dbg, "large g (sorted)")
+
+
 PAIR_DIRECT = [("verify_skewed", 12), ("decode", 32)]  # 96 and 256 routed rows
 
 
@@ -235,7 +248,7 @@ def test_pair_kernels_against_oracle(name, M):
     assert np.array_equal(ws["qa"], dbg["qa"]) and np.array_equal(ws["sa"], dbg["sa"])
     ws["row_src"] = np.arange(M * g.K, dtype=np.int32)  # pair order
     check_act(ws, dbg, g.K, f"{name} direct R={M * g.K}")
-    check_out(u16(out), out_o, f"{name} direct")
+    check_out_given_act(u16(out), out_o, ws, dbg, ids_o, w_o, x, f"{name} direct")
 
 
 def test_output_rows_beyond_m_untouched():

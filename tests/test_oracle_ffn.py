@@ -223,3 +223,36 @@ def test_threads_do_not_change_results(oracle_mod):
     a = oracle_mod.moe_forward(x.hidden, ids, wts, x.w13, x.s13, x.w2, x.s2, nthreads=1)
     b = oracle_mod.moe_forward(x.hidden, ids, wts, x.w13, x.s13, x.w2, x.s2, nthreads=3)
     assert np.array_equal(a, b)
+
+
+def test_down_combine_from_given_codes(case, oracle_mod):
+    """down_combine (steps 6-7 from given activation codes): fed the forward's own codes it
+    reproduces the forward's output bitwise; fed perturbed codes, its output matches a
+    float64 dequantised down projection and combine of those codes within the FP32 and
+    BF16 rounding bound, and only the perturbed token's row changes."""
+    x, ids, wts, out, d = case
+    same = oracle_mod.down_combine(d["qact"], d["s2"], ids, wts, x.w2, x.s2, nthreads=2)
+    assert np.array_equal(same, out)
+    q = d["qact"].copy()
+    t0 = x.M - 1
+    q[t0, 0, 5] ^= 0x01                   # one activation code one step away
+    q[t0, x.shape.top_k - 1, 130 % x.shape.inter] ^= 0x08
+    got = oracle_mod.down_combine(q, d["s2"], ids, wts, x.w2, x.s2)
+    assert np.array_equal(got[:t0], out[:t0])
+    assert not np.array_equal(got[t0], out[t0])
+    I = x.shape.inter
+    nkb = I // 128
+    K = x.shape.top_k
+    for t in range(x.M):
+        ref = np.zeros(x.shape.hidden)
+        absr = np.zeros(x.shape.hidden)
+        for j in range(K):
+            a = deq_act(q[t, j], d["s2"][t, j])
+            W = deq_weight(x.w2[ids[t, j]], x.s2[ids[t, j]])
+            Y = W @ a
+            ybound = (nkb + 3) * U * (np.abs(W) @ np.abs(a)) * 1.01
+            ref += wts[t, j] * Y
+            absr += abs(wts[t, j]) * (np.abs(Y) + ybound)
+        g = inputs.bf16_bits_to_f32(got[t]).astype(np.float64)
+        assert np.all(np.abs(g - ref) <= 2.0 ** -8 * np.abs(ref) + (2 * K + 2) * U * absr * 1.01 +
+                      (nkb + 3) * U * absr * 1.01 + 1e-38), t
