@@ -1,8 +1,9 @@
 #!/usr/bin/env python
 """Throughput of the routed FP8 block-scaled MoE layer on GB300 (one JSON line on stdout).
 
-A step is one pass of the whole layer -- moe_route then moe_fp8_forward (prepare, gate/up
-+ SiLU*up requantisation, down, combine) -- over one batch of synthetic tokens. The default
+A step is one pass of the whole layer -- moe_fp8_route_forward: routing, then prepare,
+gate/up + SiLU*up requantisation, down, combine (one launch for a few routed pairs) -- over
+one batch of synthetic tokens. The default
 workload is decode: hidden 2048, intermediate 768, 128 experts, top-8 renormalised, one
 token per step, stepping through 10,000 seeded tokens; the same line carries a "prefill"
 record (M=4096, same shapes), the metric's tensor-bound half. Other workloads
@@ -20,7 +21,8 @@ e2e     the same metric through the public API with host buffers: per step one
         inside the timed region (the Zipf workload, whose routing is given, uses a host copy,
         moe_route, moe_fp8_forward and a copy back).
 roofline the dominant kernel timed alone with CUDA events on its stream, its algorithmic
-        bytes (or FLOPs) per launch divided by the mean launch time.
+        bytes (or FLOPs) per launch divided by the mean launch time: for decode the single
+        launch that is the whole step, for prefill the gate/up grouped GEMM.
 cpu_baseline the oracle (plain C++ on the host cores) on a bounded sample of the same
         workload (rank 0, N=1 only).
 
@@ -64,6 +66,18 @@ WORKLOADS = {
 
 # routed rows up to which moe_fp8_forward runs the two pair kernels
 PAIR_ROWS = 64
+# routed pairs up to which the layer is one launch (for the shapes the bench runs, whose
+# single-launch pipeline fits the device: h2048 with up to 16 pairs, h6144 with up to 8)
+FUSED_ROWS = 16
+
+
+def launches_per_step(M, K, H, E):
+    """Our kernels per step: one launch for a few routed pairs; route, gate/up, down+combine
+    up to PAIR_ROWS; otherwise route, count+quantise, scatter, gather, gate/up, down, combine."""
+    R = M * K
+    if R <= FUSED_ROWS and (H <= 2048 or R <= 8):
+        return 1
+    return 3 if R <= PAIR_ROWS else 7
 
 
 def parse():
@@ -292,17 +306,15 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
         b = i % nbatches
         hid = hidden_all[b * M:(b + 1) * M]
         w13, s13, w2, s2 = reps[i % n_rep]
-        L.moe_route(hid, router, bias, M, shape, True, ids[b], wts[b], stream=stream)
         if given_ids is not None:   # Zipf workload: the expert load is given, not routed
+            L.moe_route(hid, router, bias, M, shape, True, ids[b], wts[b], stream=stream)
             ii, ww = given_ids
-        else:
-            ii, ww = ids[b], wts[b]
-        L.moe_fp8_forward(hid, ii, ww, M, w13, s13, w2, s2, out[b], ws, shape, stream=stream)
+            L.moe_fp8_forward(hid, ii, ww, M, w13, s13, w2, s2, out[b], ws, shape, stream=stream)
+        else:                       # the public one-call layer: routing + expert FFN
+            L.moe_fp8_route_forward(hid, router, bias, M, True, w13, s13, w2, s2, out[b], ids[b], wts[b], ws,
+                                    shape, stream=stream)
 
-    # our kernels per step: few routed rows (M*K <= PAIR_ROWS, the library's switch to sorted
-    # expert tiles) -> route, gate/up, down+combine; otherwise route,
-    # count+quantise, scatter, gather, gate/up, down, combine
-    kernels_per_step = 3 if M * K <= PAIR_ROWS else 7
+    kernels_per_step = launches_per_step(M, K, H, E)
 
     # distinct experts per step (accounting only)
     for i in range(min(nbatches, 64)):
@@ -378,9 +390,14 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
     value = replicas.throughput(world, steps, M, elapsed)
     ms_per_step = 1e3 * elapsed / steps
 
-    roof = dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, given_ids, ids, ws, shape,
-                           prefill, gu_bytes, gu_flops)
-    roof["traffic"] = recorded_traffic("gate_up", "prefill" if prefill else args.workload)
+    if kernels_per_step == 1:
+        roof = single_launch_roofline(L, torch, M, nbatches, hidden_all, reps, n_rep, router, bias, ids, wts, out,
+                                      ws, shape, alg_bytes)
+        roof["traffic"] = recorded_traffic("fused", cfg)
+    else:
+        roof = dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, given_ids, ids, ws, shape,
+                               prefill, gu_bytes, gu_flops)
+        roof["traffic"] = recorded_traffic("gate_up", "prefill" if prefill else args.workload)
 
     # ---- end to end through the public API with host buffers
     e2e_steps = min(steps * max(1, n_soak), 3000 if decode else (500 if M <= 64 else 10))
@@ -492,6 +509,41 @@ def dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, giv
     return roof
 
 
+def single_launch_roofline(L, torch, M, nbatches, hidden_all, reps, n_rep, router, bias, ids, wts, out, ws, shape,
+                           alg_bytes):
+    """The one-launch layer (routing + expert FFN) alone, back to back in a CUDA graph on its
+    own stream over rotating weight replicas: the step's algorithmic bytes per launch over
+    the mean launch time."""
+    n_k = 200
+    ks = torch.cuda.Stream()
+    ks.wait_stream(torch.cuda.current_stream())
+
+    def one(i, st):
+        b = i % nbatches
+        w13, s13, w2, s2 = reps[i % n_rep]
+        L.moe_fp8_route_forward(hidden_all[b * M:(b + 1) * M], router, bias, M, True, w13, s13, w2, s2, out[b],
+                                ids[b], wts[b], ws, shape, stream=st)
+
+    with torch.cuda.stream(ks):
+        one(0, ks)
+        kg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(kg, stream=ks):
+            for i in range(n_k):
+                one(i, ks)
+        kg.replay()
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k0.record(ks)
+        for _ in range(3):
+            kg.replay()
+        k1.record(ks)
+    ks.synchronize()
+    t = k0.elapsed_time(k1) / 1e3 / (3 * n_k)
+    hbm, _, _, peak_src = load_peaks()
+    return {"bound": "hbm", "kernel": "fused_kernel (routing + expert FFN, one launch)",
+            "achieved": alg_bytes / t / 1e9, "peak": hbm, "unit": "GB/s", "frac": alg_bytes / t / 1e9 / hbm,
+            "peak_source": f"{peak_src} hbm_gbs", "alg_per_launch": alg_bytes, "mean_launch_us": t * 1e6}
+
+
 def gpu_selector(torch):
     props = torch.cuda.get_device_properties(torch.cuda.current_device())
     uuid = str(getattr(props, "uuid", ""))
@@ -537,14 +589,15 @@ def ours_arm(args, wl, world, rank, local):
 
 
 def dominant_only(args, wl):
-    """Only the dominant kernel (the launch the roofline times), for a profiler."""
+    """Only the dominant kernel (the launch the roofline times), for a profiler: the one-launch
+    layer for a few routed pairs, else the gate/up GEMM after one prepare."""
     import torch
     from fp8_block_scaled_router_gb300 import _lib as L
     from fp8_block_scaled_router_gb300 import inputs
 
     cfg = wl["cfg"]
     M = args.m if (args.m and cfg == "wide") else wl["M"]
-    x = inputs.make(cfg, tokens=M if cfg == "decode" else None, M=M if cfg == "wide" else None)
+    x = inputs.make(cfg, tokens=max(M, 8) if cfg == "decode" else None, M=M if cfg == "wide" else None)
     H, I, E, K = x.shape.hidden, x.shape.inter, x.shape.num_experts, x.shape.top_k
 
     def dev(a):
@@ -552,22 +605,29 @@ def dominant_only(args, wl):
         return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
 
     n_rep = 2
-    reps = [(dev(x.w13), dev(x.s13)) for _ in range(n_rep)]
+    reps = [(dev(x.w13), dev(x.s13), dev(x.w2), dev(x.s2)) for _ in range(n_rep)]
     shape = L.make_shape(H, I, E, K, M)
     ws = torch.empty(L.moe_fp8_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
     L.moe_fp8_workspace_init(ws, shape)
     hid = dev(x.hidden[:M])
-    if x.ids is not None:
-        ii = dev(x.ids[:M])
-    else:
-        ii = torch.empty((M, K), dtype=torch.int32, device="cuda")
-        w = torch.empty((M, K), dtype=torch.float32, device="cuda")
-        L.moe_route(hid, dev(x.router_w), None if x.bias is None else dev(x.bias), M, shape, True, ii, w)
-    if M * K > PAIR_ROWS:
-        L.moe_fp8_prepare(hid, ii, M, ws, shape)
+    router = dev(x.router_w)
+    bias = None if x.bias is None else dev(x.bias)
+    ii = torch.empty((M, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    out = torch.empty((M, H), dtype=torch.int16, device="cuda")
+    single = launches_per_step(M, K, H, E) == 1 and x.ids is None
+    if not single:
+        if x.ids is not None:
+            ii = dev(x.ids[:M])
+        else:
+            L.moe_route(hid, router, bias, M, shape, True, ii, w)
+        if M * K > PAIR_ROWS:
+            L.moe_fp8_prepare(hid, ii, M, ws, shape)
     for i in range(args.dominant_only):
-        w13, s13 = reps[i % n_rep]
-        if M * K <= PAIR_ROWS:
+        w13, s13, w2, s2 = reps[i % n_rep]
+        if single:
+            L.moe_fp8_route_forward(hid, router, bias, M, True, w13, s13, w2, s2, out, ii, w, ws, shape)
+        elif M * K <= PAIR_ROWS:
             L.moe_fp8_gate_up_direct(hid, ii, M, w13, s13, ws, shape)
         else:
             L.moe_fp8_gate_up(w13, s13, M, ws, shape)

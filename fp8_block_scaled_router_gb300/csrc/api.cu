@@ -32,6 +32,11 @@ cudaError_t launch_pair_down(const uint8_t* w2, const float* s2w, const int32_t*
 cudaError_t launch_combine(const float* topk_w, int M, int H, int K, uint16_t* out, const WsPtrs& ws,
                            cudaStream_t st);
 cudaError_t launch_wait_selftest(Header* hdr, uint32_t limit_us, cudaStream_t st);
+bool fused_capable(int M, int H, int I, int E, int K);
+cudaError_t launch_fused(bool route, const uint16_t* hidden, const uint16_t* router_w, const float* bias,
+                         int renorm, int32_t* ids, float* wts, const uint8_t* w13, const float* s13,
+                         const uint8_t* w2, const float* s2w, uint16_t* out, int M, int H, int I, int E, int K,
+                         const WsPtrs& ws, uint32_t* tickets, cudaStream_t st);
 }  // namespace moe
 
 using namespace moe;
@@ -96,7 +101,8 @@ moe_status_t moe_fp8_workspace_init(void* workspace, size_t workspace_bytes,
   if (!shape_supported(shape)) return MOE_ERR_UNSUPPORTED;
   Layout L;
   if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
-  return launched(cudaMemsetAsync(static_cast<char*>(workspace) + L.header, 0, sizeof(Header), stream));
+  // the status word and the single-launch path's arrival tickets (contiguous)
+  return launched(cudaMemsetAsync(static_cast<char*>(workspace) + L.header, 0, L.qa - L.header, stream));
 }
 
 moe_status_t moe_route(const void* hidden, const void* router_w, const float* bias, int32_t M,
@@ -192,12 +198,21 @@ moe_status_t moe_fp8_forward(const void* hidden, const int32_t* topk_ids, const 
   Layout L;
   if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
   if (M == 0) return MOE_OK;
+  const int H = shape->hidden, I = shape->inter, E = shape->num_experts, K = shape->top_k;
+  if (fused_capable(M, H, I, E, K)) {
+    // a few routed pairs: the whole layer in one launch (gate/up with the hidden
+    // quantisation, SiLU*up requantisation, down and the combine)
+    const WsPtrs ws = ws_ptrs(workspace, L);
+    return launched(launch_fused(false, static_cast<const uint16_t*>(hidden), nullptr, nullptr, 1,
+                                 const_cast<int32_t*>(topk_ids), const_cast<float*>(topk_w), w13, w13_scale, w2,
+                                 w2_scale, static_cast<uint16_t*>(out), M, H, I, E, K, ws,
+                                 reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + L.tickets), stream));
+  }
   if (use_pair_mode((int64_t)M * shape->top_k)) {
     // few routed rows: two launches -- gate/up quantises its own hidden row and prefetches
     // the routed experts' down weights into L2, down is fused with the combine (same
     // arithmetic as the four stage calls)
     const WsPtrs ws = ws_ptrs(workspace, L);
-    const int H = shape->hidden, I = shape->inter, E = shape->num_experts, K = shape->top_k;
     if (moe_status_t st = launched(launch_pair_gateup(w13, w13_scale, topk_ids, static_cast<const uint16_t*>(hidden),
                                                       M, H, I, E, K, ws, stream, w2, w2_scale)))
       return st;
@@ -265,7 +280,32 @@ moe_status_t moe_fp8_workspace_view(void* workspace, size_t workspace_bytes,
   view->expert_offsets = ws.offsets;
   view->topk_ids = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + L.ids_stage);
   view->topk_w = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.wts_stage);
+  view->tickets = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + L.tickets);
   return MOE_OK;
+}
+
+moe_status_t moe_fp8_route_forward(const void* hidden, const void* router_w, const float* bias, int32_t M,
+                                   int32_t renormalize, const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
+                                   const float* w2_scale, void* out, int32_t* topk_ids, float* topk_w,
+                                   void* workspace, size_t workspace_bytes, const moe_fp8_shape_t* shape,
+                                   cudaStream_t stream) {
+  if (moe_status_t st = check_common(shape, M)) return st;
+  for (const void* p : {hidden, router_w, (const void*)w13, (const void*)w13_scale, (const void*)w2,
+                        (const void*)w2_scale, (const void*)out, (const void*)topk_ids, (const void*)topk_w})
+    if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (bias && !aligned16(bias)) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  if (M == 0) return MOE_OK;
+  const int H = shape->hidden, I = shape->inter, E = shape->num_experts, K = shape->top_k;
+  if (fused_capable(M, H, I, E, K))
+    return launched(launch_fused(true, static_cast<const uint16_t*>(hidden), static_cast<const uint16_t*>(router_w),
+                                 bias, renormalize ? 1 : 0, topk_ids, topk_w, w13, w13_scale, w2, w2_scale,
+                                 static_cast<uint16_t*>(out), M, H, I, E, K, ws_ptrs(workspace, L),
+                                 reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + L.tickets), stream));
+  if (moe_status_t st = moe_route(hidden, router_w, bias, M, shape, renormalize, topk_ids, topk_w, stream)) return st;
+  return moe_fp8_forward(hidden, topk_ids, topk_w, M, w13, w13_scale, w2, w2_scale, out, workspace,
+                         workspace_bytes, shape, stream);
 }
 
 moe_status_t moe_fp8_route_forward_host(const void* host_hidden, void* host_out, int32_t M,
@@ -295,9 +335,8 @@ moe_status_t moe_fp8_route_forward_host(const void* host_hidden, void* host_out,
   }
   if (copy_out) out = b + L.out_stage;
   if (!aligned16(hid) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
-  if (moe_status_t st = moe_route(hid, router_w, bias, M, shape, renormalize, ids, wts, stream)) return st;
-  if (moe_status_t st = moe_fp8_forward(hid, ids, wts, M, w13, w13_scale, w2, w2_scale, out, workspace,
-                                        workspace_bytes, shape, stream))
+  if (moe_status_t st = moe_fp8_route_forward(hid, router_w, bias, M, renormalize, w13, w13_scale, w2, w2_scale, out,
+                                              ids, wts, workspace, workspace_bytes, shape, stream))
     return st;
   if (copy_out) return launched(cudaMemcpyAsync(host_out, out, bytes, cudaMemcpyDeviceToHost, stream));
   return MOE_OK;
@@ -317,9 +356,8 @@ moe_status_t moe_fp8_route_forward_pinned(const void* host_hidden, void* host_ou
   int32_t* ids = reinterpret_cast<int32_t*>(b + L.ids_stage);
   float* wts = reinterpret_cast<float*>(b + L.wts_stage);
   // page-locked host memory under unified addressing: the host pointers are device-usable
-  if (moe_status_t st = moe_route(host_hidden, router_w, bias, M, shape, renormalize, ids, wts, stream)) return st;
-  return moe_fp8_forward(host_hidden, ids, wts, M, w13, w13_scale, w2, w2_scale, host_out, workspace,
-                         workspace_bytes, shape, stream);
+  return moe_fp8_route_forward(host_hidden, router_w, bias, M, renormalize, w13, w13_scale, w2, w2_scale, host_out,
+                               ids, wts, workspace, workspace_bytes, shape, stream);
 }
 
 moe_status_t moe_fp8_selftest_wait(void* workspace, size_t workspace_bytes, const moe_fp8_shape_t* shape,

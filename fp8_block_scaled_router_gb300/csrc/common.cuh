@@ -31,13 +31,18 @@ struct Tile {               // a run of up to `tile_rows` expert-sorted rows of 
 };
 
 struct Layout {
-  size_t header, qa, sa, offsets, row_src, perm_row, pair_expert, blk_counts, tiles, xp, sa_p, act, act_scale, y;
+  size_t header, tickets, qa, sa, offsets, row_src, perm_row, pair_expert, blk_counts, tiles, xp, sa_p, act,
+      act_scale, y;
   size_t hid_stage, out_stage, ids_stage, wts_stage;  // host-buffer calls: device copies
   size_t total;
   int64_t R, max_tiles;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Tokens per call that the single-launch path takes (its arrival tickets, one per token and
+// 128-column block, sit right after the header and are cleared with it).
+constexpr int kTicketTokens = 16;
 
 // Routed rows per tile of the grouped GEMMs (the MMA's M).
 constexpr int kTileRows = 128;
@@ -67,6 +72,7 @@ inline Layout make_layout(const moe_fp8_shape_t& s) {
   L.max_tiles = max_tiles_for(L.R, (int)E, kTileRows);
   size_t o = 0;
   L.header = o;    o = align256(o + sizeof(Header));
+  L.tickets = o;   o = align256(o + (size_t)(Mx < kTicketTokens ? Mx : kTicketTokens) * (H / kBlock) * 4);
   L.qa = o;        o = align256(o + (size_t)(Mx * H));
   L.sa = o;        o = align256(o + (size_t)(Mx * (H / kBlock)) * 4);
   L.offsets = o;   o = align256(o + (size_t)(E + 1) * 4);

@@ -55,6 +55,88 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, uint64_t
   return true;
 }
 
+// ---------------------------------------------------------------- cluster (DSMEM) signalling
+// shared::cluster address of the variable at local shared address `local` in CTA `rank`
+__device__ __forceinline__ uint32_t mapa(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+// Arrive on an mbarrier of any CTA of the cluster, releasing this thread's prior writes
+// (and, cumulatively, writes it has observed) at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait (acquire at cluster scope) for a phase completed by arrivals from other CTAs; false
+// if `limit_ns` elapsed first.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* b, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait_cluster(b, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait_cluster(b, parity))
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  return true;
+}
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+// 4-byte load from another CTA's shared memory (shared::cluster address)
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+// 16-byte load from another CTA's shared memory (shared::cluster address)
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+// 4- and 16-byte stores into another CTA's shared memory (shared::cluster address)
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// ---------------------------------------------------------------- 1-D bulk copy
+// [dst, dst + bytes) <- [src, src + bytes), completion as transaction bytes on `bar`
+// (both addresses 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 // ---------------------------------------------------------------- L2 prefetch
 // Hint: bring [p, p + bytes) into L2 (p and bytes multiples of 16).
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
@@ -85,6 +167,12 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
       "l"(m), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
       : "memory");
+}
+
+// Hint: bring one 2-D box of the tensor into L2 (x as for tma_load_2d); no completion.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* m, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(m), "r"(x), "r"(y)
+               : "memory");
 }
 
 // 2-D tiled store of one box from shared memory (bulk async group of this thread); x * 4
@@ -163,6 +251,31 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 // loads and tcgen05.wait::ld in one asm statement: the outputs are valid when it returns.
 // Shape 32x32b: thread i of the warp reads TMEM lane (32 * (warp % 4) + i), consecutive
 // 32-bit columns starting at the address's column.
+
+// one column (32-bit) per lane
+__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r)
+      : "r"(taddr)
+      : "memory");
+  return __uint_as_float(r);
+}
+// two single columns, one wait
+__device__ __forceinline__ void tmem_ld1x2(uint32_t taddr0, uint32_t taddr1, float& a, float& b) {
+  uint32_t r0, r1;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%2];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%1}, [%3];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r0), "=r"(r1)
+      : "r"(taddr0), "r"(taddr1)
+      : "memory");
+  a = __uint_as_float(r0);
+  b = __uint_as_float(r1);
+}
 
 // two runs of 16 columns (at taddr0 and taddr1)
 __device__ __forceinline__ void tmem_ld16x2(uint32_t taddr0, uint32_t taddr1, float (&a)[16], float (&b)[16]) {
