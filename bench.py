@@ -2,8 +2,7 @@
 """Throughput of the routed FP8 block-scaled MoE layer on GB300 (one JSON line on stdout).
 
 A step is one pass of the whole layer -- moe_fp8_route_forward: routing, then prepare,
-gate/up + SiLU*up requantisation, down, combine (one launch for a few routed pairs) -- over
-one batch of synthetic tokens. The default
+gate/up + SiLU*up requantisation, down, combine -- over one batch of synthetic tokens. The default
 workload is decode: hidden 2048, intermediate 768, 128 experts, top-8 renormalised, one
 token per step, stepping through 10,000 seeded tokens; the same line carries a "prefill"
 record (M=4096, same shapes), the metric's tensor-bound half. Other workloads
@@ -20,9 +19,8 @@ e2e     the same metric through the public API with host buffers: per step one
         the output to pinned host memory, route and forward enqueued by one call -- all
         inside the timed region (the Zipf workload, whose routing is given, uses a host copy,
         moe_route, moe_fp8_forward and a copy back).
-roofline the dominant kernel timed alone with CUDA events on its stream, its algorithmic
-        bytes (or FLOPs) per launch divided by the mean launch time: for decode the single
-        launch that is the whole step, for prefill the gate/up grouped GEMM.
+roofline the dominant kernel (gate/up) timed alone with CUDA events on its stream, its
+        algorithmic bytes (or FLOPs) per launch divided by the mean launch time.
 cpu_baseline the oracle (plain C++ on the host cores) on a bounded sample of the same
         workload (rank 0, N=1 only).
 
@@ -66,18 +64,10 @@ WORKLOADS = {
 
 # routed rows up to which moe_fp8_forward runs the two pair kernels
 PAIR_ROWS = 64
-# routed pairs up to which the layer is one launch (for the shapes the bench runs, whose
-# single-launch pipeline fits the device: h2048 with up to 16 pairs, h6144 with up to 8)
-FUSED_ROWS = 16
-
-
 def launches_per_step(M, K, H, E):
-    """Our kernels per step: one launch for a few routed pairs; route, gate/up, down+combine
-    up to PAIR_ROWS; otherwise route, count+quantise, scatter, gather, gate/up, down, combine."""
-    R = M * K
-    if R <= FUSED_ROWS and (H <= 2048 or R <= 8):
-        return 1
-    return 3 if R <= PAIR_ROWS else 7
+    """Our kernels per step: route, gate/up, down+combine up to PAIR_ROWS routed rows;
+    otherwise route, count+quantise, scatter, gather, gate/up, down, combine."""
+    return 3 if M * K <= PAIR_ROWS else 7
 
 
 def parse():
@@ -390,14 +380,9 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
     value = replicas.throughput(world, steps, M, elapsed)
     ms_per_step = 1e3 * elapsed / steps
 
-    if kernels_per_step == 1:
-        roof = single_launch_roofline(L, torch, M, nbatches, hidden_all, reps, n_rep, router, bias, ids, wts, out,
-                                      ws, shape, alg_bytes)
-        roof["traffic"] = recorded_traffic("fused", cfg)
-    else:
-        roof = dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, given_ids, ids, ws, shape,
-                               prefill, gu_bytes, gu_flops)
-        roof["traffic"] = recorded_traffic("gate_up", "prefill" if prefill else args.workload)
+    roof = dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, given_ids, ids, ws, shape,
+                           prefill, gu_bytes, gu_flops)
+    roof["traffic"] = recorded_traffic("gate_up", "prefill" if prefill else args.workload)
 
     # ---- end to end through the public API with host buffers
     e2e_steps = min(steps * max(1, n_soak), 3000 if decode else (500 if M <= 64 else 10))
@@ -509,41 +494,6 @@ def dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, giv
     return roof
 
 
-def single_launch_roofline(L, torch, M, nbatches, hidden_all, reps, n_rep, router, bias, ids, wts, out, ws, shape,
-                           alg_bytes):
-    """The one-launch layer (routing + expert FFN) alone, back to back in a CUDA graph on its
-    own stream over rotating weight replicas: the step's algorithmic bytes per launch over
-    the mean launch time."""
-    n_k = 200
-    ks = torch.cuda.Stream()
-    ks.wait_stream(torch.cuda.current_stream())
-
-    def one(i, st):
-        b = i % nbatches
-        w13, s13, w2, s2 = reps[i % n_rep]
-        L.moe_fp8_route_forward(hidden_all[b * M:(b + 1) * M], router, bias, M, True, w13, s13, w2, s2, out[b],
-                                ids[b], wts[b], ws, shape, stream=st)
-
-    with torch.cuda.stream(ks):
-        one(0, ks)
-        kg = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(kg, stream=ks):
-            for i in range(n_k):
-                one(i, ks)
-        kg.replay()
-        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        k0.record(ks)
-        for _ in range(3):
-            kg.replay()
-        k1.record(ks)
-    ks.synchronize()
-    t = k0.elapsed_time(k1) / 1e3 / (3 * n_k)
-    hbm, _, _, peak_src = load_peaks()
-    return {"bound": "hbm", "kernel": "fused_kernel (routing + expert FFN, one launch)",
-            "achieved": alg_bytes / t / 1e9, "peak": hbm, "unit": "GB/s", "frac": alg_bytes / t / 1e9 / hbm,
-            "peak_source": f"{peak_src} hbm_gbs", "alg_per_launch": alg_bytes, "mean_launch_us": t * 1e6}
-
-
 def gpu_selector(torch):
     props = torch.cuda.get_device_properties(torch.cuda.current_device())
     uuid = str(getattr(props, "uuid", ""))
@@ -589,8 +539,9 @@ def ours_arm(args, wl, world, rank, local):
 
 
 def dominant_only(args, wl):
-    """Only the dominant kernel (the launch the roofline times), for a profiler: the one-launch
-    layer for a few routed pairs, else the gate/up GEMM after one prepare."""
+    """Only the dominant kernel (the launch the roofline times), for a profiler: the gate/up
+    GEMM (few routed rows: the direct pair kernel; otherwise the grouped GEMM after one
+    prepare)."""
     import torch
     from fp8_block_scaled_router_gb300 import _lib as L
     from fp8_block_scaled_router_gb300 import inputs
@@ -615,19 +566,15 @@ def dominant_only(args, wl):
     ii = torch.empty((M, K), dtype=torch.int32, device="cuda")
     w = torch.empty((M, K), dtype=torch.float32, device="cuda")
     out = torch.empty((M, H), dtype=torch.int16, device="cuda")
-    single = launches_per_step(M, K, H, E) == 1 and x.ids is None
-    if not single:
-        if x.ids is not None:
-            ii = dev(x.ids[:M])
-        else:
-            L.moe_route(hid, router, bias, M, shape, True, ii, w)
-        if M * K > PAIR_ROWS:
-            L.moe_fp8_prepare(hid, ii, M, ws, shape)
+    if x.ids is not None:
+        ii = dev(x.ids[:M])
+    else:
+        L.moe_route(hid, router, bias, M, shape, True, ii, w)
+    if M * K > PAIR_ROWS:
+        L.moe_fp8_prepare(hid, ii, M, ws, shape)
     for i in range(args.dominant_only):
         w13, s13, w2, s2 = reps[i % n_rep]
-        if single:
-            L.moe_fp8_route_forward(hid, router, bias, M, True, w13, s13, w2, s2, out, ii, w, ws, shape)
-        elif M * K <= PAIR_ROWS:
+        if M * K <= PAIR_ROWS:
             L.moe_fp8_gate_up_direct(hid, ii, M, w13, s13, ws, shape)
         else:
             L.moe_fp8_gate_up(w13, s13, M, ws, shape)

@@ -27,7 +27,7 @@ EXPORTS = ("moe_fp8_version", "moe_fp8_workspace_bytes", "moe_fp8_workspace_init
            "moe_fp8_combine", "moe_fp8_workspace_view", "moe_fp8_read_status",
            "moe_fp8_forward_noalloc", "moe_fp8_gate_up_direct", "moe_fp8_down_combine",
            "moe_fp8_route_forward_host", "moe_fp8_route_forward_pinned", "moe_fp8_selftest_wait",
-           "moe_fp8_route_forward")
+           "moe_fp8_route_forward", "moe_fp8_route_forward_one_launch")
 
 
 class MoEError(RuntimeError):
@@ -77,6 +77,8 @@ def load(path: str = LIB):
             lib.moe_fp8_route_forward_pinned.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, vp, vp, vp, sz, sp, vp]
             lib.moe_fp8_selftest_wait.argtypes = [vp, sz, sp, ctypes.c_uint32, vp]
             lib.moe_fp8_route_forward.argtypes = [vp, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, sp, vp]
+            lib.moe_fp8_route_forward_one_launch.argtypes = [vp, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz,
+                                                             sp, vp]
             for f in EXPORTS[2:]:
                 if f != "moe_fp8_workspace_bytes":
                     getattr(lib, f).restype = i32
@@ -241,10 +243,21 @@ def moe_fp8_selftest_wait(workspace, shape: Shape, limit_us, stream=None, ws_byt
 
 def moe_fp8_route_forward(hidden, router_w, bias, M, renormalize, w13, w13_scale, w2, w2_scale, out, topk_ids,
                           topk_w, workspace, shape: Shape, stream=None, ws_bytes=None, check=True):
-    """Routing + the expert FFN in one call (one launch for a few routed pairs); see
-    include/moe_fp8.h."""
+    """Routing + the expert FFN in one call; see include/moe_fp8.h."""
     nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
     return _check("moe_fp8_route_forward", load().moe_fp8_route_forward(
+        _ptr(hidden), _ptr(router_w), _ptr(bias), int(M), int(bool(renormalize)), _ptr(w13), _ptr(w13_scale),
+        _ptr(w2), _ptr(w2_scale), _ptr(out), _ptr(topk_ids), _ptr(topk_w), _ptr(workspace), nb,
+        ctypes.byref(shape), _stream(stream)), check)
+
+
+def moe_fp8_route_forward_one_launch(hidden, router_w, bias, M, renormalize, w13, w13_scale, w2, w2_scale, out,
+                                     topk_ids, topk_w, workspace, shape: Shape, stream=None, ws_bytes=None,
+                                     check=True):
+    """Routing + the expert FFN as a single kernel launch (few routed pairs); see
+    include/moe_fp8.h."""
+    nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return _check("moe_fp8_route_forward_one_launch", load().moe_fp8_route_forward_one_launch(
         _ptr(hidden), _ptr(router_w), _ptr(bias), int(M), int(bool(renormalize)), _ptr(w13), _ptr(w13_scale),
         _ptr(w2), _ptr(w2_scale), _ptr(out), _ptr(topk_ids), _ptr(topk_w), _ptr(workspace), nb,
         ctypes.byref(shape), _stream(stream)), check)

@@ -36,7 +36,7 @@ bool fused_capable(int M, int H, int I, int E, int K);
 cudaError_t launch_fused(bool route, const uint16_t* hidden, const uint16_t* router_w, const float* bias,
                          int renorm, int32_t* ids, float* wts, const uint8_t* w13, const float* s13,
                          const uint8_t* w2, const float* s2w, uint16_t* out, int M, int H, int I, int E, int K,
-                         const WsPtrs& ws, uint32_t* tickets, cudaStream_t st);
+                         const WsPtrs& ws, float* yt, uint32_t* tickets, cudaStream_t st);
 }  // namespace moe
 
 using namespace moe;
@@ -199,15 +199,6 @@ moe_status_t moe_fp8_forward(const void* hidden, const int32_t* topk_ids, const 
   if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
   if (M == 0) return MOE_OK;
   const int H = shape->hidden, I = shape->inter, E = shape->num_experts, K = shape->top_k;
-  if (fused_capable(M, H, I, E, K)) {
-    // a few routed pairs: the whole layer in one launch (gate/up with the hidden
-    // quantisation, SiLU*up requantisation, down and the combine)
-    const WsPtrs ws = ws_ptrs(workspace, L);
-    return launched(launch_fused(false, static_cast<const uint16_t*>(hidden), nullptr, nullptr, 1,
-                                 const_cast<int32_t*>(topk_ids), const_cast<float*>(topk_w), w13, w13_scale, w2,
-                                 w2_scale, static_cast<uint16_t*>(out), M, H, I, E, K, ws,
-                                 reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + L.tickets), stream));
-  }
   if (use_pair_mode((int64_t)M * shape->top_k)) {
     // few routed rows: two launches -- gate/up quantises its own hidden row and prefetches
     // the routed experts' down weights into L2, down is fused with the combine (same
@@ -284,28 +275,53 @@ moe_status_t moe_fp8_workspace_view(void* workspace, size_t workspace_bytes,
   return MOE_OK;
 }
 
-moe_status_t moe_fp8_route_forward(const void* hidden, const void* router_w, const float* bias, int32_t M,
-                                   int32_t renormalize, const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
-                                   const float* w2_scale, void* out, int32_t* topk_ids, float* topk_w,
-                                   void* workspace, size_t workspace_bytes, const moe_fp8_shape_t* shape,
-                                   cudaStream_t stream) {
+namespace {
+moe_status_t check_route_forward(const void* hidden, const void* router_w, const float* bias, int32_t M,
+                                 const uint8_t* w13, const float* w13_scale, const uint8_t* w2, const float* w2_scale,
+                                 void* out, int32_t* topk_ids, float* topk_w, void* workspace, size_t workspace_bytes,
+                                 const moe_fp8_shape_t* shape, Layout* L) {
   if (moe_status_t st = check_common(shape, M)) return st;
   for (const void* p : {hidden, router_w, (const void*)w13, (const void*)w13_scale, (const void*)w2,
                         (const void*)w2_scale, (const void*)out, (const void*)topk_ids, (const void*)topk_w})
     if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
   if (bias && !aligned16(bias)) return MOE_ERR_INVALID_ARG;
+  return check_ws(workspace, workspace_bytes, shape, L);
+}
+}  // namespace
+
+moe_status_t moe_fp8_route_forward(const void* hidden, const void* router_w, const float* bias, int32_t M,
+                                   int32_t renormalize, const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
+                                   const float* w2_scale, void* out, int32_t* topk_ids, float* topk_w,
+                                   void* workspace, size_t workspace_bytes, const moe_fp8_shape_t* shape,
+                                   cudaStream_t stream) {
   Layout L;
-  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  if (moe_status_t st = check_route_forward(hidden, router_w, bias, M, w13, w13_scale, w2, w2_scale, out, topk_ids,
+                                            topk_w, workspace, workspace_bytes, shape, &L))
+    return st;
   if (M == 0) return MOE_OK;
-  const int H = shape->hidden, I = shape->inter, E = shape->num_experts, K = shape->top_k;
-  if (fused_capable(M, H, I, E, K))
-    return launched(launch_fused(true, static_cast<const uint16_t*>(hidden), static_cast<const uint16_t*>(router_w),
-                                 bias, renormalize ? 1 : 0, topk_ids, topk_w, w13, w13_scale, w2, w2_scale,
-                                 static_cast<uint16_t*>(out), M, H, I, E, K, ws_ptrs(workspace, L),
-                                 reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + L.tickets), stream));
   if (moe_status_t st = moe_route(hidden, router_w, bias, M, shape, renormalize, topk_ids, topk_w, stream)) return st;
   return moe_fp8_forward(hidden, topk_ids, topk_w, M, w13, w13_scale, w2, w2_scale, out, workspace,
                          workspace_bytes, shape, stream);
+}
+
+moe_status_t moe_fp8_route_forward_one_launch(const void* hidden, const void* router_w, const float* bias,
+                                              int32_t M, int32_t renormalize, const uint8_t* w13,
+                                              const float* w13_scale, const uint8_t* w2, const float* w2_scale,
+                                              void* out, int32_t* topk_ids, float* topk_w, void* workspace,
+                                              size_t workspace_bytes, const moe_fp8_shape_t* shape,
+                                              cudaStream_t stream) {
+  Layout L;
+  if (moe_status_t st = check_route_forward(hidden, router_w, bias, M, w13, w13_scale, w2, w2_scale, out, topk_ids,
+                                            topk_w, workspace, workspace_bytes, shape, &L))
+    return st;
+  if (M == 0) return MOE_OK;
+  const int H = shape->hidden, I = shape->inter, E = shape->num_experts, K = shape->top_k;
+  if (!fused_capable(M, H, I, E, K)) return MOE_ERR_UNSUPPORTED;
+  return launched(launch_fused(true, static_cast<const uint16_t*>(hidden), static_cast<const uint16_t*>(router_w), bias,
+                               renormalize ? 1 : 0, topk_ids, topk_w, w13, w13_scale, w2, w2_scale,
+                               static_cast<uint16_t*>(out), M, H, I, E, K, ws_ptrs(workspace, L),
+                               reinterpret_cast<float*>(static_cast<char*>(workspace) + L.yt),
+                               reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + L.tickets), stream));
 }
 
 moe_status_t moe_fp8_route_forward_host(const void* host_hidden, void* host_out, int32_t M,

@@ -32,7 +32,7 @@ struct Tile {               // a run of up to `tile_rows` expert-sorted rows of 
 
 struct Layout {
   size_t header, tickets, qa, sa, offsets, row_src, perm_row, pair_expert, blk_counts, tiles, xp, sa_p, act,
-      act_scale, y;
+      act_scale, y, yt;
   size_t hid_stage, out_stage, ids_stage, wts_stage;  // host-buffer calls: device copies
   size_t total;
   int64_t R, max_tiles;
@@ -86,6 +86,8 @@ inline Layout make_layout(const moe_fp8_shape_t& s) {
   L.act = o;       o = align256(o + (size_t)(L.R * I));
   L.act_scale = o; o = align256(o + (size_t)(L.R * (I / kBlock)) * 4);
   L.y = o;         o = align256(o + (size_t)(L.R * H) * 4);
+  // the single-launch path's down terms: per token and output row, its pairs' K blocks
+  L.yt = o;        o = align256(o + (size_t)(Mx < kTicketTokens ? Mx : kTicketTokens) * H * ((K * (I / kBlock) + 3) & ~3) * 4);
   L.hid_stage = o; o = align256(o + (size_t)(Mx * H) * 2);
   L.out_stage = o; o = align256(o + (size_t)(Mx * H) * 2);
   L.ids_stage = o; o = align256(o + (size_t)L.R * 4);

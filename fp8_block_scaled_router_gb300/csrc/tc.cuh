@@ -127,6 +127,17 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint4 v) {
                : "memory");
 }
 
+// [dst, dst + bytes) in another CTA of the cluster <- [src, src + bytes) of this CTA's shared
+// memory; completion as transaction bytes on the destination CTA's mbarrier (dst and mbar
+// are shared::cluster addresses; 16-byte aligned, bytes a multiple of 16). The source must
+// stay unchanged until the copy has completed.
+__device__ __forceinline__ void bulk_copy_cluster(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst),
+               "r"(smem_u32(src)), "r"(bytes), "r"(mbar)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- 1-D bulk copy
 // [dst, dst + bytes) <- [src, src + bytes), completion as transaction bytes on `bar`
 // (both addresses 16-byte aligned, bytes a multiple of 16).

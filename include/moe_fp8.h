@@ -9,9 +9,9 @@
  *              at one scale per routed row per 128 columns          (moe_fp8_gate_up)
  *   down       block-scaled grouped GEMM                            (moe_fp8_down)
  *   combine    top-k weighted sum in slot order, no atomics         (moe_fp8_combine)
- * moe_fp8_forward runs prepare -> gate/up -> down -> combine; for at most 64 routed rows
- * (M * top_k), gate/up (quantising hidden itself) -> down fused with the combine; and for at
- * most 16 routed rows the whole layer in one launch (see moe_fp8_route_forward).
+ * moe_fp8_forward runs prepare -> gate/up -> down -> combine, or, for at most 64 routed
+ * rows (M * top_k), gate/up (quantising hidden itself) -> down fused with the combine.
+ * moe_fp8_route_forward_one_launch runs routing and the whole layer as a single kernel.
  *
  * Sources (web pages; each entry point names the passage that defines it):
  *   [NK]   "NetraRuntime/netra-kernel" README
@@ -84,9 +84,10 @@ const char* moe_fp8_version(void);
  * standalone graph owns its deterministic static intermediates. */
 size_t moe_fp8_workspace_bytes(const moe_fp8_shape_t* shape);
 
-/* Clear the workspace's status word and the single-launch path's arrival counters. Call
- * once after allocating a workspace (enqueued on `stream`); every call leaves the counters
- * at zero, and every other region is fully rewritten by each forward call. */
+/* Clear the workspace's status word and the arrival counters of
+ * moe_fp8_route_forward_one_launch. Call once after allocating a workspace (enqueued on
+ * `stream`); every call leaves the counters at zero, and every other region is fully
+ * rewritten by each forward call. */
 moe_status_t moe_fp8_workspace_init(void* workspace, size_t workspace_bytes,
                                     const moe_fp8_shape_t* shape, cudaStream_t stream);
 
@@ -137,26 +138,38 @@ moe_status_t moe_fp8_forward(const void* hidden, const int32_t* topk_ids, const 
                              void* workspace, size_t workspace_bytes,
                              const moe_fp8_shape_t* shape, cudaStream_t stream);
 
-/* Routing and the routed expert FFN in one call ([NK] prefill-pair section: one producer made
- * of semantic routing, gate/up, SiLU and quantisation, down-partial and metadata stages, and
- * a route reducer with its own fixed reduction order). Arguments as for moe_route and
- * moe_fp8_forward; topk_ids / topk_w (device, [M][K]) receive the routing. Results are
- * bitwise those of moe_route followed by moe_fp8_forward on the same inputs.
- * For a few routed pairs (M * top_k <= 16, M <= 16, E <= 256, inter <= 2048, and the
- * pipeline fitting the device) it is ONE launch: a cluster of 16 CTAs per routed pair
- * routes the tokens (each cluster computes the routing itself, in the router's arithmetic),
- * quantises the pair's hidden row, runs gate/up, SiLU*up with the requantisation and down
- * on the tensor cores, and the last of a token's pairs to finish an output block adds the
- * pairs' rows in slot order into out. Otherwise it enqueues moe_route then moe_fp8_forward.
- * The single-launch path keeps arrival counters in the workspace that every call leaves at
- * zero; after a call that reported MOE_STATUS_WAIT_TIMEOUT, re-initialise the workspace
- * (moe_fp8_workspace_init) before the next call. router_w and bias are read while the
- * previous kernel on `stream` may still run (as for moe_route). */
+/* Routing and the routed expert FFN in one call: moe_route then moe_fp8_forward, enqueued
+ * together (arguments as for those calls; topk_ids / topk_w, device [M][K], receive the
+ * routing). Results are those of the two calls. */
 moe_status_t moe_fp8_route_forward(const void* hidden, const void* router_w, const float* bias, int32_t M,
                                    int32_t renormalize, const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
                                    const float* w2_scale, void* out, int32_t* topk_ids, float* topk_w,
                                    void* workspace, size_t workspace_bytes, const moe_fp8_shape_t* shape,
                                    cudaStream_t stream);
+
+/* The same layer as ONE kernel launch ([NK] prefill-pair section: one producer made of
+ * semantic routing, gate/up, SiLU and quantisation, down-partial and metadata stages, with
+ * the route reducer's fixed reduction order), for a few routed pairs: M * top_k <= 16,
+ * M <= 16, E <= 256 and a multiple of 8, inter <= 2048, hidden <= 8192, and the pipeline
+ * fitting the device; otherwise MOE_ERR_UNSUPPORTED. Results (routing, output, and the
+ * workspace views qa, sa, act, act_scale in pair order) are bitwise those of
+ * moe_fp8_route_forward. The work is split into (routed pair, 128-column activation block)
+ * units spread over 16-CTA clusters, one CTA per SM: each cluster routes the tokens itself
+ * (the router's arithmetic), runs its units' gate/up with the hidden quantisation, SiLU*up and
+ * the requantisation, and the down projection's K block of each unit; the last CTA to finish
+ * an output block (an arrival counter in the workspace) sums the down terms over K blocks and
+ * then slots in ascending order. It is slower than the two calls at decode on GB300 (the
+ * whole layer's latency chain sits in one grid, and consecutive launches cannot overlap it);
+ * it exists for callers that need the layer as a single launch. The arrival counters are left
+ * at zero by every call; after a call that reported MOE_STATUS_WAIT_TIMEOUT, re-initialise the
+ * workspace (moe_fp8_workspace_init) before the next call. router_w and bias are read while
+ * the previous kernel on `stream` may still run (as for moe_route). */
+moe_status_t moe_fp8_route_forward_one_launch(const void* hidden, const void* router_w, const float* bias,
+                                              int32_t M, int32_t renormalize, const uint8_t* w13,
+                                              const float* w13_scale, const uint8_t* w2, const float* w2_scale,
+                                              void* out, int32_t* topk_ids, float* topk_w, void* workspace,
+                                              size_t workspace_bytes, const moe_fp8_shape_t* shape,
+                                              cudaStream_t stream);
 
 /* The four stages of moe_fp8_forward as separate calls, for callers that interleave them
  * with other work or time them one by one. They communicate through the workspace and
@@ -199,8 +212,8 @@ moe_status_t moe_fp8_down_combine(const int32_t* topk_ids, const float* topk_w, 
  * sa f32 [M][H/128], expert-sorted routed rows: row_src i32 [R] (flat pair index t*K+j of
  * sorted row r), perm_row i32 [M*K] (sorted row of pair t*K+j, -1 if skipped), act codes
  * u8 [R][I], act scales f32 [R][I/128], y f32 [R][H]; R = M*K. Any out pointer may be
- * NULL. The single-launch path (M * top_k <= 16) writes qa, sa (its own quantiser), act and
- * act_scale in pair order (row t*K+j) and y in pair order; it writes no permutation. */
+ * NULL. moe_fp8_route_forward_one_launch writes qa, sa (its own quantiser), act and
+ * act_scale in pair order (row t*K+j); it writes no permutation and no y. */
 typedef struct {
   uint8_t* qa;
   float* sa;
@@ -212,8 +225,8 @@ typedef struct {
   int32_t* expert_offsets; /* i32 [E+1] start of each expert's rows */
   int32_t* topk_ids;       /* i32 [M][K], f32 [M][K]: the routing of the last */
   float* topk_w;           /*   moe_fp8_route_forward_host call */
-  uint32_t* tickets;       /* u32 [min(max_tokens,16)][H/128]: the single-launch path's
-                              arrival counters (zero between calls) */
+  uint32_t* tickets;       /* u32 [min(max_tokens,16)][H/128]: the arrival counters of
+                              moe_fp8_route_forward_one_launch (zero between calls) */
 } moe_fp8_ws_view_t;
 moe_status_t moe_fp8_workspace_view(void* workspace, size_t workspace_bytes,
                                     const moe_fp8_shape_t* shape, moe_fp8_ws_view_t* view);

@@ -1,13 +1,14 @@
-"""The single-launch layer (moe_fp8_route_forward; moe_fp8_forward for a few routed pairs).
+"""The single-launch layer (moe_fp8_route_forward_one_launch) and the two-call form
+(moe_fp8_route_forward).
 
-For up to 16 routed pairs the library runs the whole layer -- routing, the hidden
+For up to 16 routed pairs the library can run the whole layer -- routing, the hidden
 quantisation, gate/up, SiLU*up with the requantisation, down and the slot-order combine --
-in one launch: a 16-CTA cluster per routed pair, the producer stages and the route reducer
-of the netra-kernel README's prefill-pair section in one kernel. Its routing must be
-bit-identical to moe_route, its output bit-identical to moe_route + moe_fp8_forward, and
-both within the oracle contract (ids bit-exact, hidden codes bit-exact, activation codes in
-their window, the output bound given the activation codes); its arrival counters must be
-left at zero after every call, and rows past M untouched.
+as one kernel: the producer stages and the route reducer of the netra-kernel README's
+prefill-pair section in one launch. Its routing must be bit-identical to moe_route, its
+output bit-identical to moe_route + moe_fp8_forward (= moe_fp8_route_forward), and both within
+the oracle contract (ids bit-exact, hidden codes bit-exact, activation codes in their window,
+the output bound given the activation codes); its arrival counters must be left at zero after
+every call, and rows past M untouched. Shapes outside its limits are refused.
 """
 import numpy as np
 import pytest
@@ -51,8 +52,8 @@ def tickets(g, M):
 
 # (workload, M): decode M=1 and M=2 (8 and 16 pairs), tiny (H=256: two K blocks, so most
 # CTAs of a cluster route and compute nothing), the skewed verify router with its bias,
-# wide h6144 (three K blocks per CTA), top-1 with 16 tokens, and verify M=12 (96 pairs:
-# the two-call path, for the same equalities)
+# wide h6144 (three K blocks per CTA), top-1 with 16 tokens; verify M=12 (96 pairs) is
+# refused by the single launch
 CASES = [("decode", 1), ("decode", 2), ("tiny", 4), ("verify_skewed", 1), ("wide", 1), ("wide", 4), ("top1", 16),
          ("verify", 12)]
 
@@ -68,11 +69,20 @@ def test_route_forward_matches_two_calls_and_oracle(name, M):
     ids1 = torch.full((M, g.K), -7, dtype=torch.int32, device="cuda")
     w1 = torch.full((M, g.K), -7.0, dtype=torch.float32, device="cuda")
     out1 = torch.empty((M, g.H), dtype=torch.int16, device="cuda")
-    L.moe_fp8_route_forward(hid, g.router, g.bias, M, True, g.w13, g.s13, g.w2, g.s2, out1, ids1, w1, g.ws, g.shape)
+    rc = L.moe_fp8_route_forward_one_launch(hid, g.router, g.bias, M, True, g.w13, g.s13, g.w2, g.s2, out1, ids1,
+                                            w1, g.ws, g.shape, check=False)
+    # the single launch's limits: at most 16 routed pairs, at most 8 hidden B tiles per CTA
+    supported = M * g.K <= 16 and (g.H // 128 + 15) // 16 * M <= 8
+    if not supported:
+        assert rc == 2  # MOE_ERR_UNSUPPORTED: only the two-call form takes it
+        L.moe_fp8_route_forward(hid, g.router, g.bias, M, True, g.w13, g.s13, g.w2, g.s2, out1, ids1, w1, g.ws,
+                                g.shape)
+    else:
+        assert rc == 0
     torch.cuda.synchronize()
     assert g.status() == 0
     ws = g.ws_arrays(M)
-    # up to 64 routed pairs the intermediates are in pair order (single launch or the two
+    # up to 64 routed pairs the intermediates are in pair order (the single launch or the two
     # pair kernels, both quantising the hidden row themselves)
     pair_order = M * g.K <= 64
     assert torch.all(tickets(g, M) == 0)
@@ -85,9 +95,11 @@ def test_route_forward_matches_two_calls_and_oracle(name, M):
         ws["row_src"] = np.arange(M * g.K, dtype=np.int32)
         check_act(ws, dbg, g.K, f"route_forward {name} M={M}")
         check_out_given_act(u16(out1), out_o, ws, dbg, ids_o, w_o, x, f"route_forward {name} M={M}")
-    # the two-call sequence on the same inputs: bitwise the same routing and output
-    ids2, w2 = g.route(hid, M)
-    out2 = g.forward(hid, ids2, w2, M)
+    # the two-call form on the same inputs: bitwise the same routing and output
+    ids2 = torch.empty_like(ids1)
+    w2 = torch.empty_like(w1)
+    out2 = torch.empty_like(out1)
+    L.moe_fp8_route_forward(hid, g.router, g.bias, M, True, g.w13, g.s13, g.w2, g.s2, out2, ids2, w2, g.ws, g.shape)
     torch.cuda.synchronize()
     assert torch.equal(ids1, ids2) and torch.equal(w1.view(torch.int32), w2.view(torch.int32))
     assert torch.equal(out1, out2)
@@ -103,7 +115,8 @@ def test_route_forward_not_renormalised_and_rows_past_m():
     ids = torch.full((4, g.K), -7, dtype=torch.int32, device="cuda")
     w = torch.full((4, g.K), -7.0, dtype=torch.float32, device="cuda")
     out = torch.full((4, g.H), 0x7ABC, dtype=torch.int16, device="cuda")
-    L.moe_fp8_route_forward(hid, g.router, None, M, False, g.w13, g.s13, g.w2, g.s2, out, ids, w, g.ws, g.shape)
+    L.moe_fp8_route_forward_one_launch(hid, g.router, None, M, False, g.w13, g.s13, g.w2, g.s2, out, ids, w, g.ws,
+                                       g.shape)
     torch.cuda.synchronize()
     ids_o, w_o = oracle_route(x, rows=slice(0, M), renorm=False)
     assert np.array_equal(ids[:M].cpu().numpy(), ids_o)
@@ -126,8 +139,8 @@ def test_route_forward_100_launches_and_graph_replay():
     out = torch.empty((M, g.H), dtype=torch.int16, device="cuda")
 
     def call(st=None):
-        L.moe_fp8_route_forward(hid, g.router, g.bias, M, True, g.w13, g.s13, g.w2, g.s2, out, ids, w, g.ws,
-                                g.shape, stream=st)
+        L.moe_fp8_route_forward_one_launch(hid, g.router, g.bias, M, True, g.w13, g.s13, g.w2, g.s2, out, ids, w,
+                                           g.ws, g.shape, stream=st)
 
     call()
     torch.cuda.synchronize()
