@@ -81,6 +81,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--dominant-only", type=int, default=0, metavar="N",
                    help="run only N launches of the dominant kernel (gate/up) and exit, for ncu")
+    p.add_argument("--profile-steps", type=int, default=0, metavar="N",
+                   help="run N eager steps of the workload after 3 warm-up steps and exit, for a profiler's "
+                        "launch list")
     p.add_argument("--no-prefill", action="store_true",
                    help="decode only: leave out the prefill record of the same line")
     p.add_argument("--clock-soak", type=float, default=1.0, metavar="S",
@@ -518,6 +521,9 @@ def ours_arm(args, wl, world, rank, local):
     if args.dominant_only:
         dominant_only(args, wl)
         return
+    if args.profile_steps:
+        profile_steps(args, wl)
+        return
     want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
     rec = run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, 12.0)
     # the metric's other half: prefill (M=4096) in the same run and the same line
@@ -536,6 +542,44 @@ def ours_arm(args, wl, world, rank, local):
     if dist:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def profile_steps(args, wl):
+    """3 warm-up steps, then N eager steps of the workload (the launches a profiler lists)."""
+    import torch
+    from fp8_block_scaled_router_gb300 import _lib as L
+    from fp8_block_scaled_router_gb300 import inputs
+
+    cfg = wl["cfg"]
+    M = args.m if (args.m and cfg == "wide") else wl["M"]
+    n = 3 + args.profile_steps
+    x = inputs.make(cfg, tokens=n * M if cfg == "decode" else None, M=M if cfg == "wide" else None)
+    H, I, E, K = x.shape.hidden, x.shape.inter, x.shape.num_experts, x.shape.top_k
+
+    def dev(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
+
+    reps = [(dev(x.w13), dev(x.s13), dev(x.w2), dev(x.s2)) for _ in range(2)]
+    shape = L.make_shape(H, I, E, K, M)
+    ws = torch.empty(L.moe_fp8_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
+    L.moe_fp8_workspace_init(ws, shape)
+    hid_all = dev(x.hidden)
+    router = dev(x.router_w)
+    bias = None if x.bias is None else dev(x.bias)
+    ids = torch.empty((M, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    out = torch.empty((M, H), dtype=torch.int16, device="cuda")
+    for i in range(n):
+        b = i % (hid_all.shape[0] // M)
+        hid = hid_all[b * M:(b + 1) * M]
+        w13, s13, w2, s2 = reps[i % 2]
+        if x.ids is not None:
+            L.moe_route(hid, router, bias, M, shape, True, ids, w)
+            L.moe_fp8_forward(hid, dev(x.ids), dev(x.weights), M, w13, s13, w2, s2, out, ws, shape)
+        else:
+            L.moe_fp8_route_forward(hid, router, bias, M, True, w13, s13, w2, s2, out, ids, w, ws, shape)
+    torch.cuda.synchronize()
 
 
 def dominant_only(args, wl):

@@ -714,15 +714,14 @@ FusedPlan plan_fused(const DeviceInfo& d, int M, int H, int I, int E, int K) {
   const int RU = M * K * (I / 128);
   const int nkh = H / 128, cpc = (nkh + kFusedCL - 1) / kFusedCL;
   const size_t one_per_sm = d.smem_per_sm / 2 + 1024;
-  for (int nst = kFusedMaxStages; nst >= 4 && best.nst == 0; nst -= 2) {  // even: gate/up stage pairs
-    if ((size_t)nst * kFusedTile < (size_t)cpc * 128 * E * 2) break;
-    const size_t bound = std::max(fused_smem(nst, M, H, I, E, K, kFusedMaxUnits).total, one_per_sm);
-    if (bound > d.smem_optin) continue;
-    int nc = 0;
+  // clusters resident at once with one CTA per SM (any footprint above half an SM gives the
+  // same count)
+  int nc = 0;
+  {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kFusedCL * 64, 1, 1);
     cfg.blockDim = dim3(kFusedThreads, 1, 1);
-    cfg.dynamicSmemBytes = bound;
+    cfg.dynamicSmemBytes = one_per_sm;
     cudaLaunchAttribute a[1];
     a[0].id = cudaLaunchAttributeClusterDimension;
     a[0].val.clusterDim.x = kFusedCL;
@@ -734,15 +733,19 @@ FusedPlan plan_fused(const DeviceInfo& d, int M, int H, int I, int E, int K) {
       (void)cudaGetLastError();
       nc = 0;
     }
-    if (nc <= 0) continue;
-    // one cluster fewer than fit: the next launch's clusters (programmatic dependent launch)
-    // then always find a free GPC, instead of the last of them waiting for this launch's last
-    // cluster to leave -- a lag that otherwise carries from launch to launch
-    if (nc > 1) --nc;
-    nc = std::min(nc, RU);
-    const int U = (RU + nc - 1) / nc;
-    if (U > kFusedMaxUnits) continue;
-    best = FusedPlan{nst, nc, std::max(fused_smem(nst, M, H, I, E, K, U).total, one_per_sm)};
+  }
+  // one cluster fewer than fit: the next launch's clusters (programmatic dependent launch)
+  // then find a free GPC more often than when every GPC is taken
+  if (nc > 1) --nc;
+  nc = std::min(nc, RU);
+  const int U = nc > 0 ? (RU + nc - 1) / nc : 0;
+  for (int nst = kFusedMaxStages; nc > 0 && U <= kFusedMaxUnits && nst >= 4; nst -= 2) {  // even: gate/up pairs
+    if ((size_t)nst * kFusedTile < (size_t)cpc * 128 * E * 2) break;
+    const size_t smem = std::max(fused_smem(nst, M, H, I, E, K, U).total, one_per_sm);
+    if (smem <= d.smem_optin) {
+      best = FusedPlan{nst, nc, smem};
+      break;
+    }
   }
   std::lock_guard<std::mutex> lock(mu);
   if (used < 64) {
