@@ -16,7 +16,10 @@ amd-kernels wide-expert shape token h6144_i768_e128_top4):
 * w13 [E][2I][H] and w2 [E][H][I] ~ N(0, 0.02) in FP32, quantised per 128x128 block;
 * skewed verify: an FP32 logit bias of +3.0 on experts 0..3;
 * Zipf prefill: each token draws K distinct experts with p(e) proportional to (e+1)^-1.1,
-  without replacement (Gumbel top-k), and Dirichlet(1) weights.
+  without replacement (Gumbel top-k), and Dirichlet(1) weights;
+* the un-normalised hidden in front of an RMSNorm (the residual stream): each row
+  N(0, sigma_t^2) with sigma_t log-uniform in [2^-4, 2^4], and 4 outlier channels (drawn
+  once per seed) scaled by 16; the norm's weight BF16 ~ 1 + N(0, 0.1^2).
 
 Every stream is ``numpy.random.default_rng([seed, stream])`` (PCG64) so that each tensor
 is independent of the order in which the others are drawn.
@@ -31,6 +34,7 @@ import torch
 
 # stream ids for default_rng([seed, stream])
 _S_HIDDEN, _S_ROUTER, _S_W13, _S_W2, _S_IDS, _S_WTS = 1, 2, 3, 4, 5, 6
+_S_RESID, _S_GAMMA = 7, 8
 
 
 @dataclasses.dataclass(frozen=True)
@@ -160,6 +164,23 @@ def make(name: str, M: Optional[int] = None, E: Optional[int] = None, tokens: Op
     if "zipf" in c:
         ids, wts = zipf_routing(seed, rows, Ex, K, c["zipf"])
     return MoEInputs(sh, M, hidden, router_w, bias, w13, s13, w2, s2, ids, wts)
+
+
+def residual_states(seed: int, M: int, H: int, zero_rows: Optional[np.ndarray] = None) -> np.ndarray:
+    """Un-normalised BF16 rows [M][H] (uint16 bits) for the RMSNorm in front of the layer."""
+    g = rng(seed, _S_RESID)
+    sigma = np.exp2(g.uniform(-4.0, 4.0, size=(M, 1))).astype(np.float32)
+    x = g.standard_normal((M, H), dtype=np.float32) * sigma
+    outliers = g.choice(H, size=4, replace=False)
+    x[:, outliers] *= np.float32(16.0)
+    if zero_rows is not None:
+        x[zero_rows] = 0.0
+    return to_bf16_bits(x)
+
+
+def norm_weight(seed: int, H: int) -> np.ndarray:
+    """The RMSNorm weight, BF16 [H] (uint16 bits)."""
+    return to_bf16_bits(1.0 + 0.1 * rng(seed, _S_GAMMA).standard_normal(H, dtype=np.float32))
 
 
 def wide_padding_rows(M: int) -> np.ndarray:

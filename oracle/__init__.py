@@ -6,8 +6,8 @@ shares no code with it: the oracle is a plain C++ restatement (``oracle.cpp``) b
 g++ and called through ctypes.
 
 What it computes, step by step, is documented in ``oracle.cpp``; each function there names
-the page and section it follows. Parity status: the codec, the quantiser, the router and
-the block GEMMs are pinned by the ``-m "not gpu"`` tests in ``tests/test_oracle_*.py``
+the page and section it follows. Parity status: the codec, the quantiser, the router, the
+RMSNorm in front of the layer and the block GEMMs are pinned by the ``-m "not gpu"`` tests in ``tests/test_oracle_*.py``
 against the E4M3 format definition, torch's float8 cast, float64 library matmuls with
 rigorous error bounds, closed forms and brute force. The exact FP32 rounding order inside
 the router's 128-wide chunks and the promotion chain is this library's contract reading
@@ -67,6 +67,8 @@ def _load():
             lib.orc_moe_forward.restype = i32
             lib.orc_down_combine.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i32]
             lib.orc_down_combine.restype = i32
+            lib.orc_rmsnorm.argtypes = [vp, vp, ctypes.c_float, i32, i32, vp, vp]
+            lib.orc_rmsnorm.restype = i32
             _lib = lib
     return _lib
 
@@ -177,3 +179,16 @@ def down_combine(qact, s2, ids, weights, w2, s2w, nthreads: int = 1):
     if rc != 0:
         raise ValueError("oracle down_combine: unsupported sizes")
     return out
+
+
+def rmsnorm(x, gamma, eps: float, want_rstd: bool = False):
+    """x uint16(BF16) [M][H], gamma uint16(BF16) [H] -> y uint16(BF16) [M][H] (and r f32 [M])."""
+    x, gamma = _c(x, np.uint16), _c(gamma, np.uint16)
+    M, H = x.shape
+    assert gamma.shape == (H,)
+    y = np.empty((M, H), np.uint16)
+    r = np.empty(M, np.float32)
+    rc = _load().orc_rmsnorm(_p(x), _p(gamma), float(eps), M, H, _p(y), _p(r))
+    if rc != 0:
+        raise ValueError("oracle rmsnorm: unsupported sizes")
+    return (y, r) if want_rstd else y

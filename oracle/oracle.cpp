@@ -142,6 +142,41 @@ void orc_bf16_round(const float* x, uint16_t* out, int64_t n) {
 // Exact block dot product, exposed for the block-sum pin.
 float orc_block_dot(const uint8_t* a, const uint8_t* w, int n) { return block_dot(a, w, n); }
 
+// ---- RMS normalisation ---------------------------------------------------------------
+// RMSNorm of the hidden rows ahead of the layer (netra-kernel lab README, repository layout:
+// gfx950 "normalization and quantization fusions"; the model's RMSNorm in front of the MoE
+// block). The pages give no epsilon and no weight convention; reading: the plain definition
+//   y[k] = bf16_rn( (x[k] * r) * gamma[k] ),   r = 1 / sqrt(ss / H + eps),
+// with eps and gamma (BF16 [H]) supplied by the caller, and ss = the sum of x[k]^2 formed like
+// the router's logits: an FP32 fma chain over each 128-wide chunk (k ascending, from 0), the
+// chunks added in ascending order. Every step is one correctly rounded FP32 operation: the
+// division by H, the add of eps, the square root, the reciprocal (1 / s as a division), and
+// the two multiplies. x and y are BF16 [M][H]; rstd_out [M] (optional) receives r.
+int orc_rmsnorm(const uint16_t* x, const uint16_t* gamma, float eps, int M, int H, uint16_t* y, float* rstd_out) {
+  if (M < 0 || H <= 0 || H % 128) return -1;
+  for (int t = 0; t < M; ++t) {
+    const uint16_t* xr = x + (int64_t)t * H;
+    float ss = 0.0f;
+    for (int c = 0; c < H / 128; ++c) {
+      float acc = 0.0f;
+      for (int k = c * 128; k < c * 128 + 128; ++k) {
+        const float v = bf16_to_f32(xr[k]);
+        acc = std::fmaf(v, v, acc);
+      }
+      ss = ss + acc;
+    }
+    const float mean = ss / (float)H;
+    const float s = std::sqrt(mean + eps);
+    const float r = 1.0f / s;
+    if (rstd_out) rstd_out[t] = r;
+    for (int k = 0; k < H; ++k) {
+      const float v = (bf16_to_f32(xr[k]) * r) * bf16_to_f32(gamma[k]);
+      y[(int64_t)t * H + k] = f32_to_bf16(v);
+    }
+  }
+  return 0;
+}
+
 // ---- routing -------------------------------------------------------------------------
 // Router (netra-kernel README capability table: BF16 routing; prefill-pair section:
 // "semantic routing" stage). hidden BF16 [M][H] row-major, router_w BF16 [H][E] (E
