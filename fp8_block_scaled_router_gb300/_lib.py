@@ -27,7 +27,8 @@ EXPORTS = ("moe_fp8_version", "moe_fp8_workspace_bytes", "moe_fp8_workspace_init
            "moe_fp8_combine", "moe_fp8_workspace_view", "moe_fp8_read_status",
            "moe_fp8_forward_noalloc", "moe_fp8_gate_up_direct", "moe_fp8_down_combine",
            "moe_fp8_route_forward_host", "moe_fp8_route_forward_pinned", "moe_fp8_selftest_wait",
-           "moe_fp8_route_forward", "moe_fp8_route_forward_one_launch")
+           "moe_fp8_route_forward", "moe_fp8_route_forward_one_launch", "moe_rmsnorm", "moe_norm_route",
+           "moe_fp8_norm_forward", "moe_fp8_norm_route_forward")
 
 
 class MoEError(RuntimeError):
@@ -79,6 +80,12 @@ def load(path: str = LIB):
             lib.moe_fp8_route_forward.argtypes = [vp, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, sp, vp]
             lib.moe_fp8_route_forward_one_launch.argtypes = [vp, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz,
                                                              sp, vp]
+            f32 = ctypes.c_float
+            lib.moe_rmsnorm.argtypes = [vp, vp, f32, i32, vp, sp, vp]
+            lib.moe_norm_route.argtypes = [vp, vp, f32, vp, vp, i32, sp, i32, vp, vp, vp]
+            lib.moe_fp8_norm_forward.argtypes = [vp, vp, f32, vp, vp, i32, vp, vp, vp, vp, vp, vp, sz, sp, vp]
+            lib.moe_fp8_norm_route_forward.argtypes = [vp, vp, f32, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                       sz, sp, vp]
             for f in EXPORTS[2:]:
                 if f != "moe_fp8_workspace_bytes":
                     getattr(lib, f).restype = i32
@@ -261,3 +268,38 @@ def moe_fp8_route_forward_one_launch(hidden, router_w, bias, M, renormalize, w13
         _ptr(hidden), _ptr(router_w), _ptr(bias), int(M), int(bool(renormalize)), _ptr(w13), _ptr(w13_scale),
         _ptr(w2), _ptr(w2_scale), _ptr(out), _ptr(topk_ids), _ptr(topk_w), _ptr(workspace), nb,
         ctypes.byref(shape), _stream(stream)), check)
+
+
+def moe_rmsnorm(hidden, norm_weight, eps, M, out, shape: Shape, stream=None, check=True):
+    """out = RMSNorm(hidden) (BF16 rows); see include/moe_fp8.h for the exact arithmetic."""
+    return _check("moe_rmsnorm", load().moe_rmsnorm(
+        _ptr(hidden), _ptr(norm_weight), float(eps), int(M), _ptr(out), ctypes.byref(shape), _stream(stream)), check)
+
+
+def moe_norm_route(hidden, norm_weight, eps, router_w, bias, M, shape: Shape, renormalize, topk_ids, topk_w,
+                   stream=None, check=True):
+    """moe_route of the RMSNorm'd hidden (the router normalises as it reads)."""
+    return _check("moe_norm_route", load().moe_norm_route(
+        _ptr(hidden), _ptr(norm_weight), float(eps), _ptr(router_w), _ptr(bias), int(M), ctypes.byref(shape),
+        int(bool(renormalize)), _ptr(topk_ids), _ptr(topk_w), _stream(stream)), check)
+
+
+def moe_fp8_norm_forward(hidden, norm_weight, eps, topk_ids, topk_w, M, w13, w13_scale, w2, w2_scale, out,
+                         workspace, shape: Shape, stream=None, ws_bytes=None, check=True):
+    """moe_fp8_forward of the RMSNorm'd hidden (the quantisers normalise as they read)."""
+    nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return _check("moe_fp8_norm_forward", load().moe_fp8_norm_forward(
+        _ptr(hidden), _ptr(norm_weight), float(eps), _ptr(topk_ids), _ptr(topk_w), int(M), _ptr(w13),
+        _ptr(w13_scale), _ptr(w2), _ptr(w2_scale), _ptr(out), _ptr(workspace), nb, ctypes.byref(shape),
+        _stream(stream)), check)
+
+
+def moe_fp8_norm_route_forward(hidden, norm_weight, eps, router_w, bias, M, renormalize, w13, w13_scale, w2,
+                               w2_scale, out, topk_ids, topk_w, workspace, shape: Shape, stream=None, ws_bytes=None,
+                               check=True):
+    """moe_fp8_route_forward of the RMSNorm'd hidden; see include/moe_fp8.h."""
+    nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return _check("moe_fp8_norm_route_forward", load().moe_fp8_norm_route_forward(
+        _ptr(hidden), _ptr(norm_weight), float(eps), _ptr(router_w), _ptr(bias), int(M), int(bool(renormalize)),
+        _ptr(w13), _ptr(w13_scale), _ptr(w2), _ptr(w2_scale), _ptr(out), _ptr(topk_ids), _ptr(topk_w),
+        _ptr(workspace), nb, ctypes.byref(shape), _stream(stream)), check)

@@ -9,35 +9,10 @@
 // (caller-local kernel arguments so concurrent calls cannot mix pointers).
 #include <cstdint>
 
-#include "common.cuh"
+#include <cmath>
 
-namespace moe {
-cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const float* bias, int M,
-                         int H, int E, int K, int renorm, int32_t* ids, float* wts, cudaStream_t st);
-cudaError_t launch_prep(const uint16_t* hidden, const int32_t* ids, int M, int H, int E, int K,
-                        const WsPtrs& ws, cudaStream_t st);
-cudaError_t launch_sort_gather(const uint16_t* hidden, const int32_t* ids, int M, int H, int E, int K,
-                               const WsPtrs& ws, cudaStream_t st);
-cudaError_t launch_grouped_gateup(const uint8_t* w13, const float* s13, int64_t R, int H, int I, int E,
-                                  int64_t max_tiles, const WsPtrs& ws, cudaStream_t st);
-cudaError_t launch_grouped_down(const uint8_t* w2, const float* s2w, int64_t R, int H, int I, int E,
-                                int64_t max_tiles, const WsPtrs& ws, cudaStream_t st);
-cudaError_t launch_pair_gateup(const uint8_t* w13, const float* s13, const int32_t* ids,
-                               const uint16_t* hidden, int M, int H, int I, int E, int K,
-                               const WsPtrs& ws, cudaStream_t st, const uint8_t* w2 = nullptr,
-                               const float* s2w = nullptr);
-cudaError_t launch_pair_down(const uint8_t* w2, const float* s2w, const int32_t* ids, const float* topk_w,
-                             uint16_t* out, int M, int H, int I, int E, int K, const WsPtrs& ws,
-                             cudaStream_t st);
-cudaError_t launch_combine(const float* topk_w, int M, int H, int K, uint16_t* out, const WsPtrs& ws,
-                           cudaStream_t st);
-cudaError_t launch_wait_selftest(Header* hdr, uint32_t limit_us, cudaStream_t st);
-bool fused_capable(int M, int H, int I, int E, int K);
-cudaError_t launch_fused(bool route, const uint16_t* hidden, const uint16_t* router_w, const float* bias,
-                         int renorm, int32_t* ids, float* wts, const uint8_t* w13, const float* s13,
-                         const uint8_t* w2, const float* s2w, uint16_t* out, int M, int H, int I, int E, int K,
-                         const WsPtrs& ws, float* yt, uint32_t* tickets, cudaStream_t st);
-}  // namespace moe
+#include "launch.h"
+
 
 using namespace moe;
 
@@ -84,6 +59,34 @@ moe_status_t check_ws(void* ws, size_t bytes, const moe_fp8_shape_t* s, Layout* 
 
 moe_status_t launched(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH; }
 
+// The RMSNorm arguments: gamma a 16-byte aligned device pointer, eps finite and > 0 (eps = 0
+// would turn an all-zero row into 0 * inf = NaN).
+moe_status_t check_norm(const void* norm_weight, float eps, Norm* nm) {
+  if (!norm_weight || !aligned16(norm_weight)) return MOE_ERR_INVALID_ARG;
+  if (!(eps > 0.0f) || !std::isfinite(eps)) return MOE_ERR_INVALID_ARG;
+  *nm = Norm{static_cast<const uint16_t*>(norm_weight), eps};
+  return MOE_OK;
+}
+
+moe_status_t route_impl(const void* hidden, Norm nm, const void* router_w, const float* bias, int32_t M,
+                        const moe_fp8_shape_t* shape, int32_t renormalize, int32_t* topk_ids, float* topk_w,
+                        cudaStream_t stream) {
+  if (moe_status_t st = check_common(shape, M)) return st;
+  if (!hidden || !router_w || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(hidden) || !aligned16(router_w) || !aligned16(topk_ids) || !aligned16(topk_w) ||
+      (bias && !aligned16(bias)))
+    return MOE_ERR_INVALID_ARG;
+  if (M == 0) return MOE_OK;
+  return launched(launch_route(static_cast<const uint16_t*>(hidden), nm, static_cast<const uint16_t*>(router_w), bias,
+                               M, shape->hidden, shape->num_experts, shape->top_k, renormalize ? 1 : 0, topk_ids,
+                               topk_w, stream));
+}
+
+moe_status_t forward_impl(const void* hidden, Norm nm, const int32_t* topk_ids, const float* topk_w, int32_t M,
+                          const uint8_t* w13, const float* w13_scale, const uint8_t* w2, const float* w2_scale,
+                          void* out, void* workspace, size_t workspace_bytes, const moe_fp8_shape_t* shape,
+                          cudaStream_t stream);
+
 }  // namespace
 
 extern "C" {
@@ -108,16 +111,26 @@ moe_status_t moe_fp8_workspace_init(void* workspace, size_t workspace_bytes,
 moe_status_t moe_route(const void* hidden, const void* router_w, const float* bias, int32_t M,
                        const moe_fp8_shape_t* shape, int32_t renormalize, int32_t* topk_ids,
                        float* topk_w, cudaStream_t stream) {
+  return route_impl(hidden, Norm{nullptr, 0.0f}, router_w, bias, M, shape, renormalize, topk_ids, topk_w, stream);
+}
+
+moe_status_t moe_norm_route(const void* hidden, const void* norm_weight, float eps, const void* router_w,
+                            const float* bias, int32_t M, const moe_fp8_shape_t* shape, int32_t renormalize,
+                            int32_t* topk_ids, float* topk_w, cudaStream_t stream) {
+  Norm nm;
+  if (moe_status_t st = check_norm(norm_weight, eps, &nm)) return st;
+  return route_impl(hidden, nm, router_w, bias, M, shape, renormalize, topk_ids, topk_w, stream);
+}
+
+moe_status_t moe_rmsnorm(const void* hidden, const void* norm_weight, float eps, int32_t M, void* out,
+                         const moe_fp8_shape_t* shape, cudaStream_t stream) {
   if (moe_status_t st = check_common(shape, M)) return st;
-  if (!hidden || !router_w || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(hidden) || !aligned16(router_w) || !aligned16(topk_ids) || !aligned16(topk_w) ||
-      (bias && !aligned16(bias)))
-    return MOE_ERR_INVALID_ARG;
+  Norm nm;
+  if (moe_status_t st = check_norm(norm_weight, eps, &nm)) return st;
+  if (!hidden || !out || !aligned16(hidden) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
   if (M == 0) return MOE_OK;
-  return launched(launch_route(static_cast<const uint16_t*>(hidden),
-                               static_cast<const uint16_t*>(router_w), bias, M, shape->hidden,
-                               shape->num_experts, shape->top_k, renormalize ? 1 : 0, topk_ids,
-                               topk_w, stream));
+  return launched(launch_rmsnorm(static_cast<const uint16_t*>(hidden), nm, M, shape->hidden,
+                                 static_cast<uint16_t*>(out), stream));
 }
 
 moe_status_t moe_fp8_prepare(const void* hidden, const int32_t* topk_ids, int32_t M,
@@ -133,7 +146,7 @@ moe_status_t moe_fp8_prepare(const void* hidden, const int32_t* topk_ids, int32_
   if (use_pair_mode(R))
     return launched(launch_prep(static_cast<const uint16_t*>(hidden), topk_ids, M, shape->hidden,
                                 shape->num_experts, shape->top_k, ws, stream));
-  return launched(launch_sort_gather(static_cast<const uint16_t*>(hidden), topk_ids, M, shape->hidden,
+  return launched(launch_sort_gather(static_cast<const uint16_t*>(hidden), Norm{nullptr, 0.0f}, topk_ids, M, shape->hidden,
                                      shape->num_experts, shape->top_k, ws, stream));
 }
 
@@ -184,11 +197,13 @@ moe_status_t moe_fp8_combine(const float* topk_w, int32_t M, void* out, void* wo
                                  ws, stream));
 }
 
-moe_status_t moe_fp8_forward(const void* hidden, const int32_t* topk_ids, const float* topk_w,
-                             int32_t M, const uint8_t* w13, const float* w13_scale,
-                             const uint8_t* w2, const float* w2_scale, void* out,
-                             void* workspace, size_t workspace_bytes,
-                             const moe_fp8_shape_t* shape, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+moe_status_t forward_impl(const void* hidden, Norm nm, const int32_t* topk_ids, const float* topk_w, int32_t M,
+                          const uint8_t* w13, const float* w13_scale, const uint8_t* w2, const float* w2_scale,
+                          void* out, void* workspace, size_t workspace_bytes, const moe_fp8_shape_t* shape,
+                          cudaStream_t stream) {
   if (moe_status_t st = check_common(shape, M)) return st;
   if (!hidden || !topk_ids || !topk_w || !w13 || !w13_scale || !w2 || !w2_scale || !out)
     return MOE_ERR_INVALID_ARG;
@@ -199,24 +214,49 @@ moe_status_t moe_fp8_forward(const void* hidden, const int32_t* topk_ids, const 
   if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
   if (M == 0) return MOE_OK;
   const int H = shape->hidden, I = shape->inter, E = shape->num_experts, K = shape->top_k;
-  if (use_pair_mode((int64_t)M * shape->top_k)) {
-    // few routed rows: two launches -- gate/up quantises its own hidden row and prefetches
-    // the routed experts' down weights into L2, down is fused with the combine (same
-    // arithmetic as the four stage calls)
-    const WsPtrs ws = ws_ptrs(workspace, L);
+  const WsPtrs ws = ws_ptrs(workspace, L);
+  const int64_t R = (int64_t)M * K;
+  if (use_pair_mode(R)) {
+    // few routed rows: two launches -- gate/up quantises its own hidden row (through the
+    // norm, if any) and prefetches the routed experts' down weights into L2, down is fused
+    // with the combine (same arithmetic as the four stage calls)
     if (moe_status_t st = launched(launch_pair_gateup(w13, w13_scale, topk_ids, static_cast<const uint16_t*>(hidden),
-                                                      M, H, I, E, K, ws, stream, w2, w2_scale)))
+                                                      M, H, I, E, K, ws, stream, w2, w2_scale, nm)))
       return st;
     return launched(launch_pair_down(w2, w2_scale, topk_ids, topk_w, static_cast<uint16_t*>(out), M, H, I, E, K,
                                      ws, stream));
   }
-  if (moe_status_t st = moe_fp8_prepare(hidden, topk_ids, M, workspace, workspace_bytes, shape, stream))
+  // many routed rows: quantise (through the norm, if any) and sort into expert tiles, the
+  // two tile GEMMs, the slot-order combine
+  const int64_t tiles = max_tiles_for(R, E, kTileRows);
+  if (moe_status_t st = launched(launch_sort_gather(static_cast<const uint16_t*>(hidden), nm, topk_ids, M, H, E, K,
+                                                    ws, stream)))
     return st;
-  if (moe_status_t st = moe_fp8_gate_up(w13, w13_scale, M, workspace, workspace_bytes, shape, stream))
-    return st;
-  if (moe_status_t st = moe_fp8_down(w2, w2_scale, M, workspace, workspace_bytes, shape, stream))
-    return st;
-  return moe_fp8_combine(topk_w, M, out, workspace, workspace_bytes, shape, stream);
+  if (moe_status_t st = launched(launch_grouped_gateup(w13, w13_scale, R, H, I, E, tiles, ws, stream))) return st;
+  if (moe_status_t st = launched(launch_grouped_down(w2, w2_scale, R, H, I, E, tiles, ws, stream))) return st;
+  return launched(launch_combine(topk_w, M, H, K, static_cast<uint16_t*>(out), ws, stream));
+}
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_fp8_forward(const void* hidden, const int32_t* topk_ids, const float* topk_w,
+                             int32_t M, const uint8_t* w13, const float* w13_scale,
+                             const uint8_t* w2, const float* w2_scale, void* out,
+                             void* workspace, size_t workspace_bytes,
+                             const moe_fp8_shape_t* shape, cudaStream_t stream) {
+  return forward_impl(hidden, Norm{nullptr, 0.0f}, topk_ids, topk_w, M, w13, w13_scale, w2, w2_scale, out, workspace,
+                      workspace_bytes, shape, stream);
+}
+
+moe_status_t moe_fp8_norm_forward(const void* hidden, const void* norm_weight, float eps, const int32_t* topk_ids,
+                                  const float* topk_w, int32_t M, const uint8_t* w13, const float* w13_scale,
+                                  const uint8_t* w2, const float* w2_scale, void* out, void* workspace,
+                                  size_t workspace_bytes, const moe_fp8_shape_t* shape, cudaStream_t stream) {
+  Norm nm;
+  if (moe_status_t st = check_norm(norm_weight, eps, &nm)) return st;
+  return forward_impl(hidden, nm, topk_ids, topk_w, M, w13, w13_scale, w2, w2_scale, out, workspace, workspace_bytes,
+                      shape, stream);
 }
 
 moe_status_t moe_fp8_gate_up_direct(const void* hidden, const int32_t* topk_ids, int32_t M,
@@ -302,6 +342,24 @@ moe_status_t moe_fp8_route_forward(const void* hidden, const void* router_w, con
   if (moe_status_t st = moe_route(hidden, router_w, bias, M, shape, renormalize, topk_ids, topk_w, stream)) return st;
   return moe_fp8_forward(hidden, topk_ids, topk_w, M, w13, w13_scale, w2, w2_scale, out, workspace,
                          workspace_bytes, shape, stream);
+}
+
+moe_status_t moe_fp8_norm_route_forward(const void* hidden, const void* norm_weight, float eps, const void* router_w,
+                                        const float* bias, int32_t M, int32_t renormalize, const uint8_t* w13,
+                                        const float* w13_scale, const uint8_t* w2, const float* w2_scale, void* out,
+                                        int32_t* topk_ids, float* topk_w, void* workspace, size_t workspace_bytes,
+                                        const moe_fp8_shape_t* shape, cudaStream_t stream) {
+  Norm nm;
+  if (moe_status_t st = check_norm(norm_weight, eps, &nm)) return st;
+  Layout L;
+  if (moe_status_t st = check_route_forward(hidden, router_w, bias, M, w13, w13_scale, w2, w2_scale, out, topk_ids,
+                                            topk_w, workspace, workspace_bytes, shape, &L))
+    return st;
+  if (M == 0) return MOE_OK;
+  if (moe_status_t st = route_impl(hidden, nm, router_w, bias, M, shape, renormalize, topk_ids, topk_w, stream))
+    return st;
+  return forward_impl(hidden, nm, topk_ids, topk_w, M, w13, w13_scale, w2, w2_scale, out, workspace, workspace_bytes,
+                      shape, stream);
 }
 
 moe_status_t moe_fp8_route_forward_one_launch(const void* hidden, const void* router_w, const float* bias,

@@ -9,6 +9,7 @@
 // One thread owns 8 consecutive columns: two 128-bit loads of y per slot, one 128-bit
 // store of 8 BF16 values.
 #include "common.cuh"
+#include "launch.h"
 
 namespace moe {
 

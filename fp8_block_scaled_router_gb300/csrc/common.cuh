@@ -174,6 +174,61 @@ __device__ __forceinline__ float silu_mul_fast(float g, float u) {
   return __fmul_rn(__fdividef(g, __fadd_rn(1.0f, exp_neg_split(g))), u);
 }
 
+// --------------------------------------------------------------------------------------
+// RMSNorm in front of the layer (optional input transform of the hidden rows):
+//   y[k] = bf16_rn((x[k] * r) * gamma[k]),   r = 1 / sqrt(ss / H + eps),
+// ss = the sum of x[k]^2 formed as the router forms a logit: an FP32 fma chain over each
+// 128-wide chunk (k ascending, from 0), the chunk partials added in ascending chunk order.
+// Each step is one correctly rounded FP32 operation. Every kernel that reads y computes r
+// itself with row_rms_scale, so the router and the quantisers see the same bits.
+// --------------------------------------------------------------------------------------
+struct Norm {
+  const uint16_t* gamma;  // BF16 [H]; nullptr: no normalisation (y = x)
+  float eps;
+};
+
+// r of the BF16 row x[0, H) (H a multiple of 128, at most 64 chunks; x 16-byte aligned),
+// computed by one whole warp; every lane returns it. Lane c (and c + 32) runs chunk c's chain.
+__device__ __forceinline__ float row_rms_scale(const uint16_t* __restrict__ x, int H, float eps, int lane) {
+  const int nch = H / 128;
+  float part0 = 0.0f, part1 = 0.0f;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int c = lane + 32 * half;
+    if (c < nch) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)c * 128);
+      uint4 v[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) v[q] = src[q];
+      float acc = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const uint32_t w4[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float a = bf16_bits_to_float((uint16_t)(w4[u] & 0xFFFF));
+          const float b = bf16_bits_to_float((uint16_t)(w4[u] >> 16));
+          acc = __fmaf_rn(a, a, acc);
+          acc = __fmaf_rn(b, b, acc);
+        }
+      }
+      if (half == 0) part0 = acc; else part1 = acc;
+    }
+  }
+  float ss = 0.0f;
+  for (int c = 0; c < nch; ++c) ss = __fadd_rn(ss, __shfl_sync(0xffffffffu, c < 32 ? part0 : part1, c & 31));
+  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)H), eps)));
+}
+
+// y of one element (BF16 bits in, BF16 value out as FP32)
+__device__ __forceinline__ float norm_value(uint16_t x, float r, uint16_t g) {
+  const float v = __fmul_rn(__fmul_rn(bf16_bits_to_float(x), r), bf16_bits_to_float(g));
+  return __bfloat162float(__float2bfloat16_rn(v));
+}
+__device__ __forceinline__ uint16_t norm_bits(uint16_t x, float r, uint16_t g) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(__fmul_rn(bf16_bits_to_float(x), r), bf16_bits_to_float(g))));
+}
+
 __device__ __forceinline__ void set_status(Header* hdr, uint32_t bits) {
   atomicOr(&hdr->status, bits);  // a flag word, never a value accumulation
 }

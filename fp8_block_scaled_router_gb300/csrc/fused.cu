@@ -47,6 +47,7 @@
 #include <algorithm>
 
 #include "device.h"
+#include "launch.h"
 #include "tc.cuh"
 
 namespace moe {

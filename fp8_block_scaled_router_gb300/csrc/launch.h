@@ -1,0 +1,47 @@
+// launch.h -- the kernels' host-side launchers (internal to the library; the C ABI in
+// api.cu and noalloc.cu calls these). Every launcher enqueues on `st` and returns the launch
+// error, if any; none allocates, synchronises or reads device memory.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+// route.cu: top-k routing of M tokens (norm: an RMSNorm in front, gamma null for none)
+cudaError_t launch_route(const uint16_t* hidden, Norm nm, const uint16_t* router_w, const float* bias, int M,
+                         int H, int E, int K, int renorm, int32_t* ids, float* wts, cudaStream_t st);
+// norm.cu: y = RMSNorm(hidden) as BF16 [M][H]
+cudaError_t launch_rmsnorm(const uint16_t* hidden, Norm nm, int M, int H, uint16_t* y, cudaStream_t st);
+// prep.cu: hidden codes + the pair-mode identity permutation (few routed rows), or the
+// counting sort and the gather of codes into expert order (many routed rows)
+cudaError_t launch_prep(const uint16_t* hidden, const int32_t* ids, int M, int H, int E, int K,
+                        const WsPtrs& ws, cudaStream_t st);
+cudaError_t launch_sort_gather(const uint16_t* hidden, Norm nm, const int32_t* ids, int M, int H, int E, int K,
+                               const WsPtrs& ws, cudaStream_t st);
+// tc_grouped.cu: the expert-sorted tile GEMMs
+cudaError_t launch_grouped_gateup(const uint8_t* w13, const float* s13, int64_t R, int H, int I, int E,
+                                  int64_t max_tiles, const WsPtrs& ws, cudaStream_t st);
+cudaError_t launch_grouped_down(const uint8_t* w2, const float* s2w, int64_t R, int H, int I, int E,
+                                int64_t max_tiles, const WsPtrs& ws, cudaStream_t st);
+// tc_pair.cu: one unit per routed pair. gate/up quantises hidden itself when hidden is set
+// (then w2/s2w, if set, are prefetched into L2 and nm applies), else reads the workspace codes
+cudaError_t launch_pair_gateup(const uint8_t* w13, const float* s13, const int32_t* ids,
+                               const uint16_t* hidden, int M, int H, int I, int E, int K,
+                               const WsPtrs& ws, cudaStream_t st, const uint8_t* w2 = nullptr,
+                               const float* s2w = nullptr, Norm nm = Norm{nullptr, 0.0f});
+cudaError_t launch_pair_down(const uint8_t* w2, const float* s2w, const int32_t* ids, const float* topk_w,
+                             uint16_t* out, int M, int H, int I, int E, int K, const WsPtrs& ws,
+                             cudaStream_t st);
+// combine.cu: out = slot-order combine of y
+cudaError_t launch_combine(const float* topk_w, int M, int H, int K, uint16_t* out, const WsPtrs& ws,
+                           cudaStream_t st);
+// selftest.cu: a bounded wait that runs out
+cudaError_t launch_wait_selftest(Header* hdr, uint32_t limit_us, cudaStream_t st);
+// fused.cu: the single-launch layer for a few routed pairs
+bool fused_capable(int M, int H, int I, int E, int K);
+cudaError_t launch_fused(bool route, const uint16_t* hidden, const uint16_t* router_w, const float* bias,
+                         int renorm, int32_t* ids, float* wts, const uint8_t* w13, const float* s13,
+                         const uint8_t* w2, const float* s2w, uint16_t* out, int M, int H, int I, int E, int K,
+                         const WsPtrs& ws, float* yt, uint32_t* tickets, cudaStream_t st);
+
+}  // namespace moe

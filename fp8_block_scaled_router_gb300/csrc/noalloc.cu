@@ -21,17 +21,8 @@
 
 #include <mutex>
 
-#include "common.cuh"
+#include "launch.h"
 
-namespace moe {
-cudaError_t launch_pair_gateup(const uint8_t* w13, const float* s13, const int32_t* ids,
-                               const uint16_t* hidden, int M, int H, int I, int E, int K,
-                               const WsPtrs& ws, cudaStream_t st, const uint8_t* w2 = nullptr,
-                               const float* s2w = nullptr);
-cudaError_t launch_pair_down(const uint8_t* w2, const float* s2w, const int32_t* ids, const float* topk_w,
-                             uint16_t* out, int M, int H, int I, int E, int K, const WsPtrs& ws,
-                             cudaStream_t st);
-}  // namespace moe
 
 using namespace moe;
 

@@ -7,15 +7,31 @@
 //
 // Quantisation: one warp per (token, 128-column group), amax by a warp max reduction,
 // scale = amax/448 (IEEE division; 1.0 for an all-zero group), RNE saturating E4M3 codes.
+// With an RMSNorm in front (many-row path), one warp per token forms r and quantises the
+// token's y = bf16((x*r)*gamma) group by group.
 // Few routed rows (pair mode): block 0 records each pair's expert (-1 if out of range) and
 // the identity permutation. Many routed rows: the two-launch counting sort below.
 #include "common.cuh"
+#include "launch.h"
 #include "device.h"
 
 namespace moe {
 
 constexpr int kPrepThreads = 1024;
 constexpr int kMaxExperts = 256;
+
+// One warp quantises one 128-column group: lane l holds columns 4l..4l+3 (x0..x3).
+__device__ __forceinline__ void quant_group_store(float x0, float x1, float x2, float x3, int lane, uint8_t* qdst,
+                                                  float* sdst) {
+  float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const float s = quant_scale(amax);
+  const uint32_t lo = e4m3x2_encode(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
+  const uint32_t hi = e4m3x2_encode(__fdiv_rn(x2, s), __fdiv_rn(x3, s));
+  reinterpret_cast<uint32_t*>(qdst)[lane] = lo | (hi << 16);
+  if (lane == 0) *sdst = s;
+}
 
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const uint16_t* __restrict__ hidden,
                                                             const int32_t* __restrict__ ids, int M,
@@ -32,16 +48,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const uint16_t* __re
       const int64_t t = gidx / ngroups_row;
       const int g = (int)(gidx % ngroups_row);
       const uint2 raw = *reinterpret_cast<const uint2*>(hidden + t * H + g * 128 + lane * 4);
-      const float x0 = bf16_bits_to_float(raw.x & 0xFFFF), x1 = bf16_bits_to_float(raw.x >> 16);
-      const float x2 = bf16_bits_to_float(raw.y & 0xFFFF), x3 = bf16_bits_to_float(raw.y >> 16);
-      float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-      const float s = quant_scale(amax);
-      const uint32_t lo = e4m3x2_encode(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
-      const uint32_t hi = e4m3x2_encode(__fdiv_rn(x2, s), __fdiv_rn(x3, s));
-      *reinterpret_cast<uint32_t*>(ws.qa + t * H + g * 128 + lane * 4) = lo | (hi << 16);
-      if (lane == 0) ws.sa[t * ngroups_row + g] = s;
+      quant_group_store(bf16_bits_to_float(raw.x & 0xFFFF), bf16_bits_to_float(raw.x >> 16),
+                        bf16_bits_to_float(raw.y & 0xFFFF), bf16_bits_to_float(raw.y >> 16), lane,
+                        ws.qa + t * H + g * 128, ws.sa + t * ngroups_row + g);
     }
     return;
   }
@@ -80,7 +89,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const uint16_t* __re
 //   gather:  one warp per placed row copies the row's hidden codes (H bytes) and scales
 //            into xp / sa_p -- thousands of independent 16-byte copies in flight.
 // ---------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) count_quant_kernel(const uint16_t* __restrict__ hidden,
+__global__ void __launch_bounds__(256) count_quant_kernel(const uint16_t* __restrict__ hidden, const Norm nm,
                                                           const int32_t* __restrict__ ids, int M, int H,
                                                           int E, int K, int nblk, WsPtrs ws) {
   const int tid = threadIdx.x;
@@ -104,22 +113,30 @@ __global__ void __launch_bounds__(256) count_quant_kernel(const uint16_t* __rest
   }
   const int warp = tid / 32, lane = tid % 32;
   const int ngroups_row = H / 128;
-  const int64_t ngroups = (int64_t)M * ngroups_row;
   const int64_t nwarps = (int64_t)(gridDim.x - nblk) * 8;
+  if (nm.gamma != nullptr) {
+    // RMSNorm in front: one warp per row forms r, then quantises y = bf16((x*r)*gamma)
+    for (int64_t t = (int64_t)(blockIdx.x - nblk) * 8 + warp; t < M; t += nwarps) {
+      const uint16_t* xr = hidden + t * H;
+      const float r = row_rms_scale(xr, H, nm.eps, lane);
+      for (int g = 0; g < ngroups_row; ++g) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(xr + g * 128 + lane * 4);
+        const uint2 gm = *reinterpret_cast<const uint2*>(nm.gamma + g * 128 + lane * 4);
+        quant_group_store(norm_value(raw.x & 0xFFFF, r, gm.x & 0xFFFF), norm_value(raw.x >> 16, r, gm.x >> 16),
+                          norm_value(raw.y & 0xFFFF, r, gm.y & 0xFFFF), norm_value(raw.y >> 16, r, gm.y >> 16),
+                          lane, ws.qa + t * H + g * 128, ws.sa + t * ngroups_row + g);
+      }
+    }
+    return;
+  }
+  const int64_t ngroups = (int64_t)M * ngroups_row;
   for (int64_t gidx = (int64_t)(blockIdx.x - nblk) * 8 + warp; gidx < ngroups; gidx += nwarps) {
     const int64_t t = gidx / ngroups_row;
     const int g = (int)(gidx % ngroups_row);
     const uint2 raw = *reinterpret_cast<const uint2*>(hidden + t * H + g * 128 + lane * 4);
-    const float x0 = bf16_bits_to_float(raw.x & 0xFFFF), x1 = bf16_bits_to_float(raw.x >> 16);
-    const float x2 = bf16_bits_to_float(raw.y & 0xFFFF), x3 = bf16_bits_to_float(raw.y >> 16);
-    float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    const float s = quant_scale(amax);
-    const uint32_t lo = e4m3x2_encode(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
-    const uint32_t hi = e4m3x2_encode(__fdiv_rn(x2, s), __fdiv_rn(x3, s));
-    *reinterpret_cast<uint32_t*>(ws.qa + t * H + g * 128 + lane * 4) = lo | (hi << 16);
-    if (lane == 0) ws.sa[t * ngroups_row + g] = s;
+    quant_group_store(bf16_bits_to_float(raw.x & 0xFFFF), bf16_bits_to_float(raw.x >> 16),
+                      bf16_bits_to_float(raw.y & 0xFFFF), bf16_bits_to_float(raw.y >> 16), lane,
+                      ws.qa + t * H + g * 128, ws.sa + t * ngroups_row + g);
   }
 }
 
@@ -232,7 +249,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(int R, int H, int E, i
   for (int c = lane; c < nsc; c += 32) ws.sa_p[(size_t)p * nsc + c] = ws.sa[(size_t)t * nsc + c];
 }
 
-cudaError_t launch_sort_gather(const uint16_t* hidden, const int32_t* ids, int M, int H, int E, int K,
+cudaError_t launch_sort_gather(const uint16_t* hidden, Norm nm, const int32_t* ids, int M, int H, int E, int K,
                                const WsPtrs& ws, cudaStream_t st) {
   const int R = M * K;
   const int nblk = (R + kSortBlock - 1) / kSortBlock;
@@ -240,7 +257,7 @@ cudaError_t launch_sort_gather(const uint16_t* hidden, const int32_t* ids, int M
   int64_t qblocks = (groups + 7) / 8;
   const int64_t cap8 = 8 * (int64_t)(device_info().sms > 0 ? device_info().sms : 1);  // 8 CTAs per SM
   if (qblocks > cap8) qblocks = cap8;
-  count_quant_kernel<<<(unsigned)(nblk + qblocks), 256, 0, st>>>(hidden, ids, M, H, E, K, nblk, ws);
+  count_quant_kernel<<<(unsigned)(nblk + qblocks), 256, 0, st>>>(hidden, nm, ids, M, H, E, K, nblk, ws);
   if (cudaError_t e = cudaGetLastError()) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)nblk, 1, 1);

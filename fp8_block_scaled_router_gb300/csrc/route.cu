@@ -13,11 +13,15 @@
 // e takes slot #{e' : l[e'] > l[e] or (l[e'] == l[e] and e' < e)} when that is below K
 // (ties to the lower index). Weights: softmax over the K selected logits (renormalised) or
 // over all E. No workspace, no atomics, no spin-waits.
+// With an RMSNorm in front (Norm::gamma set), the router reads y = bf16((x*r)*gamma) in place
+// of x: each CTA first forms r of its tokens (one warp per token, common.cuh's
+// row_rms_scale) and converts the hidden values as it stages them.
 #include <cooperative_groups.h>
 
 #include <mutex>
 
 #include "common.cuh"
+#include "launch.h"
 #include "device.h"
 
 namespace cg = cooperative_groups;
@@ -28,13 +32,15 @@ constexpr int kRouteThreads = 256;
 constexpr int kRouteMaxCluster = 16;
 
 struct RouteSmem {
-  size_t ws, xs, part, logits, sel, bias, total;
+  size_t ws, xs, part, logits, sel, bias, rs, total;
 };
 
 // ws: router rows [CPC*128][E] bf16 (or one chunk [128][E] at a time when they do not fit);
 // xs: hidden [CPC*128][TB] bf16 (token-minor);
 // part (CTA 0): chunk partials [nchunks][TB][E] f32; logits [TB][E] f32;
-// sel: selected logits [TB][16] f32 + ids [TB][16] i32.
+// sel: selected logits [TB][16] f32 + ids [TB][16] i32; rs: RMSNorm r [TB] f32.
+// (All shared memory is dynamic: the kernel's dynamic limit is set to the device's opt-in
+// maximum, which leaves no room for static shared variables.)
 // stage_all: all CPC router chunks of the CTA are held in shared memory (staged before the
 // grid dependency); otherwise one chunk at a time streams through it.
 __host__ __device__ inline RouteSmem route_smem(int TB, int CPC, int E, int nchunks, bool stage_all) {
@@ -47,6 +53,7 @@ __host__ __device__ inline RouteSmem route_smem(int TB, int CPC, int E, int nchu
   s.logits = o; o += (size_t)TB * E * 4;
   s.sel = o;    o += (size_t)TB * 16 * 8;
   s.bias = o;   o += (size_t)E * 4;
+  s.rs = o;     o += (size_t)TB * 4;  // RMSNorm: r of each token
   s.total = o;
   return s;
 }
@@ -55,7 +62,7 @@ __host__ __device__ inline RouteSmem route_smem(int TB, int CPC, int E, int nchu
 // one at a time (a separate instantiation, so the common path keeps its register budget).
 template <int TB, bool STREAM>
 __global__ void __launch_bounds__(kRouteThreads)
-    route_kernel(const uint16_t* __restrict__ hidden, const uint16_t* __restrict__ router_w,
+    route_kernel(const uint16_t* __restrict__ hidden, const Norm nm, const uint16_t* __restrict__ router_w,
                  const float* __restrict__ bias, int M, int H, int E, int K, int renorm,
                  int32_t* __restrict__ ids, float* __restrict__ wts) {
   constexpr bool stage_all = !STREAM;
@@ -101,7 +108,20 @@ __global__ void __launch_bounds__(kRouteThreads)
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
-  {
+  if (nm.gamma != nullptr) {
+    float* rs = reinterpret_cast<float*>(smem + L.rs);
+    const int w = tid / 32;  // TB <= 8 warps: warp t forms r of token t
+    if (w < TB && tok0 + w < M) {
+      const float r = row_rms_scale(hidden + (size_t)(tok0 + w) * H, H, nm.eps, tid % 32);
+      if (tid % 32 == 0) rs[w] = r;
+    }
+    __syncthreads();
+    for (int i = tid; i < TB * CPC * 128; i += kRouteThreads) {
+      const int t = i / (CPC * 128), k = i % (CPC * 128);
+      xs[k * TB + t] = tok0 + t < M ? norm_bits(hidden[(size_t)(tok0 + t) * H + c0 * 128 + k], rs[t], nm.gamma[c0 * 128 + k])
+                                    : (uint16_t)0;
+    }
+  } else {
     for (int i = tid; i < TB * CPC * 128; i += kRouteThreads) {
       const int t = i / (CPC * 128), k = i % (CPC * 128);
       xs[k * TB + t] = tok0 + t < M ? hidden[(size_t)(tok0 + t) * H + c0 * 128 + k] : (uint16_t)0;
@@ -252,6 +272,8 @@ __global__ void __launch_bounds__(kRouteThreads)
 // Top-k: one warp per token, K rounds of a warp argmax over 64-bit keys (order-preserving
 // bits of the logit, then the complement of the expert index: the larger logit wins, ties
 // go to the lower index).
+// With an RMSNorm in front, the CTA first forms r of its 32 tokens (four per warp) and the
+// hidden values become y = bf16((x*r)*gamma) as they are written to the ring.
 // ---------------------------------------------------------------------------------------
 constexpr int kBigTok = 32;
 // packed FP32x2 (sm_100 family): two IEEE round-to-nearest fmas per instruction,
@@ -273,7 +295,7 @@ constexpr int kBigSlots = 4;
 
 __host__ __device__ inline size_t route_big_smem(int E) {
   return 64 + (size_t)kBigSlots * 128 * E * 2 + (size_t)2 * 128 * kBigTok * 4 + (size_t)128 * 8 * (E / 32) * 4 +
-         (size_t)kBigTok * E * 4;
+         (size_t)kBigTok * E * 4 + (size_t)kBigTok * 4;
 }
 
 __device__ __forceinline__ uint64_t logit_key(float v, int e) {
@@ -285,7 +307,7 @@ __device__ __forceinline__ uint64_t logit_key(float v, int e) {
 
 template <int EPT>
 __global__ void __launch_bounds__(256, 1)
-    route_big_kernel(const uint16_t* __restrict__ hidden, const uint16_t* __restrict__ router_w,
+    route_big_kernel(const uint16_t* __restrict__ hidden, const Norm nm, const uint16_t* __restrict__ router_w,
                      const float* __restrict__ bias, int M, int H, int K, int renorm,
                      int32_t* __restrict__ ids, float* __restrict__ wts) {
   constexpr int E = 32 * EPT;
@@ -296,6 +318,7 @@ __global__ void __launch_bounds__(256, 1)
   float* xring = reinterpret_cast<float*>(wring + (size_t)kBigSlots * 128 * E);  // [2][128][32]
   float* xch = xring + 2 * 128 * kBigTok;                                    // [NA][128]
   float* logits = xch + NA * 128;                                            // [32][E]
+  float* rs = logits + kBigTok * E;                                          // [32] RMSNorm r
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int grp = warp & 3, par = warp >> 2;
   const int tok0 = blockIdx.x * kBigTok;
@@ -325,9 +348,18 @@ __global__ void __launch_bounds__(256, 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
 
+  const bool normed = nm.gamma != nullptr;
+  if (normed) {
+    for (int t = warp; t < kBigTok; t += 8) {
+      const float r = tok0 + t < M ? row_rms_scale(hidden + (size_t)(tok0 + t) * H, H, nm.eps, lane) : 0.0f;
+      if (lane == 0) rs[t] = r;
+    }
+    __syncthreads();
+  }
+
   // hidden values of one pair of chunks: 2 x 128 x 32 BF16, four 16-byte loads per thread;
-  // element (cc, k, t) lands at xring[cc][k][t] as FP32
-  uint4 xr[4];
+  // element (cc, k, t) lands at xring[cc][k][t] as FP32 (with the norm weights beside them)
+  uint4 xr[4], gr[4];
   auto load_pair = [&](int p) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -335,6 +367,7 @@ __global__ void __launch_bounds__(256, 1)
       const int cc = g8 >> 4, k8 = (g8 & 15) * 8;
       xr[j] = tok0 + t < M ? *reinterpret_cast<const uint4*>(hidden + (size_t)(tok0 + t) * H + (2 * p + cc) * 128 + k8)
                            : make_uint4(0, 0, 0, 0);
+      if (normed) gr[j] = *reinterpret_cast<const uint4*>(nm.gamma + (2 * p + cc) * 128 + k8);
     }
   };
   auto store_pair = [&]() {
@@ -343,10 +376,13 @@ __global__ void __launch_bounds__(256, 1)
       const int idx = j * 256 + tid, t = idx & 31, g8 = idx >> 5;
       const int cc = g8 >> 4, k8 = (g8 & 15) * 8;
       const uint32_t w4[4] = {xr[j].x, xr[j].y, xr[j].z, xr[j].w};
+      const uint32_t g4[4] = {gr[j].x, gr[j].y, gr[j].z, gr[j].w};
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        xring[((size_t)cc * 128 + k8 + u) * kBigTok + t] =
-            bf16_bits_to_float((uint16_t)((u & 1) ? (w4[u / 2] >> 16) : (w4[u / 2] & 0xFFFF)));
+      for (int u = 0; u < 8; ++u) {
+        const uint16_t xb = (uint16_t)((u & 1) ? (w4[u / 2] >> 16) : (w4[u / 2] & 0xFFFF));
+        const uint16_t gb = (uint16_t)((u & 1) ? (g4[u / 2] >> 16) : (g4[u / 2] & 0xFFFF));
+        xring[((size_t)cc * 128 + k8 + u) * kBigTok + t] = normed ? norm_value(xb, rs[t], gb) : bf16_bits_to_float(xb);
+      }
     }
   };
   load_pair(0);
@@ -503,7 +539,7 @@ int route_cluster(int nchunks) {
 }
 
 template <int TB>
-cudaError_t launch_route_t(const uint16_t* hidden, const uint16_t* router_w, const float* bias, int M,
+cudaError_t launch_route_t(const uint16_t* hidden, Norm nm, const uint16_t* router_w, const float* bias, int M,
                            int H, int E, int K, int renorm, int32_t* ids, float* wts, cudaStream_t st) {
   const int nchunks = H / 128;
   const int CL = route_cluster(nchunks);
@@ -538,15 +574,15 @@ cudaError_t launch_route_t(const uint16_t* hidden, const uint16_t* router_w, con
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   if (stream)
-    return cudaLaunchKernelEx(&cfg, route_kernel<TB, true>, hidden, router_w, bias, M, H, E, K, renorm, ids, wts);
-  return cudaLaunchKernelEx(&cfg, route_kernel<TB, false>, hidden, router_w, bias, M, H, E, K, renorm, ids, wts);
+    return cudaLaunchKernelEx(&cfg, route_kernel<TB, true>, hidden, nm, router_w, bias, M, H, E, K, renorm, ids, wts);
+  return cudaLaunchKernelEx(&cfg, route_kernel<TB, false>, hidden, nm, router_w, bias, M, H, E, K, renorm, ids, wts);
 }
 
 }  // namespace
 
 // Tokens per cluster: 1 for a token or two, 8 (one 16-byte load of token values per k)
 // when there are many and CTA 0's chunk partials [nchunks][8][E] still fit.
-cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const float* bias, int M,
+cudaError_t launch_route(const uint16_t* hidden, Norm nm, const uint16_t* router_w, const float* bias, int M,
                          int H, int E, int K, int renorm, int32_t* ids, float* wts, cudaStream_t st) {
   const int nchunks = H / 128;
   if (M >= 512 && (E == 32 || E == 64 || E == 128) && nchunks % 2 == 0) {
@@ -567,17 +603,17 @@ cudaError_t launch_route(const uint16_t* hidden, const uint16_t* router_w, const
       cudaFuncSetAttribute(route_big_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
       cudaFuncSetAttribute(route_big_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     });
-    auto go = [&](auto kern) { return cudaLaunchKernelEx(&cfg, kern, hidden, router_w, bias, M, H, K, renorm, ids, wts); };
+    auto go = [&](auto kern) { return cudaLaunchKernelEx(&cfg, kern, hidden, nm, router_w, bias, M, H, K, renorm, ids, wts); };
     if (E == 128) return go(route_big_kernel<4>);
     if (E == 64) return go(route_big_kernel<2>);
     return go(route_big_kernel<1>);
   }
   const size_t optin = device_info().smem_optin;
   if (M >= 16 && route_smem(8, nchunks / route_cluster(nchunks), E, nchunks, true).total <= optin)
-    return launch_route_t<8>(hidden, router_w, bias, M, H, E, K, renorm, ids, wts, st);
+    return launch_route_t<8>(hidden, nm, router_w, bias, M, H, E, K, renorm, ids, wts, st);
   if (M >= 4 && route_smem(2, nchunks / route_cluster(nchunks), E, nchunks, true).total <= optin)
-    return launch_route_t<2>(hidden, router_w, bias, M, H, E, K, renorm, ids, wts, st);
-  return launch_route_t<1>(hidden, router_w, bias, M, H, E, K, renorm, ids, wts, st);
+    return launch_route_t<2>(hidden, nm, router_w, bias, M, H, E, K, renorm, ids, wts, st);
+  return launch_route_t<1>(hidden, nm, router_w, bias, M, H, E, K, renorm, ids, wts, st);
 }
 
 }  // namespace moe

@@ -6,6 +6,7 @@
 // The wait gives up, the kernel sets MOE_STATUS_WAIT_TIMEOUT in the workspace's status word
 // and returns, and the context stays usable -- the same path a kernel takes when one of its
 // own waits runs out.
+#include "launch.h"
 #include "tc.cuh"
 
 namespace moe {

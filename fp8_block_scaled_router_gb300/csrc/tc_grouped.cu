@@ -32,6 +32,7 @@
 #include <mutex>
 
 #include "device.h"
+#include "launch.h"
 #include "tc.cuh"
 
 namespace moe {

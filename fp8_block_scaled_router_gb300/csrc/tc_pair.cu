@@ -52,6 +52,7 @@
 
 #include "device.h"
 #include "pair_plan.h"
+#include "launch.h"
 #include "tc.cuh"
 
 namespace cg = cooperative_groups;
@@ -76,6 +77,7 @@ struct PairParams {
   const float* pf_s2;      // gate/up: its scales [E][H/128][I/128]
   uint8_t* qa_out;         // kGateUpFused: the hidden codes it quantised [M][H] (slot 0's
   float* sa_out;           //   CTAs of the first output block write them), scales [M][H/128]
+  Norm nm;                 // kGateUpFused: RMSNorm in front (gamma null: none)
 };
 
 template <int MODE>
@@ -197,11 +199,22 @@ __global__ void __launch_bounds__(kPairThreads, 3)
     }
   } else if (MODE == kGateUpFused) {
     // warps 1..5 quantise the pair's hidden row for this CTA's K blocks straight into the
-    // stage B tiles (row 0; unswizzled in the first 8-row group), the rest into bq
+    // stage B tiles (row 0; unswizzled in the first 8-row group), the rest into bq. With an
+    // RMSNorm in front each of these warps first forms the row's r itself (the whole row,
+    // from L2) and quantises y = bf16((x*r)*gamma).
+    const bool normed = p.nm.gamma != nullptr;
+    const float r = normed ? row_rms_scale(p.hidden + (size_t)tok * p.H, p.H, p.nm.eps, lane) : 0.0f;
     for (int i = warp - 1; i < p.nkb_cta; i += kPairThreads / 32 - 1) {
       const uint2 raw = *reinterpret_cast<const uint2*>(p.hidden + (size_t)tok * p.H + (kb0 + i) * 128 + lane * 4);
-      const float x0 = bf16_bits_to_float(raw.x & 0xFFFF), x1 = bf16_bits_to_float(raw.x >> 16);
-      const float x2 = bf16_bits_to_float(raw.y & 0xFFFF), x3 = bf16_bits_to_float(raw.y >> 16);
+      float x0 = bf16_bits_to_float(raw.x & 0xFFFF), x1 = bf16_bits_to_float(raw.x >> 16);
+      float x2 = bf16_bits_to_float(raw.y & 0xFFFF), x3 = bf16_bits_to_float(raw.y >> 16);
+      if (normed) {
+        const uint2 g = *reinterpret_cast<const uint2*>(p.nm.gamma + (kb0 + i) * 128 + lane * 4);
+        x0 = norm_value(raw.x & 0xFFFF, r, g.x & 0xFFFF);
+        x1 = norm_value(raw.x >> 16, r, g.x >> 16);
+        x2 = norm_value(raw.y & 0xFFFF, r, g.y & 0xFFFF);
+        x3 = norm_value(raw.y >> 16, r, g.y >> 16);
+      }
       float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
@@ -554,7 +567,7 @@ PairParams base_params(int M, int H, int I, int E, int K, const WsPtrs& ws) {
 // weights the next launch will read; each routed expert's block is prefetched into L2.
 cudaError_t launch_pair_gateup(const uint8_t* w13, const float* s13, const int32_t* ids,
                                const uint16_t* hidden, int M, int H, int I, int E, int K,
-                               const WsPtrs& ws, cudaStream_t st, const uint8_t* w2, const float* s2w) {
+                               const WsPtrs& ws, cudaStream_t st, const uint8_t* w2, const float* s2w, Norm nm) {
   CUtensorMap tA, tB;
   if (!make_tmap_u8(&tA, w13, (uint64_t)H, (uint64_t)E * 2 * I, 128)) return cudaErrorInvalidValue;
   PairParams prm = base_params(M, H, I, E, K, ws);
@@ -566,6 +579,7 @@ cudaError_t launch_pair_gateup(const uint8_t* w13, const float* s13, const int32
   prm.hidden = hidden;
   prm.pf_w2 = w2;
   prm.pf_s2 = s2w;
+  prm.nm = nm;
   const int64_t units = (int64_t)M * K * prm.ncb;
   prm.qa_out = ws.qa;
   prm.sa_out = ws.sa;

@@ -110,6 +110,28 @@ moe_status_t moe_route(const void* hidden, const void* router_w, const float* bi
                        const moe_fp8_shape_t* shape, int32_t renormalize, int32_t* topk_ids,
                        float* topk_w, cudaStream_t stream);
 
+/* RMSNorm in front of the layer ([NKL] "Repository layout": gfx950 normalisation and
+ * quantisation fusions; the Qwen3.6 RMSNorm patch listed beside it). The pages fix neither the
+ * epsilon nor the weight convention; this library computes, per token row,
+ *   y[k] = bf16_rn((x[k] * r) * norm_weight[k]),   r = 1 / sqrt(ss / H + eps),
+ * where ss = sum of x[k]^2 in the router's order (an FP32 fma chain over each 128-wide chunk,
+ * k ascending from 0, the chunk partials added in ascending order) and every other step is one
+ * correctly rounded FP32 operation (division by H, + eps, square root, 1 / s, two multiplies).
+ *   hidden       BF16 [M][H] (the un-normalised rows)
+ *   norm_weight  BF16 [H], 16-byte aligned
+ *   eps          finite and > 0 (else MOE_ERR_INVALID_ARG)
+ * The norm entry points below apply this transform inside their own kernels (the router and
+ * the hidden quantisers form r themselves; nothing is written between them) and are otherwise
+ * the calls without "norm": moe_norm_route == moe_route(y), moe_fp8_norm_forward ==
+ * moe_fp8_forward(y), moe_fp8_norm_route_forward == moe_fp8_route_forward(y), bit for bit.
+ * moe_rmsnorm writes y itself (BF16 [M][H], out may not alias hidden) for callers that also
+ * need it. M = 0 is a no-op; M <= shape->max_tokens. */
+moe_status_t moe_rmsnorm(const void* hidden, const void* norm_weight, float eps, int32_t M, void* out,
+                         const moe_fp8_shape_t* shape, cudaStream_t stream);
+moe_status_t moe_norm_route(const void* hidden, const void* norm_weight, float eps, const void* router_w,
+                            const float* bias, int32_t M, const moe_fp8_shape_t* shape, int32_t renormalize,
+                            int32_t* topk_ids, float* topk_w, cudaStream_t stream);
+
 /* The routed expert FFN ([ARCH] accepted M=1 MoE objects: gate/up, SiLU+quant and
  * down/reduce; [NK] prefill-pair section: producer stages plus a separate route reducer
  * with its own fixed reduction order; [AMDK] reduction rule: fixed order, no atomics).
@@ -138,6 +160,14 @@ moe_status_t moe_fp8_forward(const void* hidden, const int32_t* topk_ids, const 
                              void* workspace, size_t workspace_bytes,
                              const moe_fp8_shape_t* shape, cudaStream_t stream);
 
+/* moe_fp8_forward of the RMSNorm'd hidden (see moe_rmsnorm): hidden holds the un-normalised
+ * rows; the gate/up kernel (few routed rows) or the quantiser (many) normalises each row as it
+ * quantises it. The workspace views qa/sa hold the codes of y. */
+moe_status_t moe_fp8_norm_forward(const void* hidden, const void* norm_weight, float eps, const int32_t* topk_ids,
+                                  const float* topk_w, int32_t M, const uint8_t* w13, const float* w13_scale,
+                                  const uint8_t* w2, const float* w2_scale, void* out, void* workspace,
+                                  size_t workspace_bytes, const moe_fp8_shape_t* shape, cudaStream_t stream);
+
 /* Routing and the routed expert FFN in one call: moe_route then moe_fp8_forward, enqueued
  * together (arguments as for those calls; topk_ids / topk_w, device [M][K], receive the
  * routing). Results are those of the two calls. */
@@ -146,6 +176,14 @@ moe_status_t moe_fp8_route_forward(const void* hidden, const void* router_w, con
                                    const float* w2_scale, void* out, int32_t* topk_ids, float* topk_w,
                                    void* workspace, size_t workspace_bytes, const moe_fp8_shape_t* shape,
                                    cudaStream_t stream);
+
+/* moe_fp8_route_forward of the RMSNorm'd hidden: moe_norm_route then moe_fp8_norm_forward
+ * (three launches at decode, as without the norm). */
+moe_status_t moe_fp8_norm_route_forward(const void* hidden, const void* norm_weight, float eps, const void* router_w,
+                                        const float* bias, int32_t M, int32_t renormalize, const uint8_t* w13,
+                                        const float* w13_scale, const uint8_t* w2, const float* w2_scale, void* out,
+                                        int32_t* topk_ids, float* topk_w, void* workspace, size_t workspace_bytes,
+                                        const moe_fp8_shape_t* shape, cudaStream_t stream);
 
 /* The same layer as ONE kernel launch ([NK] prefill-pair section: one producer made of
  * semantic routing, gate/up, SiLU and quantisation, down-partial and metadata stages, with

@@ -10,8 +10,12 @@ Tolerances (written out where they are checked):
   GPU's FP32 block sums (at most 64+16+1 roundings of terms whose magnitudes sum to the
   oracle's gabs/uabs, 81 * 2^-24 < 5e-6) propagated through silu(g)*u and the scale;
 * activation scales: |s - s_oracle| <= 1e-6 * s_oracle + (the same bound on the block max)/448;
-* out: cosine >= 0.9999 and max|out - out_oracle| <= 2e-2 * rms(out_oracle); all-zero
-  oracle rows must be exactly zero.
+* out: cosine >= 0.9999 and, element by element, |out - out_oracle| <= max(2e-2 *
+  rms(out_oracle), one BF16 step at out_oracle); all-zero oracle rows must be exactly zero.
+  The step term is the output's own final rounding: two FP32 sums that differ at all (the
+  tensor core's block sums and the one-rounding promotion differ from the oracle's by
+  design) can round to adjacent BF16 values, and one step of an output above 2.56 * rms is
+  more than 2e-2 * rms. The counts of elements that needed it are printed.
 """
 from __future__ import annotations
 
@@ -99,6 +103,24 @@ def bf16_f64(b):
     return inputs.bf16_bits_to_f32(b).astype(np.float64)
 
 
+def bf16_step(b: np.ndarray) -> np.ndarray:
+    """The spacing of BF16 values at |b| (8 significant bits; normal range)."""
+    a = np.maximum(np.abs(b), 2.0 ** -126)
+    return np.exp2(np.floor(np.log2(a)) - 7)
+
+
+def out_bound_violations(a, b, rms, what):
+    """Elements beyond max(2e-2 * rms, one BF16 step at the oracle's value); prints how many
+    needed the step allowance."""
+    d = np.abs(a - b)
+    over_rms = d > 2e-2 * rms
+    bad = over_rms & (d > bf16_step(b))
+    if over_rms.any() and not bad.any():
+        print(f"out [{what}]: {int(over_rms.sum())} element(s) beyond 2e-2*rms, each within one BF16 step "
+              f"(|out| up to {float(np.max(np.abs(b[over_rms]))) / rms:.2f} rms)")
+    return bad
+
+
 def check_out(out_gpu: np.ndarray, out_orc: np.ndarray, what=""):
     a, b = bf16_f64(out_gpu), bf16_f64(out_orc)
     zero_rows = np.all(b == 0, axis=1)
@@ -108,7 +130,8 @@ def check_out(out_gpu: np.ndarray, out_orc: np.ndarray, what=""):
     rms = float(np.sqrt(np.mean(b * b)))
     maxabs = float(np.max(np.abs(a - b)))
     assert cos >= 0.9999, f"{what}: cosine {cos}"
-    assert maxabs <= 2e-2 * rms, f"{what}: max|d| {maxabs} > 2e-2 * rms {rms}"
+    bad = out_bound_violations(a, b, rms, what)
+    assert not bad.any(), f"{what}: max|d| {maxabs} > max(2e-2 * rms {rms}, one BF16 step)"
     return cos, maxabs / max(rms, 1e-30)
 
 
@@ -158,8 +181,11 @@ def check_out_given_act(out_gpu, out_orc, ws, dbg, ids, w, x, what=""):
     print(f"out [{what}]: cos {cos:.8f}, rms {rms:.4g}; {len(flip_tok)} of {M} tokens have a differing "
           f"activation code; max|d|/rms: other tokens {err_keep / rms:.3e}, those tokens vs the full oracle "
           f"{err_flip_full / rms:.3e}, vs the oracle from the GPU's codes {err_flip_cond / rms:.3e}")
-    assert err_keep <= 2e-2 * rms, f"{what}: max|d| {err_keep} > 2e-2 * rms {rms}"
-    assert err_flip_cond <= 2e-2 * rms, f"{what}: given the GPU's codes, max|d| {err_flip_cond} > 2e-2 * rms"
+    bad_keep = out_bound_violations(a[keep], b[keep], rms, what + ", tokens with the oracle's codes")
+    assert not bad_keep.any(), f"{what}: max|d| {err_keep} > max(2e-2 * rms {rms}, one BF16 step)"
+    if len(flip_tok):
+        bad_flip = out_bound_violations(a[flip_tok], bf16_f64(cond), rms, what + ", given the GPU's codes")
+        assert not bad_flip.any(), f"{what}: given the GPU's codes, max|d| {err_flip_cond} > 2e-2 * rms"
     return cos, max(err_keep, err_flip_cond) / max(rms, 1e-30)
 
 

@@ -119,6 +119,35 @@ def test_stage_and_route_argument_errors(lib):
     assert lib.moe_fp8_workspace_view(FAKE, 0, ctypes.byref(s), ctypes.byref(v)) == 3
 
 
+def test_norm_argument_errors(lib):
+    """The RMSNorm entry points refuse a null or misaligned weight and an eps that is not a
+    finite positive number (eps = 0 would make an all-zero row 0 * inf = NaN)."""
+    s = shape()
+    need = L.moe_fp8_workspace_bytes(s)
+    calls = {
+        "rmsnorm": lambda g, e, M=1: L.moe_rmsnorm(FAKE, g, e, M, FAKE, s, stream=0, check=False),
+        "norm_route": lambda g, e, M=1: L.moe_norm_route(FAKE, g, e, FAKE, None, M, s, 1, FAKE, FAKE, stream=0,
+                                                          check=False),
+        "norm_forward": lambda g, e, M=1: L.moe_fp8_norm_forward(FAKE, g, e, FAKE, FAKE, M, FAKE, FAKE, FAKE, FAKE,
+                                                                  FAKE, FAKE, s, stream=0, ws_bytes=need, check=False),
+        "norm_route_forward": lambda g, e, M=1: L.moe_fp8_norm_route_forward(
+            FAKE, g, e, FAKE, None, M, 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, s, stream=0, ws_bytes=need,
+            check=False),
+    }
+    for name, call in calls.items():
+        for eps in (0.0, -1e-6, float("nan"), float("inf"), float("-inf")):
+            assert call(FAKE, eps) == 1, (name, eps)
+        assert call(0, 1e-6) == 1, name
+        assert call(MIS, 1e-6) == 1, name
+        assert call(FAKE, 1e-6, M=17) == 1, name   # above max_tokens
+        assert call(FAKE, 1e-6, M=0) == 0, name    # no-op after validation
+    assert L.moe_rmsnorm(MIS, FAKE, 1e-6, 1, FAKE, s, stream=0, check=False) == 1
+    assert L.moe_rmsnorm(FAKE, FAKE, 1e-6, 1, 0, s, stream=0, check=False) == 1
+    assert L.moe_rmsnorm(FAKE, FAKE, 1e-6, 1, FAKE, shape(hidden=200), stream=0, check=False) == 2
+    assert L.moe_fp8_norm_forward(FAKE, FAKE, 1e-6, FAKE, FAKE, 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, s, stream=0,
+                                  ws_bytes=need - 1, check=False) == 3
+
+
 def test_zero_tokens_is_a_no_op(lib):
     """M = 0 returns MOE_OK after validation without touching the GPU (fake pointers)."""
     s = shape()
