@@ -79,6 +79,8 @@ def parse():
     p.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
     p.add_argument("--m", type=int, default=None, help="tokens per step (wide sweep)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-threads", type=int, default=None, metavar="N",
+                   help="host threads for the oracle (reference arm and cpu_baseline); default all")
     p.add_argument("--dominant-only", type=int, default=0, metavar="N",
                    help="run only N launches of the dominant kernel (gate/up) and exit, for ncu")
     p.add_argument("--profile-steps", type=int, default=0, metavar="N",
@@ -204,10 +206,11 @@ def dist_info():
 
 
 # ----------------------------------------------------------------------------- oracle arm
-def oracle_tokens_per_s(x, M, budget_s=15.0, max_tokens=None):
-    """Time the oracle (route + FFN) on a bounded sample of tokens on all host cores."""
+def oracle_tokens_per_s(x, M, budget_s=15.0, max_tokens=None, threads=None):
+    """Time the oracle (route + FFN) on a bounded sample of tokens on `threads` host cores
+    (default: all the process may use)."""
     import oracle
-    cores = len(os.sched_getaffinity(0))
+    cores = threads or len(os.sched_getaffinity(0))
     K = x.shape.top_k
     total = x.hidden.shape[0]
 
@@ -243,7 +246,7 @@ def reference_arm(args, wl, world, rank):
                     M=M if wl["cfg"] == "wide" else None)
     steps = args.steps or 3
     warm = args.warmup if args.warmup is not None else 1
-    tps, cores, n, dt = oracle_tokens_per_s(x, M, budget_s=20.0)
+    tps, cores, n, dt = oracle_tokens_per_s(x, M, budget_s=20.0, threads=args.cpu_threads)
     line = {"impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": 0,
             "steps": steps, "warmup": warm, "ms_per_step": 1e3 * M / tps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64-exact block sums, f32 chains",
@@ -424,7 +427,7 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
 
     cpu = None
     if want_cpu:
-        tps, cores, n, dt = oracle_tokens_per_s(x, M, budget_s=cpu_budget_s)
+        tps, cores, n, dt = oracle_tokens_per_s(x, M, budget_s=cpu_budget_s, threads=args.cpu_threads)
         cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"{n} tokens of the same workload (route + expert FFN), {dt:.1f} s, "
                          f"std::thread over tokens"}
