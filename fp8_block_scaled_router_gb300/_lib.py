@@ -28,7 +28,8 @@ EXPORTS = ("moe_fp8_version", "moe_fp8_workspace_bytes", "moe_fp8_workspace_init
            "moe_fp8_forward_noalloc", "moe_fp8_gate_up_direct", "moe_fp8_down_combine",
            "moe_fp8_route_forward_host", "moe_fp8_route_forward_pinned", "moe_fp8_selftest_wait",
            "moe_fp8_route_forward", "moe_fp8_route_forward_one_launch", "moe_rmsnorm", "moe_norm_route",
-           "moe_fp8_norm_forward", "moe_fp8_norm_route_forward")
+           "moe_fp8_norm_forward", "moe_fp8_norm_route_forward", "moe_fp8_verify_produce",
+           "moe_fp8_verify_reduce")
 
 
 class MoEError(RuntimeError):
@@ -86,6 +87,8 @@ def load(path: str = LIB):
             lib.moe_fp8_norm_forward.argtypes = [vp, vp, f32, vp, vp, i32, vp, vp, vp, vp, vp, vp, sz, sp, vp]
             lib.moe_fp8_norm_route_forward.argtypes = [vp, vp, f32, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp,
                                                        sz, sp, vp]
+            lib.moe_fp8_verify_produce.argtypes = [vp, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, sz, sp, vp]
+            lib.moe_fp8_verify_reduce.argtypes = [vp, i32, vp, vp, sz, sp, vp]
             for f in EXPORTS[2:]:
                 if f != "moe_fp8_workspace_bytes":
                     getattr(lib, f).restype = i32
@@ -303,3 +306,20 @@ def moe_fp8_norm_route_forward(hidden, norm_weight, eps, router_w, bias, M, reno
         _ptr(hidden), _ptr(norm_weight), float(eps), _ptr(router_w), _ptr(bias), int(M), int(bool(renormalize)),
         _ptr(w13), _ptr(w13_scale), _ptr(w2), _ptr(w2_scale), _ptr(out), _ptr(topk_ids), _ptr(topk_w),
         _ptr(workspace), nb, ctypes.byref(shape), _stream(stream)), check)
+
+
+def moe_fp8_verify_produce(hidden, router_w, bias, M, renormalize, w13, w13_scale, w2, w2_scale, topk_ids, topk_w,
+                           workspace, shape: Shape, stream=None, ws_bytes=None, check=True):
+    """The verify_m12 producer (routing, gate/up, SiLU+quant, down partials); see include/moe_fp8.h."""
+    nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return _check("moe_fp8_verify_produce", load().moe_fp8_verify_produce(
+        _ptr(hidden), _ptr(router_w), _ptr(bias), int(M), int(bool(renormalize)), _ptr(w13), _ptr(w13_scale),
+        _ptr(w2), _ptr(w2_scale), _ptr(topk_ids), _ptr(topk_w), _ptr(workspace), nb, ctypes.byref(shape),
+        _stream(stream)), check)
+
+
+def moe_fp8_verify_reduce(topk_w, M, out, workspace, shape: Shape, stream=None, ws_bytes=None, check=True):
+    """The verify_m12 route reducer (slot-order combine of the producer's partials)."""
+    nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return _check("moe_fp8_verify_reduce", load().moe_fp8_verify_reduce(
+        _ptr(topk_w), int(M), _ptr(out), _ptr(workspace), nb, ctypes.byref(shape), _stream(stream)), check)

@@ -362,6 +362,35 @@ moe_status_t moe_fp8_norm_route_forward(const void* hidden, const void* norm_wei
                       shape, stream);
 }
 
+moe_status_t moe_fp8_verify_produce(const void* hidden, const void* router_w, const float* bias, int32_t M,
+                                    int32_t renormalize, const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
+                                    const float* w2_scale, int32_t* topk_ids, float* topk_w, void* workspace,
+                                    size_t workspace_bytes, const moe_fp8_shape_t* shape, cudaStream_t stream) {
+  if (moe_status_t st = check_common(shape, M)) return st;
+  for (const void* p : {hidden, router_w, (const void*)w13, (const void*)w13_scale, (const void*)w2,
+                        (const void*)w2_scale, (const void*)topk_ids, (const void*)topk_w})
+    if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (bias && !aligned16(bias)) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  if (!verify_profile(M, shape->hidden, shape->inter, shape->num_experts, shape->top_k)) return MOE_ERR_UNSUPPORTED;
+  if (!verify_capable()) return MOE_ERR_UNSUPPORTED;
+  return launched(launch_verify_produce(static_cast<const uint16_t*>(hidden), static_cast<const uint16_t*>(router_w),
+                                        bias, renormalize ? 1 : 0, topk_ids, topk_w, w13, w13_scale, w2, w2_scale,
+                                        ws_ptrs(workspace, L), stream));
+}
+
+moe_status_t moe_fp8_verify_reduce(const float* topk_w, int32_t M, void* out, void* workspace, size_t workspace_bytes,
+                                   const moe_fp8_shape_t* shape, cudaStream_t stream) {
+  if (moe_status_t st = check_common(shape, M)) return st;
+  if (!topk_w || !out || !aligned16(topk_w) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  if (!verify_profile(M, shape->hidden, shape->inter, shape->num_experts, shape->top_k)) return MOE_ERR_UNSUPPORTED;
+  return launched(launch_combine(topk_w, M, shape->hidden, shape->top_k, static_cast<uint16_t*>(out),
+                                 ws_ptrs(workspace, L), stream));
+}
+
 moe_status_t moe_fp8_route_forward_one_launch(const void* hidden, const void* router_w, const float* bias,
                                               int32_t M, int32_t renormalize, const uint8_t* w13,
                                               const float* w13_scale, const uint8_t* w2, const float* w2_scale,

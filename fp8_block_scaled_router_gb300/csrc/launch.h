@@ -44,4 +44,12 @@ cudaError_t launch_fused(bool route, const uint16_t* hidden, const uint16_t* rou
                          const uint8_t* w2, const float* s2w, uint16_t* out, int M, int H, int I, int E, int K,
                          const WsPtrs& ws, float* yt, uint32_t* tickets, cudaStream_t st);
 
+// verify.cu: the verify_m12 profile's producer (routing, gate/up, SiLU and quantisation,
+// down partials y in pair order, identity permutation) -- the reducer is launch_combine
+bool verify_profile(int M, int H, int I, int E, int K);
+bool verify_capable();
+cudaError_t launch_verify_produce(const uint16_t* hidden, const uint16_t* router_w, const float* bias, int renorm,
+                                  int32_t* ids, float* wts, const uint8_t* w13, const float* s13, const uint8_t* w2,
+                                  const float* s2w, const WsPtrs& ws, cudaStream_t st);
+
 }  // namespace moe

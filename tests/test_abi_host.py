@@ -148,6 +148,38 @@ def test_norm_argument_errors(lib):
                                   ws_bytes=need - 1, check=False) == 3
 
 
+def test_verify_exact_batch_guard(lib):
+    """The verify producer and reducer compile one profile (12 tokens, h2048 i768 e128 top-8):
+    any other batch or shape is refused on the host before any launch."""
+    s = shape()
+    need = L.moe_fp8_workspace_bytes(s)
+
+    def produce(M, sh=s, nb=need, **bad):
+        a = dict(hidden=FAKE, router_w=FAKE, bias=None, w13=FAKE, w13_scale=FAKE, w2=FAKE, w2_scale=FAKE,
+                 topk_ids=FAKE, topk_w=FAKE)
+        a.update(bad)
+        return L.moe_fp8_verify_produce(a["hidden"], a["router_w"], a["bias"], M, 1, a["w13"], a["w13_scale"], a["w2"],
+                                        a["w2_scale"], a["topk_ids"], a["topk_w"], FAKE, sh, stream=0, ws_bytes=nb,
+                                        check=False)
+
+    for M in (0, 1, 11, 13, 16):
+        assert produce(M) == 2, M
+        assert L.moe_fp8_verify_reduce(FAKE, M, FAKE, FAKE, s, stream=0, ws_bytes=need, check=False) == 2, M
+    for kw in (dict(hidden=4096), dict(inter=1024), dict(num_experts=64), dict(top_k=4)):
+        s2 = shape(**kw)
+        n2 = L.moe_fp8_workspace_bytes(s2)
+        assert produce(12, s2, n2) == 2, kw
+        assert L.moe_fp8_verify_reduce(FAKE, 12, FAKE, FAKE, s2, stream=0, ws_bytes=n2, check=False) == 2, kw
+    assert produce(12, shape(max_tokens=8), L.moe_fp8_workspace_bytes(shape(max_tokens=8))) == 1  # M > max_tokens
+    for name in ("hidden", "router_w", "w13", "w13_scale", "w2", "w2_scale", "topk_ids", "topk_w"):
+        assert produce(12, **{name: 0}) == 1, name
+        assert produce(12, **{name: MIS}) == 1, name
+    assert produce(12, bias=MIS) == 1
+    assert produce(12, nb=need - 1) == 3
+    assert L.moe_fp8_verify_reduce(0, 12, FAKE, FAKE, s, stream=0, ws_bytes=need, check=False) == 1
+    assert L.moe_fp8_verify_reduce(FAKE, 12, MIS, FAKE, s, stream=0, ws_bytes=need, check=False) == 1
+
+
 def test_zero_tokens_is_a_no_op(lib):
     """M = 0 returns MOE_OK after validation without touching the GPU (fake pointers)."""
     s = shape()
