@@ -64,10 +64,18 @@ WORKLOADS = {
 
 # routed rows up to which moe_fp8_forward runs the two pair kernels
 PAIR_ROWS = 64
-def launches_per_step(M, K, H, E):
+def launches_per_step(M, K, H, E, two_op=False):
     """Our kernels per step: route, gate/up, down+combine up to PAIR_ROWS routed rows;
-    otherwise route, count+quantise, scatter, gather, gate/up, down, combine."""
+    otherwise route, count+quantise, scatter, gather, gate/up, down, combine; the verify
+    profile's producer and reducer when `two_op`."""
+    if two_op:
+        return 2
     return 3 if M * K <= PAIR_ROWS else 7
+
+
+def verify_profile(M, H, I, E, K):
+    """The batch and shape the two-operation verify entry points are compiled for."""
+    return (M, H, I, E, K) == (12, 2048, 768, 128, 8)
 
 
 def parse():
@@ -86,6 +94,10 @@ def parse():
     p.add_argument("--profile-steps", type=int, default=0, metavar="N",
                    help="run N eager steps of the workload after 3 warm-up steps and exit, for a profiler's "
                         "launch list")
+    p.add_argument("--no-verify", action="store_true",
+                   help="leave the verify M=12 record out of the decode line")
+    p.add_argument("--verify-route-forward", action="store_true",
+                   help="verify workloads through moe_fp8_route_forward instead of the producer + reducer")
     p.add_argument("--no-prefill", action="store_true",
                    help="decode only: leave out the prefill record of the same line")
     p.add_argument("--clock-soak", type=float, default=1.0, metavar="S",
@@ -298,11 +310,17 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
     wts = torch.empty((nbatches, M, K), dtype=torch.float32, device="cuda")
     out = torch.empty((nbatches, M, H), dtype=torch.int16, device="cuda")
 
+    two_op = given_ids is None and verify_profile(M, H, I, E, K) and not args.verify_route_forward
+
     def step(i, stream=None):
         b = i % nbatches
         hid = hidden_all[b * M:(b + 1) * M]
         w13, s13, w2, s2 = reps[i % n_rep]
-        if given_ids is not None:   # Zipf workload: the expert load is given, not routed
+        if two_op:                  # the verify profile's two operations: producer, route reducer
+            L.moe_fp8_verify_produce(hid, router, bias, M, True, w13, s13, w2, s2, ids[b], wts[b], ws, shape,
+                                     stream=stream)
+            L.moe_fp8_verify_reduce(wts[b], M, out[b], ws, shape, stream=stream)
+        elif given_ids is not None:   # Zipf workload: the expert load is given, not routed
             L.moe_route(hid, router, bias, M, shape, True, ids[b], wts[b], stream=stream)
             ii, ww = given_ids
             L.moe_fp8_forward(hid, ii, ww, M, w13, s13, w2, s2, out[b], ws, shape, stream=stream)
@@ -310,7 +328,7 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
             L.moe_fp8_route_forward(hid, router, bias, M, True, w13, s13, w2, s2, out[b], ids[b], wts[b], ws,
                                     shape, stream=stream)
 
-    kernels_per_step = launches_per_step(M, K, H, E)
+    kernels_per_step = launches_per_step(M, K, H, E, two_op)
 
     # distinct experts per step (accounting only)
     for i in range(min(nbatches, 64)):
@@ -386,9 +404,14 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
     value = replicas.throughput(world, steps, M, elapsed)
     ms_per_step = 1e3 * elapsed / steps
 
-    roof = dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, given_ids, ids, ws, shape,
-                           prefill, gu_bytes, gu_flops)
-    roof["traffic"] = recorded_traffic("gate_up", "prefill" if prefill else args.workload)
+    if two_op:
+        roof = producer_kernel(L, torch, M, nbatches, hidden_all, reps, n_rep, router, bias, ids, wts, ws, shape,
+                               alg_bytes - M * H * 2)
+        roof["traffic"] = recorded_traffic("verify_produce", "verify")
+    else:
+        roof = dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, given_ids, ids, ws, shape,
+                               prefill, gu_bytes, gu_flops)
+        roof["traffic"] = recorded_traffic("gate_up", "prefill" if prefill else args.workload)
 
     # ---- end to end through the public API with host buffers
     e2e_steps = min(steps * max(1, n_soak), 3000 if decode else (500 if M <= 64 else 10))
@@ -405,6 +428,14 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
     for i in range(e2e_steps):
         b = i % nbatches
         w13, s13, w2, s2 = reps[i % n_rep]
+        if two_op:
+            hid = stage[i % 2]
+            hid.copy_(host_in[b], non_blocking=True)
+            L.moe_fp8_verify_produce(hid, router, bias, M, True, w13, s13, w2, s2, ids[b], wts[b], ws, shape,
+                                     stream=cs)
+            L.moe_fp8_verify_reduce(wts[b], M, out[b], ws, shape, stream=cs)
+            host_out[b].copy_(out[b], non_blocking=True)
+            continue
         if given_ids is None:
             # the public host-buffer call: hidden read from and out written to pinned host
             # memory by the kernels, route + forward, enqueued by one call
@@ -433,6 +464,9 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
                          f"std::thread over tokens"}
     rec = {"value": value, "unit": "tokens/s", "steps": steps, "warmup": warm, "ms_per_step": ms_per_step,
            "config": {"workload": wl["desc"], "M": M, "hidden": H, "inter": I, "experts": E, "top_k": K,
+                      "entry": ("moe_fp8_verify_produce + moe_fp8_verify_reduce" if two_op else
+                                "moe_route + moe_fp8_forward (ids given)" if given_ids is not None else
+                                "moe_fp8_route_forward"),
                       "distinct_experts_per_step": distinct,
                       "l2": f"inputs larger than L2: {n_rep} weight replicas "
                             f"({n_rep * (x.w13.nbytes + x.w2.nbytes) / 1e9:.2f} GB) rotated per step",
@@ -500,6 +534,39 @@ def dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, giv
     return roof
 
 
+def producer_kernel(L, torch, M, nbatches, hidden_all, reps, n_rep, router, bias, ids, wts, ws, shape, prod_bytes):
+    """The verify producer alone (routing, gate/up, SiLU+quant, down partials: the whole
+    weight stream of the step), back to back in a CUDA graph on its own stream."""
+    n_k = 100
+    ks = torch.cuda.Stream()
+    ks.wait_stream(torch.cuda.current_stream())
+
+    def pr(i, st):
+        b = i % nbatches
+        w13, s13, w2, s2 = reps[i % n_rep]
+        L.moe_fp8_verify_produce(hidden_all[b * M:(b + 1) * M], router, bias, M, True, w13, s13, w2, s2, ids[b],
+                                 wts[b], ws, shape, stream=st)
+
+    with torch.cuda.stream(ks):
+        pr(0, ks)
+        kg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(kg, stream=ks):
+            for i in range(n_k):
+                pr(i, ks)
+        kg.replay()
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k0.record(ks)
+        for _ in range(3):
+            kg.replay()
+        k1.record(ks)
+    ks.synchronize()
+    t = k0.elapsed_time(k1) / 1e3 / (3 * n_k)
+    hbm, _, _, peak_src = load_peaks()
+    return {"bound": "hbm", "kernel": "verify_produce", "achieved": prod_bytes / t / 1e9, "peak": hbm, "unit": "GB/s",
+            "frac": prod_bytes / t / 1e9 / hbm, "peak_source": f"{peak_src} hbm_gbs", "alg_per_launch": prod_bytes,
+            "mean_launch_us": t * 1e6}
+
+
 def gpu_selector(torch):
     props = torch.cuda.get_device_properties(torch.cuda.current_device())
     uuid = str(getattr(props, "uuid", ""))
@@ -530,15 +597,21 @@ def ours_arm(args, wl, world, rank, local):
     want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
     rec = run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, 12.0)
     # the metric's other half: prefill (M=4096) in the same run and the same line
-    pre = None
+    pre = ver = None
+    if args.workload == "decode" and not args.no_verify:
+        vsteps = args.steps or 20000
+        ver = run_workload(args, WORKLOADS["verify"], vsteps, max(3, warm), world, rank, dist, want_cpu, 8.0)
     if args.workload == "decode" and not args.no_prefill:
-        pre = run_workload(args, WORKLOADS["prefill"], steps, warm, world, rank, dist, want_cpu, 12.0)
+        psteps = args.steps or 2500
+        pre = run_workload(args, WORKLOADS["prefill"], psteps, max(3, warm), world, rank, dist, want_cpu, 12.0)
     if rank == 0:
         line = {"metric": METRIC, "value": rec["value"], "unit": "tokens/s", "n_gpus": world,
                 "steps": steps, "warmup": warm, "ms_per_step": rec["ms_per_step"], "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 (f32 accumulate)",
                 "data": "synthetic"}
         line.update({k: v for k, v in rec.items() if k not in ("value", "unit", "steps", "warmup", "ms_per_step")})
+        if ver is not None:
+            line["verify"] = ver
         if pre is not None:
             line["prefill"] = pre
         print(json.dumps(line), flush=True)

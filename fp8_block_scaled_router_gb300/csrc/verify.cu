@@ -30,11 +30,13 @@
 //     each K block's sums (P_kb * (sa_kb * sw_kb), multiply then add, kb ascending from 0),
 //     applies silu(g) * u, requantises each routed token's 128 values (scale = amax/448) and
 //     writes the codes and scale of that pair (row t*8 + slot) to the workspace.
-//   * down: when all 16 CTAs of the cluster have written their activation blocks (each
-//     arrives, releasing at cluster scope, on an mbarrier of every CTA), CTA r runs output
-//     block r (128 rows) of every expert of the cluster: B = the routed tokens' activation
-//     rows, gathered from the workspace into shared memory; y = sum over the 6 K blocks
-//     ascending of P_kb * (s2_kb * sw2_kb); each routed pair's y goes to the workspace.
+//   * down: CTA r runs output block r (128 rows) of every expert of the cluster, each as soon
+//     as the expert's 6 activation blocks are written (the CTA of each block arrives,
+//     releasing at cluster scope, on that expert's mbarrier in every CTA): B = the routed
+//     tokens' activation rows, gathered from the workspace into shared memory; y = sum over
+//     the 6 K blocks ascending of P_kb * (s2_kb * sw2_kb); each routed pair's y goes to the
+//     workspace. A CTA that finishes its gate/up units early starts on the down blocks of
+//     the experts already complete.
 // The reducer then forms out[t] = bf16(sum over slots ascending of w[t][j] * y[t*8 + j]).
 // The arithmetic is that of the few-row pair kernels (moe_fp8_gate_up_direct +
 // moe_fp8_down_combine), so outputs are bitwise theirs.
@@ -83,18 +85,18 @@ struct VerifyParams {
 };
 
 // Shared memory (offsets from the 1024-aligned base).
-//   ring     kVSlots x 32 KB (two weight tiles per slot; first the CTA's router chunk)
+//   ring     kVSlots x 32 KB (two weight tiles per slot; before the weights: the CTA's router
+//            chunk in [0, 32 KB) and the 12 hidden rows (BF16) in [32 KB, 80 KB))
 //   hid      16 x 2 KB hidden B tiles (row t = token t's codes of K block kb, rows 12..15 0)
 //   acttile  2 x 6 x 2 KB down B tiles (one expert's activation rows), aliased before the
-//            down phase by xs (12 x 128 f32 hidden values of chunk r) and own (12 x 128 f32
-//            chain partials of chunk r, staged for the copies)
+//            down phase by own (12 x 128 f32 chain partials of chunk r, staged for the copies)
 //   part     16 x 128 f32 (token t's chunk partials, owner CTA t)
 //   misc     logits, selection, routes, bias, scales, metadata
 constexpr size_t kVoRing = 0;
 constexpr size_t kVoHid = kVoRing + (size_t)kVSlots * 2 * kVTile;
 constexpr size_t kVoAct = kVoHid + (size_t)kVNkh * 2048;
-constexpr size_t kVoXs = kVoAct;
-constexpr size_t kVoOwn = kVoAct + (size_t)kVM * 128 * 4;
+constexpr size_t kVoHs = kVoRing + (size_t)2 * kVTile;  // the hidden rows, in ring slot 1
+constexpr size_t kVoOwn = kVoAct;
 constexpr size_t kVoPart = kVoAct + (size_t)2 * kVNu * 2048;
 constexpr size_t kVoLogits = kVoPart + (size_t)kVCL * 128 * 4;
 constexpr size_t kVoSel = kVoLogits + 128 * 4;            // sel_v [16] f32, sel_i [16] i32
@@ -112,9 +114,10 @@ constexpr size_t kVoE2l = kVoDist + 128 * 4;                  // [128] i32 exper
 constexpr size_t kVoWcnt = kVoE2l + 128 * 4;                  // [4] i32 + n_dist
 constexpr size_t kVoSlot = kVoWcnt + 8 * 4;                   // [96][12] i8 slot of token t
 constexpr size_t kVoBars = (kVoSlot + (size_t)kVR * kVM + 15) & ~size_t(15);
-constexpr int kVNumBars = 2 * kVSlots + 16 + 16 + 3 + 1 + 2 + 2;
+constexpr int kVNumBars = 2 * kVSlots + 16 + 16 + 4 + kVMaxDn + 2 + 2;
 constexpr size_t kVSmem = kVoBars + (size_t)kVNumBars * 8 + 16 + 1024;  // + alignment slack
-static_assert(kVoOwn + (size_t)kVM * 128 * 4 <= kVoPart, "xs and own fit in the down tiles");
+static_assert(kVoOwn + (size_t)kVM * 128 * 4 <= kVoPart, "own fits in the down tiles");
+static_assert(kVoHs + (size_t)kVM * kVH * 2 <= kVoHid, "the hidden rows fit in the ring");
 
 // Byte offset of 16-byte chunk c of row r in a K-major tile of 128-byte rows with the
 // 128-byte swizzle (8-row atoms of 1024 bytes; chunk c of row r sits at c ^ (r % 8)).
@@ -133,7 +136,7 @@ __global__ void __launch_bounds__(kVThreads, 1)
   unsigned char* ring = base + kVoRing;
   unsigned char* hid = base + kVoHid;
   unsigned char* acttile = base + kVoAct;
-  float* xs = reinterpret_cast<float*>(base + kVoXs);
+  const uint16_t* hs = reinterpret_cast<const uint16_t*>(base + kVoHs);
   float* own = reinterpret_cast<float*>(base + kVoOwn);
   float* part = reinterpret_cast<float*>(base + kVoPart);
   float* logits = reinterpret_cast<float*>(base + kVoLogits);
@@ -160,10 +163,11 @@ __global__ void __launch_bounds__(kVThreads, 1)
   uint64_t* accf2 = acce + 8;              // [8] down TMEM buffer written
   uint64_t* acce2 = accf2 + 8;             // [8] down TMEM buffer read
   uint64_t* rbar = acce2 + 8;              // this CTA's router chunk has landed
-  uint64_t* part_full = rbar + 1;          // token rank's 16 chunk partials are here
+  uint64_t* hbar = rbar + 1;               // the hidden rows have landed
+  uint64_t* part_full = hbar + 1;          // token rank's 16 chunk partials are here
   uint64_t* routes_full = part_full + 1;   // all 12 routes are here
-  uint64_t* gu_done = routes_full + 1;     // every CTA of the cluster wrote its activation blocks
-  uint64_t* act_ready = gu_done + 1;       // [2] an expert's down B tiles and scales are built
+  uint64_t* eready = routes_full + 1;      // [kVMaxDn] all 6 activation blocks of expert ie are written
+  uint64_t* act_ready = eready + kVMaxDn;  // [2] an expert's down B tiles and scales are built
   uint64_t* act_free = act_ready + 2;      // [2] ... and no longer read (MMA + epilogue)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(act_free + 2);
 
@@ -187,9 +191,10 @@ __global__ void __launch_bounds__(kVThreads, 1)
       tc::mbar_init(&acce2[b], 4);
     }
     tc::mbar_init(rbar, 1);
+    tc::mbar_init(hbar, 1);
     tc::mbar_init(part_full, 1);
     tc::mbar_init(routes_full, 1);
-    tc::mbar_init(gu_done, kVCL);
+    for (int i = 0; i < kVMaxDn; ++i) tc::mbar_init(&eready[i], kVNu);  // one arrival per gate/up unit
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&act_ready[b], 1);
       tc::mbar_init(&act_free[b], 2);
@@ -202,6 +207,9 @@ __global__ void __launch_bounds__(kVThreads, 1)
     const uint32_t chunk = 128u * kVE * 2u;
     tc::mbar_arrive_expect_tx(rbar, chunk);
     tc::bulk_load(ring, p.router_w + (size_t)rank * 128 * kVE, chunk, rbar);
+    constexpr uint32_t hbytes = (uint32_t)kVM * kVH * 2u;
+    tc::mbar_arrive_expect_tx(hbar, hbytes);
+    tc::bulk_load(base + kVoHs, p.hidden, hbytes, hbar);
   }
   for (int e = tid; e < kVE; e += kVThreads) bias_s[e] = p.bias != nullptr ? p.bias[e] : 0.0f;
   if (warp == 1) {
@@ -213,41 +221,26 @@ __global__ void __launch_bounds__(kVThreads, 1)
     reinterpret_cast<uint4*>(hid + (size_t)(i / 32) * 2048 + 1536)[i % 32] = make_uint4(0, 0, 0, 0);
   tc::cluster_arrive();  // every CTA's barriers are initialised before anyone signals them
 
-  // ---- the hidden rows: codes per 128 columns into the B tiles (row t of tile kb), the
-  // scales, and the FP32 values of chunk `rank` for the router. Warp w takes the (token,
-  // K block) groups w, w + 8, ...; four groups' loads are in flight at once.
-  for (int g0 = warp; g0 < kVM * kVNkh; g0 += 32) {
-    uint2 raw[4];
+  // ---- the hidden rows (one bulk copy into the ring): codes per 128 columns into the B tiles
+  // (row t of tile kb) and the scales. Warp w takes the (token, K block) groups w, w + 8, ...
+  if (!tc::mbar_wait(hbar, 0)) ok = false;
+  for (int g = warp; g < kVM * kVNkh; g += 8) {
+    const int t = g / kVNkh, kb = g % kVNkh;
+    const uint2 raw = *reinterpret_cast<const uint2*>(hs + t * kVH + kb * 128 + lane * 4);
+    const float x0 = bf16_bits_to_float(raw.x & 0xFFFF), x1 = bf16_bits_to_float(raw.x >> 16);
+    const float x2 = bf16_bits_to_float(raw.y & 0xFFFF), x3 = bf16_bits_to_float(raw.y >> 16);
+    float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int g = g0 + 8 * q;
-      if (g < kVM * kVNkh)
-        raw[q] = *reinterpret_cast<const uint2*>(p.hidden + (size_t)(g / kVNkh) * kVH + (g % kVNkh) * 128 + lane * 4);
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int g = g0 + 8 * q;
-      if (g >= kVM * kVNkh) break;
-      const int t = g / kVNkh, kb = g % kVNkh;
-      const float x0 = bf16_bits_to_float(raw[q].x & 0xFFFF), x1 = bf16_bits_to_float(raw[q].x >> 16);
-      const float x2 = bf16_bits_to_float(raw[q].y & 0xFFFF), x3 = bf16_bits_to_float(raw[q].y >> 16);
-      if (kb == rank) {
-        float* d = xs + t * 128 + lane * 4;
-        d[0] = x0; d[1] = x1; d[2] = x2; d[3] = x3;
-      }
-      float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-      const float sc = quant_scale(amax);
-      const uint32_t lo = e4m3x2_encode(__fdiv_rn(x0, sc), __fdiv_rn(x1, sc));
-      const uint32_t hi = e4m3x2_encode(__fdiv_rn(x2, sc), __fdiv_rn(x3, sc));
-      const uint32_t codes = lo | (hi << 16);
-      *reinterpret_cast<uint32_t*>(hid + (size_t)kb * 2048 + sw128_off(t, lane >> 2) + (lane & 3) * 4) = codes;
-      if (lane == 0) sa_s[t * kVNkh + kb] = sc;
-      if (cid == 0 && rank == 0) {  // the workspace view of the hidden codes and scales
-        reinterpret_cast<uint32_t*>(p.ws.qa + (size_t)t * kVH + kb * 128)[lane] = codes;
-        if (lane == 0) p.ws.sa[t * kVNkh + kb] = sc;
-      }
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float sc = quant_scale(amax);
+    const uint32_t lo = e4m3x2_encode(__fdiv_rn(x0, sc), __fdiv_rn(x1, sc));
+    const uint32_t hi = e4m3x2_encode(__fdiv_rn(x2, sc), __fdiv_rn(x3, sc));
+    const uint32_t codes = lo | (hi << 16);
+    *reinterpret_cast<uint32_t*>(hid + (size_t)kb * 2048 + sw128_off(t, lane >> 2) + (lane & 3) * 4) = codes;
+    if (lane == 0) sa_s[t * kVNkh + kb] = sc;
+    if (cid == 0 && rank == 0) {  // the workspace view of the hidden codes and scales
+      reinterpret_cast<uint32_t*>(p.ws.qa + (size_t)t * kVH + kb * 128)[lane] = codes;
+      if (lane == 0) p.ws.sa[t * kVNkh + kb] = sc;
     }
   }
   tc::fence_proxy_async_smem();  // generic writes of the B tiles before the tensor core reads them
@@ -270,7 +263,7 @@ __global__ void __launch_bounds__(kVThreads, 1)
       const uint64_t wp = tc::f2pack(w << 16, w & 0xFFFF0000u);  // bf16 -> f32: (expert 2e2, 2e2+1)
 #pragma unroll
       for (int q = 0; q < 3; ++q) {
-        const uint32_t xb = __float_as_uint(xs[(tq + 4 * q) * 128 + k]);
+        const uint32_t xb = (uint32_t)hs[(tq + 4 * q) * kVH + rank * 128 + k] << 16;  // bf16 -> f32
         acc[q] = tc::f2fma(tc::f2pack(xb, xb), wp, acc[q]);
       }
     }
@@ -542,12 +535,13 @@ __global__ void __launch_bounds__(kVThreads, 1)
         p.ws.act[(size_t)pr * kVI + cb * 128 + row] = (uint8_t)(e4m3x2_encode(__fdiv_rn(act[t], s2), 0.0f) & 0xFF);
         if (row == 0) p.ws.act_scale[pr * kVNu + cb] = s2;
       }
-      tc::named_bar(1, 128);  // red is rewritten by the next unit
+      // every CTA of the cluster learns that this block of expert ie is written (red is
+      // rewritten by the next unit only after this barrier too)
+      __threadfence();
+      tc::named_bar(1, 128);
+      if (row < kVCL)
+        tc::mbar_arrive_cluster(tc::mapa(tc::smem_u32(&eready[(rank + kVCL * n) / kVNu]), (uint32_t)row));
     }
-    // every CTA of the cluster learns that this CTA's activation blocks are written
-    __threadfence();
-    tc::named_bar(1, 128);
-    if (row < kVCL) tc::mbar_arrive_cluster(tc::mapa(tc::smem_u32(gu_done), (uint32_t)row));
     for (int ie = 0; ie < ne; ++ie) {
       const int el = cid + ie * p.nc, ab = ie & 1;
       if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(&act_ready[ab], (ie >> 1) & 1));
@@ -583,25 +577,40 @@ __global__ void __launch_bounds__(kVThreads, 1)
       if (row == 0) tc::mbar_arrive(&act_free[ab]);
     }
   } else {
-    // ---- down B tiles: once every CTA of the cluster has written its activation blocks,
-    // each expert's routed activation rows (row t = token t's pair, other rows 0) and scales
+    // ---- down B tiles: once the 6 activation blocks of expert ie are written (by whichever
+    // CTAs of the cluster ran them), its routed activation rows (row t = token t's pair, other
+    // rows 0) and scales; all loads of an expert are issued before its stores
     const int ht = tid - 192;  // 0..63
-    if (ne > 0 && ok) ok = __all_sync(0xffffffffu, tc::mbar_wait_cluster(gu_done, 0));
+    constexpr int kPer = 16 * kVNu * 8 / 64;  // 16-byte chunks per thread and expert
     for (int ie = 0; ie < ne; ++ie) {
       const int el = cid + ie * p.nc, ab = ie & 1;
+      if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait_cluster(&eready[ie], 0));
       if (ie >= 2 && ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(&act_free[ab], ((ie - 2) >> 1) & 1));
       unsigned char* tiles = acttile + (size_t)ab * kVNu * 2048;
-      for (int x = ht; x < 16 * kVNu * 8; x += 64) {  // (row, K block, 16-byte chunk)
-        const int r = x / (kVNu * 8), kb = (x / 8) % kVNu, c = x % 8;
+      uint4 v[kPer];
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {  // (row, K block, 16-byte chunk)
+        const int x = ht + 64 * i, r = x / (kVNu * 8), kb = (x / 8) % kVNu, c = x % 8;
         const int j = r < kVM ? tslot[el * kVM + r] : -1;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (j >= 0) v = __ldcg(reinterpret_cast<const uint4*>(p.ws.act + (size_t)(r * kVK + j) * kVI + kb * 128) + c);
-        *reinterpret_cast<uint4*>(tiles + (size_t)kb * 2048 + sw128_off(r, c)) = v;
+        v[i] = make_uint4(0, 0, 0, 0);
+        if (j >= 0) v[i] = __ldcg(reinterpret_cast<const uint4*>(p.ws.act + (size_t)(r * kVK + j) * kVI + kb * 128) + c);
       }
-      for (int x = ht; x < kVM * kVNu; x += 64) {
-        const int t = x / kVNu, kb = x % kVNu;
-        const int j = tslot[el * kVM + t];
-        asc_s[(ab * kVM + t) * 8 + kb] = j >= 0 ? __ldcg(p.ws.act_scale + (t * kVK + j) * kVNu + kb) : 0.0f;
+      float sv[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int x = ht + 64 * i, t = x / kVNu, kb = x % kVNu;
+        const int j = x < kVM * kVNu ? tslot[el * kVM + t] : -1;
+        sv[i] = j >= 0 ? __ldcg(p.ws.act_scale + (t * kVK + j) * kVNu + kb) : 0.0f;
+      }
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int x = ht + 64 * i, r = x / (kVNu * 8), kb = (x / 8) % kVNu, c = x % 8;
+        *reinterpret_cast<uint4*>(tiles + (size_t)kb * 2048 + sw128_off(r, c)) = v[i];
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int x = ht + 64 * i, t = x / kVNu, kb = x % kVNu;
+        if (x < kVM * kVNu) asc_s[(ab * kVM + t) * 8 + kb] = sv[i];
       }
       tc::fence_proxy_async_smem();  // generic writes of the B tiles before the tensor core reads them
       tc::named_bar(2, 64);
