@@ -646,11 +646,15 @@ def profile_steps(args, wl):
     ids = torch.empty((M, K), dtype=torch.int32, device="cuda")
     w = torch.empty((M, K), dtype=torch.float32, device="cuda")
     out = torch.empty((M, H), dtype=torch.int16, device="cuda")
+    two_op = x.ids is None and verify_profile(M, H, I, E, K) and not args.verify_route_forward
     for i in range(n):
         b = i % (hid_all.shape[0] // M)
         hid = hid_all[b * M:(b + 1) * M]
         w13, s13, w2, s2 = reps[i % 2]
-        if x.ids is not None:
+        if two_op:
+            L.moe_fp8_verify_produce(hid, router, bias, M, True, w13, s13, w2, s2, ids, w, ws, shape)
+            L.moe_fp8_verify_reduce(w, M, out, ws, shape)
+        elif x.ids is not None:
             L.moe_route(hid, router, bias, M, shape, True, ids, w)
             L.moe_fp8_forward(hid, dev(x.ids), dev(x.weights), M, w13, s13, w2, s2, out, ws, shape)
         else:

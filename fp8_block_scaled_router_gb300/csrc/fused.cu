@@ -124,7 +124,7 @@ __host__ __device__ inline FusedSmem fused_smem(int nst, int M, int H, int I, in
   s.seq = o;     o += fused_align((size_t)U * (s.cpc + s.hpc) * 4, 16);
   s.sc = o;      o += 128 + (size_t)(U * s.cpc * 2 + U * s.hpc + M * s.cpc + U + E + 8) * 4 + (size_t)M * K * 8;
   o = fused_align(o, 16);
-  s.bars = o;    o += (size_t)(2 * nst + 27 + 2 * U) * 8 + 16;
+  s.bars = o;    o += (size_t)(2 * nst + 28 + 2 * U) * 8 + 16;
   s.total = o + 1024;  // alignment slack of the dynamic shared memory base
   return s;
 }
@@ -191,7 +191,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   uint64_t* terms_full = hid_ready + 1;    // [U] every K block's terms of the unit are here
   uint64_t* act_full = terms_full + Umax;  // [U] the unit's activation codes are here
   uint64_t* rbar = act_full + Umax;        // this CTA's router chunks have landed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rbar + 1);
+  uint64_t* drainb = rbar + 1;             // every MMA this CTA issued has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drainb + 1);
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int rank = (int)tc::cluster_rank();
@@ -218,6 +219,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     tc::mbar_init(part_full, 1);
     tc::mbar_init(hid_ready, 1);
     tc::mbar_init(rbar, 1);
+    tc::mbar_init(drainb, 1);
     for (int i = 0; i < Umax; ++i) {
       tc::mbar_init(&terms_full[i], 1);
       tc::mbar_init(&act_full[i], 1);
@@ -426,6 +428,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           n += 1;
         }
       }
+      // no load is still writing when the CTA leaves: the last phase of each stage issued has
+      // completed (a no-op unless a wait gave up)
+      for (int j = n - 1; j >= 0 && j >= n - NS; --j)
+        if (!tc::mbar_wait(&full[j % NS], (j / NS) & 1)) ok = false;
     }
   } else if (warp == 1) {
     // ---- MMA issue in piece order: gate/up into 32-column buffers (gate 0..15, up 16..31),
@@ -481,6 +487,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           ++nd;
         }
       }
+      // every arrival the MMAs owe this CTA's barriers has landed before the CTA can leave
+      tc::mma_commit(drainb);
+      if (!tc::mbar_wait(drainb, 0)) ok = false;
     }
   } else if (warp < 6) {
     // ---- epilogue: thread <-> weight row (warp % 4) * 32 + lane of the 128-row tile

@@ -77,7 +77,8 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
   uint64_t* empty = bars + kGrpStages;        // [kGrpStages]
   uint64_t* accf = bars + 2 * kGrpStages;     // [4]
   uint64_t* acce = bars + 2 * kGrpStages + 4; // [4]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kGrpStages + 8);
+  uint64_t* drainb = bars + 2 * kGrpStages + 8;  // every MMA this CTA issued has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kGrpStages + 9);
   float* red = reinterpret_cast<float*>(base + kGrpStages * kGrpStageBytes + 256);  // [128][4]
   float* ystage = red;  // down: [16 warps][32 rows][16] f32
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -93,6 +94,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
       tc::mbar_init(&accf[b], 1);
       tc::mbar_init(&acce[b], kGrpEpiWarps / 2);
     }
+    tc::mbar_init(drainb, 1);
     tc::fence_mbar_init();
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -116,7 +118,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
 
   bool ok = true;
   if (warp == 0) {
-    int it = 0;
+    int it = 0, last = -1;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const int nb = u % p.nnb;
       const Tile tl = p.tiles[u / p.nnb];
@@ -131,6 +133,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
         if (lane == 0) w_ok = tc::mbar_wait(&empty[s], ph ^ 1);
         if (!__shfl_sync(0xffffffffu, (int)w_ok, 0)) { ok = false; break; }
         unsigned char* st = stages + s * kGrpStageBytes;
+        last = it;
         if (lane == 0) tc::mbar_arrive_expect_tx(&full[s], kGrpStageBytes);
         __syncwarp();
         const int x = i * 128;
@@ -145,6 +148,8 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
         }
       }
     }
+    // no load is still writing when the CTA leaves (a no-op unless a wait gave up)
+    if (lane == 0 && last >= 0 && !tc::mbar_wait(&full[last % kGrpStages], (last / kGrpStages) & 1)) ok = false;
   } else if (warp == 1) {
     if (lane == 0) {
       // per K block two 128x128 halves into TMEM buffers (2*it + h) % 4 (128 columns each),
@@ -168,12 +173,17 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
             const uint32_t d = tmem + buf * 128;
 #pragma unroll
             for (int k = 0; k < 4; ++k) tc::mma_e4m3(d, da + 2 * k, db + 2 * k, idesc, k > 0);
+            // the stage is read once both halves are issued: released before the last
+            // accumulator, whose arrival the epilogue waits for
+            if (h == 1) tc::mma_commit(&empty[s]);
             tc::mma_commit(&accf[buf]);
           }
           if (!ok) break;
-          tc::mma_commit(&empty[s]);
         }
       }
+      // every arrival the MMAs owe this CTA's barriers has landed before the CTA can leave
+      tc::mma_commit(drainb);
+      if (!tc::mbar_wait(drainb, 0)) ok = false;
     }
   } else {
     // epilogue: 8 warps per MMA half hh; thread = (accumulator row, 64 of the half's 128

@@ -104,7 +104,8 @@ __global__ void __launch_bounds__(kPairThreads, 3)
   uint64_t* empty = bars + kMaxStages;        // [kMaxStages]
   uint64_t* accf = bars + 2 * kMaxStages;     // [2]
   uint64_t* acce = accf + 2;                  // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
+  uint64_t* drainb = acce + 2;                // every MMA this CTA issued has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drainb + 1);
   float* red = reinterpret_cast<float*>(tmem_slot + 1);  // [4] warp maxima
   int* e_sh = reinterpret_cast<int*>(red + 4);
 
@@ -127,6 +128,7 @@ __global__ void __launch_bounds__(kPairThreads, 3)
       tc::mbar_init(&accf[b], 1);
       tc::mbar_init(&acce[b], 4);
     }
+    tc::mbar_init(drainb, 1);
     tc::fence_mbar_init();
   }
   if (warp == 1) {
@@ -252,6 +254,7 @@ __global__ void __launch_bounds__(kPairThreads, 3)
   float chain0 = 0.0f, chain1 = 0.0f;
   float term0[kMaxSplitTerms], term1[kMaxSplitTerms];
   if (valid && warp == 0) {
+    int issued = npre;  // stages with loads issued (the first npre in the prologue)
     const int ya = kGateUp ? e * 2 * p.I + cb * 128 : e * p.H + cb * 128;
     const int yb = e * 2 * p.I + p.I + cb * 128;
     for (int i = npre; i < p.nkb_cta; ++i) {
@@ -274,7 +277,13 @@ __global__ void __launch_bounds__(kPairThreads, 3)
         if (kGateUp) tc::tma_load_2d(st + C::kABytes, &tmA, &full[s], x, yb);
         if (MODE != kGateUpFused) tc::tma_load_2d(st + C::kTxA, &tmB, &full[s], x, brow);
       }
+      issued = i + 1;
     }
+    // no load is still writing when the CTA leaves: the last load issued into each stage has
+    // landed (a no-op unless a wait gave up)
+    if (lane == 0)
+      for (int i = issued - 1; i >= 0 && i >= issued - nst; --i)
+        if (!tc::mbar_wait(&full[i % nst], (i / nst) & 1)) ok = false;
   } else if (valid && warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_e4m3(128, kPairN);
@@ -298,6 +307,9 @@ __global__ void __launch_bounds__(kPairThreads, 3)
         tc::mma_commit(&empty[s]);
         tc::mma_commit(&accf[buf]);
       }
+      // every arrival the MMAs owe this CTA's barriers has landed before the CTA can leave
+      tc::mma_commit(drainb);
+      if (!tc::mbar_wait(drainb, 0)) ok = false;
       if (kGateUp && ok && p.pf_w2 != nullptr) {
         // every weight byte of this CTA has landed: spend the idle memory time of the
         // epilogue on this CTA's share of the expert's down weights (and, once per pair,

@@ -41,6 +41,9 @@
 // The arithmetic is that of the few-row pair kernels (moe_fp8_gate_up_direct +
 // moe_fp8_down_combine), so outputs are bitwise theirs.
 //
+// Teardown: the MMA lane's last commit goes to a drain barrier that it waits for, and each TMA
+// lane waits for its last load, so no asynchronous arrival or write can reach this CTA's shared
+// memory after it has left (or land in the next CTA to get the SM).
 // Warp roles: 0 TMA (four issuing lanes, one per ring slot), 1 TMEM + MMA issue,
 // 2-5 epilogue (TMEM lane quadrant = warp % 4), 6-7 down B-tile builders; all eight warps
 // quantise the hidden rows and route. Every wait is bounded and reports
@@ -114,7 +117,7 @@ constexpr size_t kVoE2l = kVoDist + 128 * 4;                  // [128] i32 exper
 constexpr size_t kVoWcnt = kVoE2l + 128 * 4;                  // [4] i32 + n_dist
 constexpr size_t kVoSlot = kVoWcnt + 8 * 4;                   // [96][12] i8 slot of token t
 constexpr size_t kVoBars = (kVoSlot + (size_t)kVR * kVM + 15) & ~size_t(15);
-constexpr int kVNumBars = 2 * kVSlots + 16 + 16 + 4 + kVMaxDn + 2 + 2;
+constexpr int kVNumBars = 2 * kVSlots + 16 + 16 + 4 + kVMaxDn + 2 + 2 + 1;
 constexpr size_t kVSmem = kVoBars + (size_t)kVNumBars * 8 + 16 + 1024;  // + alignment slack
 static_assert(kVoOwn + (size_t)kVM * 128 * 4 <= kVoPart, "own fits in the down tiles");
 static_assert(kVoHs + (size_t)kVM * kVH * 2 <= kVoHid, "the hidden rows fit in the ring");
@@ -169,7 +172,8 @@ __global__ void __launch_bounds__(kVThreads, 1)
   uint64_t* eready = routes_full + 1;      // [kVMaxDn] all 6 activation blocks of expert ie are written
   uint64_t* act_ready = eready + kVMaxDn;  // [2] an expert's down B tiles and scales are built
   uint64_t* act_free = act_ready + 2;      // [2] ... and no longer read (MMA + epilogue)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(act_free + 2);
+  uint64_t* drainb = act_free + 2;         // every MMA this CTA issued has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(act_free + 3);
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int rank = (int)tc::cluster_rank();
@@ -199,6 +203,7 @@ __global__ void __launch_bounds__(kVThreads, 1)
       tc::mbar_init(&act_ready[b], 1);
       tc::mbar_init(&act_free[b], 2);
     }
+    tc::mbar_init(drainb, 1);
     // the bytes the exchanges copy into this CTA: token rank's chunk partials (owners) and
     // every token's route
     if (rank < kVM) tc::mbar_arrive_expect_tx(part_full, (uint32_t)(kVCL * 128 * 4));
@@ -391,6 +396,7 @@ __global__ void __launch_bounds__(kVThreads, 1)
     // one 3-D box (gate and up tiles of one K block), a down piece two 2-D boxes (two K blocks)
     if (lane < kVSlots) {
       tc::fence_proxy_async_smem();  // the routing reads of the ring precede these writes
+      int last_use = -1;
       for (int k = lane; k < n_pieces && ok; k += kVSlots) {
         const int s = k % kVSlots, use = k / kVSlots;
         if (!tc::mbar_wait(&emptyp[s], (use & 1) ^ 1)) {
@@ -398,6 +404,7 @@ __global__ void __launch_bounds__(kVThreads, 1)
           break;
         }
         unsigned char* dst = ring + (size_t)s * 2 * kVTile;
+        last_use = use;
         tc::mbar_arrive_expect_tx(&fullp[s], 2 * kVTile);
         if (k < n_gu * kVNkh) {
           int el, e, cb;
@@ -411,6 +418,8 @@ __global__ void __launch_bounds__(kVThreads, 1)
           tc::tma_load_2d(dst + kVTile, &tm2, &fullp[s], (kb + 1) * 128, y);
         }
       }
+      // no load of this lane is still writing when the CTA leaves (a no-op unless a wait gave up)
+      if (last_use >= 0 && !tc::mbar_wait(&fullp[lane], last_use & 1)) ok = false;
     }
   } else if (warp == 1) {
     // ---- MMA issue in piece order: swap-AB 128 x 16 x 32 steps; gate/up into 32-column
@@ -461,13 +470,19 @@ __global__ void __launch_bounds__(kVThreads, 1)
             const uint64_t dw = tc::sdesc_sw128(tc::smem_u32(a + (size_t)h * kVTile));
 #pragma unroll
             for (int q = 0; q < 4; ++q) tc::mma_e4m3(d, dw + 2 * q, db + 2 * q, idesc, q > 0);
+            if (h == 1) {  // the slot and the expert's B tiles are read: released before the last
+                           // accumulator, whose arrival the epilogue waits for
+              tc::mma_commit(&emptyp[s]);
+              if (kp == kVNu / 2 - 1) tc::mma_commit(&act_free[ab]);
+            }
             tc::mma_commit(&accf2[buf]);
             ++nd;
           }
-          tc::mma_commit(&emptyp[s]);
-          if (kp == kVNu / 2 - 1) tc::mma_commit(&act_free[ab]);  // the expert's B tiles are read
         }
       }
+      // every arrival the MMAs owe this CTA's barriers has landed before the CTA can leave
+      tc::mma_commit(drainb);
+      if (!tc::mbar_wait(drainb, 0)) ok = false;
     }
   } else if (warp < 6) {
     // ---- epilogue: thread <-> weight row (warp % 4) * 32 + lane of the 128-row tile
