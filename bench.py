@@ -96,8 +96,9 @@ def parse():
                         "launch list")
     p.add_argument("--no-verify", action="store_true",
                    help="leave the verify M=12 record out of the decode line")
-    p.add_argument("--verify-route-forward", action="store_true",
-                   help="verify workloads through moe_fp8_route_forward instead of the producer + reducer")
+    p.add_argument("--verify-two-op", action="store_true",
+                   help="verify workloads through the producer + route reducer (off by default: the "
+                        "producer is kept off the GPU while a replay-time fault is unexplained)")
     p.add_argument("--no-prefill", action="store_true",
                    help="decode only: leave out the prefill record of the same line")
     p.add_argument("--clock-soak", type=float, default=1.0, metavar="S",
@@ -310,7 +311,7 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
     wts = torch.empty((nbatches, M, K), dtype=torch.float32, device="cuda")
     out = torch.empty((nbatches, M, H), dtype=torch.int16, device="cuda")
 
-    two_op = given_ids is None and verify_profile(M, H, I, E, K) and not args.verify_route_forward
+    two_op = given_ids is None and verify_profile(M, H, I, E, K) and args.verify_two_op
 
     def step(i, stream=None):
         b = i % nbatches
@@ -646,7 +647,7 @@ def profile_steps(args, wl):
     ids = torch.empty((M, K), dtype=torch.int32, device="cuda")
     w = torch.empty((M, K), dtype=torch.float32, device="cuda")
     out = torch.empty((M, H), dtype=torch.int16, device="cuda")
-    two_op = x.ids is None and verify_profile(M, H, I, E, K) and not args.verify_route_forward
+    two_op = x.ids is None and verify_profile(M, H, I, E, K) and args.verify_two_op
     for i in range(n):
         b = i % (hid_all.shape[0] // M)
         hid = hid_all[b * M:(b + 1) * M]

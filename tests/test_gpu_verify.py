@@ -17,7 +17,13 @@ import torch
 
 from fp8_block_scaled_router_gb300 import inputs
 
-pytestmark = pytest.mark.gpu
+pytestmark = [
+    pytest.mark.gpu,
+    # Kept off the GPU: the producer passed these tests and 20,000-step timed runs, but it
+    # failed under a profiler's kernel replay (twice, with and without the teardown drain) and
+    # in a timestamp-instrumented copy; until that cause is found by reading, it does not run.
+    pytest.mark.skip(reason="verify producer kept off the GPU until the cause of its replay-time faults is found"),
+]
 
 if torch.cuda.is_available():
     import oracle
