@@ -29,7 +29,7 @@ EXPORTS = ("moe_fp8_version", "moe_fp8_workspace_bytes", "moe_fp8_workspace_init
            "moe_fp8_route_forward_host", "moe_fp8_route_forward_pinned", "moe_fp8_selftest_wait",
            "moe_fp8_route_forward", "moe_fp8_route_forward_one_launch", "moe_rmsnorm", "moe_norm_route",
            "moe_fp8_norm_forward", "moe_fp8_norm_route_forward", "moe_fp8_verify_produce",
-           "moe_fp8_verify_reduce")
+           "moe_fp8_verify_reduce", "moe_fp8_forward_partials", "moe_fp8_combine_pairs")
 
 
 class MoEError(RuntimeError):
@@ -89,6 +89,8 @@ def load(path: str = LIB):
                                                        sz, sp, vp]
             lib.moe_fp8_verify_produce.argtypes = [vp, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, sz, sp, vp]
             lib.moe_fp8_verify_reduce.argtypes = [vp, i32, vp, vp, sz, sp, vp]
+            lib.moe_fp8_forward_partials.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, sz, sp, vp]
+            lib.moe_fp8_combine_pairs.argtypes = [vp, vp, vp, i32, vp, sp, vp]
             for f in EXPORTS[2:]:
                 if f != "moe_fp8_workspace_bytes":
                     getattr(lib, f).restype = i32
@@ -323,3 +325,18 @@ def moe_fp8_verify_reduce(topk_w, M, out, workspace, shape: Shape, stream=None, 
     nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
     return _check("moe_fp8_verify_reduce", load().moe_fp8_verify_reduce(
         _ptr(topk_w), int(M), _ptr(out), _ptr(workspace), nb, ctypes.byref(shape), _stream(stream)), check)
+
+
+def moe_fp8_forward_partials(hidden, topk_ids, M, w13, w13_scale, w2, w2_scale, y_out, workspace, shape: Shape,
+                             stream=None, ws_bytes=None, check=True):
+    """Every routed pair's FP32 down projection in pair order (y_out [M*K][H]); see include/moe_fp8.h."""
+    nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return _check("moe_fp8_forward_partials", load().moe_fp8_forward_partials(
+        _ptr(hidden), _ptr(topk_ids), int(M), _ptr(w13), _ptr(w13_scale), _ptr(w2), _ptr(w2_scale), _ptr(y_out),
+        _ptr(workspace), nb, ctypes.byref(shape), _stream(stream)), check)
+
+
+def moe_fp8_combine_pairs(y, topk_ids, topk_w, M, out, shape: Shape, stream=None, check=True):
+    """The slot-order route reducer over pair-order FP32 rows y [M*K][H] -> out BF16 [M][H]."""
+    return _check("moe_fp8_combine_pairs", load().moe_fp8_combine_pairs(
+        _ptr(y), _ptr(topk_ids), _ptr(topk_w), int(M), _ptr(out), ctypes.byref(shape), _stream(stream)), check)

@@ -259,6 +259,33 @@ moe_status_t moe_fp8_norm_forward(const void* hidden, const void* norm_weight, f
                       shape, stream);
 }
 
+moe_status_t moe_fp8_forward_partials(const void* hidden, const int32_t* topk_ids, int32_t M, const uint8_t* w13,
+                                      const float* w13_scale, const uint8_t* w2, const float* w2_scale, float* y_out,
+                                      void* workspace, size_t workspace_bytes, const moe_fp8_shape_t* shape,
+                                      cudaStream_t stream) {
+  if (moe_status_t st = check_common(shape, M)) return st;
+  for (const void* p : {hidden, (const void*)topk_ids, (const void*)w13, (const void*)w13_scale, (const void*)w2,
+                        (const void*)w2_scale, (const void*)y_out})
+    if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  if (M == 0) return MOE_OK;
+  if (moe_status_t st = moe_fp8_prepare(hidden, topk_ids, M, workspace, workspace_bytes, shape, stream)) return st;
+  if (moe_status_t st = moe_fp8_gate_up(w13, w13_scale, M, workspace, workspace_bytes, shape, stream)) return st;
+  if (moe_status_t st = moe_fp8_down(w2, w2_scale, M, workspace, workspace_bytes, shape, stream)) return st;
+  return launched(launch_gather_pairs(ws_ptrs(workspace, L), M * shape->top_k, shape->hidden, y_out, stream));
+}
+
+moe_status_t moe_fp8_combine_pairs(const float* y, const int32_t* topk_ids, const float* topk_w, int32_t M, void* out,
+                                   const moe_fp8_shape_t* shape, cudaStream_t stream) {
+  if (moe_status_t st = check_common(shape, M)) return st;
+  for (const void* p : {(const void*)y, (const void*)topk_ids, (const void*)topk_w, (const void*)out})
+    if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (M == 0) return MOE_OK;
+  return launched(launch_combine_pairs(y, topk_ids, topk_w, M, shape->hidden, shape->top_k, shape->num_experts,
+                                       static_cast<uint16_t*>(out), stream));
+}
+
 moe_status_t moe_fp8_gate_up_direct(const void* hidden, const int32_t* topk_ids, int32_t M,
                                     const uint8_t* w13, const float* w13_scale, void* workspace,
                                     size_t workspace_bytes, const moe_fp8_shape_t* shape,

@@ -32,9 +32,13 @@ cudaError_t launch_pair_gateup(const uint8_t* w13, const float* s13, const int32
 cudaError_t launch_pair_down(const uint8_t* w2, const float* s2w, const int32_t* ids, const float* topk_w,
                              uint16_t* out, int M, int H, int I, int E, int K, const WsPtrs& ws,
                              cudaStream_t st);
-// combine.cu: out = slot-order combine of y
+// combine.cu: out = slot-order combine of y (workspace rows through perm_row, or given rows in
+// pair order with skipped pairs named by their ids), and the sorted y gathered into pair order
 cudaError_t launch_combine(const float* topk_w, int M, int H, int K, uint16_t* out, const WsPtrs& ws,
                            cudaStream_t st);
+cudaError_t launch_combine_pairs(const float* y, const int32_t* ids, const float* topk_w, int M, int H, int K, int E,
+                                 uint16_t* out, cudaStream_t st);
+cudaError_t launch_gather_pairs(const WsPtrs& ws, int R, int H, float* y_out, cudaStream_t st);
 // selftest.cu: a bounded wait that runs out
 cudaError_t launch_wait_selftest(Header* hdr, uint32_t limit_us, cudaStream_t st);
 // fused.cu: the single-launch layer for a few routed pairs

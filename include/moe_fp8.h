@@ -249,6 +249,24 @@ moe_status_t moe_fp8_combine(const float* topk_w, int32_t M, void* out, void* wo
                              size_t workspace_bytes, const moe_fp8_shape_t* shape,
                              cudaStream_t stream);
 
+/* The layer split at its expert partials, for callers that move routed rows between devices
+ * (expert parallelism: [AMDK] names ranks<n> kernels and sums expert partials in a fixed order
+ * "inside the next kernel"; [NK] keeps the route reducer a separate operation).
+ * moe_fp8_forward_partials runs moe_fp8_prepare, moe_fp8_gate_up and moe_fp8_down and writes
+ * every routed pair's down projection in pair order:
+ *   y_out  FP32 [M*K][H], row t*K + j = y of token t's slot j (zeros for a skipped pair)
+ * moe_fp8_combine_pairs is the route reducer over such rows (wherever they were computed):
+ *   out[t] = bf16(sum over slots j ascending of topk_w[t][j] * y[t*K + j]), FP32 multiply
+ *   then add from 0, pairs whose topk_ids entry is outside [0, E) skipped.
+ * moe_fp8_combine_pairs(moe_fp8_forward_partials(...)) equals moe_fp8_forward bit for bit;
+ * combine_pairs needs no workspace. Other arguments and limits as for moe_fp8_forward. */
+moe_status_t moe_fp8_forward_partials(const void* hidden, const int32_t* topk_ids, int32_t M, const uint8_t* w13,
+                                      const float* w13_scale, const uint8_t* w2, const float* w2_scale, float* y_out,
+                                      void* workspace, size_t workspace_bytes, const moe_fp8_shape_t* shape,
+                                      cudaStream_t stream);
+moe_status_t moe_fp8_combine_pairs(const float* y, const int32_t* topk_ids, const float* topk_w, int32_t M, void* out,
+                                   const moe_fp8_shape_t* shape, cudaStream_t stream);
+
 /* The few-routed-row path as its two kernels (one unit per (token, slot) pair; M * top_k
  * <= 256), the layout of the accepted M=1 MoE objects of [ARCH] (gate/up + SiLU +
  * quantisation, then down/reduce). moe_fp8_forward runs these two kernels when M * top_k

@@ -180,6 +180,27 @@ def test_verify_exact_batch_guard(lib):
     assert L.moe_fp8_verify_reduce(FAKE, 12, MIS, FAKE, s, stream=0, ws_bytes=need, check=False) == 1
 
 
+def test_partials_and_pair_reducer_argument_errors(lib):
+    s = shape()
+    need = L.moe_fp8_workspace_bytes(s)
+    args = [FAKE] * 7  # hidden, ids, w13, w13_scale, w2, w2_scale, y_out
+    for i in range(7):
+        for bad in (0, MIS):
+            a = list(args)
+            a[i] = bad
+            assert L.moe_fp8_forward_partials(a[0], a[1], 4, a[2], a[3], a[4], a[5], a[6], FAKE, s, stream=0,
+                                              ws_bytes=need, check=False) == 1, (i, bad)
+    assert L.moe_fp8_forward_partials(*args[:2], 4, *args[2:], FAKE, s, stream=0, ws_bytes=need - 1, check=False) == 3
+    assert L.moe_fp8_forward_partials(*args[:2], 0, *args[2:], FAKE, s, stream=0, ws_bytes=need, check=False) == 0
+    assert L.moe_fp8_forward_partials(*args[:2], 17, *args[2:], FAKE, s, stream=0, ws_bytes=need, check=False) == 1
+    for i in range(4):
+        a = [FAKE] * 4
+        a[i] = MIS
+        assert L.moe_fp8_combine_pairs(a[0], a[1], a[2], 4, a[3], s, stream=0, check=False) == 1, i
+    assert L.moe_fp8_combine_pairs(FAKE, FAKE, FAKE, 0, FAKE, s, stream=0, check=False) == 0
+    assert L.moe_fp8_combine_pairs(FAKE, FAKE, FAKE, 4, FAKE, shape(hidden=200), stream=0, check=False) == 2
+
+
 def test_zero_tokens_is_a_no_op(lib):
     """M = 0 returns MOE_OK after validation without touching the GPU (fake pointers)."""
     s = shape()
