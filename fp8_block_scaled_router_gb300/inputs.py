@@ -17,6 +17,9 @@ amd-kernels wide-expert shape token h6144_i768_e128_top4):
 * skewed verify: an FP32 logit bias of +3.0 on experts 0..3;
 * Zipf prefill: each token draws K distinct experts with p(e) proportional to (e+1)^-1.1,
   without replacement (Gumbel top-k), and Dirichlet(1) weights;
+* MXFP4 expert weights (the h6144/i768/e128/top-4 shape token): the same N(0, 0.02) draws,
+  quantised per 32 consecutive K elements with scale 2^(floor(log2(amax)) - 2) and
+  round-to-nearest-even E2M1 codes saturating at 6 (OCP microscaling);
 * the un-normalised hidden in front of an RMSNorm (the residual stream): each row
   N(0, sigma_t^2) with sigma_t log-uniform in [2^-4, 2^4], and 4 outlier channels (drawn
   once per seed) scaled by 16; the norm's weight BF16 ~ 1 + N(0, 0.1^2).
@@ -164,6 +167,82 @@ def make(name: str, M: Optional[int] = None, E: Optional[int] = None, tokens: Op
     if "zipf" in c:
         ids, wts = zipf_routing(seed, rows, Ex, K, c["zipf"])
     return MoEInputs(sh, M, hidden, router_w, bias, w13, s13, w2, s2, ids, wts)
+
+
+# ---- MXFP4 weights (OCP microscaling: E2M1 codes, one UE8M0 scale per 32 elements) -------
+# The magnitudes of E2M1 codes 0..7 (the format's value table; the sign is bit 3).
+E2M1_MAGNITUDES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+_E2M1_MIDPOINTS = ((E2M1_MAGNITUDES[:-1] + E2M1_MAGNITUDES[1:]) / 2).astype(np.float32)  # exact in FP32
+
+
+def e2m1_encode(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest E2M1 value, ties to the even code, saturating at +-6; uint8 codes.
+    (FP32 input: every midpoint between E2M1 values is exact in FP32.)"""
+    x = np.asarray(x, np.float32)
+    a = np.abs(x)
+    mag = np.searchsorted(_E2M1_MIDPOINTS, a, side="left").astype(np.uint8)  # midpoints below a
+    at_mid = a == _E2M1_MIDPOINTS[np.minimum(mag, 6)]
+    mag += (at_mid & (mag < 7) & ((mag & 1) == 1)).astype(np.uint8)         # halfway: the even code
+    return mag | (np.signbit(x).astype(np.uint8) << 3)
+
+
+def mx_quantise_blocks(w: np.ndarray):
+    """One expert matrix [N][Kd] FP32 -> (codes [N][Kd/2], two per byte, the lower K index in
+    the low nibble; UE8M0 scales [N][Kd/32]). Scale = 2^(floor(log2(block amax)) - 2) (the
+    largest E2M1 exponent is 2); an all-zero block takes 2^-127. The codes are e2m1_encode of
+    the scaled values (computed here with torch's CPU kernels, which run on every core)."""
+    N, Kd = w.shape
+    mids = torch.from_numpy(_E2M1_MIDPOINTS)
+    b = torch.from_numpy(np.ascontiguousarray(w, np.float32)).reshape(N, Kd // 32, 32)
+    amax = b.abs().amax(dim=-1)
+    _, e2 = torch.frexp(amax)  # amax = f * 2^e2 with f in [0.5, 1): floor(log2(amax)) = e2 - 1
+    ex = torch.where(amax > 0, e2 - 3, torch.full_like(e2, -127)).clamp(-127, 127)
+    scaled = b * torch.ldexp(torch.ones_like(amax), -ex)[..., None]  # exact: a power of two
+    a = scaled.abs()
+    mag = torch.bucketize(a, mids, right=False).to(torch.uint8)  # midpoints below a
+    at_mid = a == mids[mag.clamp(max=6).long()]
+    mag = mag + (at_mid & (mag < 7) & ((mag & 1) == 1)).to(torch.uint8)  # halfway: the even code
+    codes = (mag | (torch.signbit(scaled).to(torch.uint8) << 3)).reshape(N, Kd)
+    packed = codes[:, 0::2] | (codes[:, 1::2] << 4)
+    return packed.numpy().astype(np.uint8), (ex + 127).to(torch.uint8).numpy()
+
+
+def mx_expert_weights(seed: int, stream: int, E: int, N: int, Kd: int, std: float = 0.02):
+    """[E][N][Kd/2] packed E2M1 codes and [E][N][Kd/32] UE8M0 scales, one expert at a time."""
+    g = rng(seed, stream)
+    codes = np.empty((E, N, Kd // 2), np.uint8)
+    scales = np.empty((E, N, Kd // 32), np.uint8)
+    for e in range(E):
+        codes[e], scales[e] = mx_quantise_blocks(g.standard_normal((N, Kd), dtype=np.float32) * np.float32(std))
+    return codes, scales
+
+
+MX_CONFIGS = {
+    # the amd-kernels MXFP4 shape token h6144_i768_e128_top4, token count a runtime argument
+    "wide_mxfp4": dict(shape=Shape(6144, 768, 128, 4), M=64, router_std=0.02, seed=9),
+    "tiny_mxfp4": dict(shape=Shape(256, 128, 8, 2), M=4, router_std=0.02, seed=10),
+}
+
+
+def make_mx(name: str, M: Optional[int] = None, tokens: Optional[int] = None, E: Optional[int] = None) -> "MoEInputs":
+    """A named MXFP4 workload: w13 / w2 hold packed E2M1 codes, s13 / s2 UE8M0 scales. ``E``
+    overrides the expert count (a smaller draw for a fast test; the per-expert shapes are
+    unchanged)."""
+    c = MX_CONFIGS[name]
+    sh: Shape = c["shape"]
+    if E is not None:
+        sh = dataclasses.replace(sh, num_experts=E)
+    M = c["M"] if M is None else M
+    rows = M if tokens is None else tokens
+    seed = c["seed"]
+    H, I, E = sh.hidden, sh.inter, sh.num_experts
+    hidden = hidden_states(seed, rows, H)
+    router_w = router_weights(seed, H, E, c["router_std"])
+    w13, s13 = mx_expert_weights(seed, _S_W13, E, 2 * I, H)
+    w2, s2 = mx_expert_weights(seed, _S_W2, E, H, I)
+    return MoEInputs(sh, M, hidden, router_w, None, w13, s13, w2, s2, None, None)
 
 
 def residual_states(seed: int, M: int, H: int, zero_rows: Optional[np.ndarray] = None) -> np.ndarray:

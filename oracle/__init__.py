@@ -69,6 +69,15 @@ def _load():
             lib.orc_down_combine.restype = i32
             lib.orc_rmsnorm.argtypes = [vp, vp, ctypes.c_float, i32, i32, vp, vp]
             lib.orc_rmsnorm.restype = i32
+            lib.orc_e2m1_table.argtypes = [vp]
+            lib.orc_ue8m0_decode.argtypes = [vp, vp, i64]
+            lib.orc_mx_row.argtypes = [vp, vp, vp, vp, i32]
+            lib.orc_mx_row.restype = ctypes.c_float
+            lib.orc_mxfp4_forward.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp,
+                                              ctypes.POINTER(_Debug), i32]
+            lib.orc_mxfp4_forward.restype = i32
+            lib.orc_mxfp4_down_combine.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i32]
+            lib.orc_mxfp4_down_combine.restype = i32
             _lib = lib
     return _lib
 
@@ -192,3 +201,67 @@ def rmsnorm(x, gamma, eps: float, want_rstd: bool = False):
     if rc != 0:
         raise ValueError("oracle rmsnorm: unsupported sizes")
     return (y, r) if want_rstd else y
+
+
+# ---- MXFP4 weight variant ---------------------------------------------------------------
+def e2m1_table() -> np.ndarray:
+    out = np.empty(16, np.float32)
+    _load().orc_e2m1_table(_p(out))
+    return out
+
+
+def ue8m0_decode(e) -> np.ndarray:
+    e = _c(e, np.uint8)
+    out = np.empty(e.shape, np.float32)
+    _load().orc_ue8m0_decode(_p(e), _p(out), e.size)
+    return out
+
+
+def mx_row(a, sa, wq, ws) -> float:
+    """One MXFP4 block-scaled row: a E4M3 codes [K], sa f32 [K/128], wq packed [K/2], ws [K/32]."""
+    a, sa, wq, ws = _c(a, np.uint8), _c(sa, np.float32), _c(wq, np.uint8), _c(ws, np.uint8)
+    assert a.size % 128 == 0 and wq.size * 2 == a.size and ws.size * 32 == a.size and sa.size * 128 == a.size
+    return float(_load().orc_mx_row(_p(a), _p(sa), _p(wq), _p(ws), a.size // 128))
+
+
+def mxfp4_forward(hidden, ids, weights, w13q, w13s, w2q, w2s, debug: bool = False, nthreads: int = 1):
+    """The layer with MXFP4 expert weights (codes [E][N][K/2], UE8M0 scales [E][N][K/32])."""
+    hidden = _c(hidden, np.uint16)
+    ids, weights = _c(ids, np.int32), _c(weights, np.float32)
+    w13q, w13s, w2q, w2s = _c(w13q, np.uint8), _c(w13s, np.uint8), _c(w2q, np.uint8), _c(w2s, np.uint8)
+    M, H = hidden.shape
+    K = ids.shape[1]
+    E, twoI, Hh = w13q.shape
+    I = twoI // 2
+    assert Hh * 2 == H and w13s.shape == (E, twoI, H // 32)
+    assert w2q.shape == (E, H, I // 2) and w2s.shape == (E, H, I // 32) and ids.shape == weights.shape == (M, K)
+    out = np.empty((M, H), np.uint16)
+    dbg = None
+    arrays = {}
+    if debug:
+        arrays = dict(qa=np.zeros((M, H), np.uint8), sa=np.zeros((M, H // 128), np.float32),
+                      g=np.zeros((M, K, I), np.float32), u=np.zeros((M, K, I), np.float32),
+                      gabs=np.zeros((M, K, I), np.float32), uabs=np.zeros((M, K, I), np.float32),
+                      act=np.zeros((M, K, I), np.float32), qact=np.zeros((M, K, I), np.uint8),
+                      s2=np.zeros((M, K, I // 128), np.float32), y=np.zeros((M, K, H), np.float32))
+        dbg = _Debug(**{k: v.ctypes.data for k, v in arrays.items()})
+    rc = _load().orc_mxfp4_forward(_p(hidden), _p(ids), _p(weights), M, H, I, E, K, _p(w13q), _p(w13s), _p(w2q),
+                                   _p(w2s), _p(out), ctypes.byref(dbg) if dbg is not None else None, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle mxfp4 forward: unsupported sizes")
+    return (out, arrays) if debug else out
+
+
+def mxfp4_down_combine(qact, s2, ids, weights, w2q, w2s, nthreads: int = 1):
+    qact, s2 = _c(qact, np.uint8), _c(s2, np.float32)
+    ids, weights = _c(ids, np.int32), _c(weights, np.float32)
+    w2q, w2s = _c(w2q, np.uint8), _c(w2s, np.uint8)
+    M, K, I = qact.shape
+    E, H, I2 = w2q.shape
+    assert I2 * 2 == I and w2s.shape == (E, H, I // 32)
+    out = np.empty((M, H), np.uint16)
+    rc = _load().orc_mxfp4_down_combine(_p(qact), _p(s2), _p(ids), _p(weights), M, H, I, E, K, _p(w2q), _p(w2s),
+                                        _p(out), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle mxfp4 down_combine: unsupported sizes")
+    return out

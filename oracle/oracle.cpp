@@ -119,6 +119,63 @@ float block_dot(const uint8_t* a, const uint8_t* w, int n) {
 
 struct Dims { int M, H, I, E, K; };
 
+// ---------------------------------------------------------------------------------------
+// MXFP4 (OCP microscaling, FP4 elements): E2M1 codes -- 1 sign bit, 2 exponent bits with
+// bias 1, 1 mantissa bit; exponent field 0 is subnormal (m * 0.5); no infinities or NaN; the
+// largest magnitude is 1.5 * 2^2 = 6 -- with one UE8M0 scale per 32 consecutive elements
+// (8 exponent bits, value 2^(e - 127), e = 255 is NaN).
+// ---------------------------------------------------------------------------------------
+double e2m1_value(unsigned code) {
+  const unsigned s = (code >> 3) & 1u, ex = (code >> 1) & 3u, m = code & 1u;
+  const double mag = ex == 0u ? 0.5 * m : std::ldexp(1.0 + 0.5 * m, (int)ex - 1);
+  return s ? -mag : mag;
+}
+float ue8m0_value(unsigned e) { return e == 255u ? NAN : (float)std::ldexp(1.0, (int)e - 127); }
+
+// One MXFP4 block-scaled GEMV row (reading for the MXFP4 weight variant): for each 128-wide
+// K block kb (the activation's quantisation group),
+//   T_kb = sum over its 32-wide sub-blocks s ascending of fl32(P_s) * 2^(e_s - 127),
+// with P_s the exact 32-term dot product of the E4M3 activation values and the E2M1 weight
+// values, each multiply and add one FP32 operation from 0; then, as for FP8 weights,
+//   out = sum over kb ascending of fl32(T_kb * sa[kb]), from 0.
+// wq: the row's codes, two per byte, the lower K index in the low nibble; ws: its scales.
+// abs_sum receives sum |P_s * 2^e_s * sa| (the error-scale reference of the tests).
+float mx_row(const uint8_t* a, const float* sa, const uint8_t* wq, const uint8_t* ws, int nkb, float* abs_sum) {
+  const float* t = table().v;
+  float acc = 0.0f;
+  double asum = 0.0;
+  for (int kb = 0; kb < nkb; ++kb) {
+    float T = 0.0f;
+    for (int j = 0; j < 4; ++j) {
+      const int s = kb * 4 + j;
+      double d = 0.0;  // exact: multiples of 2^-10 below 2^12 in magnitude, 32 terms
+      for (int k = s * 32; k < s * 32 + 32; ++k) {
+        const unsigned code = (wq[k / 2] >> (4 * (k & 1))) & 15u;
+        d += (double)t[a[k]] * e2m1_value(code);
+      }
+      const float p = (float)d;
+      const float sc = ue8m0_value(ws[s]);
+      const float term = p * sc;
+      T = T + term;
+      asum += std::fabs((double)term * (double)sa[kb]);
+    }
+    const float term = T * sa[kb];
+    acc = acc + term;
+  }
+  if (abs_sum) *abs_sum = (float)asum;
+  return acc;
+}
+
+// Down projection of one routed pair with MXFP4 w2: codes [E][H][I/2], scales [E][H][I/32].
+void mx_down_row(const uint8_t* qact, const float* s2, int e, const Dims d, const uint8_t* w2q, const uint8_t* w2s,
+                 float* y) {
+  const int H = d.H, I = d.I;
+  for (int h = 0; h < H; ++h) {
+    const int64_t row = (int64_t)e * H + h;
+    y[h] = mx_row(qact, s2, w2q + row * (I / 2), w2s + row * (I / 32), I / 128, nullptr);
+  }
+}
+
 }  // namespace
 
 extern "C" {
@@ -342,6 +399,68 @@ void forward_tokens(const uint16_t* hidden, const int32_t* ids, const float* w, 
   }
 }
 
+// The MXFP4 forward for tokens [t0, t1): the FP8 steps with MXFP4 weight rows (mx_row).
+void mx_forward_tokens(const uint16_t* hidden, const int32_t* ids, const float* w, const Dims d,
+                       const uint8_t* w13q, const uint8_t* w13s, const uint8_t* w2q, const uint8_t* w2s,
+                       uint16_t* out, const orc_debug_t* dbg, int t0, int t1) {
+  const int H = d.H, I = d.I, E = d.E, K = d.K;
+  const int nkh = H / 128, nki = I / 128;
+  std::vector<float> x(H), sa(nkh), G(2 * I), Gabs(2 * I), act(I), s2(nki), Y((size_t)K * H);
+  std::vector<uint8_t> qa(H), qact(I);
+  std::vector<char> valid(K);
+  for (int t = t0; t < t1; ++t) {
+    for (int k = 0; k < H; ++k) x[k] = bf16_to_f32(hidden[(int64_t)t * H + k]);
+    for (int kb = 0; kb < nkh; ++kb) sa[kb] = quantise_group(&x[kb * 128], 128, &qa[kb * 128]);
+    if (dbg && dbg->qa) std::memcpy(dbg->qa + (int64_t)t * H, qa.data(), H);
+    if (dbg && dbg->sa) std::memcpy(dbg->sa + (int64_t)t * nkh, sa.data(), nkh * 4);
+    for (int j = 0; j < K; ++j) {
+      const int e = ids[(int64_t)t * K + j];
+      valid[j] = (e >= 0 && e < E);
+      if (!valid[j]) continue;
+      const int64_t pj = (int64_t)t * K + j;
+      for (int n = 0; n < 2 * I; ++n) {
+        const int64_t row = (int64_t)e * 2 * I + n;
+        G[n] = mx_row(qa.data(), sa.data(), w13q + row * (H / 2), w13s + row * (H / 32), nkh, &Gabs[n]);
+      }
+      for (int i = 0; i < I; ++i) {
+        const double g = G[i], u = G[I + i];
+        act[i] = (float)(g / (1.0 + std::exp(-g)) * u);
+      }
+      for (int kb = 0; kb < nki; ++kb) s2[kb] = quantise_group(&act[kb * 128], 128, &qact[kb * 128]);
+      float* y = &Y[(size_t)j * H];
+      mx_down_row(qact.data(), s2.data(), e, d, w2q, w2s, y);
+      if (dbg) {
+        if (dbg->g) std::memcpy(dbg->g + pj * I, G.data(), I * 4);
+        if (dbg->u) std::memcpy(dbg->u + pj * I, G.data() + I, I * 4);
+        if (dbg->gabs) std::memcpy(dbg->gabs + pj * I, Gabs.data(), I * 4);
+        if (dbg->uabs) std::memcpy(dbg->uabs + pj * I, Gabs.data() + I, I * 4);
+        if (dbg->act) std::memcpy(dbg->act + pj * I, act.data(), I * 4);
+        if (dbg->qact) std::memcpy(dbg->qact + pj * I, qact.data(), I);
+        if (dbg->s2) std::memcpy(dbg->s2 + pj * nki, s2.data(), nki * 4);
+        if (dbg->y) std::memcpy(dbg->y + pj * H, y, (size_t)H * 4);
+      }
+    }
+    combine_token(Y.data(), w + (int64_t)t * K, valid.data(), K, H, out + (int64_t)t * H);
+  }
+}
+
+void mx_down_combine_tokens(const uint8_t* qact, const float* s2, const int32_t* ids, const float* w, const Dims d,
+                            const uint8_t* w2q, const uint8_t* w2s, uint16_t* out, int t0, int t1) {
+  const int H = d.H, I = d.I, E = d.E, K = d.K, nki = I / 128;
+  std::vector<float> Y((size_t)K * H);
+  std::vector<char> valid(K);
+  for (int t = t0; t < t1; ++t) {
+    for (int j = 0; j < K; ++j) {
+      const int e = ids[(int64_t)t * K + j];
+      valid[j] = (e >= 0 && e < E);
+      if (!valid[j]) continue;
+      const int64_t pj = (int64_t)t * K + j;
+      mx_down_row(qact + pj * I, s2 + pj * nki, e, d, w2q, w2s, &Y[(size_t)j * H]);
+    }
+    combine_token(Y.data(), w + (int64_t)t * K, valid.data(), K, H, out + (int64_t)t * H);
+  }
+}
+
 // Steps 6 and 7 for M tokens from given activation codes and scales (per routed pair).
 void down_combine_tokens(const uint8_t* qact, const float* s2, const int32_t* ids, const float* w, const Dims d,
                          const uint8_t* w2, const float* s2w, uint16_t* out, int t0, int t1) {
@@ -407,6 +526,57 @@ int orc_down_combine(const uint8_t* qact, const float* s2, const int32_t* ids, c
   for (int i = 0; i < nthreads; ++i) {
     const int t0 = (int)((int64_t)M * i / nthreads), t1 = (int)((int64_t)M * (i + 1) / nthreads);
     th.emplace_back(down_combine_tokens, qact, s2, ids, w, d, w2, s2w, out, t0, t1);
+  }
+  for (auto& x : th) x.join();
+  return 0;
+}
+
+// ---- MXFP4 weight variant --------------------------------------------------------------
+void orc_e2m1_table(float* out16) { for (unsigned c = 0; c < 16; ++c) out16[c] = (float)e2m1_value(c); }
+void orc_ue8m0_decode(const uint8_t* e, float* out, int64_t n) { for (int64_t i = 0; i < n; ++i) out[i] = ue8m0_value(e[i]); }
+float orc_mx_row(const uint8_t* a, const float* sa, const uint8_t* wq, const uint8_t* ws, int nkb) {
+  return mx_row(a, sa, wq, ws, nkb, nullptr);
+}
+
+// The FFN of orc_moe_forward with MXFP4 expert weights: w13q u8 [E][2I][H/2] and w13s u8
+// [E][2I][H/32]; w2q u8 [E][H][I/2] and w2s u8 [E][H][I/32] (codes two per byte, lower K
+// index in the low nibble; one UE8M0 scale per 32 elements along K). Activations, SiLU, the
+// requantisation and the combine are those of the FP8 layer. Returns 0 or -1.
+int orc_mxfp4_forward(const uint16_t* hidden, const int32_t* ids, const float* w, int M, int H, int I, int E, int K,
+                      const uint8_t* w13q, const uint8_t* w13s, const uint8_t* w2q, const uint8_t* w2s,
+                      uint16_t* out, const orc_debug_t* dbg, int nthreads) {
+  if (M < 0 || H <= 0 || I <= 0 || H % 128 || I % 128 || E <= 0 || K <= 0) return -1;
+  const Dims d{M, H, I, E, K};
+  table();
+  if (nthreads <= 1 || M <= 1) {
+    mx_forward_tokens(hidden, ids, w, d, w13q, w13s, w2q, w2s, out, dbg, 0, M);
+    return 0;
+  }
+  nthreads = std::min(nthreads, M);
+  std::vector<std::thread> th;
+  for (int i = 0; i < nthreads; ++i) {
+    const int t0 = (int)((int64_t)M * i / nthreads), t1 = (int)((int64_t)M * (i + 1) / nthreads);
+    th.emplace_back(mx_forward_tokens, hidden, ids, w, d, w13q, w13s, w2q, w2s, out, dbg, t0, t1);
+  }
+  for (auto& x : th) x.join();
+  return 0;
+}
+
+// orc_down_combine with MXFP4 w2.
+int orc_mxfp4_down_combine(const uint8_t* qact, const float* s2, const int32_t* ids, const float* w, int M, int H,
+                           int I, int E, int K, const uint8_t* w2q, const uint8_t* w2s, uint16_t* out, int nthreads) {
+  if (M < 0 || H <= 0 || I <= 0 || H % 128 || I % 128 || E <= 0 || K <= 0) return -1;
+  const Dims d{M, H, I, E, K};
+  table();
+  if (nthreads <= 1 || M <= 1) {
+    mx_down_combine_tokens(qact, s2, ids, w, d, w2q, w2s, out, 0, M);
+    return 0;
+  }
+  nthreads = std::min(nthreads, M);
+  std::vector<std::thread> th;
+  for (int i = 0; i < nthreads; ++i) {
+    const int t0 = (int)((int64_t)M * i / nthreads), t1 = (int)((int64_t)M * (i + 1) / nthreads);
+    th.emplace_back(mx_down_combine_tokens, qact, s2, ids, w, d, w2q, w2s, out, t0, t1);
   }
   for (auto& x : th) x.join();
   return 0;
