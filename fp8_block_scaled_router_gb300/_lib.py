@@ -29,7 +29,8 @@ EXPORTS = ("moe_fp8_version", "moe_fp8_workspace_bytes", "moe_fp8_workspace_init
            "moe_fp8_route_forward_host", "moe_fp8_route_forward_pinned", "moe_fp8_selftest_wait",
            "moe_fp8_route_forward", "moe_fp8_route_forward_one_launch", "moe_rmsnorm", "moe_norm_route",
            "moe_fp8_norm_forward", "moe_fp8_norm_route_forward", "moe_fp8_verify_produce",
-           "moe_fp8_verify_reduce", "moe_fp8_forward_partials", "moe_fp8_combine_pairs")
+           "moe_fp8_verify_reduce", "moe_fp8_forward_partials", "moe_fp8_combine_pairs", "moe_mxfp4_forward",
+           "moe_mxfp4_route_forward")
 
 
 class MoEError(RuntimeError):
@@ -91,6 +92,8 @@ def load(path: str = LIB):
             lib.moe_fp8_verify_reduce.argtypes = [vp, i32, vp, vp, sz, sp, vp]
             lib.moe_fp8_forward_partials.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, sz, sp, vp]
             lib.moe_fp8_combine_pairs.argtypes = [vp, vp, vp, i32, vp, sp, vp]
+            lib.moe_mxfp4_forward.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, sz, sp, vp]
+            lib.moe_mxfp4_route_forward.argtypes = [vp, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, sp, vp]
             for f in EXPORTS[2:]:
                 if f != "moe_fp8_workspace_bytes":
                     getattr(lib, f).restype = i32
@@ -157,6 +160,26 @@ def moe_fp8_forward(hidden, topk_ids, topk_w, M, w13, w13_scale, w2, w2_scale, o
     return _check("moe_fp8_forward", load().moe_fp8_forward(
         _ptr(hidden), _ptr(topk_ids), _ptr(topk_w), int(M), _ptr(w13), _ptr(w13_scale), _ptr(w2),
         _ptr(w2_scale), _ptr(out), _ptr(workspace), nb, ctypes.byref(shape), _stream(stream)), check)
+
+
+def moe_mxfp4_forward(hidden, topk_ids, topk_w, M, w13q, w13_scale, w2q, w2_scale, out, workspace,
+                      shape: Shape, stream=None, ws_bytes=None, check=True):
+    """The layer with MXFP4 expert weights (packed E2M1 codes, UE8M0 scales per 32); see
+    include/moe_fp8.h."""
+    nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return _check("moe_mxfp4_forward", load().moe_mxfp4_forward(
+        _ptr(hidden), _ptr(topk_ids), _ptr(topk_w), int(M), _ptr(w13q), _ptr(w13_scale), _ptr(w2q),
+        _ptr(w2_scale), _ptr(out), _ptr(workspace), nb, ctypes.byref(shape), _stream(stream)), check)
+
+
+def moe_mxfp4_route_forward(hidden, router_w, bias, M, renormalize, w13q, w13_scale, w2q, w2_scale, out, topk_ids,
+                            topk_w, workspace, shape: Shape, stream=None, ws_bytes=None, check=True):
+    """moe_route then moe_mxfp4_forward; see include/moe_fp8.h."""
+    nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return _check("moe_mxfp4_route_forward", load().moe_mxfp4_route_forward(
+        _ptr(hidden), _ptr(router_w), _ptr(bias), int(M), int(bool(renormalize)), _ptr(w13q), _ptr(w13_scale),
+        _ptr(w2q), _ptr(w2_scale), _ptr(out), _ptr(topk_ids), _ptr(topk_w), _ptr(workspace), nb,
+        ctypes.byref(shape), _stream(stream)), check)
 
 
 def moe_fp8_prepare(hidden, topk_ids, M, workspace, shape: Shape, stream=None, ws_bytes=None, check=True):

@@ -286,6 +286,46 @@ moe_status_t moe_fp8_combine_pairs(const float* y, const int32_t* topk_ids, cons
                                        static_cast<uint16_t*>(out), stream));
 }
 
+moe_status_t moe_mxfp4_forward(const void* hidden, const int32_t* topk_ids, const float* topk_w, int32_t M,
+                               const uint8_t* w13q, const uint8_t* w13_scale, const uint8_t* w2q,
+                               const uint8_t* w2_scale, void* out, void* workspace, size_t workspace_bytes,
+                               const moe_fp8_shape_t* shape, cudaStream_t stream) {
+  if (moe_status_t st = check_common(shape, M)) return st;
+  for (const void* p : {hidden, (const void*)topk_ids, (const void*)topk_w, (const void*)w13q,
+                        (const void*)w13_scale, (const void*)w2q, (const void*)w2_scale, (const void*)out})
+    if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  if (M == 0) return MOE_OK;
+  if (!pair_capable((int64_t)M * shape->top_k)) return MOE_ERR_UNSUPPORTED;
+  const int H = shape->hidden, I = shape->inter, E = shape->num_experts, K = shape->top_k;
+  const WsPtrs ws = ws_ptrs(workspace, L);
+  if (moe_status_t st = launched(launch_mx_gateup(w13q, w13_scale, topk_ids, static_cast<const uint16_t*>(hidden), M,
+                                                  H, I, E, K, ws, stream)))
+    return st;
+  return launched(launch_mx_down_combine(w2q, w2_scale, topk_ids, topk_w, static_cast<uint16_t*>(out), M, H, I, E, K,
+                                         ws, stream));
+}
+
+moe_status_t moe_mxfp4_route_forward(const void* hidden, const void* router_w, const float* bias, int32_t M,
+                                     int32_t renormalize, const uint8_t* w13q, const uint8_t* w13_scale,
+                                     const uint8_t* w2q, const uint8_t* w2_scale, void* out, int32_t* topk_ids,
+                                     float* topk_w, void* workspace, size_t workspace_bytes,
+                                     const moe_fp8_shape_t* shape, cudaStream_t stream) {
+  if (moe_status_t st = check_common(shape, M)) return st;
+  for (const void* p : {hidden, router_w, (const void*)w13q, (const void*)w13_scale, (const void*)w2q,
+                        (const void*)w2_scale, (const void*)out, (const void*)topk_ids, (const void*)topk_w})
+    if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (bias && !aligned16(bias)) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  if (M == 0) return MOE_OK;
+  if (!pair_capable((int64_t)M * shape->top_k)) return MOE_ERR_UNSUPPORTED;
+  if (moe_status_t st = moe_route(hidden, router_w, bias, M, shape, renormalize, topk_ids, topk_w, stream)) return st;
+  return moe_mxfp4_forward(hidden, topk_ids, topk_w, M, w13q, w13_scale, w2q, w2_scale, out, workspace,
+                           workspace_bytes, shape, stream);
+}
+
 moe_status_t moe_fp8_gate_up_direct(const void* hidden, const int32_t* topk_ids, int32_t M,
                                     const uint8_t* w13, const float* w13_scale, void* workspace,
                                     size_t workspace_bytes, const moe_fp8_shape_t* shape,

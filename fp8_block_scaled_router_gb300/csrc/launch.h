@@ -32,6 +32,12 @@ cudaError_t launch_pair_gateup(const uint8_t* w13, const float* s13, const int32
 cudaError_t launch_pair_down(const uint8_t* w2, const float* s2w, const int32_t* ids, const float* topk_w,
                              uint16_t* out, int M, int H, int I, int E, int K, const WsPtrs& ws,
                              cudaStream_t st);
+// mx_pair.cu: the pair kernels with MXFP4 weights (packed E2M1 codes, UE8M0 scales per 32)
+cudaError_t launch_mx_gateup(const uint8_t* w13q, const uint8_t* w13s, const int32_t* ids, const uint16_t* hidden,
+                             int M, int H, int I, int E, int K, const WsPtrs& ws, cudaStream_t st);
+cudaError_t launch_mx_down_combine(const uint8_t* w2q, const uint8_t* w2s, const int32_t* ids, const float* topk_w,
+                                   uint16_t* out, int M, int H, int I, int E, int K, const WsPtrs& ws,
+                                   cudaStream_t st);
 // combine.cu: out = slot-order combine of y (workspace rows through perm_row, or given rows in
 // pair order with skipped pairs named by their ids), and the sorted y gathered into pair order
 cudaError_t launch_combine(const float* topk_w, int M, int H, int K, uint16_t* out, const WsPtrs& ws,

@@ -118,4 +118,76 @@ inline PairPlan plan_pair(const PlanDevice& d, int nkb, int64_t units, int K, bo
   return best;
 }
 
+// ---- MXFP4 weights (mx_pair.cu): a stage holds the packed E2M1 tiles as TMA lands them
+// (64 bytes per weight row and K block) and the E4M3 operand tiles the converter warps
+// expand them into; one accumulator per 32-wide sub-block (four per K block and tile).
+constexpr int kMxThreads = 320;  // TMA, MMA, 4 epilogue, 4 converter warps
+
+template <bool GATEUP>
+struct MxCfg {
+  static constexpr int kATiles = GATEUP ? 2 : 1;
+  static constexpr int kABytes = 128 * 128;  // E4M3 operand tile (128-byte swizzle)
+  static constexpr int kPBytes = 128 * 64;   // packed E2M1 tile (rows of 64 bytes)
+  static constexpr int kBBytes = kPairN * 128;
+  static constexpr int kPOff = kATiles * kABytes + kBBytes;
+  static constexpr int kStageBytes = ((kPOff + kATiles * kPBytes + 1023) / 1024) * 1024;
+  static constexpr int kAccCols = kATiles * 4 * kPairN;
+  static constexpr int kTmemCols = 2 * kAccCols;
+  static constexpr int kMaxCtasPerSm = 512 / kTmemCols;  // TMEM columns of one SM
+};
+
+struct MxSmem {
+  size_t stages, bq, sas, comb, cw, bars, total;
+};
+
+template <bool GATEUP>
+__host__ __device__ inline MxSmem mx_smem(int nst, int nkb_cta, int K) {
+  using C = MxCfg<GATEUP>;
+  MxSmem s{};
+  size_t o = 0;
+  s.stages = o; o += (size_t)nst * C::kStageBytes;
+  s.bq = o;     o += GATEUP ? (size_t)nkb_cta * 128 : 0;  // hidden codes past the stages
+  s.sas = o;    o += (size_t)nkb_cta * 4;                 // activation scales
+  o = (o + 15) & ~size_t(15);
+  s.comb = o;   o += GATEUP ? 0 : (size_t)K * 512;        // combine rows
+  s.cw = o;     o += GATEUP ? 0 : 16 * 8;                 // combine weights + ids
+  s.bars = o;   o += 512;
+  s.total = o + 1024;
+  return s;
+}
+
+// Dynamic shared memory a launch requests: the layout, raised so that no more CTAs of the
+// launch share an SM than its TMEM columns hold.
+template <bool GATEUP>
+inline size_t mx_request(const PlanDevice& d, int nst, int nkb_cta, int K) {
+  using C = MxCfg<GATEUP>;
+  return std::max(mx_smem<GATEUP>(nst, nkb_cta, K).total, d.smem_per_sm / (C::kMaxCtasPerSm + 1) + 1);
+}
+
+// As plan_pair: gate/up may split its K blocks over a cluster (split-K terms land in CTA 0's
+// stages); down is fused with the combine, a cluster of K CTAs with every K block each.
+template <bool GATEUP>
+inline PairPlan plan_mx(const PlanDevice& d, int nkb, int64_t units, int K) {
+  using C = MxCfg<GATEUP>;
+  PairPlan best{1, std::min(nkb, 2)};
+  for (int s = 1; s <= (GATEUP ? 8 : 1); ++s) {
+    if (nkb % s) continue;
+    const int per = nkb / s;
+    if (s > 1 && per > kMaxSplitTerms) continue;
+    const int cluster = GATEUP ? s : K;
+    int chosen = 0;
+    for (int n = std::min(per, kMaxStages); n >= std::min(per, 2); --n) {
+      if (s > 1 && (size_t)C::kATiles * nkb * 512 > (size_t)n * C::kStageBytes) break;
+      const size_t smem = mx_request<GATEUP>(d, n, per, K);
+      if (smem > d.smem_optin) continue;
+      if (units * cluster <= resident_ctas(d, cluster, smem)) {
+        chosen = n;
+        break;
+      }
+    }
+    if (chosen) best = {s, chosen};
+  }
+  return best;
+}
+
 }  // namespace moe

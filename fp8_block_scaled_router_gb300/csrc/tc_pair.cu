@@ -135,9 +135,9 @@ __global__ void __launch_bounds__(kPairThreads, 3)
     tc::tmem_alloc(tmem_slot, C::kTmemCols);
     tc::tmem_relinquish();
   }
-  if (MODE == kGateUpFused) {  // B tile rows 1..15 stay zero
-    for (int i = threadIdx.x; i < nst * (C::kBBytes / 16); i += kPairThreads) {
-      const int s = i / (C::kBBytes / 16), c = i % (C::kBBytes / 16);
+  if (MODE == kGateUpFused) {  // B tile rows 1..15 stay zero (row 0, the first 128 bytes, is the quantisers')
+    for (int i = threadIdx.x; i < nst * (C::kBBytes / 16 - 8); i += kPairThreads) {
+      const int s = i / (C::kBBytes / 16 - 8), c = 8 + i % (C::kBBytes / 16 - 8);
       reinterpret_cast<uint4*>(stages + s * C::kStageBytes + C::kTxA)[c] = make_uint4(0, 0, 0, 0);
     }
   }
@@ -493,6 +493,21 @@ bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t row
   g_tmap_next = (g_tmap_next + 1) % kTmapCache;
   if (g_tmap_used < kTmapCache) ++g_tmap_used;
   return true;
+}
+
+// 2-D u8 tensor [rows][inner] (row stride = inner bytes), box box_inner bytes x box_rows, no
+// swizzle: the box lands as box_rows rows of box_inner bytes (packed sub-byte weights).
+bool make_tmap_u8_rows(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                       uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // 2-D FP32 tensor [rows][inner] (row stride inner * 4 bytes), box box_inner x box_rows

@@ -267,6 +267,33 @@ moe_status_t moe_fp8_forward_partials(const void* hidden, const int32_t* topk_id
 moe_status_t moe_fp8_combine_pairs(const float* y, const int32_t* topk_ids, const float* topk_w, int32_t M, void* out,
                                    const moe_fp8_shape_t* shape, cudaStream_t stream);
 
+/* The layer with MXFP4 expert weights ([AMDK] MoE shape token mxfp4_h6144_i768_e128_top4;
+ * [NKL] supported-targets table: MXFP4 kernels checked against FP64 dequantised references),
+ * few routed rows only (one unit per (token, slot) pair, M * top_k <= 256, else
+ * MOE_ERR_UNSUPPORTED). Two launches: gate/up quantising hidden itself, then down fused with
+ * the combine.
+ *   hidden, topk_ids, topk_w, out, workspace, shape: as for moe_fp8_forward
+ *   w13q       u8 [E][2I][H/2]  E2M1 codes, two per byte, the lower K index in the low nibble
+ *                               (rows 0..I-1 gate, I..2I-1 up)
+ *   w13_scale  u8 [E][2I][H/32] UE8M0 scale of each 32 consecutive K elements of a row
+ *                               (2^(e - 127); e = 255 is NaN)
+ *   w2q        u8 [E][H][I/2];  w2_scale u8 [E][H][I/32]
+ * Numerics: hidden and the activation as for moe_fp8_forward (E4M3 per 128 columns); each
+ * GEMM output is, per 128-wide K block kb ascending, T_kb = sum over its four 32-wide
+ * sub-blocks s ascending of P_s * 2^(e_s - 127) (FP32 from 0; P_s the 32-term dot product of
+ * the E4M3 activation and E2M1 weight values, summed in FP32 on the tensor core), then
+ * acc = acc + T_kb * sa_kb (FP32 from 0); SiLU, requantisation and the slot-order combine as
+ * for moe_fp8_forward. moe_mxfp4_route_forward is moe_route then moe_mxfp4_forward. */
+moe_status_t moe_mxfp4_forward(const void* hidden, const int32_t* topk_ids, const float* topk_w, int32_t M,
+                               const uint8_t* w13q, const uint8_t* w13_scale, const uint8_t* w2q,
+                               const uint8_t* w2_scale, void* out, void* workspace, size_t workspace_bytes,
+                               const moe_fp8_shape_t* shape, cudaStream_t stream);
+moe_status_t moe_mxfp4_route_forward(const void* hidden, const void* router_w, const float* bias, int32_t M,
+                                     int32_t renormalize, const uint8_t* w13q, const uint8_t* w13_scale,
+                                     const uint8_t* w2q, const uint8_t* w2_scale, void* out, int32_t* topk_ids,
+                                     float* topk_w, void* workspace, size_t workspace_bytes,
+                                     const moe_fp8_shape_t* shape, cudaStream_t stream);
+
 /* The few-routed-row path as its two kernels (one unit per (token, slot) pair; M * top_k
  * <= 256), the layout of the accepted M=1 MoE objects of [ARCH] (gate/up + SiLU +
  * quantisation, then down/reduce). moe_fp8_forward runs these two kernels when M * top_k

@@ -146,7 +146,7 @@ def pair_act_from_ws(ws, M, K, I):
     return q.reshape(M, K, I), sc.reshape(M, K, I // 128)
 
 
-def check_out_given_act(out_gpu, out_orc, ws, dbg, ids, w, x, what=""):
+def check_out_given_act(out_gpu, out_orc, ws, dbg, ids, w, x, what="", down_combine=None):
     """The output bound with the contract's allowed activation-code differences accounted for.
 
     An activation code that check_act accepted one step away from the oracle's (its value
@@ -155,7 +155,8 @@ def check_out_given_act(out_gpu, out_orc, ws, dbg, ids, w, x, what=""):
     cosine and exact zero rows; tokens whose activation codes all equal the oracle's against
     the full oracle for max|d| <= 2e-2 * rms(out_oracle); tokens with a differing code
     against the oracle's down projection and combine evaluated from the GPU's own codes and
-    scales (oracle.down_combine), with the same bound."""
+    scales (oracle.down_combine, or the ``down_combine(qact, s2, ids, w)`` given), with the
+    same bound."""
     M, K, I = ids.shape[0], ids.shape[1], x.shape.inter
     q_gpu, s_gpu = pair_act_from_ws(ws, M, K, I)
     valid = (ids >= 0) & (ids < x.shape.num_experts)
@@ -175,8 +176,11 @@ def check_out_given_act(out_gpu, out_orc, ws, dbg, ids, w, x, what=""):
     err_flip_full = float(np.max(np.abs(a[flip_tok] - b[flip_tok]))) if len(flip_tok) else 0.0
     err_flip_cond = 0.0
     if len(flip_tok):
-        cond = oracle.down_combine(q_gpu[flip_tok], s_gpu[flip_tok], ids[flip_tok], w[flip_tok], x.w2, x.s2,
-                                   nthreads=NTHREADS)
+        if down_combine is None:
+            cond = oracle.down_combine(q_gpu[flip_tok], s_gpu[flip_tok], ids[flip_tok], w[flip_tok], x.w2, x.s2,
+                                       nthreads=NTHREADS)
+        else:
+            cond = down_combine(q_gpu[flip_tok], s_gpu[flip_tok], ids[flip_tok], w[flip_tok])
         err_flip_cond = float(np.max(np.abs(a[flip_tok] - bf16_f64(cond))))
     print(f"out [{what}]: cos {cos:.8f}, rms {rms:.4g}; {len(flip_tok)} of {M} tokens have a differing "
           f"activation code; max|d|/rms: other tokens {err_keep / rms:.3e}, those tokens vs the full oracle "

@@ -201,6 +201,38 @@ def test_partials_and_pair_reducer_argument_errors(lib):
     assert L.moe_fp8_combine_pairs(FAKE, FAKE, FAKE, 4, FAKE, shape(hidden=200), stream=0, check=False) == 2
 
 
+def test_mxfp4_argument_errors(lib):
+    """moe_mxfp4_forward / moe_mxfp4_route_forward: null or misaligned pointers, a short
+    workspace, more routed rows than the pair kernels take (M * top_k > 256), M = 0."""
+    s = shape(max_tokens=64)
+    need = L.moe_fp8_workspace_bytes(s)
+    for i in range(8):  # hidden, ids, w, w13q, w13_scale, w2q, w2_scale, out
+        for bad in (0, MIS):
+            a = [FAKE] * 8
+            a[i] = bad
+            assert L.moe_mxfp4_forward(a[0], a[1], a[2], 4, *a[3:], FAKE, s, stream=0, ws_bytes=need,
+                                       check=False) == 1, (i, bad)
+    f = [FAKE] * 8
+    assert L.moe_mxfp4_forward(*f[:3], 4, *f[3:], FAKE, s, stream=0, ws_bytes=need - 1, check=False) == 3
+    assert L.moe_mxfp4_forward(*f[:3], 4, *f[3:], MIS, s, stream=0, ws_bytes=need, check=False) == 1
+    assert L.moe_mxfp4_forward(*f[:3], 0, *f[3:], FAKE, s, stream=0, ws_bytes=need, check=False) == 0
+    assert L.moe_mxfp4_forward(*f[:3], 33, *f[3:], FAKE, s, stream=0, ws_bytes=need, check=False) == 2  # 264 rows
+    assert L.moe_mxfp4_forward(*f[:3], 4, *f[3:], FAKE, shape(hidden=200), stream=0, ws_bytes=need,
+                               check=False) == 2
+    r = [FAKE] * 11  # hidden, router, (bias), w13q, w13_scale, w2q, w2_scale, out, ids, w
+    for i in [0, 1, 3, 4, 5, 6, 7, 8, 9]:
+        a = list(r)
+        a[i] = MIS
+        assert L.moe_mxfp4_route_forward(a[0], a[1], None, 4, 1, a[3], a[4], a[5], a[6], a[7], a[8], a[9], FAKE,
+                                         s, stream=0, ws_bytes=need, check=False) == 1, i
+    assert L.moe_mxfp4_route_forward(FAKE, FAKE, MIS, 4, 1, *[FAKE] * 7, FAKE, s, stream=0, ws_bytes=need,
+                                     check=False) == 1
+    assert L.moe_mxfp4_route_forward(FAKE, FAKE, None, 33, 1, *[FAKE] * 7, FAKE, s, stream=0, ws_bytes=need,
+                                     check=False) == 2
+    assert L.moe_mxfp4_route_forward(FAKE, FAKE, None, 0, 1, *[FAKE] * 7, FAKE, s, stream=0, ws_bytes=need,
+                                     check=False) == 0
+
+
 def test_zero_tokens_is_a_no_op(lib):
     """M = 0 returns MOE_OK after validation without touching the GPU (fake pointers)."""
     s = shape()

@@ -34,7 +34,7 @@ def plans(tmp_path_factory):
         sms, per_sm, mode, nkb, units, K, split, nst, smem, resident = (int(v) for v in line.split())
         rows.append(dict(sms=sms, per_sm=per_sm, mode=mode, nkb=nkb, units=units, K=K, split=split, nst=nst,
                          smem=smem, resident=resident))
-    assert len(rows) == 7 * 7
+    assert len(rows) == 7 * 12
     return rows
 
 
@@ -44,7 +44,7 @@ def test_plans_are_valid_on_every_device(plans):
         per = r["nkb"] // r["split"]
         assert 1 <= r["nst"] <= min(per, K_MAX_STAGES), r
         assert r["smem"] <= r["per_sm"] - 1024 or r["split"] == 1, r
-        cluster = 8 if r["mode"] == 3 else r["split"]
+        cluster = {3: 8, 11: 4}.get(r["mode"], r["split"])
         fits = r["units"] * cluster <= r["resident"]
         # a split is only chosen when the whole launch is resident at once
         assert r["split"] == 1 or fits, r
@@ -69,3 +69,23 @@ def test_decode_gate_up_plan_on_the_full_part_and_a_small_one(plans):
     # 8 SMs cannot hold a split launch: the unsplit plan with two stages
     assert dec[8]["split"] == 1 and dec[8]["nst"] == 2
     assert dec[38]["split"] < dec[152]["split"]
+
+
+TMEM_COLS = {10: 256, 11: 128}  # MXFP4 gate/up, down: columns one CTA allocates
+
+
+def test_mxfp4_plans_keep_tmem_within_the_sm(plans):
+    """No more MXFP4 CTAs of one launch fit on an SM (by shared memory, even without the
+    per-block reserve) than its 512 TMEM columns hold, on every device."""
+    for r in plans:
+        if r["mode"] not in TMEM_COLS:
+            continue
+        per_sm = r["per_sm"] // r["smem"]
+        assert per_sm * TMEM_COLS[r["mode"]] <= 512, r
+
+
+def test_mxfp4_decode_plan_splits_on_the_full_part(plans):
+    mx = {r["sms"]: r for r in plans if r["mode"] == 10 and r["units"] == 24 and r["per_sm"] == 233472}
+    assert mx[152]["split"] == 8 and 24 * 8 <= mx[152]["resident"]
+    tiny = [r for r in plans if r["mode"] == 10 and r["nkb"] == 2 and r["per_sm"] == 233472 and r["sms"] == 152]
+    assert tiny and tiny[0]["split"] == 2 and tiny[0]["nst"] == 1
