@@ -7,7 +7,8 @@ workload is decode: hidden 2048, intermediate 768, 128 experts, top-8 renormalis
 token per step, stepping through 10,000 seeded tokens; the same line carries a "prefill"
 record (M=4096, same shapes), the metric's tensor-bound half. Other workloads
 (--workload): verify, verify_skewed (M=12), wide (M=1..64, h6144/i768/e128/top4),
-prefill, prefill_zipf (M=4096).
+wide_mxfp4 (the same shape with MXFP4 expert weights: moe_mxfp4_route_forward), prefill,
+prefill_zipf (M=4096).
 
 value   tokens/s with inputs resident in HBM: exactly --steps steps timed with CUDA events
         around CUDA-graph replays; 8 weight replicas (decode/verify/wide) or 2 (prefill)
@@ -59,7 +60,13 @@ WORKLOADS = {
                                                 "router logits ~N(0,1)"),
     "prefill_zipf": dict(cfg="prefill_zipf", M=4096,
                          desc="prefill M=4096: h2048 i768 e128 top-8, Zipf(1.1) expert load"),
+    "wide_mxfp4": dict(cfg="wide_mxfp4", M=64, desc="wide expert, MXFP4 weights (E2M1 codes, UE8M0 scale per 32): "
+                                                   "h6144 i768 e128 top-4"),
 }
+
+
+def is_mx(cfg):
+    return cfg.endswith("_mxfp4")
 
 
 # routed rows up to which moe_fp8_forward runs the two pair kernels
@@ -107,15 +114,19 @@ def parse():
 
 
 # ----------------------------------------------------------------------------- helpers
-def per_expert_bytes(H, I):
+def per_expert_bytes(H, I, mx=False):
+    """Weight bytes of one expert: FP8 codes + FP32 scales per 128x128 block, or MXFP4 codes
+    (half a byte each) + one UE8M0 byte per 32 elements."""
+    if mx:
+        return 2 * I * H // 2 + 2 * I * H // 32, H * I // 2 + H * I // 32
     w13 = 2 * I * H + (2 * I // 128) * (H // 128) * 4
     w2 = H * I + (H // 128) * (I // 128) * 4
     return w13, w2
 
 
-def algorithmic(H, I, E, K, M, distinct):
+def algorithmic(H, I, E, K, M, distinct, mx=False):
     """Bytes and FLOPs one step must move / do at minimum."""
-    w13, w2 = per_expert_bytes(H, I)
+    w13, w2 = per_expert_bytes(H, I, mx)
     R = M * K
     byts = distinct * (w13 + w2) + H * E * 2 + M * H * 2 * 2 + M * K * 8
     flops = 2 * M * H * E + 6 * H * I * R
@@ -227,6 +238,8 @@ def oracle_tokens_per_s(x, M, budget_s=15.0, max_tokens=None, threads=None):
     K = x.shape.top_k
     total = x.hidden.shape[0]
 
+    mx = x.w13.shape[2] * 2 == x.shape.hidden  # packed E2M1 weights
+
     def run(n):
         hid = x.hidden[:n]
         t0 = time.perf_counter()
@@ -234,7 +247,10 @@ def oracle_tokens_per_s(x, M, budget_s=15.0, max_tokens=None, threads=None):
             ids, w = x.ids[:n], x.weights[:n]
         else:
             ids, w = oracle.route(hid, x.router_w, x.bias, K)
-        oracle.moe_forward(hid, ids, w, x.w13, x.s13, x.w2, x.s2, nthreads=cores)
+        if mx:
+            oracle.mxfp4_forward(hid, ids, w, x.w13, x.s13, x.w2, x.s2, nthreads=cores)
+        else:
+            oracle.moe_forward(hid, ids, w, x.w13, x.s13, x.w2, x.s2, nthreads=cores)
         return time.perf_counter() - t0
 
     n = min(cores, total)
@@ -255,8 +271,11 @@ def reference_arm(args, wl, world, rank):
     import oracle
     oracle.build()
     M = args.m or wl["M"]
-    x = inputs.make(wl["cfg"], tokens=10000 if wl["cfg"] == "decode" else None,
-                    M=M if wl["cfg"] == "wide" else None)
+    if is_mx(wl["cfg"]):
+        x = inputs.make_mx(wl["cfg"], M=M, tokens=M)
+    else:
+        x = inputs.make(wl["cfg"], tokens=10000 if wl["cfg"] == "decode" else None,
+                        M=M if wl["cfg"] == "wide" else None)
     steps = args.steps or 3
     warm = args.warmup if args.warmup is not None else 1
     tps, cores, n, dt = oracle_tokens_per_s(x, M, budget_s=20.0, threads=args.cpu_threads)
@@ -282,10 +301,14 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
 
     cfg = wl["cfg"]
     decode = cfg == "decode"
-    M = args.m if (args.m and cfg == "wide") else wl["M"]
+    mx = is_mx(cfg)
+    M = args.m if (args.m and cfg in ("wide", "wide_mxfp4")) else wl["M"]
     prefill = M >= 1024
     ntok = 10000 if decode else M
-    x = inputs.make(cfg, tokens=ntok if decode else None, M=M if cfg == "wide" else None)
+    if mx:
+        x = inputs.make_mx(cfg, M=M, tokens=M)
+    else:
+        x = inputs.make(cfg, tokens=ntok if decode else None, M=M if cfg == "wide" else None)
     H, I, E, K = x.shape.hidden, x.shape.inter, x.shape.num_experts, x.shape.top_k
     # each rank steps through its own token stream (a different slice of the seeded rows)
     if decode and world > 1:
@@ -317,7 +340,10 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
         b = i % nbatches
         hid = hidden_all[b * M:(b + 1) * M]
         w13, s13, w2, s2 = reps[i % n_rep]
-        if two_op:                  # the verify profile's two operations: producer, route reducer
+        if mx:                      # MXFP4 expert weights: routing + the two MXFP4 pair kernels
+            L.moe_mxfp4_route_forward(hid, router, bias, M, True, w13, s13, w2, s2, out[b], ids[b], wts[b], ws,
+                                      shape, stream=stream)
+        elif two_op:                # the verify profile's two operations: producer, route reducer
             L.moe_fp8_verify_produce(hid, router, bias, M, True, w13, s13, w2, s2, ids[b], wts[b], ws, shape,
                                      stream=stream)
             L.moe_fp8_verify_reduce(wts[b], M, out[b], ws, shape, stream=stream)
@@ -329,7 +355,7 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
             L.moe_fp8_route_forward(hid, router, bias, M, True, w13, s13, w2, s2, out[b], ids[b], wts[b], ws,
                                     shape, stream=stream)
 
-    kernels_per_step = launches_per_step(M, K, H, E, two_op)
+    kernels_per_step = 3 if mx else launches_per_step(M, K, H, E, two_op)
 
     # distinct experts per step (accounting only)
     for i in range(min(nbatches, 64)):
@@ -339,7 +365,7 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
     sample = src.reshape(-1, M * K)[: min(nbatches, 64)].cpu().numpy() if given_ids is None else \
         src.reshape(1, -1).cpu().numpy()
     distinct = float(np.mean([len(np.unique(r)) for r in sample]))
-    alg_bytes, alg_flops, gu_bytes, gu_flops = algorithmic(H, I, E, K, M, distinct)
+    alg_bytes, alg_flops, gu_bytes, gu_flops = algorithmic(H, I, E, K, M, distinct, mx)
 
     # ---- CUDA graphs: exactly `steps` steps are timed -- `full` replays of a G-step graph
     # (rotating over a few graphs so that consecutive replays walk different tokens) and one
@@ -411,7 +437,7 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
         roof["traffic"] = recorded_traffic("verify_produce", "verify")
     else:
         roof = dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, given_ids, ids, ws, shape,
-                               prefill, gu_bytes, gu_flops)
+                               prefill, gu_bytes, gu_flops, mx)
         roof["traffic"] = recorded_traffic("gate_up", "prefill" if prefill else args.workload)
 
     # ---- end to end through the public API with host buffers
@@ -435,6 +461,13 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
             L.moe_fp8_verify_produce(hid, router, bias, M, True, w13, s13, w2, s2, ids[b], wts[b], ws, shape,
                                      stream=cs)
             L.moe_fp8_verify_reduce(wts[b], M, out[b], ws, shape, stream=cs)
+            host_out[b].copy_(out[b], non_blocking=True)
+            continue
+        if mx:  # host copy in, the one-call MXFP4 layer, copy back
+            hid = stage[i % 2]
+            hid.copy_(host_in[b], non_blocking=True)
+            L.moe_mxfp4_route_forward(hid, router, bias, M, True, w13, s13, w2, s2, out[b], ids[b], wts[b], ws, shape,
+                                      stream=cs)
             host_out[b].copy_(out[b], non_blocking=True)
             continue
         if given_ids is None:
@@ -465,7 +498,8 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
                          f"std::thread over tokens"}
     rec = {"value": value, "unit": "tokens/s", "steps": steps, "warmup": warm, "ms_per_step": ms_per_step,
            "config": {"workload": wl["desc"], "M": M, "hidden": H, "inter": I, "experts": E, "top_k": K,
-                      "entry": ("moe_fp8_verify_produce + moe_fp8_verify_reduce" if two_op else
+                      "entry": ("moe_mxfp4_route_forward" if mx else
+                                "moe_fp8_verify_produce + moe_fp8_verify_reduce" if two_op else
                                 "moe_route + moe_fp8_forward (ids given)" if given_ids is not None else
                                 "moe_fp8_route_forward"),
                       "distinct_experts_per_step": distinct,
@@ -485,11 +519,11 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
 
 
 def dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, given_ids, ids, ws, shape, prefill,
-                    gu_bytes, gu_flops):
+                    gu_bytes, gu_flops, mx=False):
     """gate/up alone, back to back in a CUDA graph on its own stream (few routed rows: the
     direct gate/up kernel; otherwise the stage kernel, the same launch the forward makes,
     after one prepare), rotating weight replicas and the steps' expert sets."""
-    pair_mode = M * K <= PAIR_ROWS
+    pair_mode = mx or M * K <= PAIR_ROWS
     n_k = 200 if pair_mode else 10
     ks = torch.cuda.Stream()
     ks.wait_stream(torch.cuda.current_stream())
@@ -499,7 +533,9 @@ def dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, giv
         hid = hidden_all[b * M:(b + 1) * M]
         w13, s13, _, _ = reps[i % n_rep]
         ii = given_ids[0] if given_ids is not None else ids[b]
-        if pair_mode:
+        if mx:
+            L.moe_mxfp4_gate_up_direct(hid, ii, M, w13, s13, ws, shape, stream=st)
+        elif pair_mode:
             L.moe_fp8_gate_up_direct(hid, ii, M, w13, s13, ws, shape, stream=st)
         else:
             L.moe_fp8_gate_up(w13, s13, M, ws, shape, stream=st)
@@ -608,7 +644,9 @@ def ours_arm(args, wl, world, rank, local):
     if rank == 0:
         line = {"metric": METRIC, "value": rec["value"], "unit": "tokens/s", "n_gpus": world,
                 "steps": steps, "warmup": warm, "ms_per_step": rec["ms_per_step"], "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 (f32 accumulate)",
+                "scaling": "weak", "vs_baseline": None,
+                "dtype": ("mxfp4 weights (e2m1 + ue8m0 per 32), fp8_e4m3 activations, f32 accumulate"
+                          if is_mx(wl["cfg"]) else "fp8_e4m3 (f32 accumulate)"),
                 "data": "synthetic"}
         line.update({k: v for k, v in rec.items() if k not in ("value", "unit", "steps", "warmup", "ms_per_step")})
         if ver is not None:
@@ -628,9 +666,13 @@ def profile_steps(args, wl):
     from fp8_block_scaled_router_gb300 import inputs
 
     cfg = wl["cfg"]
-    M = args.m if (args.m and cfg == "wide") else wl["M"]
+    mx = is_mx(cfg)
+    M = args.m if (args.m and cfg in ("wide", "wide_mxfp4")) else wl["M"]
     n = 3 + args.profile_steps
-    x = inputs.make(cfg, tokens=n * M if cfg == "decode" else None, M=M if cfg == "wide" else None)
+    if mx:
+        x = inputs.make_mx(cfg, M=M, tokens=M)
+    else:
+        x = inputs.make(cfg, tokens=n * M if cfg == "decode" else None, M=M if cfg == "wide" else None)
     H, I, E, K = x.shape.hidden, x.shape.inter, x.shape.num_experts, x.shape.top_k
 
     def dev(a):
@@ -652,7 +694,9 @@ def profile_steps(args, wl):
         b = i % (hid_all.shape[0] // M)
         hid = hid_all[b * M:(b + 1) * M]
         w13, s13, w2, s2 = reps[i % 2]
-        if two_op:
+        if mx:
+            L.moe_mxfp4_route_forward(hid, router, bias, M, True, w13, s13, w2, s2, out, ids, w, ws, shape)
+        elif two_op:
             L.moe_fp8_verify_produce(hid, router, bias, M, True, w13, s13, w2, s2, ids, w, ws, shape)
             L.moe_fp8_verify_reduce(w, M, out, ws, shape)
         elif x.ids is not None:
@@ -672,8 +716,12 @@ def dominant_only(args, wl):
     from fp8_block_scaled_router_gb300 import inputs
 
     cfg = wl["cfg"]
-    M = args.m if (args.m and cfg == "wide") else wl["M"]
-    x = inputs.make(cfg, tokens=max(M, 8) if cfg == "decode" else None, M=M if cfg == "wide" else None)
+    mx = is_mx(cfg)
+    M = args.m if (args.m and cfg in ("wide", "wide_mxfp4")) else wl["M"]
+    if mx:
+        x = inputs.make_mx(cfg, M=M, tokens=M)
+    else:
+        x = inputs.make(cfg, tokens=max(M, 8) if cfg == "decode" else None, M=M if cfg == "wide" else None)
     H, I, E, K = x.shape.hidden, x.shape.inter, x.shape.num_experts, x.shape.top_k
 
     def dev(a):
@@ -695,11 +743,13 @@ def dominant_only(args, wl):
         ii = dev(x.ids[:M])
     else:
         L.moe_route(hid, router, bias, M, shape, True, ii, w)
-    if M * K > PAIR_ROWS:
+    if M * K > PAIR_ROWS and not mx:
         L.moe_fp8_prepare(hid, ii, M, ws, shape)
     for i in range(args.dominant_only):
         w13, s13, w2, s2 = reps[i % n_rep]
-        if M * K <= PAIR_ROWS:
+        if mx:
+            L.moe_mxfp4_gate_up_direct(hid, ii, M, w13, s13, ws, shape)
+        elif M * K <= PAIR_ROWS:
             L.moe_fp8_gate_up_direct(hid, ii, M, w13, s13, ws, shape)
         else:
             L.moe_fp8_gate_up(w13, s13, M, ws, shape)

@@ -19,6 +19,7 @@ using namespace moe;
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 // Device address of page-locked (pinned or registered) host memory, or null for any other
 // pointer (pageable host memory, device memory, unknown).
@@ -294,6 +295,7 @@ moe_status_t moe_mxfp4_forward(const void* hidden, const int32_t* topk_ids, cons
   for (const void* p : {hidden, (const void*)topk_ids, (const void*)topk_w, (const void*)w13q,
                         (const void*)w13_scale, (const void*)w2q, (const void*)w2_scale, (const void*)out})
     if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (!aligned32(w13q) || !aligned32(w2q)) return MOE_ERR_INVALID_ARG;
   Layout L;
   if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
   if (M == 0) return MOE_OK;
@@ -307,6 +309,38 @@ moe_status_t moe_mxfp4_forward(const void* hidden, const int32_t* topk_ids, cons
                                          ws, stream));
 }
 
+moe_status_t moe_mxfp4_gate_up_direct(const void* hidden, const int32_t* topk_ids, int32_t M, const uint8_t* w13q,
+                                      const uint8_t* w13_scale, void* workspace, size_t workspace_bytes,
+                                      const moe_fp8_shape_t* shape, cudaStream_t stream) {
+  if (moe_status_t st = check_common(shape, M)) return st;
+  for (const void* p : {hidden, (const void*)topk_ids, (const void*)w13q, (const void*)w13_scale})
+    if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (!aligned32(w13q)) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  if (M == 0) return MOE_OK;
+  if (!pair_capable((int64_t)M * shape->top_k)) return MOE_ERR_UNSUPPORTED;
+  return launched(launch_mx_gateup(w13q, w13_scale, topk_ids, static_cast<const uint16_t*>(hidden), M, shape->hidden,
+                                   shape->inter, shape->num_experts, shape->top_k, ws_ptrs(workspace, L), stream));
+}
+
+moe_status_t moe_mxfp4_down_combine(const int32_t* topk_ids, const float* topk_w, int32_t M, const uint8_t* w2q,
+                                    const uint8_t* w2_scale, void* out, void* workspace, size_t workspace_bytes,
+                                    const moe_fp8_shape_t* shape, cudaStream_t stream) {
+  if (moe_status_t st = check_common(shape, M)) return st;
+  for (const void* p : {(const void*)topk_ids, (const void*)topk_w, (const void*)w2q, (const void*)w2_scale,
+                        (const void*)out})
+    if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (!aligned32(w2q)) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  if (M == 0) return MOE_OK;
+  if (!pair_capable((int64_t)M * shape->top_k)) return MOE_ERR_UNSUPPORTED;
+  return launched(launch_mx_down_combine(w2q, w2_scale, topk_ids, topk_w, static_cast<uint16_t*>(out), M,
+                                         shape->hidden, shape->inter, shape->num_experts, shape->top_k,
+                                         ws_ptrs(workspace, L), stream));
+}
+
 moe_status_t moe_mxfp4_route_forward(const void* hidden, const void* router_w, const float* bias, int32_t M,
                                      int32_t renormalize, const uint8_t* w13q, const uint8_t* w13_scale,
                                      const uint8_t* w2q, const uint8_t* w2_scale, void* out, int32_t* topk_ids,
@@ -317,6 +351,7 @@ moe_status_t moe_mxfp4_route_forward(const void* hidden, const void* router_w, c
                         (const void*)w2_scale, (const void*)out, (const void*)topk_ids, (const void*)topk_w})
     if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
   if (bias && !aligned16(bias)) return MOE_ERR_INVALID_ARG;
+  if (!aligned32(w13q) || !aligned32(w2q)) return MOE_ERR_INVALID_ARG;
   Layout L;
   if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
   if (M == 0) return MOE_OK;

@@ -13,18 +13,20 @@
 // SiLU*up and the E4M3 requantisation (gate/up) or the slot-order combine (down), exactly as
 // for FP8 weights.
 //
-// GB300 design: the pair kernels of the FP8 path with an expansion stage. TMA brings each K
-// block's packed codes (64 bytes per weight row) into a staging buffer of the stage; two
-// converter warps expand them into the E4M3 operand tile (every E2M1 value is an E4M3 value:
-// a byte permute over the eight magnitudes and one over the sign) in the 128-byte
-// swizzled layout and release the stage to the MMA warp; the MMA warp issues one 128x16x32
-// MMA per 32-wide sub-block into its own accumulator (four per K block and weight tile); the
-// epilogue reads the four sums of its row, scales each by its row's UE8M0 factor and adds them
-// in sub-block order. Warp roles: 0 TMA, 1 TMEM + MMA, 2-5 epilogue (TMEM lane quadrant =
-// warp % 4), 6-9 converters; in the gate/up launch warps 1-9 first quantise the hidden row.
-// Split-K over a cluster and the down launch's fused combine are those of the FP8 pair
-// kernels (distributed-shared-memory stores between cluster barriers). Shared memory is
-// padded so that no more CTAs of one launch share an SM than its 512 TMEM columns hold.
+// GB300 design: the pair kernels of the FP8 path with the weight tile in E2M1. The tensor
+// map reads the packed codes (64 bytes per weight row and K block) and the TMA unit writes
+// them in the tensor core's padded 4-bit layout (each 16 codes in the low 8 bytes of a 16-byte
+// chunk, 128-byte swizzle), so a tile has the FP8 tile's footprint and descriptors, while
+// the load reads (and its barrier counts) the 64 packed bytes per row: half an FP8 tile. The MMA is kind::f8f6f4 with A = E2M1 (weights) and
+// B = E4M3 (the pair's activation row): every E2M1 value is an E4M3 value and every product
+// is exact in FP32. One 128x16x32 MMA per 32-wide sub-block writes its own accumulator (four
+// per K block and weight tile); the epilogue reads the four sums of its row, scales each by
+// the row's UE8M0 factor and adds them in sub-block order. The per-row scale bytes are loaded
+// four K blocks ahead of their use. Warp roles: 0 TMA, 1 TMEM + MMA, 2-5 epilogue (TMEM lane
+// quadrant = warp % 4); in the gate/up launch warps 1-5 first quantise the hidden row. Split-K
+// over a cluster and the down launch's fused combine are those of the FP8 pair kernels
+// (distributed-shared-memory stores between cluster barriers). Shared memory is padded so
+// that no more CTAs of one launch share an SM than its 512 TMEM columns hold.
 #include <cooperative_groups.h>
 #include <cudaTypedefs.h>
 
@@ -57,15 +59,8 @@ struct MxParams {
   Header* hdr;
 };
 
-// Four E2M1 codes (the low 16 bits of w, code i in bits 4i..4i+3) -> four E4M3 bytes: the
-// magnitude from a byte permute over the eight E4M3 codes of 0, 0.5, 1, 1.5, 2, 3, 4, 6, the
-// sign from a permute that picks 0x80 where bit 3 of the code is set.
-__device__ __forceinline__ uint32_t e2m1x4_to_e4m3(uint32_t w) {
-  constexpr uint32_t kLo = 0x3C383000u, kHi = 0x4C484440u;
-  const uint32_t mag = __byte_perm(kLo, kHi, w & 0x7777u);
-  const uint32_t sign = __byte_perm(0u, 0x80808080u, (w >> 1) & 0x4444u);
-  return mag | sign;
-}
+// kind::f8f6f4 instruction descriptor with A = E2M1 (type code 5), B = E4M3, D = FP32
+__host__ __device__ constexpr uint32_t idesc_e2m1_e4m3(int M, int N) { return tc::idesc_e4m3(M, N) | (5u << 7); }
 
 __device__ __forceinline__ float ue8m0(uint32_t e) {
   return e == 255u ? __uint_as_float(0x7FC00000u) : e == 0u ? __uint_as_float(0x00400000u) : __uint_as_float(e << 23);
@@ -114,8 +109,9 @@ __device__ __forceinline__ float mx_block_sum(const float* p, uint32_t e4) {
   return t;
 }
 
-// tmA: packed codes [rows][Kd/2] (box 64 bytes x 128 rows, no swizzle); tmB (down): the
-// activation codes [R][I] (box 128 bytes x 16 rows, 128-byte swizzle).
+// tmA: the packed codes as 4-bit elements [rows][Kd] (box 128 codes x 128 rows, padded 4-bit
+// layout, 128-byte swizzle); tmB (down): the activation codes [R][I] (box 128 bytes x 16
+// rows, 128-byte swizzle).
 template <bool GATEUP>
 __global__ void __launch_bounds__(kMxThreads, 2)
     mx_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -134,11 +130,9 @@ __global__ void __launch_bounds__(kMxThreads, 2)
   float* cwt = reinterpret_cast<float*>(base + SL.cw);  // [16] combine weights
   int* cid = reinterpret_cast<int*>(cwt + 16);           // [16] their expert ids
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + SL.bars);
-  uint64_t* fullA = bars;                     // [kMaxStages] packed weight codes landed
-  uint64_t* fullB = bars + kMaxStages;        // [kMaxStages] down: activation tile landed
-  uint64_t* conv = bars + 2 * kMaxStages;     // [kMaxStages] E4M3 tiles written
-  uint64_t* empty = bars + 3 * kMaxStages;    // [kMaxStages] the stage's MMAs are done
-  uint64_t* accf = bars + 4 * kMaxStages;     // [2]
+  uint64_t* full = bars;                      // [kMaxStages] the stage's tiles landed
+  uint64_t* empty = bars + kMaxStages;        // [kMaxStages] the stage's MMAs are done
+  uint64_t* accf = bars + 2 * kMaxStages;     // [2]
   uint64_t* acce = accf + 2;                  // [2]
   uint64_t* drainb = acce + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drainb + 1);
@@ -156,9 +150,7 @@ __global__ void __launch_bounds__(kMxThreads, 2)
     tc::prefetch_tmap(&tmA);
     if (!GATEUP) tc::prefetch_tmap(&tmB);
     for (int s = 0; s < nst; ++s) {
-      tc::mbar_init(&fullA[s], 1);
-      tc::mbar_init(&fullB[s], 1);
-      tc::mbar_init(&conv[s], 1);
+      tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -201,10 +193,9 @@ __global__ void __launch_bounds__(kMxThreads, 2)
   if (!GATEUP && warp == 0) {
     const int e = p.ids[pr];
     if (lane == 0) *e_sh = e;
-    if (e >= 0 && e < p.E && lane < npre) {
-      unsigned char* st = stages + lane * C::kStageBytes;
-      tc::mbar_arrive_expect_tx(&fullA[lane], C::kPBytes);
-      tc::tma_load_2d(st + C::kPOff, &tmA, &fullA[lane], (kb0 + lane) * 64, e * nrows_e + cb * 128);
+    if (e >= 0 && e < p.E && lane < npre) {  // one lane per stage: the weight tile, then the B tile
+      tc::mbar_arrive_expect_tx(&full[lane], C::kATx + C::kBBytes);
+      tc::tma_load_2d(stages + lane * C::kStageBytes, &tmA, &full[lane], (kb0 + lane) * 128, e * nrows_e + cb * 128);
     }
   }
   if (!GATEUP && rank == 0 && warp == 1 && lane < p.K) {
@@ -218,23 +209,21 @@ __global__ void __launch_bounds__(kMxThreads, 2)
     if (lane == 0) {
       const int e = *e_sh;
       if (e >= 0 && e < p.E)
-        for (int i = 0; i < npre; ++i) {
-          tc::mbar_arrive_expect_tx(&fullB[i], C::kBBytes);
-          tc::tma_load_2d(stages + i * C::kStageBytes + C::kABytes, &tmB, &fullB[i], (kb0 + i) * 128, pr);
-        }
+        for (int i = 0; i < npre; ++i)
+          tc::tma_load_2d(stages + i * C::kStageBytes + C::kABytes, &tmB, &full[i], (kb0 + i) * 128, pr);
     }
   } else if (warp == 0) {
     const int e = p.ids[pr];
     if (lane == 0) *e_sh = e;
-    if (e >= 0 && e < p.E && lane < npre) {  // one lane per stage: gate and up packed tiles
+    if (e >= 0 && e < p.E && lane < npre) {  // one lane per stage: the gate and up tiles
       unsigned char* st = stages + lane * C::kStageBytes;
-      tc::mbar_arrive_expect_tx(&fullA[lane], C::kATiles * C::kPBytes);
-      const int x = (kb0 + lane) * 64;
-      tc::tma_load_2d(st + C::kPOff, &tmA, &fullA[lane], x, e * nrows_e + cb * 128);
-      tc::tma_load_2d(st + C::kPOff + C::kPBytes, &tmA, &fullA[lane], x, e * nrows_e + p.I + cb * 128);
+      tc::mbar_arrive_expect_tx(&full[lane], C::kATiles * C::kATx);
+      const int x = (kb0 + lane) * 128;
+      tc::tma_load_2d(st, &tmA, &full[lane], x, e * nrows_e + cb * 128);
+      tc::tma_load_2d(st + C::kABytes, &tmA, &full[lane], x, e * nrows_e + p.I + cb * 128);
     }
   } else if (GATEUP) {
-    // warps 1..9 quantise the pair's hidden row for this CTA's K blocks: row 0 of the stage
+    // warps 1..5 quantise the pair's hidden row for this CTA's K blocks: row 0 of the stage
     // B tiles for the first stages, the rest into bq
     for (int i = warp - 1; i < p.nkb_cta; i += kMxThreads / 32 - 1) {
       const uint2 raw = *reinterpret_cast<const uint2*>(p.hidden + (size_t)tok * p.H + (kb0 + i) * 128 + lane * 4);
@@ -290,67 +279,26 @@ __global__ void __launch_bounds__(kMxThreads, 2)
         __syncwarp();
       }
       if (lane == 0) {
-        const int x = (kb0 + i) * 64;
-        tc::mbar_arrive_expect_tx(&fullA[s], C::kATiles * C::kPBytes);
-        tc::tma_load_2d(st + C::kPOff, &tmA, &fullA[s], x, e * nrows_e + cb * 128);
-        if (GATEUP) tc::tma_load_2d(st + C::kPOff + C::kPBytes, &tmA, &fullA[s], x, e * nrows_e + p.I + cb * 128);
-        if (!GATEUP) {
-          tc::mbar_arrive_expect_tx(&fullB[s], C::kBBytes);
-          tc::tma_load_2d(st + C::kABytes, &tmB, &fullB[s], (kb0 + i) * 128, pr);
-        }
+        const int x = (kb0 + i) * 128;
+        tc::mbar_arrive_expect_tx(&full[s], GATEUP ? C::kATiles * C::kATx : C::kATx + C::kBBytes);
+        tc::tma_load_2d(st, &tmA, &full[s], x, e * nrows_e + cb * 128);
+        if (GATEUP) tc::tma_load_2d(st + C::kABytes, &tmA, &full[s], x, e * nrows_e + p.I + cb * 128);
+        if (!GATEUP) tc::tma_load_2d(st + C::kABytes, &tmB, &full[s], x, pr);
       }
       issued = i + 1;
     }
     // no load is still writing when the CTA leaves (a no-op unless a wait gave up)
     if (lane == 0)
-      for (int i = issued - 1; i >= 0 && i >= issued - nst; --i) {
-        if (!tc::mbar_wait(&fullA[i % nst], (i / nst) & 1)) ok = false;
-        if (!GATEUP && !tc::mbar_wait(&fullB[i % nst], (i / nst) & 1)) ok = false;
-      }
-  } else if (valid && warp >= 6) {
-    // converters: 128 threads expand each stage's packed tiles into its E4M3 tiles; a thread
-    // takes 16 packed bytes (32 codes) of a row -> two 16-byte chunks of the swizzled row
-    const int ct = threadIdx.x - 192;
-    for (int i = 0; i < p.nkb_cta; ++i) {
-      const int s = i % nst;
-      const uint32_t ph = (i / nst) & 1;
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(&fullA[s], ph))) { ok = false; break; }
-      unsigned char* st = stages + s * C::kStageBytes;
-#pragma unroll
-      for (int t = 0; t < C::kATiles; ++t) {
-        const unsigned char* src = st + C::kPOff + t * C::kPBytes;
-        unsigned char* dst = st + t * C::kABytes;
-#pragma unroll 4
-        for (int x = ct; x < 128 * 4; x += 128) {
-          const int r = x >> 2, c = x & 3;  // packed chunk c of row r -> output chunks 2c, 2c + 1
-          const uint4 q = *reinterpret_cast<const uint4*>(src + r * 64 + c * 16);
-          uint4 o0, o1;
-          o0.x = e2m1x4_to_e4m3(q.x);
-          o0.y = e2m1x4_to_e4m3(q.x >> 16);
-          o0.z = e2m1x4_to_e4m3(q.y);
-          o0.w = e2m1x4_to_e4m3(q.y >> 16);
-          o1.x = e2m1x4_to_e4m3(q.z);
-          o1.y = e2m1x4_to_e4m3(q.z >> 16);
-          o1.z = e2m1x4_to_e4m3(q.w);
-          o1.w = e2m1x4_to_e4m3(q.w >> 16);
-          unsigned char* row = dst + (r >> 3) * 1024 + (r & 7) * 128;
-          *reinterpret_cast<uint4*>(row + (((2 * c) ^ (r & 7)) << 4)) = o0;
-          *reinterpret_cast<uint4*>(row + (((2 * c + 1) ^ (r & 7)) << 4)) = o1;
-        }
-      }
-      tc::fence_proxy_async_smem();  // generic writes of the operand tiles before the MMAs read them
-      tc::named_bar(2, 128);
-      if (ct == 0) tc::mbar_arrive(&conv[s]);
-    }
+      for (int i = issued - 1; i >= 0 && i >= issued - nst; --i)
+        if (!tc::mbar_wait(&full[i % nst], (i / nst) & 1)) ok = false;
   } else if (valid && warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = tc::idesc_e4m3(128, kPairN);
+      constexpr uint32_t idesc = idesc_e2m1_e4m3(128, kPairN);
       for (int i = 0; i < p.nkb_cta; ++i) {
         const int s = i % nst;
         const uint32_t ph = (i / nst) & 1;
         const int buf = i & 1;
-        if (!tc::mbar_wait(&conv[s], ph)) { ok = false; break; }
-        if (!GATEUP && !tc::mbar_wait(&fullB[s], ph)) { ok = false; break; }
+        if (!tc::mbar_wait(&full[s], ph)) { ok = false; break; }
         if (!tc::mbar_wait(&acce[buf], ((i >> 1) & 1) ^ 1)) { ok = false; break; }
         tc::fence_after_sync();
         const uint32_t sa = tc::smem_u32(stages + s * C::kStageBytes);
@@ -371,40 +319,57 @@ __global__ void __launch_bounds__(kMxThreads, 2)
       if (!tc::mbar_wait(drainb, 0)) ok = false;
     }
   } else if (valid && warp >= 2) {
-    // epilogue: thread <-> weight row (warp % 4) * 32 + lane of the 128-row tile
+    // epilogue: thread <-> weight row (warp % 4) * 32 + lane of the 128-row tile; the row's
+    // four scale bytes of K block i (one 32-bit load per tile) are loaded kAhead blocks early
+    constexpr int kAhead = 4;
     const int q = warp & 3, r = q * 32 + lane;
-    const size_t row0 = (size_t)e * nrows_e + cb * 128 + r;      // gate row (or down row)
-    const size_t row1 = (size_t)e * nrows_e + p.I + cb * 128 + r;  // up row
     const int nsub = p.nkb * 4;
-    for (int i = 0; i < p.nkb_cta; ++i) {
-      const int buf = i & 1;
-      const uint32_t e0 = *reinterpret_cast<const uint32_t*>(p.wscale + row0 * nsub + (kb0 + i) * 4);
-      const uint32_t e1 = GATEUP ? *reinterpret_cast<const uint32_t*>(p.wscale + row1 * nsub + (kb0 + i) * 4) : 0u;
-      if (!tc::mbar_wait(&accf[buf], (i >> 1) & 1)) { ok = false; break; }
-      tc::fence_after_sync();
-      const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + buf * C::kAccCols;
-      float v[8];
-      if (GATEUP) {
-        tmem_ld_sub8(ta, v);
-      } else {
-        float v4[4];
-        tmem_ld_sub4(ta, v4);
+    const uint8_t* sc0 = p.wscale + ((size_t)e * nrows_e + cb * 128 + r) * nsub + kb0 * 4;  // gate (or down) row
+    const uint8_t* sc1 = p.wscale + ((size_t)e * nrows_e + p.I + cb * 128 + r) * nsub + kb0 * 4;  // up row
+    const int n = p.nkb_cta;
+    uint32_t ea[kAhead], eb[kAhead];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) v[j] = v4[j];
-      }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&acce[buf]);
-      const float a = sas[i];
-      const float t0 = __fmul_rn(mx_block_sum(v, e0), a);
-      const float t1 = GATEUP ? __fmul_rn(mx_block_sum(v + 4, e1), a) : 0.0f;
-      if (split == 1) {
-        chain0 = __fadd_rn(chain0, t0);
-        if (GATEUP) chain1 = __fadd_rn(chain1, t1);
-      } else {
+    for (int j = 0; j < kAhead; ++j) {
+      ea[j] = j < n ? *reinterpret_cast<const uint32_t*>(sc0 + 4 * j) : 0u;
+      eb[j] = (GATEUP && j < n) ? *reinterpret_cast<const uint32_t*>(sc1 + 4 * j) : 0u;
+    }
+    for (int i0 = 0; i0 < n && ok; i0 += kAhead) {
 #pragma unroll
-        for (int j = 0; j < kMaxSplitTerms; ++j)
-          if (j == i) { term0[j] = t0; term1[j] = t1; }
+      for (int j = 0; j < kAhead; ++j) {
+        const int i = i0 + j;
+        if (i >= n || !ok) break;
+        const uint32_t e0 = ea[j], e1 = eb[j];
+        if (i + kAhead < n) {
+          ea[j] = *reinterpret_cast<const uint32_t*>(sc0 + 4 * (i + kAhead));
+          if (GATEUP) eb[j] = *reinterpret_cast<const uint32_t*>(sc1 + 4 * (i + kAhead));
+        }
+        const int buf = i & 1;
+        if (!tc::mbar_wait(&accf[buf], (i >> 1) & 1)) { ok = false; break; }
+        tc::fence_after_sync();
+        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + buf * C::kAccCols;
+        float v[8];
+        if (GATEUP) {
+          tmem_ld_sub8(ta, v);
+        } else {
+          float v4[4];
+          tmem_ld_sub4(ta, v4);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) v[k] = v4[k];
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&acce[buf]);
+        const float a = sas[i];
+        const float t0 = __fmul_rn(mx_block_sum(v, e0), a);
+        const float t1 = GATEUP ? __fmul_rn(mx_block_sum(v + 4, e1), a) : 0.0f;
+        if (split == 1) {
+          chain0 = __fadd_rn(chain0, t0);
+          if (GATEUP) chain1 = __fadd_rn(chain1, t1);
+        } else {
+#pragma unroll
+          for (int k = 0; k < kMaxSplitTerms; ++k)
+            if (k == i) { term0[k] = t0; term1[k] = t1; }
+        }
       }
     }
   }
@@ -414,7 +379,7 @@ __global__ void __launch_bounds__(kMxThreads, 2)
   if (clustered) {
     if (GATEUP) cluster.sync();
     else tc::cluster_wait();
-    if (warp >= 2 && warp < 6) {
+    if (warp >= 2) {
       const int r = (warp & 3) * 32 + lane;
       if (!GATEUP) {
         cluster.map_shared_rank(comb, 0)[rank * 128 + r] = chain0;
@@ -430,12 +395,12 @@ __global__ void __launch_bounds__(kMxThreads, 2)
       }
     }
     cluster.sync();
-  } else if (!GATEUP && warp >= 2 && warp < 6) {
+  } else if (!GATEUP && warp >= 2) {
     comb[(warp & 3) * 32 + lane] = chain0;
   }
   if (!ok) set_status(p.hdr, MOE_STATUS_WAIT_TIMEOUT);
 
-  if (rank == 0 && warp >= 2 && warp < 6) {
+  if (rank == 0 && warp >= 2) {
     const int q = warp & 3;
     const int r = q * 32 + lane;
     float g = chain0, u = chain1;
@@ -479,8 +444,7 @@ __global__ void __launch_bounds__(kMxThreads, 2)
 
 // ------------------------------------------------------------------------------ host side
 bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
-bool make_tmap_u8_rows(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
-                       uint32_t box_rows);
+bool make_tmap_e2m1(CUtensorMap* m, const void* base, uint64_t codes, uint64_t rows);
 
 namespace {
 
@@ -528,7 +492,7 @@ cudaError_t launch_mx_gateup(const uint8_t* w13q, const uint8_t* w13s, const int
   const DeviceInfo d = device_info();
   if (d.sms == 0) return cudaErrorInvalidDevice;
   CUtensorMap tA;
-  if (!make_tmap_u8_rows(&tA, w13q, (uint64_t)H / 2, (uint64_t)E * 2 * I, 64, 128)) return cudaErrorInvalidValue;
+  if (!make_tmap_e2m1(&tA, w13q, (uint64_t)H, (uint64_t)E * 2 * I)) return cudaErrorInvalidValue;
   MxParams prm{};
   prm.H = H; prm.I = I; prm.K = K; prm.E = E;
   prm.nkb = H / 128;
@@ -557,7 +521,7 @@ cudaError_t launch_mx_down_combine(const uint8_t* w2q, const uint8_t* w2s, const
   if (d.sms == 0) return cudaErrorInvalidDevice;
   CUtensorMap tA, tB;
   const int R = M * K;
-  if (!make_tmap_u8_rows(&tA, w2q, (uint64_t)I / 2, (uint64_t)E * H, 64, 128)) return cudaErrorInvalidValue;
+  if (!make_tmap_e2m1(&tA, w2q, (uint64_t)I, (uint64_t)E * H)) return cudaErrorInvalidValue;
   if (!make_tmap_u8(&tB, ws.act, (uint64_t)I, (uint64_t)R, kPairN)) return cudaErrorInvalidValue;
   MxParams prm{};
   prm.H = H; prm.I = I; prm.K = K; prm.E = E;

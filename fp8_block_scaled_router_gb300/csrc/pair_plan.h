@@ -118,19 +118,19 @@ inline PairPlan plan_pair(const PlanDevice& d, int nkb, int64_t units, int K, bo
   return best;
 }
 
-// ---- MXFP4 weights (mx_pair.cu): a stage holds the packed E2M1 tiles as TMA lands them
-// (64 bytes per weight row and K block) and the E4M3 operand tiles the converter warps
-// expand them into; one accumulator per 32-wide sub-block (four per K block and tile).
-constexpr int kMxThreads = 320;  // TMA, MMA, 4 epilogue, 4 converter warps
+// ---- MXFP4 weights (mx_pair.cu): TMA expands each K block's packed E2M1 codes (64 bytes
+// per weight row) into the tensor core's padded 4-bit layout (16 codes in the low half of
+// each 16-byte chunk), so an operand tile has the FP8 tile's 128 x 128-byte footprint; one
+// accumulator per 32-wide sub-block (four per K block and tile).
+constexpr int kMxThreads = 192;  // TMA, MMA, 4 epilogue warps
 
 template <bool GATEUP>
 struct MxCfg {
   static constexpr int kATiles = GATEUP ? 2 : 1;
-  static constexpr int kABytes = 128 * 128;  // E4M3 operand tile (128-byte swizzle)
-  static constexpr int kPBytes = 128 * 64;   // packed E2M1 tile (rows of 64 bytes)
+  static constexpr int kABytes = 128 * 128;  // one weight tile in shared memory (128-byte swizzle)
+  static constexpr int kATx = 128 * 64;      // the bytes its load counts: the packed codes read
   static constexpr int kBBytes = kPairN * 128;
-  static constexpr int kPOff = kATiles * kABytes + kBBytes;
-  static constexpr int kStageBytes = ((kPOff + kATiles * kPBytes + 1023) / 1024) * 1024;
+  static constexpr int kStageBytes = ((kATiles * kABytes + kBBytes + 1023) / 1024) * 1024;
   static constexpr int kAccCols = kATiles * 4 * kPairN;
   static constexpr int kTmemCols = 2 * kAccCols;
   static constexpr int kMaxCtasPerSm = 512 / kTmemCols;  // TMEM columns of one SM

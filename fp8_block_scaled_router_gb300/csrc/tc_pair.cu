@@ -495,18 +495,20 @@ bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t row
   return true;
 }
 
-// 2-D u8 tensor [rows][inner] (row stride = inner bytes), box box_inner bytes x box_rows, no
-// swizzle: the box lands as box_rows rows of box_inner bytes (packed sub-byte weights).
-bool make_tmap_u8_rows(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
-                       uint32_t box_rows) {
+// 2-D tensor of packed 4-bit codes [rows][codes] (two per byte, row stride codes / 2 bytes),
+// box 128 codes x 128 rows, written to shared memory in the tensor core's padded 4-bit layout
+// (the 8 bytes of each 16 codes in the low half of a 16-byte chunk) with the 128-byte swizzle:
+// a box occupies 128 x 128 bytes, like an FP8 tile. Needs a 32-byte aligned base, codes a
+// multiple of 128 and a row stride that is a multiple of 32 bytes.
+bool make_tmap_e2m1(CUtensorMap* m, const void* base, uint64_t codes, uint64_t rows) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {inner};
-  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint64_t dims[2] = {codes, rows};
+  cuuint64_t strides[1] = {codes / 2};
+  cuuint32_t box[2] = {128, 128};
   cuuint32_t es[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

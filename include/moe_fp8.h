@@ -278,12 +278,16 @@ moe_status_t moe_fp8_combine_pairs(const float* y, const int32_t* topk_ids, cons
  *   w13_scale  u8 [E][2I][H/32] UE8M0 scale of each 32 consecutive K elements of a row
  *                               (2^(e - 127); e = 255 is NaN)
  *   w2q        u8 [E][H][I/2];  w2_scale u8 [E][H][I/32]
+ *   w13q and w2q must be 32-byte aligned (the tensor maps that expand the packed codes for
+ *   the tensor core require it), else MOE_ERR_INVALID_ARG.
  * Numerics: hidden and the activation as for moe_fp8_forward (E4M3 per 128 columns); each
  * GEMM output is, per 128-wide K block kb ascending, T_kb = sum over its four 32-wide
  * sub-blocks s ascending of P_s * 2^(e_s - 127) (FP32 from 0; P_s the 32-term dot product of
  * the E4M3 activation and E2M1 weight values, summed in FP32 on the tensor core), then
  * acc = acc + T_kb * sa_kb (FP32 from 0); SiLU, requantisation and the slot-order combine as
- * for moe_fp8_forward. moe_mxfp4_route_forward is moe_route then moe_mxfp4_forward. */
+ * for moe_fp8_forward. The tensor core reads the E2M1 codes directly (kind::f8f6f4 with an
+ * E2M1 operand; every E2M1 value is an E4M3 value, so each product is exact).
+ * moe_mxfp4_route_forward is moe_route then moe_mxfp4_forward. */
 moe_status_t moe_mxfp4_forward(const void* hidden, const int32_t* topk_ids, const float* topk_w, int32_t M,
                                const uint8_t* w13q, const uint8_t* w13_scale, const uint8_t* w2q,
                                const uint8_t* w2_scale, void* out, void* workspace, size_t workspace_bytes,
@@ -293,6 +297,19 @@ moe_status_t moe_mxfp4_route_forward(const void* hidden, const void* router_w, c
                                      const uint8_t* w2q, const uint8_t* w2_scale, void* out, int32_t* topk_ids,
                                      float* topk_w, void* workspace, size_t workspace_bytes,
                                      const moe_fp8_shape_t* shape, cudaStream_t stream);
+
+/* moe_mxfp4_forward as its two kernels (as moe_fp8_gate_up_direct / moe_fp8_down_combine):
+ * moe_mxfp4_gate_up_direct quantises hidden and writes the activation codes and scales in
+ * pair order to the workspace; moe_mxfp4_down_combine reads them and writes out. The down
+ * call reads topk_ids, topk_w, w2q and w2_scale while the kernel launched before it on
+ * `stream` may still be running (that kernel must not write them). Limits and errors as
+ * for moe_mxfp4_forward. */
+moe_status_t moe_mxfp4_gate_up_direct(const void* hidden, const int32_t* topk_ids, int32_t M, const uint8_t* w13q,
+                                      const uint8_t* w13_scale, void* workspace, size_t workspace_bytes,
+                                      const moe_fp8_shape_t* shape, cudaStream_t stream);
+moe_status_t moe_mxfp4_down_combine(const int32_t* topk_ids, const float* topk_w, int32_t M, const uint8_t* w2q,
+                                    const uint8_t* w2_scale, void* out, void* workspace, size_t workspace_bytes,
+                                    const moe_fp8_shape_t* shape, cudaStream_t stream);
 
 /* The few-routed-row path as its two kernels (one unit per (token, slot) pair; M * top_k
  * <= 256), the layout of the accepted M=1 MoE objects of [ARCH] (gate/up + SiLU +

@@ -213,6 +213,15 @@ def test_mxfp4_argument_errors(lib):
             assert L.moe_mxfp4_forward(a[0], a[1], a[2], 4, *a[3:], FAKE, s, stream=0, ws_bytes=need,
                                        check=False) == 1, (i, bad)
     f = [FAKE] * 8
+    for i in (3, 5):  # the packed weight codes must be 32-byte aligned
+        a = list(f)
+        a[i] = FAKE + 16
+        assert L.moe_mxfp4_forward(a[0], a[1], a[2], 4, *a[3:], FAKE, s, stream=0, ws_bytes=need,
+                                   check=False) == 1, i
+    assert L.moe_mxfp4_gate_up_direct(FAKE, FAKE, 4, FAKE + 16, FAKE, FAKE, s, stream=0, ws_bytes=need,
+                                      check=False) == 1
+    assert L.moe_mxfp4_down_combine(FAKE, FAKE, 4, FAKE + 16, FAKE, FAKE, FAKE, s, stream=0, ws_bytes=need,
+                                    check=False) == 1
     assert L.moe_mxfp4_forward(*f[:3], 4, *f[3:], FAKE, s, stream=0, ws_bytes=need - 1, check=False) == 3
     assert L.moe_mxfp4_forward(*f[:3], 4, *f[3:], MIS, s, stream=0, ws_bytes=need, check=False) == 1
     assert L.moe_mxfp4_forward(*f[:3], 0, *f[3:], FAKE, s, stream=0, ws_bytes=need, check=False) == 0
@@ -231,6 +240,19 @@ def test_mxfp4_argument_errors(lib):
                                      check=False) == 2
     assert L.moe_mxfp4_route_forward(FAKE, FAKE, None, 0, 1, *[FAKE] * 7, FAKE, s, stream=0, ws_bytes=need,
                                      check=False) == 0
+    for i in range(4):  # hidden, ids, w13q, w13_scale
+        a = [FAKE] * 4
+        a[i] = MIS
+        assert L.moe_mxfp4_gate_up_direct(a[0], a[1], 4, a[2], a[3], FAKE, s, stream=0, ws_bytes=need,
+                                          check=False) == 1, i
+    assert L.moe_mxfp4_gate_up_direct(FAKE, FAKE, 33, FAKE, FAKE, FAKE, s, stream=0, ws_bytes=need, check=False) == 2
+    for i in range(5):  # ids, w, w2q, w2_scale, out
+        a = [FAKE] * 5
+        a[i] = 0
+        assert L.moe_mxfp4_down_combine(a[0], a[1], 4, a[2], a[3], a[4], FAKE, s, stream=0, ws_bytes=need,
+                                        check=False) == 1, i
+    assert L.moe_mxfp4_down_combine(*[FAKE] * 2, 4, *[FAKE] * 3, FAKE, s, stream=0, ws_bytes=need - 1,
+                                    check=False) == 3
 
 
 def test_zero_tokens_is_a_no_op(lib):

@@ -115,7 +115,9 @@ def test_mxfp4_extreme_exponents():
     check_against_oracle(x, g, M, ids_o, w_o, out, "tiny_mxfp4 extreme exponents")
 
 
-def test_mxfp4_deterministic_and_route_forward_equal():
+def test_mxfp4_deterministic_route_forward_and_stages_equal():
+    """Two runs bit-identical; moe_mxfp4_route_forward == moe_route + moe_mxfp4_forward ==
+    moe_mxfp4_gate_up_direct + moe_mxfp4_down_combine, bit for bit."""
     x = workload("wide_mxfp4", E=16, tokens=64)
     M = 16
     g = GpuMoE(x, M)
@@ -127,7 +129,11 @@ def test_mxfp4_deterministic_and_route_forward_equal():
     ids2 = torch.empty_like(ids)
     w2 = torch.empty_like(w)
     L.moe_mxfp4_route_forward(hid, g.router, None, M, True, g.w13, g.s13, g.w2, g.s2, out, ids2, w2, g.ws, g.shape)
+    staged = torch.empty_like(a)
+    L.moe_mxfp4_gate_up_direct(hid, ids, M, g.w13, g.s13, g.ws, g.shape)
+    L.moe_mxfp4_down_combine(ids, w, M, g.w2, g.s2, staged, g.ws, g.shape)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
     assert torch.equal(ids, ids2) and torch.equal(w, w2) and torch.equal(a, out)
+    assert torch.equal(a, staged)
     assert g.status() == 0
