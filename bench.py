@@ -155,13 +155,16 @@ def kernel_source_hash(files=None):
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel, workload):
+def recorded_traffic(kernel, workload, M=None):
     """DRAM bytes per launch from a committed ncu summary, if the sources of that kernel
-    (the files the record lists) are unchanged since the counters were taken."""
+    (the files the record lists) are unchanged since the counters were taken and the record
+    was taken at this token count (when it names one)."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             d = json.load(f)
         rec = d.get(workload, {}).get(kernel)
+        if rec and "M" in rec and M is not None and rec["M"] != M:
+            return None
         if rec and rec.get("source_hash") == kernel_source_hash(rec.get("source_files")):
             return rec["dram_bytes_per_launch"]
     except Exception:
@@ -438,7 +441,7 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
     else:
         roof = dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, given_ids, ids, ws, shape,
                                prefill, gu_bytes, gu_flops, mx)
-        roof["traffic"] = recorded_traffic("gate_up", "prefill" if prefill else args.workload)
+        roof["traffic"] = recorded_traffic("gate_up", "prefill" if prefill else args.workload, M)
 
     # ---- end to end through the public API with host buffers
     e2e_steps = min(steps * max(1, n_soak), 3000 if decode else (500 if M <= 64 else 10))
