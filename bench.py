@@ -72,9 +72,9 @@ def is_mx(cfg):
 # routed rows up to which moe_fp8_forward runs the two pair kernels
 PAIR_ROWS = 64
 def launches_per_step(M, K, H, E, two_op=False):
-    """Our kernels per step: route, gate/up, down+combine up to PAIR_ROWS routed rows;
-    otherwise route, count+quantise, scatter, gather, gate/up, down, combine; the verify
-    profile's producer and reducer when `two_op`."""
+    """Our kernels per step (FP8 and MXFP4 alike): route, gate/up, down+combine up to PAIR_ROWS
+    routed rows; otherwise route, count+quantise, scatter, gather, gate/up, down, combine; the
+    verify profile's producer and reducer when `two_op`."""
     if two_op:
         return 2
     return 3 if M * K <= PAIR_ROWS else 7
@@ -358,7 +358,7 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
             L.moe_fp8_route_forward(hid, router, bias, M, True, w13, s13, w2, s2, out[b], ids[b], wts[b], ws,
                                     shape, stream=stream)
 
-    kernels_per_step = 3 if mx else launches_per_step(M, K, H, E, two_op)
+    kernels_per_step = launches_per_step(M, K, H, E, two_op)
 
     # distinct experts per step (accounting only)
     for i in range(min(nbatches, 64)):
@@ -526,8 +526,8 @@ def dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, giv
     """gate/up alone, back to back in a CUDA graph on its own stream (few routed rows: the
     direct gate/up kernel; otherwise the stage kernel, the same launch the forward makes,
     after one prepare), rotating weight replicas and the steps' expert sets."""
-    pair_mode = mx or M * K <= PAIR_ROWS
-    n_k = 200 if pair_mode else 10
+    pair_mode = M * K <= PAIR_ROWS
+    n_k = 200 if (pair_mode or mx) else 10
     ks = torch.cuda.Stream()
     ks.wait_stream(torch.cuda.current_stream())
 
@@ -536,15 +536,17 @@ def dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, giv
         hid = hidden_all[b * M:(b + 1) * M]
         w13, s13, _, _ = reps[i % n_rep]
         ii = given_ids[0] if given_ids is not None else ids[b]
-        if mx:
+        if mx and M * K <= PAIR_ROWS:
             L.moe_mxfp4_gate_up_direct(hid, ii, M, w13, s13, ws, shape, stream=st)
+        elif mx:
+            L.moe_mxfp4_gate_up(w13, s13, M, ws, shape, stream=st)
         elif pair_mode:
             L.moe_fp8_gate_up_direct(hid, ii, M, w13, s13, ws, shape, stream=st)
         else:
             L.moe_fp8_gate_up(w13, s13, M, ws, shape, stream=st)
 
     with torch.cuda.stream(ks):
-        if not pair_mode:
+        if not pair_mode:  # the stage kernels read the sort of one step
             ii0 = given_ids[0] if given_ids is not None else ids[0]
             L.moe_fp8_prepare(hidden_all[:M], ii0, M, ws, shape, stream=ks)
         gu(0, ks)
@@ -746,12 +748,14 @@ def dominant_only(args, wl):
         ii = dev(x.ids[:M])
     else:
         L.moe_route(hid, router, bias, M, shape, True, ii, w)
-    if M * K > PAIR_ROWS and not mx:
+    if M * K > PAIR_ROWS:
         L.moe_fp8_prepare(hid, ii, M, ws, shape)
     for i in range(args.dominant_only):
         w13, s13, w2, s2 = reps[i % n_rep]
-        if mx:
+        if mx and M * K <= PAIR_ROWS:
             L.moe_mxfp4_gate_up_direct(hid, ii, M, w13, s13, ws, shape)
+        elif mx:
+            L.moe_mxfp4_gate_up(w13, s13, M, ws, shape)
         elif M * K <= PAIR_ROWS:
             L.moe_fp8_gate_up_direct(hid, ii, M, w13, s13, ws, shape)
         else:

@@ -164,6 +164,9 @@ moe_status_t moe_fp8_gate_up(const uint8_t* w13, const float* w13_scale, int32_t
   if (use_pair_mode(R))
     return launched(launch_pair_gateup(w13, w13_scale, ws.pair_expert, nullptr, M, shape->hidden,
                                        shape->inter, shape->num_experts, shape->top_k, ws, stream));
+  if (use_group_mode(R))
+    return launched(launch_gpair_gateup(false, w13, w13_scale, R, shape->hidden, shape->inter, shape->num_experts,
+                                        L.max_groups, ws, stream));
   return launched(launch_grouped_gateup(w13, w13_scale, R, shape->hidden, shape->inter, shape->num_experts,
                                         max_tiles_for(R, shape->num_experts, kTileRows), ws, stream));
 }
@@ -181,6 +184,9 @@ moe_status_t moe_fp8_down(const uint8_t* w2, const float* w2_scale, int32_t M, v
   if (use_pair_mode(R))
     return launched(launch_pair_down(w2, w2_scale, ws.pair_expert, nullptr, nullptr, M, shape->hidden,
                                      shape->inter, shape->num_experts, shape->top_k, ws, stream));
+  if (use_group_mode(R))
+    return launched(launch_gpair_down(false, w2, w2_scale, R, shape->hidden, shape->inter, shape->num_experts,
+                                      L.max_groups, ws, stream));
   return launched(launch_grouped_down(w2, w2_scale, R, shape->hidden, shape->inter, shape->num_experts,
                                       max_tiles_for(R, shape->num_experts, kTileRows), ws, stream));
 }
@@ -227,14 +233,22 @@ moe_status_t forward_impl(const void* hidden, Norm nm, const int32_t* topk_ids, 
     return launched(launch_pair_down(w2, w2_scale, topk_ids, topk_w, static_cast<uint16_t*>(out), M, H, I, E, K,
                                      ws, stream));
   }
-  // many routed rows: quantise (through the norm, if any) and sort into expert tiles, the
-  // two tile GEMMs, the slot-order combine
-  const int64_t tiles = max_tiles_for(R, E, kTileRows);
+  // more routed rows: quantise (through the norm, if any) and sort by expert; then the
+  // expert-grouped pair kernels (groups of up to 16 rows) or, for many rows, the two tile
+  // GEMMs over 128-row tiles; the slot-order combine
   if (moe_status_t st = launched(launch_sort_gather(static_cast<const uint16_t*>(hidden), nm, topk_ids, M, H, E, K,
                                                     ws, stream)))
     return st;
-  if (moe_status_t st = launched(launch_grouped_gateup(w13, w13_scale, R, H, I, E, tiles, ws, stream))) return st;
-  if (moe_status_t st = launched(launch_grouped_down(w2, w2_scale, R, H, I, E, tiles, ws, stream))) return st;
+  if (use_group_mode(R)) {
+    if (moe_status_t st = launched(launch_gpair_gateup(false, w13, w13_scale, R, H, I, E, L.max_groups, ws, stream)))
+      return st;
+    if (moe_status_t st = launched(launch_gpair_down(false, w2, w2_scale, R, H, I, E, L.max_groups, ws, stream)))
+      return st;
+  } else {
+    const int64_t tiles = max_tiles_for(R, E, kTileRows);
+    if (moe_status_t st = launched(launch_grouped_gateup(w13, w13_scale, R, H, I, E, tiles, ws, stream))) return st;
+    if (moe_status_t st = launched(launch_grouped_down(w2, w2_scale, R, H, I, E, tiles, ws, stream))) return st;
+  }
   return launched(launch_combine(topk_w, M, H, K, static_cast<uint16_t*>(out), ws, stream));
 }
 }  // namespace
@@ -299,14 +313,25 @@ moe_status_t moe_mxfp4_forward(const void* hidden, const int32_t* topk_ids, cons
   Layout L;
   if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
   if (M == 0) return MOE_OK;
-  if (!pair_capable((int64_t)M * shape->top_k)) return MOE_ERR_UNSUPPORTED;
   const int H = shape->hidden, I = shape->inter, E = shape->num_experts, K = shape->top_k;
   const WsPtrs ws = ws_ptrs(workspace, L);
-  if (moe_status_t st = launched(launch_mx_gateup(w13q, w13_scale, topk_ids, static_cast<const uint16_t*>(hidden), M,
-                                                  H, I, E, K, ws, stream)))
+  const int64_t R = (int64_t)M * K;
+  if (use_pair_mode(R)) {  // one unit per routed pair: gate/up, then down fused with the combine
+    if (moe_status_t st = launched(launch_mx_gateup(w13q, w13_scale, topk_ids, static_cast<const uint16_t*>(hidden),
+                                                    M, H, I, E, K, ws, stream)))
+      return st;
+    return launched(launch_mx_down_combine(w2q, w2_scale, topk_ids, topk_w, static_cast<uint16_t*>(out), M, H, I, E,
+                                           K, ws, stream));
+  }
+  // more rows: quantise and sort by expert, the expert-grouped pair kernels, the combine
+  if (moe_status_t st = launched(launch_sort_gather(static_cast<const uint16_t*>(hidden), Norm{nullptr, 0.0f}, topk_ids,
+                                                    M, H, E, K, ws, stream)))
     return st;
-  return launched(launch_mx_down_combine(w2q, w2_scale, topk_ids, topk_w, static_cast<uint16_t*>(out), M, H, I, E, K,
-                                         ws, stream));
+  if (moe_status_t st = launched(launch_gpair_gateup(true, w13q, w13_scale, R, H, I, E, L.max_groups, ws, stream)))
+    return st;
+  if (moe_status_t st = launched(launch_gpair_down(true, w2q, w2_scale, R, H, I, E, L.max_groups, ws, stream)))
+    return st;
+  return launched(launch_combine(topk_w, M, H, K, static_cast<uint16_t*>(out), ws, stream));
 }
 
 moe_status_t moe_mxfp4_gate_up_direct(const void* hidden, const int32_t* topk_ids, int32_t M, const uint8_t* w13q,
@@ -341,6 +366,32 @@ moe_status_t moe_mxfp4_down_combine(const int32_t* topk_ids, const float* topk_w
                                          ws_ptrs(workspace, L), stream));
 }
 
+moe_status_t moe_mxfp4_gate_up(const uint8_t* w13q, const uint8_t* w13_scale, int32_t M, void* workspace,
+                               size_t workspace_bytes, const moe_fp8_shape_t* shape, cudaStream_t stream) {
+  if (moe_status_t st = check_common(shape, M)) return st;
+  if (!w13q || !w13_scale || !aligned32(w13q) || !aligned16(w13_scale)) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  if (M == 0) return MOE_OK;
+  const int64_t R = (int64_t)M * shape->top_k;
+  if (use_pair_mode(R)) return MOE_ERR_UNSUPPORTED;  // the workspace holds no sort at so few rows
+  return launched(launch_gpair_gateup(true, w13q, w13_scale, R, shape->hidden, shape->inter, shape->num_experts,
+                                      L.max_groups, ws_ptrs(workspace, L), stream));
+}
+
+moe_status_t moe_mxfp4_down(const uint8_t* w2q, const uint8_t* w2_scale, int32_t M, void* workspace,
+                            size_t workspace_bytes, const moe_fp8_shape_t* shape, cudaStream_t stream) {
+  if (moe_status_t st = check_common(shape, M)) return st;
+  if (!w2q || !w2_scale || !aligned32(w2q) || !aligned16(w2_scale)) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  if (M == 0) return MOE_OK;
+  const int64_t R = (int64_t)M * shape->top_k;
+  if (use_pair_mode(R)) return MOE_ERR_UNSUPPORTED;
+  return launched(launch_gpair_down(true, w2q, w2_scale, R, shape->hidden, shape->inter, shape->num_experts,
+                                    L.max_groups, ws_ptrs(workspace, L), stream));
+}
+
 moe_status_t moe_mxfp4_route_forward(const void* hidden, const void* router_w, const float* bias, int32_t M,
                                      int32_t renormalize, const uint8_t* w13q, const uint8_t* w13_scale,
                                      const uint8_t* w2q, const uint8_t* w2_scale, void* out, int32_t* topk_ids,
@@ -355,7 +406,6 @@ moe_status_t moe_mxfp4_route_forward(const void* hidden, const void* router_w, c
   Layout L;
   if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
   if (M == 0) return MOE_OK;
-  if (!pair_capable((int64_t)M * shape->top_k)) return MOE_ERR_UNSUPPORTED;
   if (moe_status_t st = moe_route(hidden, router_w, bias, M, shape, renormalize, topk_ids, topk_w, stream)) return st;
   return moe_mxfp4_forward(hidden, topk_ids, topk_w, M, w13q, w13_scale, w2q, w2_scale, out, workspace,
                            workspace_bytes, shape, stream);

@@ -20,7 +20,8 @@ constexpr int kBlock = 128;  // block-scale grid: 128x128 for weights, 1x128 for
 struct Header {             // first 256 bytes
   uint32_t status;          // MOE_STATUS_* bits, cleared by moe_fp8_workspace_init
   uint32_t n_tiles;         // tiles written by the last prepare
-  uint32_t pad[62];
+  uint32_t n_groups;        // groups of up to kGroupRows rows written by the last prepare
+  uint32_t pad[61];
 };
 
 struct Tile {               // a run of up to `tile_rows` expert-sorted rows of one expert
@@ -31,11 +32,11 @@ struct Tile {               // a run of up to `tile_rows` expert-sorted rows of 
 };
 
 struct Layout {
-  size_t header, tickets, qa, sa, offsets, row_src, perm_row, pair_expert, blk_counts, tiles, xp, sa_p, act,
-      act_scale, y, yt;
+  size_t header, tickets, qa, sa, offsets, row_src, perm_row, pair_expert, blk_counts, tiles, groups, xp, sa_p,
+      act, act_scale, y, yt;
   size_t hid_stage, out_stage, ids_stage, wts_stage;  // host-buffer calls: device copies
   size_t total;
-  int64_t R, max_tiles;
+  int64_t R, max_tiles, max_groups;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -46,6 +47,9 @@ constexpr int kTicketTokens = 16;
 
 // Routed rows per tile of the grouped GEMMs (the MMA's M).
 constexpr int kTileRows = 128;
+
+// Routed rows per group of the expert-grouped pair kernels (the MMA's N).
+constexpr int kGroupRows = 16;
 
 // Routed pairs per block of the multi-block counting sort.
 constexpr int kSortBlock = 256;
@@ -60,6 +64,12 @@ constexpr int kPairPreferRows = 64;
 inline bool pair_capable(int64_t R) { return R <= kPairMaxRows; }
 inline bool use_pair_mode(int64_t R) { return R <= kPairPreferRows; }
 
+// Above kPairPreferRows and up to kGroupMaxRows routed rows the layer sorts the rows and runs
+// the expert-grouped pair kernels (each expert's weights read once per 16 of its rows);
+// above that, the grouped GEMM over 128-row tiles.
+constexpr int kGroupMaxRows = 256;
+inline bool use_group_mode(int64_t R) { return R > kPairPreferRows && R <= kGroupMaxRows; }
+
 inline int64_t max_tiles_for(int64_t R, int E, int tile_rows) {
   // sum over experts of ceil(n_e / tile_rows) <= R / tile_rows + (non-empty experts)
   return R / tile_rows + (R < E ? R : E) + 1;
@@ -70,6 +80,7 @@ inline Layout make_layout(const moe_fp8_shape_t& s) {
   const int64_t H = s.hidden, I = s.inter, E = s.num_experts, K = s.top_k, Mx = s.max_tokens;
   L.R = Mx * K;
   L.max_tiles = max_tiles_for(L.R, (int)E, kTileRows);
+  L.max_groups = max_tiles_for(L.R, (int)E, kGroupRows);
   size_t o = 0;
   L.header = o;    o = align256(o + sizeof(Header));
   L.tickets = o;   o = align256(o + (size_t)(Mx < kTicketTokens ? Mx : kTicketTokens) * (H / kBlock) * 4);
@@ -81,6 +92,7 @@ inline Layout make_layout(const moe_fp8_shape_t& s) {
   L.pair_expert = o; o = align256(o + (size_t)L.R * 4);
   L.blk_counts = o; o = align256(o + (size_t)((L.R + kSortBlock - 1) / kSortBlock) * E * 4);
   L.tiles = o;     o = align256(o + (size_t)L.max_tiles * sizeof(Tile));
+  L.groups = o;    o = align256(o + (size_t)L.max_groups * sizeof(Tile));
   L.xp = o;        o = align256(o + (size_t)(L.R * H));
   L.sa_p = o;      o = align256(o + (size_t)(L.R * (H / kBlock)) * 4);
   L.act = o;       o = align256(o + (size_t)(L.R * I));
@@ -107,6 +119,7 @@ struct WsPtrs {
   int32_t* pair_expert;  // [R] expert of each routed pair, -1 if skipped (pair mode)
   int32_t* blk_counts;   // [R/kSortBlock][E] per-block expert histograms (sorted mode)
   Tile* tiles;
+  Tile* groups;     // runs of up to kGroupRows expert-sorted rows of one expert
   uint8_t* xp;      // [R][H] hidden codes gathered into expert-sorted row order
   float* sa_p;      // [R][H/128] their scales
   uint8_t* act;
@@ -120,7 +133,7 @@ inline WsPtrs ws_ptrs(void* ws, const Layout& L) {
                 reinterpret_cast<float*>(b + L.sa), reinterpret_cast<int32_t*>(b + L.offsets),
                 reinterpret_cast<int32_t*>(b + L.row_src), reinterpret_cast<int32_t*>(b + L.perm_row),
                 reinterpret_cast<int32_t*>(b + L.pair_expert), reinterpret_cast<int32_t*>(b + L.blk_counts),
-                reinterpret_cast<Tile*>(b + L.tiles),
+                reinterpret_cast<Tile*>(b + L.tiles), reinterpret_cast<Tile*>(b + L.groups),
                 reinterpret_cast<uint8_t*>(b + L.xp), reinterpret_cast<float*>(b + L.sa_p),
                 reinterpret_cast<uint8_t*>(b + L.act),
                 reinterpret_cast<float*>(b + L.act_scale), reinterpret_cast<float*>(b + L.y)};

@@ -38,6 +38,12 @@ cudaError_t launch_mx_gateup(const uint8_t* w13q, const uint8_t* w13s, const int
 cudaError_t launch_mx_down_combine(const uint8_t* w2q, const uint8_t* w2s, const int32_t* ids, const float* topk_w,
                                    uint16_t* out, int M, int H, int I, int E, int K, const WsPtrs& ws,
                                    cudaStream_t st);
+// gpair.cu: expert-grouped pair kernels over the sort's groups of up to kGroupRows rows
+// (FP8 or MXFP4 weights; scales FP32 or UE8M0)
+cudaError_t launch_gpair_gateup(bool mx, const uint8_t* w13, const void* s13, int64_t R, int H, int I, int E,
+                                int64_t max_groups, const WsPtrs& ws, cudaStream_t st);
+cudaError_t launch_gpair_down(bool mx, const uint8_t* w2, const void* s2, int64_t R, int H, int I, int E,
+                              int64_t max_groups, const WsPtrs& ws, cudaStream_t st);
 // combine.cu: out = slot-order combine of y (workspace rows through perm_row, or given rows in
 // pair order with skipped pairs named by their ids), and the sorted y gathered into pair order
 cudaError_t launch_combine(const float* topk_w, int M, int H, int K, uint16_t* out, const WsPtrs& ws,

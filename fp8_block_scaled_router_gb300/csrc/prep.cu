@@ -222,6 +222,22 @@ __global__ void __launch_bounds__(256) scatter_kernel(const int32_t* __restrict_
       for (int j = 0; j < tot; j += kTileRows, ++tb) ws.tiles[tb] = Tile{tid, base_e + j, min(kTileRows, tot - j), 0};
     }
     if (tid == 255) ws.hdr->n_tiles = (uint32_t)scan[255];
+    // and the list of groups of up to kGroupRows rows (the expert-grouped pair kernels' units)
+    __syncthreads();
+    const int ngroup = tid < E ? (tot + kGroupRows - 1) / kGroupRows : 0;
+    scan[tid] = ngroup;
+    __syncthreads();
+    for (int off = 1; off < 256; off <<= 1) {
+      const int v = tid >= off ? scan[tid - off] : 0;
+      __syncthreads();
+      scan[tid] += v;
+      __syncthreads();
+    }
+    if (tid < E) {
+      int gb = scan[tid] - ngroup;
+      for (int j = 0; j < tot; j += kGroupRows, ++gb) ws.groups[gb] = Tile{tid, base_e + j, min(kGroupRows, tot - j), 0};
+    }
+    if (tid == 255) ws.hdr->n_groups = (uint32_t)scan[255];
   }
 }
 

@@ -11,6 +11,8 @@
  *   combine    top-k weighted sum in slot order, no atomics         (moe_fp8_combine)
  * moe_fp8_forward runs prepare -> gate/up -> down -> combine, or, for at most 64 routed
  * rows (M * top_k), gate/up (quantising hidden itself) -> down fused with the combine.
+ * Between 65 and 256 routed rows gate/up and down run over groups of up to 16 sorted rows
+ * of one expert (each expert's weights read once per group); above, over 128-row tiles.
  * moe_fp8_route_forward_one_launch runs routing and the whole layer as a single kernel.
  *
  * Sources (web pages; each entry point names the passage that defines it):
@@ -148,8 +150,8 @@ moe_status_t moe_norm_route(const void* hidden, const void* norm_weight, float e
  * codes; each GEMM output is sum over 128-blocks kb ascending of P_kb * (sa_kb * sw_kb)
  * in FP32 (P_kb = the block's FP8 dot product on the tensor core or in FP32);
  * act = silu(g) * u in FP32; out = bf16(sum over slots j ascending of w_j * y_j).
- * With more than 64 routed rows (sorted expert tiles) the promotion is one fused
- * multiply-add per block (one rounding instead of two per step), silu's exponential is the
+ * Up to 256 routed rows the arithmetic is exactly the above. With more (128-row expert
+ * tiles) the promotion is one fused multiply-add per block (one rounding instead of two per step), silu's exponential is the
  * hardware base-2 exponential of a split argument with a fast division (a few ulp for every
  * g) and the requantisation multiplies by 448/amax (within one ulp of the division): inside
  * the same tolerances (activation codes may move one step next to a rounding boundary).
@@ -268,10 +270,11 @@ moe_status_t moe_fp8_combine_pairs(const float* y, const int32_t* topk_ids, cons
                                    const moe_fp8_shape_t* shape, cudaStream_t stream);
 
 /* The layer with MXFP4 expert weights ([AMDK] MoE shape token mxfp4_h6144_i768_e128_top4;
- * [NKL] supported-targets table: MXFP4 kernels checked against FP64 dequantised references),
- * few routed rows only (one unit per (token, slot) pair, M * top_k <= 256, else
- * MOE_ERR_UNSUPPORTED). Two launches: gate/up quantising hidden itself, then down fused with
- * the combine.
+ * [NKL] supported-targets table: MXFP4 kernels checked against FP64 dequantised references).
+ * Up to 64 routed rows (M * top_k): two launches, one unit per (token, slot) pair -- gate/up
+ * quantising hidden itself, then down fused with the combine. Above: quantise and sort the
+ * pairs by expert (as moe_fp8_prepare), gate/up and down over groups of up to 16 rows of one
+ * expert (each expert's weights read once per group), then the slot-order combine.
  *   hidden, topk_ids, topk_w, out, workspace, shape: as for moe_fp8_forward
  *   w13q       u8 [E][2I][H/2]  E2M1 codes, two per byte, the lower K index in the low nibble
  *                               (rows 0..I-1 gate, I..2I-1 up)
@@ -298,7 +301,19 @@ moe_status_t moe_mxfp4_route_forward(const void* hidden, const void* router_w, c
                                      float* topk_w, void* workspace, size_t workspace_bytes,
                                      const moe_fp8_shape_t* shape, cudaStream_t stream);
 
-/* moe_mxfp4_forward as its two kernels (as moe_fp8_gate_up_direct / moe_fp8_down_combine):
+/* moe_mxfp4_forward's path above 64 routed rows as stage calls, between moe_fp8_prepare
+ * (quantise and sort) and moe_fp8_combine, all on one stream with the same M and shape:
+ * moe_mxfp4_gate_up writes the activation codes and scales at the sorted rows, moe_mxfp4_down
+ * the FP32 down projections y at the sorted rows. MOE_ERR_UNSUPPORTED for M * top_k <= 64
+ * (moe_fp8_prepare does not sort so few rows). Weights and numerics as moe_mxfp4_forward;
+ * prepare + gate_up + down + combine equals moe_mxfp4_forward bit for bit. */
+moe_status_t moe_mxfp4_gate_up(const uint8_t* w13q, const uint8_t* w13_scale, int32_t M, void* workspace,
+                               size_t workspace_bytes, const moe_fp8_shape_t* shape, cudaStream_t stream);
+moe_status_t moe_mxfp4_down(const uint8_t* w2q, const uint8_t* w2_scale, int32_t M, void* workspace,
+                            size_t workspace_bytes, const moe_fp8_shape_t* shape, cudaStream_t stream);
+
+/* moe_mxfp4_forward's pair path (up to 256 routed rows) as its two kernels (as
+ * moe_fp8_gate_up_direct / moe_fp8_down_combine):
  * moe_mxfp4_gate_up_direct quantises hidden and writes the activation codes and scales in
  * pair order to the workspace; moe_mxfp4_down_combine reads them and writes out. The down
  * call reads topk_ids, topk_w, w2q and w2_scale while the kernel launched before it on
@@ -315,8 +330,8 @@ moe_status_t moe_mxfp4_down_combine(const int32_t* topk_ids, const float* topk_w
  * <= 256), the layout of the accepted M=1 MoE objects of [ARCH] (gate/up + SiLU +
  * quantisation, then down/reduce). moe_fp8_forward runs these two kernels when M * top_k
  * <= 64 (its gate/up launch also prefetches the routed experts' w2 blocks into L2; the
- * arithmetic is the same); above that it sorts the pairs into expert tiles, which re-reads
- * fewer weights. MOE_ERR_UNSUPPORTED above 256 rows. moe_fp8_gate_up_direct quantises hidden itself and writes the activation codes
+ * arithmetic is the same); above that it sorts the pairs by expert, which re-reads fewer
+ * weights. MOE_ERR_UNSUPPORTED above 256 rows. moe_fp8_gate_up_direct quantises hidden itself and writes the activation codes
  * and scales (pair order) to the workspace; moe_fp8_down_combine reads them and writes out
  * with the combine of moe_fp8_combine (slot order, FP32 multiply then add, from 0).
  * moe_fp8_down_combine reads topk_ids, topk_w, w2 and w2_scale while the kernel launched

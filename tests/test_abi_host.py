@@ -202,8 +202,9 @@ def test_partials_and_pair_reducer_argument_errors(lib):
 
 
 def test_mxfp4_argument_errors(lib):
-    """moe_mxfp4_forward / moe_mxfp4_route_forward: null or misaligned pointers, a short
-    workspace, more routed rows than the pair kernels take (M * top_k > 256), M = 0."""
+    """moe_mxfp4_forward / moe_mxfp4_route_forward and the two stage calls: null or misaligned
+    pointers, a short workspace, M = 0; the stage calls (pair kernels) refuse more than 256
+    routed rows."""
     s = shape(max_tokens=64)
     need = L.moe_fp8_workspace_bytes(s)
     for i in range(8):  # hidden, ids, w, w13q, w13_scale, w2q, w2_scale, out
@@ -225,7 +226,6 @@ def test_mxfp4_argument_errors(lib):
     assert L.moe_mxfp4_forward(*f[:3], 4, *f[3:], FAKE, s, stream=0, ws_bytes=need - 1, check=False) == 3
     assert L.moe_mxfp4_forward(*f[:3], 4, *f[3:], MIS, s, stream=0, ws_bytes=need, check=False) == 1
     assert L.moe_mxfp4_forward(*f[:3], 0, *f[3:], FAKE, s, stream=0, ws_bytes=need, check=False) == 0
-    assert L.moe_mxfp4_forward(*f[:3], 33, *f[3:], FAKE, s, stream=0, ws_bytes=need, check=False) == 2  # 264 rows
     assert L.moe_mxfp4_forward(*f[:3], 4, *f[3:], FAKE, shape(hidden=200), stream=0, ws_bytes=need,
                                check=False) == 2
     r = [FAKE] * 11  # hidden, router, (bias), w13q, w13_scale, w2q, w2_scale, out, ids, w
@@ -236,8 +236,6 @@ def test_mxfp4_argument_errors(lib):
                                          s, stream=0, ws_bytes=need, check=False) == 1, i
     assert L.moe_mxfp4_route_forward(FAKE, FAKE, MIS, 4, 1, *[FAKE] * 7, FAKE, s, stream=0, ws_bytes=need,
                                      check=False) == 1
-    assert L.moe_mxfp4_route_forward(FAKE, FAKE, None, 33, 1, *[FAKE] * 7, FAKE, s, stream=0, ws_bytes=need,
-                                     check=False) == 2
     assert L.moe_mxfp4_route_forward(FAKE, FAKE, None, 0, 1, *[FAKE] * 7, FAKE, s, stream=0, ws_bytes=need,
                                      check=False) == 0
     for i in range(4):  # hidden, ids, w13q, w13_scale
@@ -253,6 +251,13 @@ def test_mxfp4_argument_errors(lib):
                                         check=False) == 1, i
     assert L.moe_mxfp4_down_combine(*[FAKE] * 2, 4, *[FAKE] * 3, FAKE, s, stream=0, ws_bytes=need - 1,
                                     check=False) == 3
+    # group-mode stage calls: alignment, a short workspace, too few rows to have been sorted
+    assert L.moe_mxfp4_gate_up(FAKE + 16, FAKE, 16, FAKE, s, stream=0, ws_bytes=need, check=False) == 1
+    assert L.moe_mxfp4_down(FAKE, MIS, 16, FAKE, s, stream=0, ws_bytes=need, check=False) == 1
+    assert L.moe_mxfp4_gate_up(FAKE, FAKE, 16, FAKE, s, stream=0, ws_bytes=need - 1, check=False) == 3
+    assert L.moe_mxfp4_gate_up(FAKE, FAKE, 8, FAKE, s, stream=0, ws_bytes=need, check=False) == 2  # 64 rows
+    assert L.moe_mxfp4_down(FAKE, FAKE, 8, FAKE, s, stream=0, ws_bytes=need, check=False) == 2
+    assert L.moe_mxfp4_down(FAKE, FAKE, 0, FAKE, s, stream=0, ws_bytes=need, check=False) == 0
 
 
 def test_zero_tokens_is_a_no_op(lib):

@@ -25,12 +25,14 @@ def _build_lib():
 def _workload(name, M):
     if name == "grouped":  # 64 tokens x top-8 over 16 experts: the sorted-tile path
         return inputs.make("decode", E=16, tokens=M)
+    if name == "groups":   # 32 tokens x top-8 over 16 experts: the expert-grouped pair kernels
+        return inputs.make("decode", E=16, tokens=M)
     if name == "decode":
         return inputs.make(name, tokens=M)
     return inputs.make(name, M=M)
 
 
-DET_CASES = [("decode", 1), ("verify", 12), ("tiny", 4), ("grouped", 64), ("wide", 1), ("wide", 64),
+DET_CASES = [("decode", 1), ("verify", 12), ("tiny", 4), ("groups", 32), ("grouped", 64), ("wide", 1), ("wide", 64),
              ("prefill", 4096), ("prefill_zipf", 4096)]
 
 
@@ -87,7 +89,7 @@ def test_graph_capture_replay_matches_eager():
         assert torch.equal(ids2, ids_eager) and torch.equal(w2, w_eager)
 
 
-@pytest.mark.parametrize("name,M", [("decode", 1), ("verify_skewed", 12), ("tiny", 4), ("grouped", 64)])
+@pytest.mark.parametrize("name,M", [("decode", 1), ("verify_skewed", 12), ("tiny", 4), ("groups", 32), ("grouped", 64)])
 def test_forward_equals_stage_calls(name, M):
     """moe_fp8_forward (which may fuse stages) and the four stage calls give bitwise equal
     outputs: the fused kernels use the same arithmetic in the same order."""

@@ -21,7 +21,9 @@ pytestmark = pytest.mark.gpu
 if torch.cuda.is_available():
     import oracle
     from fp8_block_scaled_router_gb300 import _lib as L
-    from gpu_harness import NTHREADS, GpuMoE, check_act, check_out_given_act, to_dev, u16
+    from gpu_harness import NTHREADS, GpuMoE, check_act, check_out_given_act, check_permutation, to_dev, u16
+
+PAIR_ROWS = 64  # up to this many routed rows the layer runs one unit per pair
 
 _CACHE = {}
 
@@ -53,7 +55,11 @@ def check_against_oracle(x, g, M, ids_o, w_o, out, what):
                                       nthreads=NTHREADS)
     ws = g.ws_arrays(M)
     assert np.array_equal(ws["qa"], dbg["qa"]) and np.array_equal(ws["sa"], dbg["sa"]), what
-    ws["row_src"] = np.arange(M * g.K, dtype=np.int32)  # pair order
+    if M * g.K <= PAIR_ROWS:  # pair kernels: activation rows in pair order
+        ws["row_src"] = np.arange(M * g.K, dtype=np.int32)
+    else:                     # expert-grouped kernels: rows in the sort's order
+        check_permutation(ws, ids_o, x.shape.num_experts)
+        ws["row_src"] = ws["row_src"][: int(ws["offsets"][-1])]  # the placed rows (valid ids)
     valid = (ids_o >= 0) & (ids_o < x.shape.num_experts)
     if valid.all():
         check_act(ws, dbg, g.K, what)
@@ -62,13 +68,16 @@ def check_against_oracle(x, g, M, ids_o, w_o, out, what):
                                                                                   nthreads=NTHREADS))
 
 
+# pair kernels up to 64 routed rows, expert-grouped kernels above (groups of up to 16 rows of
+# one expert; at M=256 over 16 experts each expert spans about four groups)
 CASES = [("tiny_mxfp4", None, 1), ("tiny_mxfp4", None, 4), ("wide_mxfp4", 16, 1), ("wide_mxfp4", 16, 4),
-         ("wide_mxfp4", 16, 16), ("wide_mxfp4", 16, 64), ("wide_mxfp4", None, 1), ("wide_mxfp4", None, 64)]
+         ("wide_mxfp4", 16, 16), ("wide_mxfp4", 16, 32), ("wide_mxfp4", 16, 64), ("wide_mxfp4", 16, 256),
+         ("wide_mxfp4", None, 1), ("wide_mxfp4", None, 64)]
 
 
 @pytest.mark.parametrize("name,E,M", CASES, ids=[f"{n}-E{e or 'full'}-M{m}" for n, e, m in CASES])
 def test_mxfp4_forward_against_oracle(name, E, M):
-    x = workload(name, E=E, tokens=64 if name == "wide_mxfp4" else None)
+    x = workload(name, E=E, tokens=max(64, M) if name == "wide_mxfp4" else None)
     g = GpuMoE(x, M)
     ids_o, w_o = oracle.route(x.hidden[:M], x.router_w, None, x.shape.top_k)
     out = run_mx(g, to_dev(x.hidden[:M]), to_dev(ids_o), to_dev(w_o), M)
@@ -89,6 +98,22 @@ def test_mxfp4_skipped_pairs_flagged():
     torch.cuda.synchronize()
     assert g.status() & L.STATUS_BAD_EXPERT_ID
     check_against_oracle(x, g, M, bad, w_o, out, "tiny_mxfp4 skipped pairs")
+
+
+def test_mxfp4_skipped_pairs_group_mode():
+    """Skipped pairs with the expert-grouped kernels (48 tokens x top-2 = 96 routed rows)."""
+    x = workload("tiny_mxfp4", tokens=48)
+    M = 48
+    g = GpuMoE(x, M)
+    ids_o, w_o = oracle.route(x.hidden[:M], x.router_w, None, x.shape.top_k)
+    bad = ids_o.copy()
+    bad[0, 1] = -1
+    bad[7, 0] = 99
+    bad[30, 1] = -3
+    out = run_mx(g, to_dev(x.hidden[:M]), to_dev(bad), to_dev(w_o), M)
+    torch.cuda.synchronize()
+    assert g.status() & L.STATUS_BAD_EXPERT_ID  # the sort skips and flags them
+    check_against_oracle(x, g, M, bad, w_o, out, "tiny_mxfp4 skipped pairs, group mode")
 
 
 def test_mxfp4_extreme_exponents():
@@ -135,5 +160,24 @@ def test_mxfp4_deterministic_route_forward_and_stages_equal():
     torch.cuda.synchronize()
     assert torch.equal(a, b)
     assert torch.equal(ids, ids2) and torch.equal(w, w2) and torch.equal(a, out)
+    assert torch.equal(a, staged)
+    assert g.status() == 0
+
+
+def test_mxfp4_group_mode_stages_equal_forward():
+    """Above 64 routed rows: moe_fp8_prepare + moe_mxfp4_gate_up + moe_mxfp4_down +
+    moe_fp8_combine == moe_mxfp4_forward, bit for bit (48 tokens x top-4 = 192 rows)."""
+    x = workload("wide_mxfp4", E=16, tokens=64)
+    M = 48
+    g = GpuMoE(x, M)
+    hid = to_dev(x.hidden[:M])
+    ids, w = g.route(hid, M)
+    a = run_mx(g, hid, ids, w, M)
+    staged = torch.empty_like(a)
+    L.moe_fp8_prepare(hid, ids, M, g.ws, g.shape)
+    L.moe_mxfp4_gate_up(g.w13, g.s13, M, g.ws, g.shape)
+    L.moe_mxfp4_down(g.w2, g.s2, M, g.ws, g.shape)
+    L.moe_fp8_combine(w, M, staged, g.ws, g.shape)
+    torch.cuda.synchronize()
     assert torch.equal(a, staged)
     assert g.status() == 0

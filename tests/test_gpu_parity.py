@@ -201,6 +201,17 @@ def test_many_tiles_with_ragged_tails():
     check_all(x, 300, ids_o, ws, out, out_o, dbg, "ragged")
 
 
+def test_expert_groups_spanning_several_groups():
+    """The expert-grouped pair kernels (64 < routed rows <= 256) with experts holding more
+    than one group of 16 rows: 32 tokens top-8 over 16 experts (256 rows, 16 per expert on
+    average)."""
+    x = workload("decode", E=16, tokens=32)
+    _, ids_o, ws, out, out_o, dbg = run_forward_case(x, 32)
+    counts = np.bincount(ids_o.ravel(), minlength=16)
+    assert counts.max() > 16
+    check_all(x, 32, ids_o, ws, out, out_o, dbg, "expert groups")
+
+
 @pytest.mark.parametrize("name", ["prefill", "prefill_zipf"])
 def test_prefill_full_size(name):
     """The full M=4096 launch against the oracle on every token: hidden codes and scales,
