@@ -27,9 +27,9 @@
 // Warp roles: 0 TMA (weight tiles and the group's 16 B rows), 1 TMEM + MMA, 2-5 epilogue (TMEM
 // lane quadrant = warp % 4). MXFP4 weight tiles are written by TMA in the tensor core's
 // padded 4-bit layout (kind::f8f6f4, A = E2M1), one accumulator per 32-wide sub-block.
-// Every wait is bounded and reports MOE_STATUS_WAIT_TIMEOUT. The kernels are persistent (two
-// CTAs per SM) and deal the (group, output block) items round-robin, so the load stays even
-// for any group count the sort produces.
+// Every wait is bounded and reports MOE_STATUS_WAIT_TIMEOUT. The kernels are persistent (three
+// CTAs per SM, two for the MXFP4 gate/up) and deal the (group, output block) items
+// round-robin, so the load stays even for any group count the sort produces.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -54,11 +54,15 @@ struct GpCfg {
   static constexpr int kAccCols = kATiles * kSubs * kGroupRows;
   static constexpr int kTmemCols = 2 * kAccCols < 32 ? 32 : 2 * kAccCols;
   static constexpr int kMaxCtasPerSm = 512 / kTmemCols;
+  // CTAs per SM the launch plans for (and the register budget it is compiled to): three,
+  // except for the MXFP4 gate/up, whose 256 TMEM columns allow two
+  static constexpr int kCtasPerSm = kMaxCtasPerSm >= 3 ? 3 : 2;
 };
 
 struct GpParams {
   int H, I, E;
   int nkb, ncb, nst;
+  int sms;                // multiprocessors of the device
   const Tile* groups;
   const Header* hdr_ro;
   const void* w_scale;    // FP8: FP32 [E][N/128][Kd/128]; MXFP4: UE8M0 [E][N][Kd/32]
@@ -231,7 +235,7 @@ __device__ __forceinline__ void gp_promote(uint32_t ta, uint64_t* acce_buf, int 
 // buffer; the epilogue finishes an item (SiLU and requantisation, or the y stores) as its
 // last K block is promoted.
 template <bool MX, bool GATEUP>
-__global__ void __launch_bounds__(kGpThreads, 2)
+__global__ void __launch_bounds__(kGpThreads, GpCfg<MX, GATEUP>::kCtasPerSm)
     gpair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const GpParams p) {
   using C = GpCfg<MX, GATEUP>;
@@ -268,8 +272,19 @@ __global__ void __launch_bounds__(kGpThreads, 2)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   const int n_items = (int)*reinterpret_cast<volatile const uint32_t*>(&p.hdr_ro->n_groups) * p.ncb;
-  const int G = (int)gridDim.x;
-  if ((int)blockIdx.x >= n_items) return;
+  // the CTAs that take items: all the items at once if the grid holds them; for up to two
+  // rounds of the grid, two or three per SM, whichever needs fewer rounds x CTAs per SM (the
+  // items cost the same and an SM's bandwidth is shared by its CTAs); for more, the whole grid
+  // (the last round's share is small and more CTAs hide more latency); the rest leave at once
+  int G = (int)gridDim.x;
+  if (n_items <= G) {
+    G = n_items;
+  } else if (G > 2 * p.sms && n_items <= 2 * G) {
+    const int g2 = 2 * p.sms;
+    const long long c2 = (long long)((n_items + g2 - 1) / g2) * g2, c3 = (long long)((n_items + G - 1) / G) * G;
+    if (c2 < c3) G = g2;
+  }
+  if ((int)blockIdx.x >= G) return;
   const int my_items = (n_items - (int)blockIdx.x + G - 1) / G;
   const int total = my_items * nkb;  // (item, K block) steps
   if (warp == 1) {
@@ -473,23 +488,31 @@ void set_gp_attrs(const DeviceInfo& d) {
   });
 }
 
-// The launch plan: two CTAs per SM (persistent), the deepest ring (<= kMaxStages) that keeps
-// them there; shared memory raised so that the CTAs on an SM never need more TMEM columns than
-// it has. The grid never exceeds the host's bound on the work items.
+// The launch plan (persistent): three CTAs per SM where their TMEM columns fit and a ring of
+// at least two stages does too (more CTAs split a small item count finer), else two; the
+// deepest ring (<= kMaxStages) at that count; shared memory raised so that the CTAs on an SM
+// never need more TMEM columns than it has. The grid never exceeds the host's bound on the
+// work items.
 template <bool MX, bool GATEUP>
 cudaError_t launch_gp(const CUtensorMap& tA, const CUtensorMap& tB, GpParams prm, int64_t max_groups,
                       cudaStream_t st) {
   using C = GpCfg<MX, GATEUP>;
   const DeviceInfo d = device_info();
   if (d.sms == 0) return cudaErrorInvalidDevice;
-  int n = kMaxStages;
-  for (; n > 1; --n)
-    if ((gp_smem<MX, GATEUP>(n).total + 1024) * 2 <= d.smem_per_sm) break;
-  prm.nst = n;
-  const size_t smem = std::max(gp_smem<MX, GATEUP>(n).total, d.smem_per_sm / (C::kMaxCtasPerSm + 1) + 1);
+  auto stages_for = [&](int cps) {
+    int n = kMaxStages;
+    for (; n > 1; --n)
+      if ((gp_smem<MX, GATEUP>(n).total + 1024) * cps <= d.smem_per_sm) break;
+    return n;
+  };
+  int cps = 2;
+  if (C::kCtasPerSm >= 3 && stages_for(3) >= 2) cps = 3;
+  prm.nst = stages_for(cps);
+  prm.sms = d.sms;
+  const size_t smem = std::max(gp_smem<MX, GATEUP>(prm.nst).total, d.smem_per_sm / (C::kMaxCtasPerSm + 1) + 1);
   if (smem > d.smem_optin) return cudaErrorInvalidConfiguration;
   set_gp_attrs<MX, GATEUP>(d);
-  const int64_t grid = std::min<int64_t>(2 * (int64_t)d.sms, max_groups * prm.ncb);
+  const int64_t grid = std::min<int64_t>((int64_t)cps * d.sms, max_groups * prm.ncb);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(kGpThreads, 1, 1);
