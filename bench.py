@@ -441,7 +441,7 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
     else:
         roof = dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, given_ids, ids, ws, shape,
                                prefill, gu_bytes, gu_flops, mx)
-        roof["traffic"] = recorded_traffic("gate_up", "prefill" if prefill else args.workload, M)
+        roof["traffic"] = recorded_traffic("gate_up", "prefill" if prefill else cfg, M)
 
     # ---- end to end through the public API with host buffers
     e2e_steps = min(steps * max(1, n_soak), 3000 if decode else (500 if M <= 64 else 10))

@@ -142,6 +142,9 @@ __global__ void __launch_bounds__(kRouteThreads)
       if constexpr (TB == 8) {
         const uint4 q = *reinterpret_cast<const uint4*>(xk + k * TB);
         xw[0] = q.x; xw[1] = q.y; xw[2] = q.z; xw[3] = q.w;
+      } else if constexpr (TB == 4) {
+        const uint2 q = *reinterpret_cast<const uint2*>(xk + k * TB);
+        xw[0] = q.x; xw[1] = q.y;
       } else if constexpr (TB == 2) {
         xw[0] = *reinterpret_cast<const uint32_t*>(xk + k * TB);
       } else {
@@ -184,6 +187,9 @@ __global__ void __launch_bounds__(kRouteThreads)
         if constexpr (TB == 8) {
           const uint4 q = *reinterpret_cast<const uint4*>(xk + k * TB);
           xw[0] = q.x; xw[1] = q.y; xw[2] = q.z; xw[3] = q.w;
+        } else if constexpr (TB == 4) {
+          const uint2 q = *reinterpret_cast<const uint2*>(xk + k * TB);
+          xw[0] = q.x; xw[1] = q.y;
         } else if constexpr (TB == 2) {
           xw[0] = *reinterpret_cast<const uint32_t*>(xk + k * TB);
         } else {
@@ -581,7 +587,8 @@ cudaError_t launch_route_t(const uint16_t* hidden, Norm nm, const uint16_t* rout
 }  // namespace
 
 // Tokens per cluster: 1 for a token or two, 8 (one 16-byte load of token values per k)
-// when there are many and CTA 0's chunk partials [nchunks][8][E] still fit.
+// when there are many and CTA 0's chunk partials [nchunks][8][E] still fit, else 4 or 2
+// (the wide hidden sizes: 48 chunks of partials for 8 tokens do not fit).
 cudaError_t launch_route(const uint16_t* hidden, Norm nm, const uint16_t* router_w, const float* bias, int M,
                          int H, int E, int K, int renorm, int32_t* ids, float* wts, cudaStream_t st) {
   const int nchunks = H / 128;
@@ -611,6 +618,16 @@ cudaError_t launch_route(const uint16_t* hidden, Norm nm, const uint16_t* router
   const size_t optin = device_info().smem_optin;
   if (M >= 16 && route_smem(8, nchunks / route_cluster(nchunks), E, nchunks, true).total <= optin)
     return launch_route_t<8>(hidden, nm, router_w, bias, M, H, E, K, renorm, ids, wts, st);
+  // 4 tokens per cluster only when 2 would need more than one wave of resident CTAs (wide
+  // hidden sizes: the CTA's router chunks fill an SM's shared memory): half the clusters, each
+  // CTA staging the same router rows
+  const int CL = route_cluster(nchunks);
+  const size_t smem2 = route_smem(2, nchunks / CL, E, nchunks, true).total;
+  const int64_t per_sm2 = (int64_t)(device_info().smem_per_sm / (smem2 + 1024));
+  const int64_t resident2 = (int64_t)device_info().sms * per_sm2 * 9 / 10;
+  if (M >= 8 && (int64_t)((M + 1) / 2) * CL > resident2 &&
+      route_smem(4, nchunks / CL, E, nchunks, true).total <= optin)
+    return launch_route_t<4>(hidden, nm, router_w, bias, M, H, E, K, renorm, ids, wts, st);
   if (M >= 4 && route_smem(2, nchunks / route_cluster(nchunks), E, nchunks, true).total <= optin)
     return launch_route_t<2>(hidden, nm, router_w, bias, M, H, E, K, renorm, ids, wts, st);
   return launch_route_t<1>(hidden, nm, router_w, bias, M, H, E, K, renorm, ids, wts, st);
