@@ -20,8 +20,10 @@ e2e     the same metric through the public API with host buffers: per step one
         the output to pinned host memory, route and forward enqueued by one call -- all
         inside the timed region (the Zipf workload, whose routing is given, uses a host copy,
         moe_route, moe_fp8_forward and a copy back).
-roofline the dominant kernel (gate/up) timed alone with CUDA events on its stream, its
-        algorithmic bytes (or FLOPs) per launch divided by the mean launch time.
+roofline the dominant kernel (gate/up, the launch the step makes; at few routed rows it also
+        prefetches the routed experts' w2 into L2, and those bytes count) timed alone with
+        CUDA events on its stream, its algorithmic bytes (or FLOPs) per launch divided by the
+        mean launch time; `direct` is the same kernel without the prefetch.
 cpu_baseline the oracle (plain C++ on the host cores) on a bounded sample of the same
         workload (rank 0, N=1 only).
 
@@ -97,7 +99,10 @@ def parse():
     p.add_argument("--cpu-threads", type=int, default=None, metavar="N",
                    help="host threads for the oracle (reference arm and cpu_baseline); default all")
     p.add_argument("--dominant-only", type=int, default=0, metavar="N",
-                   help="run only N launches of the dominant kernel (gate/up) and exit, for ncu")
+                   help="run only N launches of the dominant kernel (gate/up, as the step launches it) and exit, "
+                        "for ncu")
+    p.add_argument("--dominant-direct", action="store_true",
+                   help="with --dominant-only at few routed rows: the FP8 gate/up kernel without the w2 prefetch")
     p.add_argument("--profile-steps", type=int, default=0, metavar="N",
                    help="run N eager steps of the workload after 3 warm-up steps and exit, for a profiler's "
                         "launch list")
@@ -439,9 +444,15 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
                                alg_bytes - M * H * 2)
         roof["traffic"] = recorded_traffic("verify_produce", "verify")
     else:
+        w2_step = distinct * per_expert_bytes(H, I, mx)[1]
         roof = dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, given_ids, ids, ws, shape,
-                               prefill, gu_bytes, gu_flops, mx)
-        roof["traffic"] = recorded_traffic("gate_up", "prefill" if prefill else cfg, M)
+                               prefill, gu_bytes, gu_flops, mx, w2_bytes=w2_step)
+        roof["traffic"] = recorded_traffic(roof["kernel"], "prefill" if prefill else cfg, M)
+        if M * K <= PAIR_ROWS and not mx:  # the same kernel without the prefetch, for reference
+            dr = dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, given_ids, ids, ws, shape,
+                                 prefill, gu_bytes, gu_flops, mx, direct=True)
+            roof["direct"] = {k: dr[k] for k in ("kernel", "achieved", "frac", "alg_per_launch", "mean_launch_us")}
+            roof["direct"]["traffic"] = recorded_traffic("gate_up", cfg, M)
 
     # ---- end to end through the public API with host buffers
     e2e_steps = min(steps * max(1, n_soak), 3000 if decode else (500 if M <= 64 else 10))
@@ -522,11 +533,13 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
 
 
 def dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, given_ids, ids, ws, shape, prefill,
-                    gu_bytes, gu_flops, mx=False):
-    """gate/up alone, back to back in a CUDA graph on its own stream (few routed rows: the
-    direct gate/up kernel; otherwise the stage kernel, the same launch the forward makes,
-    after one prepare), rotating weight replicas and the steps' expert sets."""
+                    gu_bytes, gu_flops, mx=False, w2_bytes=0, direct=False):
+    """gate/up alone, back to back in a CUDA graph on its own stream, rotating weight replicas
+    and the steps' expert sets: the same launch the step makes (FP8, few routed rows: the
+    gate/up kernel with the routed experts' w2 L2 prefetch, whose bytes count; otherwise the
+    stage kernel after one prepare). `direct`: the FP8 few-row kernel without the prefetch."""
     pair_mode = M * K <= PAIR_ROWS
+    prefetch = pair_mode and not mx and not direct
     n_k = 200 if (pair_mode or mx) else 10
     ks = torch.cuda.Stream()
     ks.wait_stream(torch.cuda.current_stream())
@@ -534,9 +547,11 @@ def dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, giv
     def gu(i, st):
         b = i % nbatches
         hid = hidden_all[b * M:(b + 1) * M]
-        w13, s13, _, _ = reps[i % n_rep]
+        w13, s13, w2, s2 = reps[i % n_rep]
         ii = given_ids[0] if given_ids is not None else ids[b]
-        if mx and M * K <= PAIR_ROWS:
+        if prefetch:
+            L.moe_fp8_gate_up_prefetch(hid, ii, M, w13, s13, w2, s2, ws, shape, stream=st)
+        elif mx and M * K <= PAIR_ROWS:
             L.moe_mxfp4_gate_up_direct(hid, ii, M, w13, s13, ws, shape, stream=st)
         elif mx:
             L.moe_mxfp4_gate_up(w13, s13, M, ws, shape, stream=st)
@@ -569,8 +584,11 @@ def dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, giv
                 "peak": fp8_peak, "unit": "TFLOP/s", "frac": gu_flops / t_gu / 1e12 / fp8_peak,
                 "peak_source": f"{peak_src} bf16 x 2 (fp8/bf16 nominal ratio), burst"}
     else:
-        roof = {"bound": "hbm", "kernel": "gate_up", "achieved": gu_bytes / t_gu / 1e9, "peak": hbm,
-                "unit": "GB/s", "frac": gu_bytes / t_gu / 1e9 / hbm, "peak_source": f"{peak_src} hbm_gbs"}
+        nbytes = gu_bytes + (w2_bytes if prefetch else 0)
+        roof = {"bound": "hbm", "kernel": "gate_up" + (" (+ w2 L2 prefetch)" if prefetch else ""),
+                "achieved": nbytes / t_gu / 1e9, "peak": hbm, "unit": "GB/s", "frac": nbytes / t_gu / 1e9 / hbm,
+                "peak_source": f"{peak_src} hbm_gbs"}
+        gu_bytes = nbytes
     roof["alg_per_launch"] = gu_flops if prefill else gu_bytes
     roof["mean_launch_us"] = t_gu * 1e6
     return roof
@@ -756,6 +774,8 @@ def dominant_only(args, wl):
             L.moe_mxfp4_gate_up_direct(hid, ii, M, w13, s13, ws, shape)
         elif mx:
             L.moe_mxfp4_gate_up(w13, s13, M, ws, shape)
+        elif M * K <= PAIR_ROWS and not args.dominant_direct:
+            L.moe_fp8_gate_up_prefetch(hid, ii, M, w13, s13, w2, s2, ws, shape)
         elif M * K <= PAIR_ROWS:
             L.moe_fp8_gate_up_direct(hid, ii, M, w13, s13, ws, shape)
         else:

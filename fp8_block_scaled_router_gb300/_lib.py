@@ -31,7 +31,7 @@ EXPORTS = ("moe_fp8_version", "moe_fp8_workspace_bytes", "moe_fp8_workspace_init
            "moe_fp8_norm_forward", "moe_fp8_norm_route_forward", "moe_fp8_verify_produce",
            "moe_fp8_verify_reduce", "moe_fp8_forward_partials", "moe_fp8_combine_pairs", "moe_mxfp4_forward",
            "moe_mxfp4_route_forward", "moe_mxfp4_gate_up_direct", "moe_mxfp4_down_combine",
-           "moe_mxfp4_gate_up", "moe_mxfp4_down")
+           "moe_mxfp4_gate_up", "moe_mxfp4_down", "moe_fp8_gate_up_prefetch")
 
 
 class MoEError(RuntimeError):
@@ -94,6 +94,7 @@ def load(path: str = LIB):
             lib.moe_fp8_forward_partials.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, sz, sp, vp]
             lib.moe_fp8_combine_pairs.argtypes = [vp, vp, vp, i32, vp, sp, vp]
             lib.moe_mxfp4_forward.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, sz, sp, vp]
+            lib.moe_fp8_gate_up_prefetch.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, sz, sp, vp]
             lib.moe_mxfp4_gate_up.argtypes = [vp, vp, i32, vp, sz, sp, vp]
             lib.moe_mxfp4_down.argtypes = [vp, vp, i32, vp, sz, sp, vp]
             lib.moe_mxfp4_gate_up_direct.argtypes = [vp, vp, i32, vp, vp, vp, sz, sp, vp]
@@ -175,6 +176,15 @@ def moe_mxfp4_forward(hidden, topk_ids, topk_w, M, w13q, w13_scale, w2q, w2_scal
     return _check("moe_mxfp4_forward", load().moe_mxfp4_forward(
         _ptr(hidden), _ptr(topk_ids), _ptr(topk_w), int(M), _ptr(w13q), _ptr(w13_scale), _ptr(w2q),
         _ptr(w2_scale), _ptr(out), _ptr(workspace), nb, ctypes.byref(shape), _stream(stream)), check)
+
+
+def moe_fp8_gate_up_prefetch(hidden, topk_ids, M, w13, w13_scale, w2, w2_scale, workspace, shape: Shape,
+                             stream=None, ws_bytes=None, check=True):
+    """The forward's few-row gate/up launch (with the routed experts' w2 L2 prefetch)."""
+    nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return _check("moe_fp8_gate_up_prefetch", load().moe_fp8_gate_up_prefetch(
+        _ptr(hidden), _ptr(topk_ids), int(M), _ptr(w13), _ptr(w13_scale), _ptr(w2), _ptr(w2_scale),
+        _ptr(workspace), nb, ctypes.byref(shape), _stream(stream)), check)
 
 
 def moe_mxfp4_gate_up(w13q, w13_scale, M, workspace, shape: Shape, stream=None, ws_bytes=None, check=True):

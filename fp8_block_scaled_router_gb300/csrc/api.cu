@@ -428,6 +428,23 @@ moe_status_t moe_fp8_gate_up_direct(const void* hidden, const int32_t* topk_ids,
                                      stream));
 }
 
+moe_status_t moe_fp8_gate_up_prefetch(const void* hidden, const int32_t* topk_ids, int32_t M, const uint8_t* w13,
+                                      const float* w13_scale, const uint8_t* w2, const float* w2_scale,
+                                      void* workspace, size_t workspace_bytes, const moe_fp8_shape_t* shape,
+                                      cudaStream_t stream) {
+  if (moe_status_t st = check_common(shape, M)) return st;
+  for (const void* p : {hidden, (const void*)topk_ids, (const void*)w13, (const void*)w13_scale, (const void*)w2,
+                        (const void*)w2_scale})
+    if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  if (M == 0) return MOE_OK;
+  if (!pair_capable((int64_t)M * shape->top_k)) return MOE_ERR_UNSUPPORTED;
+  const WsPtrs ws = ws_ptrs(workspace, L);
+  return launched(launch_pair_gateup(w13, w13_scale, topk_ids, static_cast<const uint16_t*>(hidden), M, shape->hidden,
+                                     shape->inter, shape->num_experts, shape->top_k, ws, stream, w2, w2_scale));
+}
+
 moe_status_t moe_fp8_down_combine(const int32_t* topk_ids, const float* topk_w, int32_t M,
                                   const uint8_t* w2, const float* w2_scale, void* out, void* workspace,
                                   size_t workspace_bytes, const moe_fp8_shape_t* shape,

@@ -341,6 +341,14 @@ moe_status_t moe_fp8_gate_up_direct(const void* hidden, const int32_t* topk_ids,
                                     const uint8_t* w13, const float* w13_scale, void* workspace,
                                     size_t workspace_bytes, const moe_fp8_shape_t* shape,
                                     cudaStream_t stream);
+/* moe_fp8_gate_up_direct as moe_fp8_forward launches it for few routed rows: the same kernel,
+ * which also prefetches the routed experts' w2 and w2_scale blocks into L2 once its own
+ * weights have landed (so the down launch after it reads them from L2). Outputs equal
+ * moe_fp8_gate_up_direct's bit for bit; arguments and limits as for it, plus w2 / w2_scale. */
+moe_status_t moe_fp8_gate_up_prefetch(const void* hidden, const int32_t* topk_ids, int32_t M, const uint8_t* w13,
+                                      const float* w13_scale, const uint8_t* w2, const float* w2_scale,
+                                      void* workspace, size_t workspace_bytes, const moe_fp8_shape_t* shape,
+                                      cudaStream_t stream);
 moe_status_t moe_fp8_down_combine(const int32_t* topk_ids, const float* topk_w, int32_t M,
                                   const uint8_t* w2, const float* w2_scale, void* out, void* workspace,
                                   size_t workspace_bytes, const moe_fp8_shape_t* shape,

@@ -201,6 +201,21 @@ def test_partials_and_pair_reducer_argument_errors(lib):
     assert L.moe_fp8_combine_pairs(FAKE, FAKE, FAKE, 4, FAKE, shape(hidden=200), stream=0, check=False) == 2
 
 
+def test_gate_up_prefetch_argument_errors(lib):
+    s = shape()
+    need = L.moe_fp8_workspace_bytes(s)
+    for i in range(6):  # hidden, ids, w13, w13_scale, w2, w2_scale
+        for bad in (0, MIS):
+            a = [FAKE] * 6
+            a[i] = bad
+            assert L.moe_fp8_gate_up_prefetch(a[0], a[1], 1, *a[2:], FAKE, s, stream=0, ws_bytes=need,
+                                              check=False) == 1, (i, bad)
+    assert L.moe_fp8_gate_up_prefetch(*[FAKE] * 2, 1, *[FAKE] * 4, FAKE, s, stream=0, ws_bytes=need - 1,
+                                      check=False) == 3
+    assert L.moe_fp8_gate_up_prefetch(*[FAKE] * 2, 0, *[FAKE] * 4, FAKE, s, stream=0, ws_bytes=need,
+                                      check=False) == 0
+
+
 def test_mxfp4_argument_errors(lib):
     """moe_mxfp4_forward / moe_mxfp4_route_forward and the two stage calls: null or misaligned
     pointers, a short workspace, M = 0; the stage calls (pair kernels) refuse more than 256

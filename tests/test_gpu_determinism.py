@@ -106,3 +106,21 @@ def test_forward_equals_stage_calls(name, M):
     L.moe_fp8_combine(w, M, out_staged, g.ws, g.shape)
     torch.cuda.synchronize()
     assert torch.equal(out_fused, out_staged)
+
+
+def test_gate_up_prefetch_equals_direct():
+    """The forward's few-row gate/up launch (with the w2 L2 prefetch) writes the same
+    activation codes and scales as moe_fp8_gate_up_direct, bit for bit."""
+    from fp8_block_scaled_router_gb300 import _lib as L
+    x = _workload("decode", 4)
+    g = GpuMoE(x, 4)
+    hid = to_dev(x.hidden[:4])
+    ids, w = g.route(hid, 4)
+    L.moe_fp8_gate_up_direct(hid, ids, 4, g.w13, g.s13, g.ws, g.shape)
+    a = g.ws_arrays(4)
+    L.moe_fp8_gate_up_prefetch(hid, ids, 4, g.w13, g.s13, g.w2, g.s2, g.ws, g.shape)
+    b = g.ws_arrays(4)
+    torch.cuda.synchronize()
+    assert np.array_equal(a["act"], b["act"]) and np.array_equal(a["act_scale"], b["act_scale"])
+    assert np.array_equal(a["qa"], b["qa"]) and np.array_equal(a["sa"], b["sa"])
+    assert g.status() == 0
