@@ -75,10 +75,8 @@ def is_mx(cfg):
 PAIR_ROWS = 64
 def launches_per_step(M, K, H, E, two_op=False):
     """Our kernels per step (FP8 and MXFP4 alike): route, gate/up, down+combine up to PAIR_ROWS
-    routed rows; otherwise route, count+quantise, scatter, gather, gate/up, down, combine; the
-    verify profile's producer and reducer when `two_op`."""
-    if two_op:
-        return 2
+    routed rows; otherwise route, count+quantise, scatter, gather, gate/up, down, combine (the
+    verify profile's producer and reducer, `two_op`, are the same seven launches)."""
     return 3 if M * K <= PAIR_ROWS else 7
 
 
@@ -108,9 +106,9 @@ def parse():
                         "launch list")
     p.add_argument("--no-verify", action="store_true",
                    help="leave the verify M=12 record out of the decode line")
-    p.add_argument("--verify-two-op", action="store_true",
-                   help="verify workloads through the producer + route reducer (off by default: the "
-                        "producer is kept off the GPU while a replay-time fault is unexplained)")
+    p.add_argument("--verify-route-forward", action="store_true",
+                   help="verify workloads through moe_fp8_route_forward instead of the two verify operations "
+                        "(moe_fp8_verify_produce + moe_fp8_verify_reduce; the same kernels)")
     p.add_argument("--no-prefill", action="store_true",
                    help="decode only: leave out the prefill record of the same line")
     p.add_argument("--clock-soak", type=float, default=1.0, metavar="S",
@@ -342,7 +340,7 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
     wts = torch.empty((nbatches, M, K), dtype=torch.float32, device="cuda")
     out = torch.empty((nbatches, M, H), dtype=torch.int16, device="cuda")
 
-    two_op = given_ids is None and verify_profile(M, H, I, E, K) and args.verify_two_op
+    two_op = given_ids is None and verify_profile(M, H, I, E, K) and not args.verify_route_forward
 
     def step(i, stream=None):
         b = i % nbatches
@@ -439,20 +437,16 @@ def run_workload(args, wl, steps, warm, world, rank, dist, want_cpu, cpu_budget_
     value = replicas.throughput(world, steps, M, elapsed)
     ms_per_step = 1e3 * elapsed / steps
 
-    if two_op:
-        roof = producer_kernel(L, torch, M, nbatches, hidden_all, reps, n_rep, router, bias, ids, wts, ws, shape,
-                               alg_bytes - M * H * 2)
-        roof["traffic"] = recorded_traffic("verify_produce", "verify")
-    else:
-        w2_step = distinct * per_expert_bytes(H, I, mx)[1]
-        roof = dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, given_ids, ids, ws, shape,
-                               prefill, gu_bytes, gu_flops, mx, w2_bytes=w2_step)
-        roof["traffic"] = recorded_traffic(roof["kernel"], "prefill" if prefill else cfg, M)
-        if M * K <= PAIR_ROWS and not mx:  # the same kernel without the prefetch, for reference
-            dr = dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, given_ids, ids, ws, shape,
-                                 prefill, gu_bytes, gu_flops, mx, direct=True)
-            roof["direct"] = {k: dr[k] for k in ("kernel", "achieved", "frac", "alg_per_launch", "mean_launch_us")}
-            roof["direct"]["traffic"] = recorded_traffic("gate_up", cfg, M)
+    # the dominant kernel: gate/up as the step launches it
+    w2_step = distinct * per_expert_bytes(H, I, mx)[1]
+    roof = dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, given_ids, ids, ws, shape,
+                           prefill, gu_bytes, gu_flops, mx, w2_bytes=w2_step)
+    roof["traffic"] = recorded_traffic(roof["kernel"], "prefill" if prefill else cfg, M)
+    if M * K <= PAIR_ROWS and not mx:  # the same kernel without the prefetch, for reference
+        dr = dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, given_ids, ids, ws, shape,
+                             prefill, gu_bytes, gu_flops, mx, direct=True)
+        roof["direct"] = {k: dr[k] for k in ("kernel", "achieved", "frac", "alg_per_launch", "mean_launch_us")}
+        roof["direct"]["traffic"] = recorded_traffic("gate_up", cfg, M)
 
     # ---- end to end through the public API with host buffers
     e2e_steps = min(steps * max(1, n_soak), 3000 if decode else (500 if M <= 64 else 10))
@@ -594,39 +588,6 @@ def dominant_kernel(L, torch, args, M, K, nbatches, hidden_all, reps, n_rep, giv
     return roof
 
 
-def producer_kernel(L, torch, M, nbatches, hidden_all, reps, n_rep, router, bias, ids, wts, ws, shape, prod_bytes):
-    """The verify producer alone (routing, gate/up, SiLU+quant, down partials: the whole
-    weight stream of the step), back to back in a CUDA graph on its own stream."""
-    n_k = 100
-    ks = torch.cuda.Stream()
-    ks.wait_stream(torch.cuda.current_stream())
-
-    def pr(i, st):
-        b = i % nbatches
-        w13, s13, w2, s2 = reps[i % n_rep]
-        L.moe_fp8_verify_produce(hidden_all[b * M:(b + 1) * M], router, bias, M, True, w13, s13, w2, s2, ids[b],
-                                 wts[b], ws, shape, stream=st)
-
-    with torch.cuda.stream(ks):
-        pr(0, ks)
-        kg = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(kg, stream=ks):
-            for i in range(n_k):
-                pr(i, ks)
-        kg.replay()
-        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        k0.record(ks)
-        for _ in range(3):
-            kg.replay()
-        k1.record(ks)
-    ks.synchronize()
-    t = k0.elapsed_time(k1) / 1e3 / (3 * n_k)
-    hbm, _, _, peak_src = load_peaks()
-    return {"bound": "hbm", "kernel": "verify_produce", "achieved": prod_bytes / t / 1e9, "peak": hbm, "unit": "GB/s",
-            "frac": prod_bytes / t / 1e9 / hbm, "peak_source": f"{peak_src} hbm_gbs", "alg_per_launch": prod_bytes,
-            "mean_launch_us": t * 1e6}
-
-
 def gpu_selector(torch):
     props = torch.cuda.get_device_properties(torch.cuda.current_device())
     uuid = str(getattr(props, "uuid", ""))
@@ -712,7 +673,7 @@ def profile_steps(args, wl):
     ids = torch.empty((M, K), dtype=torch.int32, device="cuda")
     w = torch.empty((M, K), dtype=torch.float32, device="cuda")
     out = torch.empty((M, H), dtype=torch.int16, device="cuda")
-    two_op = x.ids is None and verify_profile(M, H, I, E, K) and args.verify_two_op
+    two_op = x.ids is None and verify_profile(M, H, I, E, K) and not args.verify_route_forward
     for i in range(n):
         b = i % (hid_all.shape[0] // M)
         hid = hid_all[b * M:(b + 1) * M]

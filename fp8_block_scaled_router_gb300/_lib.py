@@ -31,7 +31,8 @@ EXPORTS = ("moe_fp8_version", "moe_fp8_workspace_bytes", "moe_fp8_workspace_init
            "moe_fp8_norm_forward", "moe_fp8_norm_route_forward", "moe_fp8_verify_produce",
            "moe_fp8_verify_reduce", "moe_fp8_forward_partials", "moe_fp8_combine_pairs", "moe_mxfp4_forward",
            "moe_mxfp4_route_forward", "moe_mxfp4_gate_up_direct", "moe_mxfp4_down_combine",
-           "moe_mxfp4_gate_up", "moe_mxfp4_down", "moe_fp8_gate_up_prefetch")
+           "moe_mxfp4_gate_up", "moe_mxfp4_down", "moe_fp8_gate_up_prefetch",
+           "moe_fp8_verify_produce_one_launch")
 
 
 class MoEError(RuntimeError):
@@ -90,6 +91,8 @@ def load(path: str = LIB):
             lib.moe_fp8_norm_route_forward.argtypes = [vp, vp, f32, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp,
                                                        sz, sp, vp]
             lib.moe_fp8_verify_produce.argtypes = [vp, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, sz, sp, vp]
+            lib.moe_fp8_verify_produce_one_launch.argtypes = [vp, vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, sz,
+                                                              sp, vp]
             lib.moe_fp8_verify_reduce.argtypes = [vp, i32, vp, vp, sz, sp, vp]
             lib.moe_fp8_forward_partials.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, sz, sp, vp]
             lib.moe_fp8_combine_pairs.argtypes = [vp, vp, vp, i32, vp, sp, vp]
@@ -381,6 +384,17 @@ def moe_fp8_verify_produce(hidden, router_w, bias, M, renormalize, w13, w13_scal
     """The verify_m12 producer (routing, gate/up, SiLU+quant, down partials); see include/moe_fp8.h."""
     nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
     return _check("moe_fp8_verify_produce", load().moe_fp8_verify_produce(
+        _ptr(hidden), _ptr(router_w), _ptr(bias), int(M), int(bool(renormalize)), _ptr(w13), _ptr(w13_scale),
+        _ptr(w2), _ptr(w2_scale), _ptr(topk_ids), _ptr(topk_w), _ptr(workspace), nb, ctypes.byref(shape),
+        _stream(stream)), check)
+
+
+def moe_fp8_verify_produce_one_launch(hidden, router_w, bias, M, renormalize, w13, w13_scale, w2, w2_scale,
+                                      topk_ids, topk_w, workspace, shape: Shape, stream=None, ws_bytes=None,
+                                      check=True):
+    """The verify_m12 producer as one launch (opt-in); see include/moe_fp8.h."""
+    nb = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return _check("moe_fp8_verify_produce_one_launch", load().moe_fp8_verify_produce_one_launch(
         _ptr(hidden), _ptr(router_w), _ptr(bias), int(M), int(bool(renormalize)), _ptr(w13), _ptr(w13_scale),
         _ptr(w2), _ptr(w2_scale), _ptr(topk_ids), _ptr(topk_w), _ptr(workspace), nb, ctypes.byref(shape),
         _stream(stream)), check)

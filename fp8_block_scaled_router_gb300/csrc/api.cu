@@ -543,6 +543,36 @@ moe_status_t moe_fp8_verify_produce(const void* hidden, const void* router_w, co
   Layout L;
   if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
   if (!verify_profile(M, shape->hidden, shape->inter, shape->num_experts, shape->top_k)) return MOE_ERR_UNSUPPORTED;
+  // routing, then the 96 routed rows quantised and sorted by expert, gate/up with SiLU and
+  // the requantisation, and the down partials y (FP32, the sort's rows), by the expert-grouped
+  // kernels; the reducer sums them in slot order through the sort's permutation
+  const int H = shape->hidden, I = shape->inter, E = shape->num_experts, K = shape->top_k;
+  const WsPtrs ws = ws_ptrs(workspace, L);
+  const int64_t R = (int64_t)M * K;
+  if (moe_status_t st = route_impl(hidden, Norm{nullptr, 0.0f}, router_w, bias, M, shape, renormalize, topk_ids,
+                                   topk_w, stream))
+    return st;
+  if (moe_status_t st = launched(launch_sort_gather(static_cast<const uint16_t*>(hidden), Norm{nullptr, 0.0f},
+                                                    topk_ids, M, H, E, K, ws, stream)))
+    return st;
+  if (moe_status_t st = launched(launch_gpair_gateup(false, w13, w13_scale, R, H, I, E, L.max_groups, ws, stream)))
+    return st;
+  return launched(launch_gpair_down(false, w2, w2_scale, R, H, I, E, L.max_groups, ws, stream));
+}
+
+moe_status_t moe_fp8_verify_produce_one_launch(const void* hidden, const void* router_w, const float* bias, int32_t M,
+                                               int32_t renormalize, const uint8_t* w13, const float* w13_scale,
+                                               const uint8_t* w2, const float* w2_scale, int32_t* topk_ids,
+                                               float* topk_w, void* workspace, size_t workspace_bytes,
+                                               const moe_fp8_shape_t* shape, cudaStream_t stream) {
+  if (moe_status_t st = check_common(shape, M)) return st;
+  for (const void* p : {hidden, router_w, (const void*)w13, (const void*)w13_scale, (const void*)w2,
+                        (const void*)w2_scale, (const void*)topk_ids, (const void*)topk_w})
+    if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (bias && !aligned16(bias)) return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if (moe_status_t st = check_ws(workspace, workspace_bytes, shape, &L)) return st;
+  if (!verify_profile(M, shape->hidden, shape->inter, shape->num_experts, shape->top_k)) return MOE_ERR_UNSUPPORTED;
   if (!verify_capable()) return MOE_ERR_UNSUPPORTED;
   return launched(launch_verify_produce(static_cast<const uint16_t*>(hidden), static_cast<const uint16_t*>(router_w),
                                         bias, renormalize ? 1 : 0, topk_ids, topk_w, w13, w13_scale, w2, w2_scale,

@@ -216,22 +216,31 @@ moe_status_t moe_fp8_route_forward_one_launch(const void* hidden, const void* ro
  * a route reducer with its own ABI, launch geometry and fixed reduction order. Both carry an
  * exact batch guard ([NK]: a kernel whose grid depends on the batch takes one; the profile
  * compiled here is verify_m12 with one request): M == 12 with hidden 2048, inter 768,
- * 128 experts and top-8, else MOE_ERR_UNSUPPORTED (also when the device cannot hold the
- * producer's clusters).
+ * 128 experts and top-8, else MOE_ERR_UNSUPPORTED.
  * moe_fp8_verify_produce routes the 12 tokens (ids and weights into topk_ids / topk_w, as
  * moe_route; arguments as for moe_fp8_route_forward) and leaves in the workspace every routed
- * pair's down projection y (FP32, pair order t*8 + j), the activation codes and scales and the
- * hidden codes (the views of moe_fp8_workspace_view) and the identity permutation. It runs as
- * one launch of 16-CTA clusters: each cluster routes for itself, then takes a share of the
- * distinct routed experts, reading each expert's weights once for every token routed to it.
+ * pair's down projection y (FP32, at the row the sort gives it: perm_row[t*8 + j]), the
+ * activation codes and scales and the hidden codes (the views of moe_fp8_workspace_view).
+ * It runs the router, the quantise-and-sort of moe_fp8_prepare and the expert-grouped
+ * gate/up and down kernels (each expert's weights read once for the tokens routed to it).
  * moe_fp8_verify_reduce then writes out[t] = bf16(sum over slots j ascending of
- * topk_w[t][j] * y[t*8 + j]) (FP32 multiply then add, from 0); call it after the producer on
- * the same stream and workspace. The arithmetic is that of moe_fp8_gate_up_direct +
- * moe_fp8_down_combine (pair kernels), whose outputs these are bit for bit. */
+ * topk_w[t][j] * y[perm_row[t*8 + j]]) (FP32 multiply then add, from 0); call it after the
+ * producer on the same stream and workspace. produce + reduce equals moe_fp8_route_forward
+ * bit for bit, and its arithmetic is that of the pair kernels (moe_fp8_gate_up_direct +
+ * moe_fp8_down_combine).
+ * moe_fp8_verify_produce_one_launch is the same producer as one launch of 16-CTA clusters
+ * (each cluster routes for itself, then takes a share of the distinct routed experts), with
+ * the identity permutation and y in pair order; the same reducer follows it. It is opt-in:
+ * MOE_ERR_UNSUPPORTED also when the device cannot hold its clusters. */
 moe_status_t moe_fp8_verify_produce(const void* hidden, const void* router_w, const float* bias, int32_t M,
                                     int32_t renormalize, const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
                                     const float* w2_scale, int32_t* topk_ids, float* topk_w, void* workspace,
                                     size_t workspace_bytes, const moe_fp8_shape_t* shape, cudaStream_t stream);
+moe_status_t moe_fp8_verify_produce_one_launch(const void* hidden, const void* router_w, const float* bias, int32_t M,
+                                               int32_t renormalize, const uint8_t* w13, const float* w13_scale,
+                                               const uint8_t* w2, const float* w2_scale, int32_t* topk_ids,
+                                               float* topk_w, void* workspace, size_t workspace_bytes,
+                                               const moe_fp8_shape_t* shape, cudaStream_t stream);
 moe_status_t moe_fp8_verify_reduce(const float* topk_w, int32_t M, void* out, void* workspace, size_t workspace_bytes,
                                    const moe_fp8_shape_t* shape, cudaStream_t stream);
 

@@ -178,6 +178,14 @@ def test_verify_exact_batch_guard(lib):
     assert produce(12, nb=need - 1) == 3
     assert L.moe_fp8_verify_reduce(0, 12, FAKE, FAKE, s, stream=0, ws_bytes=need, check=False) == 1
     assert L.moe_fp8_verify_reduce(FAKE, 12, MIS, FAKE, s, stream=0, ws_bytes=need, check=False) == 1
+    # the one-launch producer keeps the same guard
+    for M in (0, 11, 13):
+        assert L.moe_fp8_verify_produce_one_launch(FAKE, FAKE, None, M, 1, *[FAKE] * 6, FAKE, s, stream=0,
+                                                   ws_bytes=need, check=False) == 2, M
+    assert L.moe_fp8_verify_produce_one_launch(FAKE, FAKE, None, 12, 1, *[FAKE] * 6, FAKE, shape(top_k=4), stream=0,
+                                               ws_bytes=L.moe_fp8_workspace_bytes(shape(top_k=4)), check=False) == 2
+    assert L.moe_fp8_verify_produce_one_launch(MIS, FAKE, None, 12, 1, *[FAKE] * 6, FAKE, s, stream=0, ws_bytes=need,
+                                               check=False) == 1
 
 
 def test_partials_and_pair_reducer_argument_errors(lib):

@@ -1,13 +1,14 @@
 """The speculative-verify layer as two operations (netra-kernel README, prefill-pair build
-section): moe_fp8_verify_produce (routing, gate/up, SiLU and quantisation, down partials and
-metadata in one launch) and moe_fp8_verify_reduce (the route reducer), behind the exact
+section): moe_fp8_verify_produce (routing, then the quantise-and-sort and the expert-grouped
+gate/up, SiLU and requantisation and down kernels, leaving the down partials and the
+permutation in the workspace) and moe_fp8_verify_reduce (the route reducer), behind the exact
 batch guard of the verify_m12 profile (12 tokens, h2048 i768 e128 top-8).
 
-Checked here: the routing equals moe_route bit for bit; the activation codes and scales and
-the output equal the few-row pair kernels (moe_fp8_gate_up_direct + moe_fp8_down_combine)
-bit for bit; everything is inside the oracle contract (ids and hidden codes bit-exact,
-activation codes in their window, the output bound given the activation codes); 100
-launches are bitwise identical; a CUDA graph replays it; the status word stays clean.
+Checked here: produce + reduce equals moe_fp8_route_forward bit for bit (ids, weights, out and
+the workspace's codes); the routing equals the oracle's; everything is inside the oracle
+contract (hidden codes bit-exact, the permutation stable and complete, activation codes in
+their window, the output bound given the activation codes); zero rows give zero output and
+rows past M stay untouched; 100 launches are bitwise identical and a CUDA graph replays them.
 The host-side guard (any other batch or shape refused) is tested on the CPU in
 tests/test_abi_host.py.
 """
@@ -17,18 +18,12 @@ import torch
 
 from fp8_block_scaled_router_gb300 import inputs
 
-pytestmark = [
-    pytest.mark.gpu,
-    # Kept off the GPU: the producer passed these tests and 20,000-step timed runs, but it
-    # failed under a profiler's kernel replay (twice, with and without the teardown drain) and
-    # in a timestamp-instrumented copy; until that cause is found by reading, it does not run.
-    pytest.mark.skip(reason="verify producer kept off the GPU until the cause of its replay-time faults is found"),
-]
+pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
     import oracle
     from fp8_block_scaled_router_gb300 import _lib as L
-    from gpu_harness import GpuMoE, check_act, check_out_given_act, oracle_forward, to_dev, u16
+    from gpu_harness import GpuMoE, check_act, check_out_given_act, check_permutation, oracle_forward, to_dev, u16
 
 M = 12
 _CACHE = {}
@@ -49,25 +44,25 @@ def workload(name):
     return _CACHE[name]
 
 
-def produce_reduce(g, hid_d, renorm=True):
-    ids = torch.full((M, g.K), -5, dtype=torch.int32, device="cuda")
-    w = torch.full((M, g.K), -5.0, dtype=torch.float32, device="cuda")
-    out = torch.empty((M, g.H), dtype=torch.int16, device="cuda")
+def produce_reduce(g, hid_d, renorm=True, out=None, ids=None, w=None):
+    ids = torch.full((M, g.K), -5, dtype=torch.int32, device="cuda") if ids is None else ids
+    w = torch.full((M, g.K), -5.0, dtype=torch.float32, device="cuda") if w is None else w
+    out = torch.empty((M, g.H), dtype=torch.int16, device="cuda") if out is None else out
     L.moe_fp8_verify_produce(hid_d, g.router, g.bias, M, renorm, g.w13, g.s13, g.w2, g.s2, ids, w, g.ws, g.shape)
     L.moe_fp8_verify_reduce(w, M, out, g.ws, g.shape)
     return ids, w, out
 
 
-def pair_views(g):
+def views(g):
     a = g.ws_arrays(M)
-    return {k: a[k].copy() for k in ("qa", "sa", "act", "act_scale", "row_src", "perm_row")}
+    return {k: a[k].copy() for k in ("qa", "sa", "act", "act_scale", "row_src", "perm_row", "offsets")}
 
 
 CASES = [("verify", True), ("verify_skewed", True), ("verify", False)]
 
 
 @pytest.mark.parametrize("name,renorm", CASES, ids=[f"{n}-{'renorm' if r else 'full'}" for n, r in CASES])
-def test_verify_matches_router_and_pair_kernels(name, renorm):
+def test_verify_equals_route_forward_and_oracle(name, renorm):
     x = workload(name)
     g = GpuMoE(x, M)
     g.ws.fill_(0xFF)
@@ -76,29 +71,26 @@ def test_verify_matches_router_and_pair_kernels(name, renorm):
     ids, w, out = produce_reduce(g, hid_d, renorm)
     torch.cuda.synchronize()
     assert g.status() == 0
-    got = pair_views(g)
-    # the same layer through moe_route and the two pair kernels
-    ids2, w2 = g.route(hid_d, M, renorm=renorm)
+    got = views(g)
+    # the same layer in one call
+    ids2 = torch.empty_like(ids)
+    w2 = torch.empty_like(w)
     out2 = torch.empty_like(out)
-    L.moe_fp8_gate_up_direct(hid_d, ids2, M, g.w13, g.s13, g.ws, g.shape)
-    L.moe_fp8_down_combine(ids2, w2, M, g.w2, g.s2, out2, g.ws, g.shape)
+    L.moe_fp8_route_forward(hid_d, g.router, g.bias, M, renorm, g.w13, g.s13, g.w2, g.s2, out2, ids2, w2, g.ws, g.shape)
     torch.cuda.synchronize()
-    ref = pair_views(g)
-    assert torch.equal(ids, ids2) and torch.equal(w, w2)
-    for k in ("qa", "sa", "act", "act_scale"):
+    ref = views(g)
+    assert torch.equal(ids, ids2) and torch.equal(w, w2) and torch.equal(out, out2)
+    for k in ("qa", "sa", "act", "act_scale", "perm_row"):
         assert np.array_equal(got[k], ref[k]), k
-    assert torch.equal(out, out2)
-    assert np.array_equal(got["perm_row"][:M * g.K], np.arange(M * g.K))
     # the oracle contract
     ids_o, w_o = oracle.route(x.hidden[:M], x.router_w, x.bias, g.K, renormalize=renorm)
     assert np.array_equal(ids.cpu().numpy(), ids_o)
     assert np.all(np.abs(w.cpu().numpy() - w_o) <= 2e-6 * w_o)
     out_o, dbg = oracle_forward(x, x.hidden[:M], ids_o, w_o, debug=True)
     assert np.array_equal(got["qa"], dbg["qa"]) and np.array_equal(got["sa"], dbg["sa"])
-    ws = dict(got)
-    ws["row_src"] = np.arange(M * g.K, dtype=np.int32)
-    check_act(ws, dbg, g.K, f"verify producer {name}")
-    check_out_given_act(u16(out), out_o, ws, dbg, ids_o, w_o, x, f"verify producer {name}")
+    check_permutation(got, ids_o, g.E)
+    check_act(got, dbg, g.K, f"verify producer {name}")
+    check_out_given_act(u16(out), out_o, got, dbg, ids_o, w_o, x, f"verify producer {name}")
 
 
 def test_verify_zero_rows_and_rows_past_m():
@@ -128,27 +120,22 @@ def test_verify_100_launches_and_graph_replay():
     hid_d = to_dev(x.hidden[:M])
     ids, w, out = produce_reduce(g, hid_d)
     torch.cuda.synchronize()
-    ref = (ids.clone(), w.clone(), out.clone(), pair_views(g)["act"])
+    ref = (ids.clone(), w.clone(), out.clone(), views(g)["act"])
     for _ in range(100):
         i2, w2, o2 = produce_reduce(g, hid_d)
         torch.cuda.synchronize()
         assert torch.equal(i2, ref[0]) and torch.equal(w2, ref[1]) and torch.equal(o2, ref[2])
-    assert np.array_equal(pair_views(g)["act"], ref[3])
+    assert np.array_equal(views(g)["act"], ref[3])
     s = torch.cuda.Stream()
     ids3 = torch.empty_like(ids)
     w3 = torch.empty_like(w)
     out3 = torch.empty_like(out)
-
-    def step():
-        L.moe_fp8_verify_produce(hid_d, g.router, g.bias, M, True, g.w13, g.s13, g.w2, g.s2, ids3, w3, g.ws, g.shape)
-        L.moe_fp8_verify_reduce(w3, M, out3, g.ws, g.shape)
-
     with torch.cuda.stream(s):
-        step()
+        produce_reduce(g, hid_d, out=out3, ids=ids3, w=w3)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=s):
-        step()
+        produce_reduce(g, hid_d, out=out3, ids=ids3, w=w3)
     out3.zero_()
     for _ in range(5):
         graph.replay()
