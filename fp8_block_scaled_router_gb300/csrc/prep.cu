@@ -140,10 +140,34 @@ __global__ void __launch_bounds__(256) count_quant_kernel(const uint16_t* __rest
   }
 }
 
+// Exclusive prefix sum of v over the 256 threads of the block in thread order (warp
+// shuffles, then the 8 warp totals); `total` receives the sum. wsum: 8 ints of shared memory.
+__device__ __forceinline__ int scan256(int v, int* wsum, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  int base = 0;
+  total = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const int t = wsum[w];
+    base += w < warp ? t : 0;
+    total += t;
+  }
+  __syncthreads();  // wsum is rewritten by the next scan
+  return base + x - v;
+}
+
 __global__ void __launch_bounds__(256) scatter_kernel(const int32_t* __restrict__ ids, int M, int H,
                                                              int E, int K, int nblk, WsPtrs ws) {
   __shared__ int start[kMaxExperts];
-  __shared__ int scan[kMaxExperts];
+  __shared__ int wsum[8];
   __shared__ int wcnt[8][kMaxExperts];
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int R = M * K;
@@ -151,42 +175,41 @@ __global__ void __launch_bounds__(256) scatter_kernel(const int32_t* __restrict_
   (void)lane;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
-  // per expert: total over all blocks and the count in blocks before this one; the
-  // 256 / E thread groups each sum a slice of the blocks (independent loads in flight)
-  __shared__ int part_tot[256], part_pre[256];
+  // per expert: total over all blocks and the count in blocks before this one. Thread
+  // (g, q) sums experts 4q .. 4q+3 over blocks g, g + ng, ... with 16-byte loads (E is a
+  // multiple of 4 and a histogram row E * 4 bytes), so few load rounds are in flight
+  __shared__ int4 part_tot[256], part_pre[256];
   {
-    const int e = tid % E, g = tid / E, ng = 256 / E;
-    int t_ = 0, p_ = 0;
+    const int nq = E / 4, q = tid % nq, g = tid / nq, ng = 256 / nq;
+    const int4* bc = reinterpret_cast<const int4*>(ws.blk_counts);
+    int4 t_ = make_int4(0, 0, 0, 0), p_ = make_int4(0, 0, 0, 0);
 #pragma unroll 8
     for (int bb = g; bb < nblk; bb += ng) {
-      const int c = ws.blk_counts[(size_t)bb * E + e];
-      t_ += c;
-      p_ += bb < b ? c : 0;
+      const int4 c = bc[(size_t)bb * nq + q];
+      t_.x += c.x; t_.y += c.y; t_.z += c.z; t_.w += c.w;
+      if (bb < b) { p_.x += c.x; p_.y += c.y; p_.z += c.z; p_.w += c.w; }
     }
     part_tot[tid] = t_;
     part_pre[tid] = p_;
   }
   __syncthreads();
   int tot = 0, pre = 0;
-  if (tid < E)
-    for (int g = 0; g < 256 / E; ++g) {
-      tot += part_tot[g * E + tid];
-      pre += part_pre[g * E + tid];
+  if (tid < E) {
+    const int nq = E / 4, q = tid / 4, comp = tid % 4;
+    const int* pt = reinterpret_cast<const int*>(part_tot);
+    const int* pp = reinterpret_cast<const int*>(part_pre);
+    for (int g = 0; g < 256 / nq; ++g) {
+      tot += pt[(g * nq + q) * 4 + comp];
+      pre += pp[(g * nq + q) * 4 + comp];
     }
-  // exclusive scan of tot over experts (Hillis-Steele on 256 entries)
-  scan[tid] = tid < E ? tot : 0;
-  __syncthreads();
-  for (int off = 1; off < 256; off <<= 1) {
-    const int v = tid >= off ? scan[tid - off] : 0;
-    __syncthreads();
-    scan[tid] += v;
-    __syncthreads();
   }
-  const int base_e = tid < E ? scan[tid] - tot : 0;  // exclusive
+  // exclusive scan of tot over experts
+  int placed = 0;
+  const int base_e = scan256(tid < E ? tot : 0, wsum, placed);
   if (tid < E) start[tid] = base_e + pre;
   if (b == 0) {
     if (tid < E) ws.offsets[tid] = base_e;
-    if (tid == E - 1) ws.offsets[E] = scan[tid];
+    if (tid == 0) ws.offsets[E] = placed;
   }
   // per-warp counts of each expert in this block (stable order: warp, then lane)
   for (int i = tid; i < 8 * E; i += 256) wcnt[i / E][i % E] = 0;
@@ -207,37 +230,17 @@ __global__ void __launch_bounds__(256) scatter_kernel(const int32_t* __restrict_
   if (i < R) ws.perm_row[i] = pos;
   // block 0: the 128-row tile list (expert counts are the totals)
   if (b == 0) {
-    __syncthreads();
-    const int ntile = tid < E ? (tot + kTileRows - 1) / kTileRows : 0;
-    scan[tid] = ntile;
-    __syncthreads();
-    for (int off = 1; off < 256; off <<= 1) {
-      const int v = tid >= off ? scan[tid - off] : 0;
-      __syncthreads();
-      scan[tid] += v;
-      __syncthreads();
-    }
-    if (tid < E) {
-      int tb = scan[tid] - ntile;
+    int n_tiles = 0;
+    int tb = scan256(tid < E ? (tot + kTileRows - 1) / kTileRows : 0, wsum, n_tiles);
+    if (tid < E)
       for (int j = 0; j < tot; j += kTileRows, ++tb) ws.tiles[tb] = Tile{tid, base_e + j, min(kTileRows, tot - j), 0};
-    }
-    if (tid == 255) ws.hdr->n_tiles = (uint32_t)scan[255];
+    if (tid == 0) ws.hdr->n_tiles = (uint32_t)n_tiles;
     // and the list of groups of up to kGroupRows rows (the expert-grouped pair kernels' units)
-    __syncthreads();
-    const int ngroup = tid < E ? (tot + kGroupRows - 1) / kGroupRows : 0;
-    scan[tid] = ngroup;
-    __syncthreads();
-    for (int off = 1; off < 256; off <<= 1) {
-      const int v = tid >= off ? scan[tid - off] : 0;
-      __syncthreads();
-      scan[tid] += v;
-      __syncthreads();
-    }
-    if (tid < E) {
-      int gb = scan[tid] - ngroup;
+    int n_groups = 0;
+    int gb = scan256(tid < E ? (tot + kGroupRows - 1) / kGroupRows : 0, wsum, n_groups);
+    if (tid < E)
       for (int j = 0; j < tot; j += kGroupRows, ++gb) ws.groups[gb] = Tile{tid, base_e + j, min(kGroupRows, tot - j), 0};
-    }
-    if (tid == 255) ws.hdr->n_groups = (uint32_t)scan[255];
+    if (tid == 0) ws.hdr->n_groups = (uint32_t)n_groups;
   }
 }
 
