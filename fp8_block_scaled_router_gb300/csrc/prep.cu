@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const uint16_t* __re
 //            pre[e] = sum over blocks before b, the exclusive scan base[e] over experts, and
 //            places its pairs at base[e] + pre[e] + (earlier pairs of e in this block), so
 //            rows keep ascending flat pair order t*K + j within each expert. Block 0 also
-//            writes the expert offsets and the 128-row tile list.
+//            writes the expert offsets, the 128-row tile list and the 16-row group list.
 //   gather:  one warp per placed row copies the row's hidden codes (H bytes) and scales
 //            into xp / sa_p -- thousands of independent 16-byte copies in flight.
 // ---------------------------------------------------------------------------------------
@@ -129,14 +129,27 @@ __global__ void __launch_bounds__(256) count_quant_kernel(const uint16_t* __rest
     }
     return;
   }
+  // four groups per warp and pass, their loads issued before the first reduction
   const int64_t ngroups = (int64_t)M * ngroups_row;
-  for (int64_t gidx = (int64_t)(blockIdx.x - nblk) * 8 + warp; gidx < ngroups; gidx += nwarps) {
-    const int64_t t = gidx / ngroups_row;
-    const int g = (int)(gidx % ngroups_row);
-    const uint2 raw = *reinterpret_cast<const uint2*>(hidden + t * H + g * 128 + lane * 4);
-    quant_group_store(bf16_bits_to_float(raw.x & 0xFFFF), bf16_bits_to_float(raw.x >> 16),
-                      bf16_bits_to_float(raw.y & 0xFFFF), bf16_bits_to_float(raw.y >> 16), lane,
-                      ws.qa + t * H + g * 128, ws.sa + t * ngroups_row + g);
+  for (int64_t g0 = (int64_t)(blockIdx.x - nblk) * 8 + warp; g0 < ngroups; g0 += 4 * nwarps) {
+    uint2 raw[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t gidx = g0 + u * nwarps;
+      if (gidx < ngroups)
+        raw[u] = *reinterpret_cast<const uint2*>(hidden + (gidx / ngroups_row) * H + (gidx % ngroups_row) * 128 +
+                                                 lane * 4);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t gidx = g0 + u * nwarps;  // the same for every lane of the warp
+      if (gidx >= ngroups) break;
+      const int64_t t = gidx / ngroups_row;
+      const int g = (int)(gidx % ngroups_row);
+      quant_group_store(bf16_bits_to_float(raw[u].x & 0xFFFF), bf16_bits_to_float(raw[u].x >> 16),
+                        bf16_bits_to_float(raw[u].y & 0xFFFF), bf16_bits_to_float(raw[u].y >> 16), lane,
+                        ws.qa + t * H + g * 128, ws.sa + t * ngroups_row + g);
+    }
   }
 }
 
