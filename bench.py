@@ -73,11 +73,16 @@ def is_mx(cfg):
 
 # routed rows up to which moe_fp8_forward runs the two pair kernels
 PAIR_ROWS = 64
+SORT_BLOCK = 256  # routed pairs one sort block covers
+
+
 def launches_per_step(M, K, H, E, two_op=False):
     """Our kernels per step (FP8 and MXFP4 alike): route, gate/up, down+combine up to PAIR_ROWS
-    routed rows; otherwise route, count+quantise, scatter, gather, gate/up, down, combine (the
-    verify profile's producer and reducer, `two_op`, are the same seven launches)."""
-    return 3 if M * K <= PAIR_ROWS else 7
+    routed rows; up to SORT_BLOCK, route, the one-launch sort (quantise, sort, gather), gate/up,
+    down, combine; beyond, route, count+quantise, scatter, gather, gate/up, down, combine (the
+    verify profile's producer and reducer, `two_op`, are the same five launches)."""
+    R = M * K
+    return 3 if R <= PAIR_ROWS else (5 if R <= SORT_BLOCK else 7)
 
 
 def verify_profile(M, H, I, E, K):

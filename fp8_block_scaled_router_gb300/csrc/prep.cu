@@ -10,7 +10,11 @@
 // With an RMSNorm in front (many-row path), one warp per token forms r and quantises the
 // token's y = bf16((x*r)*gamma) group by group.
 // Few routed rows (pair mode): block 0 records each pair's expert (-1 if out of range) and
-// the identity permutation. Many routed rows: the two-launch counting sort below.
+// the identity permutation. Routed rows sorted by expert: up to one sort block of pairs, one
+// launch that sorts, quantises and gathers (sort_small_kernel); more, the two-launch counting
+// sort and the gather below.
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
 #include "device.h"
@@ -20,16 +24,23 @@ namespace moe {
 constexpr int kPrepThreads = 1024;
 constexpr int kMaxExperts = 256;
 
-// One warp quantises one 128-column group: lane l holds columns 4l..4l+3 (x0..x3).
-__device__ __forceinline__ void quant_group_store(float x0, float x1, float x2, float x3, int lane, uint8_t* qdst,
-                                                  float* sdst) {
+// One warp quantises one 128-column group: lane l holds columns 4l..4l+3 (x0..x3) and gets
+// their four codes (one 32-bit word, column 4l in the low byte); every lane gets the scale.
+__device__ __forceinline__ uint32_t quant_group(float x0, float x1, float x2, float x3, float& s) {
   float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  const float s = quant_scale(amax);
+  s = quant_scale(amax);
   const uint32_t lo = e4m3x2_encode(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
   const uint32_t hi = e4m3x2_encode(__fdiv_rn(x2, s), __fdiv_rn(x3, s));
-  reinterpret_cast<uint32_t*>(qdst)[lane] = lo | (hi << 16);
+  return lo | (hi << 16);
+}
+
+__device__ __forceinline__ void quant_group_store(float x0, float x1, float x2, float x3, int lane, uint8_t* qdst,
+                                                  float* sdst) {
+  float s;
+  const uint32_t w = quant_group(x0, x1, x2, x3, s);
+  reinterpret_cast<uint32_t*>(qdst)[lane] = w;
   if (lane == 0) *sdst = s;
 }
 
@@ -257,6 +268,118 @@ __global__ void __launch_bounds__(256) scatter_kernel(const int32_t* __restrict_
   }
 }
 
+// ---------------------------------------------------------------------------------------
+// Few routed pairs (R <= kSortBlock, one sort block): the sort, the hidden quantisation and
+// the gather in one launch. Every block repeats the counting sort of the R pairs in shared
+// memory -- the arithmetic of the two-launch sort with a single block, so the positions are
+// the same -- and block 0 writes its results (offsets, row_src, perm_row, the tile and group
+// lists, the invalid-id status). Each warp then quantises (token, 128-column group) units
+// (with an RMSNorm in front: whole tokens) and writes the codes and scale to qa / sa and to
+// each of the token's placed rows in xp / sa_p. No block waits for another.
+// ---------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) sort_small_kernel(const uint16_t* __restrict__ hidden, const Norm nm,
+                                                         const int32_t* __restrict__ ids, int M, int H, int E, int K,
+                                                         WsPtrs ws) {
+  __shared__ int start[kMaxExperts];
+  __shared__ int wsum[8];
+  __shared__ int wcnt[8][kMaxExperts];
+  __shared__ int s_pos[kSortBlock];
+  __shared__ int bad;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int R = M * K;
+  const int nsc = H / 128;
+  const int64_t nwarps = (int64_t)gridDim.x * 8;
+  const int64_t w0 = (int64_t)blockIdx.x * 8 + warp;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  // the warp's first group of hidden values is on its way while the block sorts
+  const bool normed = nm.gamma != nullptr;
+  const int64_t ngroups = (int64_t)M * nsc;
+  uint2 raw0 = make_uint2(0, 0);
+  if (!normed && w0 < ngroups)
+    raw0 = *reinterpret_cast<const uint2*>(hidden + (w0 / nsc) * H + (w0 % nsc) * 128 + lane * 4);
+
+  for (int j = tid; j < 8 * E; j += 256) wcnt[j / E][j % E] = 0;
+  if (tid == 0) bad = 0;
+  __syncthreads();
+  const int i = tid;
+  const int e = i < R ? ids[i] : -1;
+  const bool valid = i < R && e >= 0 && e < E;
+  if (i < R && !valid) bad = 1;
+  const unsigned mask = __match_any_sync(0xffffffffu, valid ? e : -1);
+  const int rank = __popc(mask & ((1u << lane) - 1u));
+  if (valid && rank == 0) wcnt[warp][e] = __popc(mask);
+  __syncthreads();
+  int tot = 0;
+  if (tid < E)
+    for (int w = 0; w < 8; ++w) tot += wcnt[w][tid];
+  int placed = 0;
+  const int base_e = scan256(tid < E ? tot : 0, wsum, placed);
+  if (tid < E) start[tid] = base_e;
+  __syncthreads();
+  int pos = -1;
+  if (valid) {
+    pos = start[e] + rank;
+    for (int w = 0; w < warp; ++w) pos += wcnt[w][e];
+  }
+  s_pos[tid] = pos;
+  if (blockIdx.x == 0) {
+    if (valid) ws.row_src[pos] = i;
+    if (i < R) ws.perm_row[i] = pos;
+    if (tid < E) ws.offsets[tid] = base_e;
+    if (tid == 0) ws.offsets[E] = placed;
+    if (tid == 0 && bad) set_status(ws.hdr, MOE_STATUS_BAD_EXPERT_ID);
+    int n_tiles = 0;
+    int tb = scan256(tid < E ? (tot + kTileRows - 1) / kTileRows : 0, wsum, n_tiles);
+    if (tid < E)
+      for (int j = 0; j < tot; j += kTileRows, ++tb) ws.tiles[tb] = Tile{tid, base_e + j, min(kTileRows, tot - j), 0};
+    if (tid == 0) ws.hdr->n_tiles = (uint32_t)n_tiles;
+    int n_groups = 0;
+    int gb = scan256(tid < E ? (tot + kGroupRows - 1) / kGroupRows : 0, wsum, n_groups);
+    if (tid < E)
+      for (int j = 0; j < tot; j += kGroupRows, ++gb) ws.groups[gb] = Tile{tid, base_e + j, min(kGroupRows, tot - j), 0};
+    if (tid == 0) ws.hdr->n_groups = (uint32_t)n_groups;
+  }
+  __syncthreads();  // s_pos is complete
+
+  // codes and scale of group g of token t, to qa / sa and to the token's placed rows
+  auto store = [&](int64_t t, int g, uint32_t word, float sc) {
+    reinterpret_cast<uint32_t*>(ws.qa + t * H + g * 128)[lane] = word;
+    if (lane == 0) ws.sa[t * nsc + g] = sc;
+    for (int j = 0; j < K; ++j) {
+      const int p = s_pos[t * K + j];
+      if (p < 0) continue;
+      reinterpret_cast<uint32_t*>(ws.xp + (size_t)p * H + g * 128)[lane] = word;
+      if (lane == 0) ws.sa_p[(size_t)p * nsc + g] = sc;
+    }
+  };
+  if (normed) {
+    for (int64_t t = w0; t < M; t += nwarps) {
+      const uint16_t* xr = hidden + t * H;
+      const float r = row_rms_scale(xr, H, nm.eps, lane);
+      for (int g = 0; g < nsc; ++g) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(xr + g * 128 + lane * 4);
+        const uint2 gm = *reinterpret_cast<const uint2*>(nm.gamma + g * 128 + lane * 4);
+        float sc;
+        const uint32_t word = quant_group(norm_value(raw.x & 0xFFFF, r, gm.x & 0xFFFF), norm_value(raw.x >> 16, r, gm.x >> 16),
+                                          norm_value(raw.y & 0xFFFF, r, gm.y & 0xFFFF), norm_value(raw.y >> 16, r, gm.y >> 16),
+                                          sc);
+        store(t, g, word, sc);
+      }
+    }
+    return;
+  }
+  for (int64_t gidx = w0; gidx < ngroups; gidx += nwarps) {
+    const uint2 raw = gidx == w0 ? raw0
+                                 : *reinterpret_cast<const uint2*>(hidden + (gidx / nsc) * H + (gidx % nsc) * 128 +
+                                                                   lane * 4);
+    float sc;
+    const uint32_t word = quant_group(bf16_bits_to_float(raw.x & 0xFFFF), bf16_bits_to_float(raw.x >> 16),
+                                      bf16_bits_to_float(raw.y & 0xFFFF), bf16_bits_to_float(raw.y >> 16), sc);
+    store(gidx / nsc, (int)(gidx % nsc), word, sc);
+  }
+}
+
 // xp[p] = qa[row_src[p] / K], sa_p[p] = sa[row_src[p] / K]: one warp per placed row. Only
 // the first offsets[E] rows are placed (pairs with an invalid id are not); row_src past them
 // is not written by this call and is never read.
@@ -286,8 +409,24 @@ cudaError_t launch_sort_gather(const uint16_t* hidden, Norm nm, const int32_t* i
   const int R = M * K;
   const int nblk = (R + kSortBlock - 1) / kSortBlock;
   const int64_t groups = (int64_t)M * (H / 128);
+  const int sms = device_info().sms > 0 ? device_info().sms : 1;
+  if (nblk == 1) {
+    // one launch: a warp per hidden group (per token with an RMSNorm), at most 2 CTAs per SM
+    int64_t blocks = nm.gamma != nullptr ? (M + 7) / 8 : (groups + 7) / 8;
+    blocks = std::max<int64_t>(1, std::min<int64_t>(blocks, 2 * (int64_t)sms));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, sort_small_kernel, hidden, nm, ids, M, H, E, K, ws);
+  }
   int64_t qblocks = (groups + 7) / 8;
-  const int64_t cap8 = 8 * (int64_t)(device_info().sms > 0 ? device_info().sms : 1);  // 8 CTAs per SM
+  const int64_t cap8 = 8 * (int64_t)sms;  // 8 CTAs per SM
   if (qblocks > cap8) qblocks = cap8;
   count_quant_kernel<<<(unsigned)(nblk + qblocks), 256, 0, st>>>(hidden, nm, ids, M, H, E, K, nblk, ws);
   if (cudaError_t e = cudaGetLastError()) return e;
