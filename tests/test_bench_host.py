@@ -29,6 +29,19 @@ def test_algorithmic_decode_step():
     assert flops == 2 * 2048 * 128 + 6 * 2048 * 768 * 8 == 76_021_760
 
 
+def test_launch_count_follows_the_library_modes():
+    """The kernels the bench claims per step switch where the library switches modes: the
+    pair kernels up to kPairPreferRows routed rows, the one-launch sort up to one sort block
+    (kSortBlock pairs), the two-launch sort and the gather above."""
+    import re
+    src = open(os.path.join(bench.ROOT, "fp8_block_scaled_router_gb300", "csrc", "common.cuh")).read()
+    pair = int(re.search(r"constexpr int kPairPreferRows = (\d+);", src).group(1))
+    block = int(re.search(r"constexpr int kSortBlock = (\d+);", src).group(1))
+    assert (bench.PAIR_ROWS, bench.SORT_BLOCK) == (pair, block)
+    assert [bench.launches_per_step(m, 8, 2048, 128) for m in (1, 8, 9, 12, 32, 33, 4096)] == [3, 3, 5, 5, 5, 7, 7]
+    assert [bench.launches_per_step(m, 1, 2048, 16) for m in (64, 65, 256, 257)] == [3, 5, 5, 7]
+
+
 def test_algorithmic_prefill_gate_up_flops():
     _, _, _, gu_flops = bench.algorithmic(2048, 768, 128, 8, 4096, 128)
     assert gu_flops == 206_158_430_208  # 4 * 2048 * 768 * 32768 routed rows
