@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const uint16_t* __re
 //            places its pairs at base[e] + pre[e] + (earlier pairs of e in this block), so
 //            rows keep ascending flat pair order t*K + j within each expert. Block 0 also
 //            writes the expert offsets, the 128-row tile list and the 16-row group list.
-//   gather:  one warp per placed row copies the row's hidden codes (H bytes) and scales
+//   gather:  each warp copies up to four placed rows' hidden codes (H bytes) and scales
 //            into xp / sa_p -- thousands of independent 16-byte copies in flight.
 // ---------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) count_quant_kernel(const uint16_t* __restrict__ hidden, const Norm nm,
@@ -380,28 +380,38 @@ __global__ void __launch_bounds__(256) sort_small_kernel(const uint16_t* __restr
   }
 }
 
-// xp[p] = qa[row_src[p] / K], sa_p[p] = sa[row_src[p] / K]: one warp per placed row. Only
-// the first offsets[E] rows are placed (pairs with an invalid id are not); row_src past them
-// is not written by this call and is never read.
-__global__ void __launch_bounds__(256) gather_rows_kernel(int R, int H, int E, int K, WsPtrs ws) {
+// xp[p] = qa[row_src[p] / K], sa_p[p] = sa[row_src[p] / K]: each warp copies rpw consecutive
+// placed rows (rpw * H / 16 <= 512 16-byte pieces, at most 16 per lane, all loaded before the
+// first store). Only the first offsets[E] rows are placed (pairs with an invalid id are not);
+// row_src past them is not written by this call and is never read.
+__global__ void __launch_bounds__(256) gather_rows_kernel(int R, int H, int E, int K, int rpw, WsPtrs ws) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int p = blockIdx.x * 8 + warp;
-  if (p >= R || p >= ws.offsets[E]) return;
-  const int t = ws.row_src[p] / K;
-  const uint4* src = reinterpret_cast<const uint4*>(ws.qa + (size_t)t * H);
-  uint4* dst = reinterpret_cast<uint4*>(ws.xp + (size_t)p * H);
-  const int n16 = H / 16;  // <= 512: at most 16 per lane
+  const int p0 = (blockIdx.x * 8 + warp) * rpw;
+  const int placed = min(R, ws.offsets[E]);
+  if (p0 >= placed) return;
+  const int nr = min(rpw, placed - p0);
+  const int n16 = H / 16;
+  // lane r < nr holds the source token of row p0 + r
+  const int my_tok = lane < nr ? ws.row_src[p0 + lane] / K : 0;
   uint4 v[16];
 #pragma unroll
-  for (int j = 0; j < 16; ++j)
-    if (lane + 32 * j < n16) v[j] = src[lane + 32 * j];
+  for (int j = 0; j < 16; ++j) {
+    const int idx = lane + 32 * j, r = idx / n16;
+    const int t = __shfl_sync(0xffffffffu, my_tok, r & 31);
+    if (r < nr) v[j] = reinterpret_cast<const uint4*>(ws.qa + (size_t)t * H)[idx % n16];
+  }
 #pragma unroll
-  for (int j = 0; j < 16; ++j)
-    if (lane + 32 * j < n16) dst[lane + 32 * j] = v[j];
+  for (int j = 0; j < 16; ++j) {
+    const int idx = lane + 32 * j, r = idx / n16;
+    if (r < nr) reinterpret_cast<uint4*>(ws.xp + (size_t)(p0 + r) * H)[idx % n16] = v[j];
+  }
   const int nsc = H / 128;  // <= 64
-  for (int c = lane; c < nsc; c += 32) ws.sa_p[(size_t)p * nsc + c] = ws.sa[(size_t)t * nsc + c];
+  for (int r = 0; r < nr; ++r) {
+    const int t = __shfl_sync(0xffffffffu, my_tok, r);
+    for (int c = lane; c < nsc; c += 32) ws.sa_p[(size_t)(p0 + r) * nsc + c] = ws.sa[(size_t)t * nsc + c];
+  }
 }
 
 cudaError_t launch_sort_gather(const uint16_t* hidden, Norm nm, const int32_t* ids, int M, int H, int E, int K,
@@ -440,8 +450,10 @@ cudaError_t launch_sort_gather(const uint16_t* hidden, Norm nm, const int32_t* i
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (cudaError_t e = cudaLaunchKernelEx(&cfg, scatter_kernel, ids, M, H, E, K, nblk, ws)) return e;
-  cfg.gridDim = dim3((unsigned)((R + 7) / 8), 1, 1);  // one warp per row, R rows at most
-  return cudaLaunchKernelEx(&cfg, gather_rows_kernel, R, H, E, K, ws);
+  // rows per warp: as many as 16 pieces of 16 bytes per lane hold, at most 4
+  const int rpw = std::max(1, std::min(4, 512 / (H / 16)));
+  cfg.gridDim = dim3((unsigned)((R + 8 * rpw - 1) / (8 * rpw)), 1, 1);  // R rows at most
+  return cudaLaunchKernelEx(&cfg, gather_rows_kernel, R, H, E, K, rpw, ws);
 }
 
 cudaError_t launch_prep(const uint16_t* hidden, const int32_t* ids, int M, int H, int E, int K,
